@@ -1,0 +1,385 @@
+"""Decode benchmark: batch-1 greedy decode of the Qwen3-8B-shaped Q4_0 model
+(vocab 151936, hidden 4096, 36 layers, 32/8 heads, head_dim 128, FFN 12288,
+f16 KV cache) after a 2048-token prompt, on one GB300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+One "step" is one full decode step (embedding, 36 layers, final norm, tied LM
+head, argmax) through the CUDA-graph replay of tq_decode_step.  Inputs are
+device-resident; the model (4.26 GB of weights) exceeds L2, so every step
+reads its weights from HBM.  Prints one JSON line.  Under torchrun each rank
+runs an independent replica (the step does not shard); `value` is the sum of
+tokens over all ranks divided by the slowest rank's time.
+
+`--impl reference` times the CPU oracle on this host's cores on a bounded
+sample of the same step (2 of the 36 layers at full size plus the LM head,
+scaled to a full step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s (B=1, Q4_0 Qwen3-8B shape) and achieved HBM GB/s vs peak"
+PROMPT = 2048
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def dist_init(n):
+    rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        dist.init_process_group(backend)
+    return rank, world
+
+
+def barrier_max(value, world):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.path = index, None, None
+
+    def start(self):
+        try:
+            import tempfile
+            self.path = tempfile.mktemp(suffix=".csv")
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+N_SAMPLE_LAYERS = 2
+
+
+class OracleSample:
+    """The oracle (as it stands, float32) on a bounded sample of one decode
+    step of the 8B workload: 2 of the 36 full-size layers at a context of 2048
+    cached positions, plus the full 151936x4096 LM head.  One call of step()
+    returns the time of a full 36-layer step, scaled from the sample."""
+
+    def __init__(self, ctx=PROMPT):
+        import numpy as np
+        import synth
+        from oracle import model as om
+        from oracle import quant
+        w = self.w = synth.QWEN3_8B_Q4
+        weights = {}
+        names = [f"blk.{i}.{t}" for i in range(N_SAMPLE_LAYERS) for t in synth.LAYER_TENSORS[:7]]
+        for n in names + ["token_embd"]:
+            weights[n] = quant.quantize(synth.host_tensor(w, n), w.wtype)
+        for n in [f"blk.{i}.{t}" for i in range(N_SAMPLE_LAYERS) for t in synth.LAYER_TENSORS[7:]]:
+            weights[n] = synth.host_tensor(w, n)
+        weights["output_norm"] = synth.host_tensor(w, "output_norm")
+        self.m = om.OracleModel(w, weights, dtype=np.float32)
+        for n in names + ["token_embd"]:
+            self.m.matrix(n)                      # decoded once, outside the timed region
+        kv = synth.host_normal(w.seed, synth.KV_STREAM, 2 * w.n_kv_heads * ctx * w.head_dim,
+                               sigma=1.0).reshape(2, w.n_kv_heads, ctx, w.head_dim)
+        self.kv = kv.astype(np.float16).astype(np.float32)
+        self.ctx = ctx
+        self.x0 = self.m.embed([1])
+        self.cores = len(os.sched_getaffinity(0))
+        self.desc = (f"oracle float32 decode step at context {ctx}: {N_SAMPLE_LAYERS} of "
+                     f"{w.n_layers} full-size layers and the 151936x4096 LM head timed, the "
+                     f"layer time scaled to {w.n_layers} layers; weights decoded before timing")
+
+    def step(self) -> float:
+        import numpy as np
+        cache = [(self.kv[0].copy(), self.kv[1].copy()) for _ in range(N_SAMPLE_LAYERS)]
+        t0 = time.perf_counter()
+        x = self.x0
+        for i in range(N_SAMPLE_LAYERS):
+            x = self.m.block(i, x, cache, np.array([self.ctx]))
+        t1 = time.perf_counter()
+        self.m.head(x[-1])
+        t2 = time.perf_counter()
+        return (t1 - t0) / N_SAMPLE_LAYERS * self.w.n_layers + (t2 - t1)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    o = OracleSample()
+    for _ in range(args.warmup):
+        o.step()
+    total = sum(o.step() for _ in range(args.steps))
+    value = args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 / value, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "qwen3_8b_q4_0 batch-1 greedy decode after a 2048-token prompt",
+                       "sample": o.desc},
+            "cpu_baseline": {"value": round(value, 5), "unit": "tokens/s", "cores": o.cores,
+                             "kind": "oracle", "sample": o.desc},
+            "e2e": {"value": round(value, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU bench
+
+def file_hash(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def traffic_from_profile(kernel_src):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "gemv_q4_0_swiglu_8b.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("source_sha256_16") != file_hash(kernel_src):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def run_gpu(args, rank, world):
+    import numpy as np
+    import torch
+    import synth
+    import block_quantized_transformer_gb300 as tq
+    from block_quantized_transformer_gb300.synthetic import build_weights, build_model
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = synth.QWEN3_8B_Q4
+    K, W = args.steps, args.warmup
+    max_ctx = PROMPT + W + K + 8
+    mats, gains = build_weights(w, dev)
+    model = build_model(w, device=dev, max_ctx=max_ctx, max_prefill=PROMPT,
+                        weights=(mats, gains))
+    torch.cuda.synchronize()
+    weight_bytes = model.weight_bytes() + sum(g.numel() * 4 for g in gains.values())
+    stream = torch.cuda.Stream(device=dev)
+    prompt = torch.tensor(w.prompt(), dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):
+        t0 = time.perf_counter()
+        am = model.prefill(prompt)
+        stream.synchronize()
+        prefill_s = time.perf_counter() - t0
+        tok = torch.empty(1, dtype=torch.int32, device=dev)
+        tok.copy_(am)
+        pos = torch.full((1,), PROMPT, dtype=torch.int32, device=dev)
+        logits = None
+        # warm-up (graph capture happens on the first replay)
+        for _ in range(W):
+            model.decode_step(tok, pos, pos, argmax=tok, graph=True)
+            pos.add_(1)
+        stream.synchronize()
+        ctx0 = int(pos.item())
+        barrier(world)
+        torch.cuda.synchronize()
+        clocks = Clocks(local)
+        clocks.start()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            model.decode_step(tok, pos, pos, argmax=tok, graph=True)
+            pos.add_(1)
+        e1.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        clk = clocks.stop()
+        barrier(world)
+        assert model.status() == 0
+    ms_max = barrier_max(ms, world)
+    ms_step = ms_max / K
+
+    # algorithmic bytes per step: all weights + KV read at each step's context + KV write
+    kv_row = 2 * w.n_kv_heads * w.head_dim * 2 * w.n_layers          # bytes per cached position
+    mean_ctx = ctx0 + (K - 1) / 2.0 + 1
+    step_bytes = weight_bytes + kv_row * mean_ctx + kv_row
+    value = world * K / (ms_max / 1e3)
+    hbm, bf16, peak_kind = peaks()
+
+    # ---- dominant kernel alone: fused RMSNorm + gate/up GEMV + SwiGLU over all 36 layers
+    x = torch.randn(1, w.hidden, device=dev)
+    act = torch.empty(1, w.ffn, device=dev)
+    g_bytes = [mats[f"blk.{i}.ffn_gate"].nbytes + mats[f"blk.{i}.ffn_up"].nbytes for i in range(w.n_layers)]
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for i in range(w.n_layers):
+                tq.tq_swiglu_gemv(mats[f"blk.{i}.ffn_gate"], mats[f"blk.{i}.ffn_up"], x,
+                                  gains[f"blk.{i}.ffn_norm"], out=act)
+        stream.synchronize()
+        k0 = torch.cuda.Event(enable_timing=True)
+        k1 = torch.cuda.Event(enable_timing=True)
+        reps = 5
+        k0.record(stream)
+        for _ in range(reps):
+            for i in range(w.n_layers):
+                tq.tq_swiglu_gemv(mats[f"blk.{i}.ffn_gate"], mats[f"blk.{i}.ffn_up"], x,
+                                  gains[f"blk.{i}.ffn_norm"], out=act)
+        k1.record(stream)
+        stream.synchronize()
+    kern_ms = k0.elapsed_time(k1) / (reps * w.n_layers)
+    kern_bytes = sum(g_bytes) / w.n_layers + 4 * (w.hidden * 2 + w.ffn)
+    achieved = kern_bytes / (kern_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4),
+                "traffic": traffic_from_profile(os.path.join(ROOT, "block_quantized_transformer_gb300",
+                                                              "csrc", "gemv.cu")),
+                "kernel": "gemv_kernel<Q4_0, SWIGLU> (RMSNorm + gate/up + SwiGLU), 2x12288x4096",
+                "peak_kind": peak_kind + " (burst copy, kernel timed alone)",
+                "launch_ms": round(kern_ms, 5), "bytes_per_launch": int(kern_bytes)}
+
+    # ---- end to end: host token in, host argmax out, every step
+    h_tok = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    h_pos = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    h_out = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    d_tok = torch.empty(1, dtype=torch.int32, device=dev)
+    d_pos = torch.empty(1, dtype=torch.int32, device=dev)
+    d_out = torch.empty(1, dtype=torch.int32, device=dev)
+    h_tok[0] = int(tok.item())
+    p = int(pos.item())
+    e2e_steps = min(K, max(1, max_ctx - p - 1))
+    with torch.cuda.stream(stream):
+        h_pos[0] = p
+        d_tok.copy_(h_tok, non_blocking=True)
+        d_pos.copy_(h_pos, non_blocking=True)
+        model.decode_step(d_tok, d_pos, d_pos, argmax=d_out, graph=True)   # capture
+        h_out.copy_(d_out, non_blocking=True)
+        stream.synchronize()
+        p += 1
+        h_tok[0] = int(h_out[0])
+        e2e_steps = min(e2e_steps, max_ctx - p - 1)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            h_pos[0] = p
+            d_tok.copy_(h_tok, non_blocking=True)
+            d_pos.copy_(h_pos, non_blocking=True)
+            model.decode_step(d_tok, d_pos, d_pos, argmax=d_out, graph=True)
+            h_out.copy_(d_out, non_blocking=True)
+            stream.synchronize()
+            h_tok[0] = int(h_out[0])
+            p += 1
+        e2e_s = time.perf_counter() - t0
+    e2e_s = barrier_max(e2e_s, world)
+    e2e = {"value": world * e2e_steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 8,
+           "d2h_bytes_per_step": 4, "steps": e2e_steps}
+
+    launches = model.launches_per_step * K
+    model.close()
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "qwen3_8b_q4_0 batch-1 greedy decode after a 2048-token prompt "
+                                   f"(context {ctx0}..{ctx0 + K - 1})",
+                       "weights": "Q4_0, 4.26 GB, seeded N(0,0.02)", "kv_cache": "f16",
+                       "l2": "inputs exceed L2 (4.3 GB of weights read every step)",
+                       "parallelism": f"replicas x{world}"},
+            "hbm": {"step_bytes": int(step_bytes), "achieved_gbs": round(step_bytes / (ms_step / 1e3) / 1e9, 1),
+                    "frac_of_peak": round(step_bytes / (ms_step / 1e3) / 1e9 / hbm, 4),
+                    "peak_gbs": hbm, "peak_kind": peak_kind,
+                    "roofline_tokens_per_s": round(hbm * 1e9 / step_bytes, 1)},
+            "roofline": roofline, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+            "prefill": {"tokens": PROMPT, "seconds": round(prefill_s, 4),
+                        "tokens_per_s": round(PROMPT / prefill_s, 1)}}
+    if rank == 0 and not args.no_cpu_baseline:
+        o = OracleSample()
+        o.step()
+        per_step = min(o.step() for _ in range(3))
+        line["cpu_baseline"] = {"value": round(1.0 / per_step, 5), "unit": "tokens/s",
+                                "cores": o.cores, "kind": "oracle", "sample": o.desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+        run_reference(args, rank, world)
+        return
+    rank, world = dist_init(args.gpus)
+    run_gpu(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

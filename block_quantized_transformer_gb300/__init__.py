@@ -1,0 +1,454 @@
+"""Python binding of libtq.so: block-quantized (Q8_0 / Q4_0) Qwen3-style decode
+on one GB300.
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+kernels behind the C ABI (include/tq.h); PyTorch provides device memory and
+streams.  The functions named ``tq_*`` mirror the C entry points one for one;
+``Model``, ``QMat`` and the small helpers wrap them.
+
+Conventions follow the tessl_torch README ("Handle ownership, closing and
+errors"): a handle is freed exactly once (``Model.close()``, idempotent; copies
+and pickling are refused); a handle is used from the thread that made it;
+every integer headed for a C field is range-checked first; a refusal (status
+1) raises ``TqError`` and leaves the model usable; a library failure (status 2)
+raises ``TqPoisoned`` and the model refuses further work.  There is no CPU
+fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.environ.get("TQ_LIB", os.path.join(_PKG, "_build", "libtq.so"))
+
+TQ_OK, TQ_REFUSED, TQ_INTERNAL = 0, 1, 2
+TQ_Q4_0, TQ_Q8_0 = 2, 8
+TQ_KV_F32, TQ_KV_F16 = 0, 1
+TQ_DEV_BAD_TOKEN, TQ_DEV_KV_OVERFLOW, TQ_DEV_WAIT_TIMEOUT = 1, 2, 4
+WTYPES = {"q4_0": TQ_Q4_0, "q8_0": TQ_Q8_0}
+BLOCK_BYTES = {TQ_Q4_0: 18, TQ_Q8_0: 34}
+QS_BYTES = {TQ_Q4_0: 16, TQ_Q8_0: 32}
+
+EXPORTS = ("tq_workspace_bytes", "tq_kv_cache_bytes", "tq_model_create", "tq_prefill",
+           "tq_decode_step", "tq_decode_step_graph", "tq_model_status", "tq_model_poisoned",
+           "tq_decode_launches", "tq_model_free", "tq_last_error", "tq_repack", "tq_quantize",
+           "tq_dequantize", "tq_gemv", "tq_swiglu_gemv", "tq_lm_head")
+
+
+class TqError(RuntimeError):
+    """The library refused a call (bad argument); nothing was enqueued."""
+
+
+class TqPoisoned(TqError):
+    """A CUDA error or device status bit: the model is closed for further work."""
+
+
+# ----------------------------------------------------------------------------- ABI structs
+
+class TqConfig(ctypes.Structure):
+    _fields_ = [("vocab", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("n_layers", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("ffn", ctypes.c_int32), ("rms_eps", ctypes.c_float),
+                ("rope_theta", ctypes.c_float), ("wtype", ctypes.c_int32),
+                ("kvtype", ctypes.c_int32), ("max_batch", ctypes.c_int32),
+                ("max_ctx", ctypes.c_int32), ("max_prefill", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("n_pages", ctypes.c_int32)]
+
+
+class TqQmat(ctypes.Structure):
+    _fields_ = [("qs_dev", ctypes.c_void_p), ("d_dev", ctypes.c_void_p)]
+
+
+class TqLayer(ctypes.Structure):
+    _fields_ = [(n, TqQmat) for n in ("attn_q", "attn_k", "attn_v", "attn_output", "ffn_gate",
+                                      "ffn_up", "ffn_down")] + \
+               [(n, ctypes.c_void_p) for n in ("attn_norm_dev", "ffn_norm_dev",
+                                               "attn_q_norm_dev", "attn_k_norm_dev")]
+
+
+class TqWeights(ctypes.Structure):
+    _fields_ = [("token_embd", TqQmat), ("output", TqQmat), ("output_norm_dev", ctypes.c_void_p),
+                ("layers", ctypes.POINTER(TqLayer))]
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """Load libtq.so (raises if it has not been built: there is no fallback)."""
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise TqError(f"libtq.so not built at {LIB_PATH}; run "
+                              "block_quantized_transformer_gb300.build.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+            cfgp = ctypes.POINTER(TqConfig)
+            sig = {
+                "tq_workspace_bytes": (ctypes.c_size_t, [cfgp]),
+                "tq_kv_cache_bytes": (ctypes.c_size_t, [cfgp]),
+                "tq_model_create": (i32, [cfgp, ctypes.POINTER(TqWeights), vp, vp, vp,
+                                          ctypes.POINTER(vp)]),
+                "tq_prefill": (i32, [vp, i32, vp, i32, i32, vp, vp, vp, vp]),
+                "tq_decode_step": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
+                "tq_decode_step_graph": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
+                "tq_model_status": (i32, [vp, vp, ctypes.POINTER(ctypes.c_uint32)]),
+                "tq_model_poisoned": (ctypes.c_int, [vp]),
+                "tq_decode_launches": (i32, [vp, i32]),
+                "tq_model_free": (None, [vp]),
+                "tq_last_error": (ctypes.c_char_p, []),
+                "tq_repack": (i32, [i32, vp, i64, i64, vp, vp, vp]),
+                "tq_quantize": (i32, [i32, vp, i64, i64, vp, vp]),
+                "tq_dequantize": (i32, [i32, TqQmat, i64, i64, i64, vp, vp]),
+                "tq_gemv": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, vp, vp]),
+                "tq_swiglu_gemv": (i32, [i32, TqQmat, TqQmat, i32, i32, vp, i32, vp, f32, vp, vp]),
+                "tq_lm_head": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, f32, vp, vp, vp, vp]),
+            }
+            for name, (res, args) in sig.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def exported_symbols() -> list:
+    L = lib()
+    return [n for n in EXPORTS if hasattr(L, n)]
+
+
+# ----------------------------------------------------------------------------- checks
+
+def _int(name: str, v, lo: int, hi: int) -> int:
+    if isinstance(v, bool) or not isinstance(v, int):
+        raise TqError(f"{name} must be an int (got {type(v).__name__})")
+    if not lo <= v <= hi:
+        raise TqError(f"{name}={v} outside [{lo}, {hi}]")
+    return v
+
+
+I32 = (-2**31, 2**31 - 1)
+I64 = (-2**63, 2**63 - 1)
+
+
+def _dev(t: Optional[torch.Tensor], name: str, dtype=None, min_numel: int = 0):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TqError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise TqError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TqError(f"{name} must have dtype {dtype} (got {t.dtype})")
+    if t.numel() < min_numel:
+        raise TqError(f"{name} holds {t.numel()} elements, needs {min_numel}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device=None) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _status(rc: int, what: str):
+    if rc == TQ_OK:
+        return
+    msg = lib().tq_last_error().decode(errors="replace")
+    if rc == TQ_REFUSED:
+        raise TqError(f"{what}: {msg}")
+    raise TqPoisoned(f"{what}: {msg}")
+
+
+# ----------------------------------------------------------------------------- raw entry points
+
+def tq_workspace_bytes(cfg: TqConfig) -> int:
+    return int(lib().tq_workspace_bytes(ctypes.byref(cfg)))
+
+
+def tq_kv_cache_bytes(cfg: TqConfig) -> int:
+    return int(lib().tq_kv_cache_bytes(ctypes.byref(cfg)))
+
+
+def tq_last_error() -> str:
+    return lib().tq_last_error().decode(errors="replace")
+
+
+def tq_repack(wtype: int, blocks: torch.Tensor, rows: int, cols: int, qs: torch.Tensor,
+              d: torch.Tensor) -> None:
+    _int("rows", rows, 0, I64[1])
+    _int("cols", cols, 0, I64[1])
+    nb = cols // 32
+    rc = lib().tq_repack(wtype, _dev(blocks, "blocks", torch.uint8, rows * nb * BLOCK_BYTES[wtype]),
+                         rows, cols, _dev(qs, "qs", torch.uint8, rows * nb * QS_BYTES[wtype]),
+                         _dev(d, "d", torch.int16, rows * nb), _stream())
+    _status(rc, "tq_repack")
+
+
+def tq_quantize(wtype: int, w: torch.Tensor, rows: int, cols: int, blocks: torch.Tensor) -> None:
+    _int("rows", rows, 0, I64[1])
+    _int("cols", cols, 0, I64[1])
+    rc = lib().tq_quantize(wtype, _dev(w, "w", torch.float32, rows * cols), rows, cols,
+                           _dev(blocks, "blocks", torch.uint8, rows * (cols // 32) * BLOCK_BYTES[wtype]),
+                           _stream())
+    _status(rc, "tq_quantize")
+
+
+# ----------------------------------------------------------------------------- matrices
+
+class QMat:
+    """One planar quantized matrix [rows][cols] in device memory (torch-owned)."""
+
+    def __init__(self, wtype: int, rows: int, cols: int, qs: torch.Tensor, d: torch.Tensor):
+        self.wtype, self.rows, self.cols, self.qs, self.d = wtype, rows, cols, qs, d
+
+    @property
+    def abi(self) -> TqQmat:
+        return TqQmat(self.qs.data_ptr(), self.d.data_ptr())
+
+    @property
+    def nbytes(self) -> int:
+        return self.qs.numel() + 2 * self.d.numel()
+
+    @classmethod
+    def empty(cls, wtype: int, rows: int, cols: int, device) -> "QMat":
+        nb = cols // 32
+        qs = torch.empty(rows * nb * QS_BYTES[wtype], dtype=torch.uint8, device=device)
+        d = torch.empty(rows * nb, dtype=torch.int16, device=device)
+        return cls(wtype, rows, cols, qs, d)
+
+    @classmethod
+    def from_blocks(cls, wtype: int, blocks: torch.Tensor, rows: int, cols: int) -> "QMat":
+        """GGUF-order block bytes (device uint8, [rows][cols/32][34|18]) -> planar."""
+        m = cls.empty(wtype, rows, cols, blocks.device)
+        tq_repack(wtype, blocks, rows, cols, m.qs, m.d)
+        return m
+
+
+def quantize(w: torch.Tensor, wtype: int) -> torch.Tensor:
+    """f32 [rows][cols] (device) -> GGUF-order blocks uint8 [rows][cols/32][34|18]."""
+    rows, cols = w.shape
+    out = torch.empty(rows, cols // 32, BLOCK_BYTES[wtype], dtype=torch.uint8, device=w.device)
+    tq_quantize(wtype, w.contiguous(), rows, cols, out)
+    return out
+
+
+def tq_dequantize(m: QMat, row0: int = 0, n_rows: Optional[int] = None,
+                  out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    n_rows = m.rows - row0 if n_rows is None else n_rows
+    _int("row0", row0, 0, m.rows)
+    _int("n_rows", n_rows, 0, m.rows - row0)
+    if out is None:
+        out = torch.empty(n_rows, m.cols, dtype=torch.float32, device=m.qs.device)
+    rc = lib().tq_dequantize(m.wtype, m.abi, m.cols, row0, n_rows,
+                             _dev(out, "out", torch.float32, n_rows * m.cols), _stream())
+    _status(rc, "tq_dequantize")
+    return out
+
+
+def tq_gemv(m: QMat, x: torch.Tensor, residual: Optional[torch.Tensor] = None,
+            out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """y[b] = residual[b] + W x[b] for x [batch][cols] f32."""
+    x2 = x.reshape(-1, m.cols)
+    B = _int("batch", x2.shape[0], 1, I32[1])
+    if out is None:
+        out = torch.empty(B, m.rows, dtype=torch.float32, device=x.device)
+    rc = lib().tq_gemv(m.wtype, m.abi, m.rows, m.cols, _dev(x2, "x", torch.float32, B * m.cols), B,
+                       _dev(residual, "residual", torch.float32, B * m.rows),
+                       _dev(out, "y", torch.float32, B * m.rows), _stream())
+    _status(rc, "tq_gemv")
+    return out
+
+
+def tq_swiglu_gemv(gate: QMat, up: QMat, x: torch.Tensor, gain: Optional[torch.Tensor] = None,
+                   eps: float = 1e-6, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """silu(Wg h) * (Wu h) with h = rms_norm(x, gain) (or x when gain is None)."""
+    x2 = x.reshape(-1, gate.cols)
+    B = _int("batch", x2.shape[0], 1, I32[1])
+    if out is None:
+        out = torch.empty(B, gate.rows, dtype=torch.float32, device=x.device)
+    rc = lib().tq_swiglu_gemv(gate.wtype, gate.abi, up.abi, gate.rows, gate.cols,
+                              _dev(x2, "x", torch.float32, B * gate.cols), B,
+                              _dev(gain, "gain", torch.float32, gate.cols), float(eps),
+                              _dev(out, "out", torch.float32, B * gate.rows), _stream())
+    _status(rc, "tq_swiglu_gemv")
+    return out
+
+
+def tq_lm_head(m: QMat, x: torch.Tensor, gain: torch.Tensor, eps: float = 1e-6,
+               want_logits: bool = True):
+    """(logits [batch][vocab] or None, argmax [batch] int32) of rms_norm(x) through W."""
+    x2 = x.reshape(-1, m.cols)
+    B = _int("batch", x2.shape[0], 1, I32[1])
+    logits = torch.empty(B, m.rows, dtype=torch.float32, device=x.device) if want_logits else None
+    am = torch.empty(B, dtype=torch.int32, device=x.device)
+    scratch = torch.empty(B, dtype=torch.int64, device=x.device)
+    rc = lib().tq_lm_head(m.wtype, m.abi, m.rows, m.cols, _dev(x2, "x", torch.float32), B,
+                          _dev(gain, "gain", torch.float32, m.cols), float(eps),
+                          _dev(logits, "logits", torch.float32), _dev(am, "argmax", torch.int32),
+                          _dev(scratch, "scratch", torch.int64), _stream())
+    _status(rc, "tq_lm_head")
+    return logits, am
+
+
+# ----------------------------------------------------------------------------- model
+
+LAYER_MATS = ("attn_q", "attn_k", "attn_v", "attn_output", "ffn_gate", "ffn_up", "ffn_down")
+LAYER_GAINS = ("attn_norm", "ffn_norm", "attn_q_norm", "attn_k_norm")
+
+
+class Model:
+    """A decoder over planar quantized weights, a torch-allocated workspace and
+    KV cache.  ``mats`` maps GGUF-style names (``token_embd``,
+    ``blk.{i}.attn_q`` ...; optionally ``output``) to QMat; ``gains`` maps
+    ``blk.{i}.attn_norm`` ... and ``output_norm`` to f32 device tensors."""
+
+    def __init__(self, *, vocab, hidden, n_layers, n_heads, n_kv_heads, head_dim, ffn,
+                 wtype, kv, mats: dict, gains: dict, max_batch=1, max_ctx=4096,
+                 max_prefill=512, page_size=0, n_pages=0, rms_eps=1e-6, rope_theta=1e6,
+                 device="cuda"):
+        self._handle = None
+        self._thread = threading.get_ident()
+        wt = WTYPES[wtype] if isinstance(wtype, str) else wtype
+        kvt = {"f32": TQ_KV_F32, "f16": TQ_KV_F16}[kv] if isinstance(kv, str) else kv
+        vals = dict(vocab=vocab, hidden=hidden, n_layers=n_layers, n_heads=n_heads,
+                    n_kv_heads=n_kv_heads, head_dim=head_dim, ffn=ffn, max_batch=max_batch,
+                    max_ctx=max_ctx, max_prefill=max_prefill, page_size=page_size,
+                    n_pages=n_pages)
+        for k, v in vals.items():
+            _int(k, v, 0, I32[1])
+        self.cfg = TqConfig(rms_eps=float(rms_eps), rope_theta=float(rope_theta), wtype=wt,
+                            kvtype=kvt, **vals)
+        self.device = torch.device(device)
+        ws = tq_workspace_bytes(self.cfg)
+        if ws == 0:
+            raise TqError(f"invalid configuration: {tq_last_error()}")
+        kvb = tq_kv_cache_bytes(self.cfg)
+        self.workspace = torch.empty(ws + 256, dtype=torch.uint8, device=self.device)
+        self._ws_off = (-self.workspace.data_ptr()) % 256
+        elt = torch.float16 if kvt == TQ_KV_F16 else torch.float32
+        esz = 2 if kvt == TQ_KV_F16 else 4
+        self.k_cache = torch.zeros(kvb // esz, dtype=elt, device=self.device)
+        self.v_cache = torch.zeros(kvb // esz, dtype=elt, device=self.device)
+        self.mats, self.gains = mats, gains
+        layers = (TqLayer * n_layers)()
+        for i in range(n_layers):
+            L = layers[i]
+            for n in LAYER_MATS:
+                setattr(L, n, mats[f"blk.{i}.{n}"].abi)
+            for n in LAYER_GAINS:
+                setattr(L, n + "_dev", gains[f"blk.{i}.{n}"].data_ptr())
+        self._layers = layers
+        out = mats.get("output")
+        self._weights = TqWeights(mats["token_embd"].abi, out.abi if out is not None else TqQmat(0, 0),
+                                  gains["output_norm"].data_ptr(),
+                                  ctypes.cast(layers, ctypes.POINTER(TqLayer)))
+        h = ctypes.c_void_p()
+        rc = lib().tq_model_create(ctypes.byref(self.cfg), ctypes.byref(self._weights),
+                                   ctypes.c_void_p(self.workspace.data_ptr() + self._ws_off),
+                                   ctypes.c_void_p(self.k_cache.data_ptr()),
+                                   ctypes.c_void_p(self.v_cache.data_ptr()), ctypes.byref(h))
+        _status(rc, "tq_model_create")
+        self._handle = h
+
+    # -- handle discipline
+    def __copy__(self):
+        raise TypeError("Model owns a C handle and cannot be copied")
+
+    __deepcopy__ = lambda self, memo: self.__copy__()  # noqa: E731
+
+    def __reduce__(self):
+        raise TypeError("Model owns a C handle and cannot be pickled")
+
+    def _h(self) -> ctypes.c_void_p:
+        if self._handle is None:
+            raise TqError("model is closed")
+        if threading.get_ident() != self._thread:
+            raise TqError("model used from a thread other than the one that created it")
+        return self._handle
+
+    def _after(self, rc: int, what: str):
+        if rc != TQ_OK and self._handle is not None and lib().tq_model_poisoned(self._handle):
+            msg = tq_last_error()
+            self.close()
+            raise TqPoisoned(f"{what}: {msg}")
+        _status(rc, what)
+
+    def close(self):
+        if self._handle is not None:
+            if threading.get_ident() != self._thread:
+                self._handle = None        # leak rather than free on a foreign thread
+                raise TqError("close() from another thread: handle leaked")
+            lib().tq_model_free(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            if self._handle is not None and threading.get_ident() == self._thread:
+                lib().tq_model_free(self._handle)
+                self._handle = None
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # -- work
+    @property
+    def launches_per_step(self) -> int:
+        return int(lib().tq_decode_launches(self._h(), 1))
+
+    def prefill(self, tokens: torch.Tensor, start_pos: int = 0, seq: int = 0,
+                block_table: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
+                argmax: Optional[torch.Tensor] = None) -> torch.Tensor:
+        n = _int("n_tokens", tokens.numel(), 1, I32[1])
+        _int("start_pos", start_pos, 0, I32[1])
+        _int("seq", seq, 0, I32[1])
+        if argmax is None:
+            argmax = torch.empty(1, dtype=torch.int32, device=self.device)
+        rc = lib().tq_prefill(self._h(), seq, _dev(tokens, "tokens", torch.int32), n, start_pos,
+                              _dev(block_table, "block_table", torch.int32),
+                              _dev(logits, "logits", torch.float32, self.cfg.vocab),
+                              _dev(argmax, "argmax", torch.int32, 1), _stream(self.device))
+        self._after(rc, "tq_prefill")
+        return argmax
+
+    def decode_step(self, tokens: torch.Tensor, positions: torch.Tensor, kv_lens: torch.Tensor,
+                    block_table: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
+                    argmax: Optional[torch.Tensor] = None, graph: bool = False) -> torch.Tensor:
+        B = _int("batch", tokens.numel(), 1, I32[1])
+        if argmax is None:
+            argmax = torch.empty(B, dtype=torch.int32, device=self.device)
+        fn = lib().tq_decode_step_graph if graph else lib().tq_decode_step
+        rc = fn(self._h(), B, _dev(tokens, "tokens", torch.int32, B),
+                _dev(positions, "positions", torch.int32, B), _dev(kv_lens, "kv_lens", torch.int32, B),
+                _dev(block_table, "block_table", torch.int32),
+                _dev(logits, "logits", torch.float32, B * self.cfg.vocab),
+                _dev(argmax, "argmax", torch.int32, B), _stream(self.device))
+        self._after(rc, "tq_decode_step_graph" if graph else "tq_decode_step")
+        return argmax
+
+    def status(self) -> int:
+        bits = ctypes.c_uint32(0)
+        rc = lib().tq_model_status(self._h(), _stream(self.device), ctypes.byref(bits))
+        if rc != TQ_OK:
+            msg = tq_last_error()
+            self.close()
+            raise TqPoisoned(f"tq_model_status: {msg}")
+        return int(bits.value)
+
+    def weight_bytes(self) -> int:
+        return sum(m.nbytes for m in self.mats.values())
+
+
+def tq_model_create(*args, **kw) -> Model:
+    return Model(*args, **kw)

@@ -1,0 +1,652 @@
+// C ABI of libtq.so (declared in include/tq.h): argument checks on the host
+// before anything is enqueued, the model object over caller-owned memory, the
+// decode and prefill launch sequences, CUDA-graph replay of the decode step,
+// and the status / poisoning rules of the tessl_torch README ("Handle
+// ownership, closing and errors").
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "kernels.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+void set_error(const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+}
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Layout {
+  size_t x, qkv, att, act, cos_t, sin_t, part, counters, keys, status, total;
+  int T;                 // rows of activation buffers
+  int split_dec, splits_dec, split_pf, splits_pf;
+};
+
+int qkv_width(const tq_config& c) { return (c.n_heads + 2 * c.n_kv_heads) * c.head_dim; }
+
+bool validate(const tq_config* c) {
+  if (c == nullptr) return set_error("config is NULL"), false;
+  if (c->vocab <= 0 || c->hidden <= 0 || c->n_layers <= 0 || c->n_heads <= 0 ||
+      c->n_kv_heads <= 0 || c->ffn <= 0)
+    return set_error("config: sizes must be positive"), false;
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return set_error("config: head_dim must be 64 or 128 (got %d)", c->head_dim), false;
+  if (c->n_heads % c->n_kv_heads != 0)
+    return set_error("config: n_heads must be a multiple of n_kv_heads"), false;
+  const int G = c->n_heads / c->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return set_error("config: n_heads / n_kv_heads must be 1, 2, 4 or 8 (got %d)", G), false;
+  if (c->wtype != TQ_Q4_0 && c->wtype != TQ_Q8_0)
+    return set_error("config: wtype must be TQ_Q4_0 (2) or TQ_Q8_0 (8)"), false;
+  if (c->kvtype != TQ_KV_F32 && c->kvtype != TQ_KV_F16)
+    return set_error("config: kvtype must be TQ_KV_F32 (0) or TQ_KV_F16 (1)"), false;
+  const int ks[3] = {c->hidden, c->n_heads * c->head_dim, c->ffn};
+  for (int k : ks)
+    if (!tq::gemv_supported(k))
+      return set_error("config: no GEMV thread mapping for an input width of %d "
+                       "(need 32*kpt*p, kpt in 1..4, p in {8,...,128})", k), false;
+  if (c->max_batch < 1 || c->max_ctx < 1 || c->max_prefill < 1)
+    return set_error("config: max_batch, max_ctx and max_prefill must be >= 1"), false;
+  if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f))
+    return set_error("config: rms_eps and rope_theta must be positive"), false;
+  if (c->page_size < 0) return set_error("config: page_size must be >= 0"), false;
+  if (c->page_size > 0) {
+    if (c->page_size % 32 != 0) return set_error("config: page_size must be a multiple of 32"), false;
+    if (c->max_ctx % c->page_size != 0)
+      return set_error("config: max_ctx must be a multiple of page_size"), false;
+    if (c->n_pages < 1) return set_error("config: n_pages must be >= 1"), false;
+  }
+  return true;
+}
+
+Layout layout_of(const tq_config& c) {
+  Layout L{};
+  const int G = c.n_heads / c.n_kv_heads;
+  L.T = c.max_batch > c.max_prefill ? c.max_batch : c.max_prefill;
+  L.split_dec = 128 * (1 + (c.max_ctx - 1) / 8192);
+  L.splits_dec = (c.max_ctx + L.split_dec - 1) / L.split_dec;
+  L.split_pf = 1024;
+  L.splits_pf = (c.max_ctx + L.split_pf - 1) / L.split_pf;
+  const size_t part_dec = (size_t)c.max_batch * c.n_kv_heads * L.splits_dec;
+  const size_t part_pf = (size_t)c.max_prefill * c.n_kv_heads * L.splits_pf;
+  const size_t part_rows = part_dec > part_pf ? part_dec : part_pf;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.x = take((size_t)L.T * c.hidden * 4);
+  L.qkv = take((size_t)L.T * qkv_width(c) * 4);
+  L.att = take((size_t)L.T * c.n_heads * c.head_dim * 4);
+  L.act = take((size_t)L.T * c.ffn * 4);
+  L.cos_t = take((size_t)c.max_ctx * (c.head_dim / 2) * 4);
+  L.sin_t = take((size_t)c.max_ctx * (c.head_dim / 2) * 4);
+  L.part = take(part_rows * G * (c.head_dim + 2) * 4);
+  L.counters = take((size_t)L.T * c.n_kv_heads * 4);
+  L.keys = take((size_t)L.T * 8);
+  L.status = take(16);
+  L.total = off;
+  return L;
+}
+
+size_t kv_bytes(const tq_config& c) {
+  const size_t esz = c.kvtype == TQ_KV_F16 ? 2 : 4;
+  const size_t per_layer =
+      c.page_size > 0 ? (size_t)c.n_pages * c.n_kv_heads * c.page_size * c.head_dim
+                      : (size_t)c.max_batch * c.n_kv_heads * c.max_ctx * c.head_dim;
+  return (size_t)c.n_layers * per_layer * esz;
+}
+
+bool check_qmat(const tq_qmat& m, const char* name) {
+  if (m.qs_dev == nullptr || m.d_dev == nullptr) return set_error("weights: %s is NULL", name), false;
+  if (!aligned16(m.qs_dev) || !aligned16(m.d_dev))
+    return set_error("weights: %s must be 16-byte aligned", name), false;
+  return true;
+}
+
+}  // namespace
+
+struct tq_model {
+  tq_config cfg;
+  std::vector<tq_layer> layers;
+  tq_qmat embd, head;
+  const float* out_norm;
+  uint8_t* ws;
+  Layout L;
+  void* kc;
+  void* vc;
+  size_t layer_kv_bytes;
+  bool poisoned = false;
+  std::string poison_reason;
+  // decode-step graph
+  cudaGraphExec_t gexec = nullptr;
+  struct {
+    int batch;
+    const void* p[6];
+    void* stream;
+  } gkey{};
+
+  float* x() const { return reinterpret_cast<float*>(ws + L.x); }
+  float* qkv() const { return reinterpret_cast<float*>(ws + L.qkv); }
+  float* att() const { return reinterpret_cast<float*>(ws + L.att); }
+  float* act() const { return reinterpret_cast<float*>(ws + L.act); }
+  float* cos_t() const { return reinterpret_cast<float*>(ws + L.cos_t); }
+  float* sin_t() const { return reinterpret_cast<float*>(ws + L.sin_t); }
+  float* part() const { return reinterpret_cast<float*>(ws + L.part); }
+  unsigned* counters() const { return reinterpret_cast<unsigned*>(ws + L.counters); }
+  unsigned long long* keys() const { return reinterpret_cast<unsigned long long*>(ws + L.keys); }
+  uint32_t* status() const { return reinterpret_cast<uint32_t*>(ws + L.status); }
+  void* kc_layer(int l) const { return static_cast<uint8_t*>(kc) + (size_t)l * layer_kv_bytes; }
+  void* vc_layer(int l) const { return static_cast<uint8_t*>(vc) + (size_t)l * layer_kv_bytes; }
+};
+
+namespace {
+
+tq_status fail_cuda(tq_model* m, cudaError_t e, const char* what) {
+  set_error("%s: CUDA error %s (%s); the model is poisoned: free it and create a new one",
+            what, cudaGetErrorName(e), cudaGetErrorString(e));
+  (void)cudaGetLastError();  // the error is reported here; do not leave it for the caller's next call
+  if (m != nullptr) {
+    m->poisoned = true;
+    m->poison_reason = g_last_error;
+  }
+  return TQ_INTERNAL;
+}
+
+bool refuse_if_poisoned(tq_model* m) {
+  if (m == nullptr) return set_error("model is NULL"), true;
+  if (m->poisoned) {
+    set_error("model is poisoned (%s); recreate it", m->poison_reason.c_str());
+    return true;
+  }
+  return false;
+}
+
+tq::GemvSeg seg_of(const tq_qmat& q, int rows) {
+  return tq::GemvSeg{static_cast<const uint8_t*>(q.qs_dev), q.d_dev, rows};
+}
+
+tq::CacheView cache_view(const tq_model* m, const int32_t* block_table) {
+  const tq_config& c = m->cfg;
+  tq::CacheView v{};
+  v.max_ctx = c.max_ctx;
+  v.n_kv = c.n_kv_heads;
+  v.page_size = c.page_size;
+  v.n_pages = c.n_pages;
+  v.block_table = block_table;
+  v.bt_stride = c.page_size > 0 ? c.max_ctx / c.page_size : 0;
+  return v;
+}
+
+// The layer loop shared by decode (T = batch, one token per sequence) and
+// prefill (T tokens of sequence `seq` at positions pos_base..).
+cudaError_t run_layers(tq_model* m, int T, const int32_t* pos, const int32_t* kv_len, int pos_base,
+                       int seq_fixed, const int32_t* block_table, bool prefill, cudaStream_t s) {
+  const tq_config& c = m->cfg;
+  const int hd = c.head_dim, nq = c.n_heads, nkv = c.n_kv_heads, G = nq / nkv;
+  cudaError_t e;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const tq_layer& ly = m->layers[l];
+    // RMSNorm + Q/K/V projections
+    tq::GemvArgs g{};
+    g.seg[0] = seg_of(ly.attn_q, nq * hd);
+    g.seg[1] = seg_of(ly.attn_k, nkv * hd);
+    g.seg[2] = seg_of(ly.attn_v, nkv * hd);
+    g.nseg = 3;
+    g.K = c.hidden;
+    g.N = (nq + 2 * nkv) * hd;
+    g.B = T;
+    g.x = m->x();
+    g.gain = ly.attn_norm_dev;
+    g.eps = c.rms_eps;
+    g.y = m->qkv();
+    if ((e = tq::launch_gemv(c.wtype, tq::GEMV_STORE, g, s)) != cudaSuccess) return e;
+    // QK-norm + RoPE + KV append
+    tq::RopeArgs r{};
+    r.qkv = m->qkv();
+    r.T = T;
+    r.nq = nq;
+    r.nkv = nkv;
+    r.pos = pos;
+    r.kv_len = kv_len;
+    r.pos_base = pos_base;
+    r.seq_fixed = seq_fixed;
+    r.kc = m->kc_layer(l);
+    r.vc = m->vc_layer(l);
+    r.cache = cache_view(m, block_table);
+    r.cos_t = m->cos_t();
+    r.sin_t = m->sin_t();
+    r.gq = ly.attn_q_norm_dev;
+    r.gk = ly.attn_k_norm_dev;
+    r.eps = c.rms_eps;
+    r.status = m->status();
+    if ((e = tq::launch_rope_append(c.kvtype, hd, r, s)) != cudaSuccess) return e;
+    // attention
+    tq::AttnArgs a{};
+    a.q = m->qkv();
+    a.q_stride = qkv_width(c);
+    a.o = m->att();
+    a.T = T;
+    a.nq = nq;
+    a.nkv = nkv;
+    a.kv_len = kv_len;
+    a.pos_base = pos_base;
+    a.seq_fixed = seq_fixed;
+    a.kc = m->kc_layer(l);
+    a.vc = m->vc_layer(l);
+    a.cache = cache_view(m, block_table);
+    a.split_keys = prefill ? m->L.split_pf : m->L.split_dec;
+    a.max_splits = prefill ? m->L.splits_pf : m->L.splits_dec;
+    a.part = m->part();
+    a.counters = m->counters();
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
+    a.status = m->status();
+    if ((e = tq::launch_attn_decode(c.kvtype, hd, G, a, s)) != cudaSuccess) return e;
+    // output projection + residual
+    tq::GemvArgs o{};
+    o.seg[0] = seg_of(ly.attn_output, c.hidden);
+    o.nseg = 1;
+    o.K = nq * hd;
+    o.N = c.hidden;
+    o.B = T;
+    o.x = m->att();
+    o.y = m->x();
+    o.residual = m->x();
+    if ((e = tq::launch_gemv(c.wtype, tq::GEMV_STORE, o, s)) != cudaSuccess) return e;
+    // RMSNorm + gate/up + SwiGLU
+    tq::GemvArgs f{};
+    f.seg[0] = seg_of(ly.ffn_gate, c.ffn);
+    f.seg[1] = seg_of(ly.ffn_up, c.ffn);
+    f.nseg = 2;
+    f.K = c.hidden;
+    f.N = c.ffn;
+    f.B = T;
+    f.x = m->x();
+    f.gain = ly.ffn_norm_dev;
+    f.eps = c.rms_eps;
+    f.y = m->act();
+    if ((e = tq::launch_gemv(c.wtype, tq::GEMV_SWIGLU, f, s)) != cudaSuccess) return e;
+    // down projection + residual
+    tq::GemvArgs d{};
+    d.seg[0] = seg_of(ly.ffn_down, c.hidden);
+    d.nseg = 1;
+    d.K = c.ffn;
+    d.N = c.hidden;
+    d.B = T;
+    d.x = m->act();
+    d.y = m->x();
+    d.residual = m->x();
+    if ((e = tq::launch_gemv(c.wtype, tq::GEMV_STORE, d, s)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t run_head(tq_model* m, const float* x, int B, float* logits, int32_t* argmax, cudaStream_t s) {
+  const tq_config& c = m->cfg;
+  tq::GemvArgs h{};
+  h.seg[0] = seg_of(m->head, c.vocab);
+  h.nseg = 1;
+  h.K = c.hidden;
+  h.N = c.vocab;
+  h.B = B;
+  h.x = x;
+  h.gain = m->out_norm;
+  h.eps = c.rms_eps;
+  h.y = logits;
+  h.argmax_keys = m->keys();
+  cudaError_t e = tq::launch_gemv(c.wtype, tq::GEMV_ARGMAX, h, s);
+  if (e != cudaSuccess) return e;
+  return tq::launch_argmax_finish(m->keys(), B, argmax, s);
+}
+
+cudaError_t enqueue_decode(tq_model* m, int batch, const int32_t* tokens, const int32_t* positions,
+                           const int32_t* kv_lens, const int32_t* block_table, float* logits,
+                           int32_t* argmax, cudaStream_t s) {
+  const tq_config& c = m->cfg;
+  cudaError_t e = tq::launch_embed(c.wtype, m->embd.qs_dev, m->embd.d_dev, c.vocab, c.hidden, tokens,
+                                   batch, m->x(), m->status(), m->keys(), batch, s);
+  if (e != cudaSuccess) return e;
+  if ((e = run_layers(m, batch, positions, kv_lens, 0, -1, block_table, false, s)) != cudaSuccess)
+    return e;
+  return run_head(m, m->x(), batch, logits, argmax, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tq_last_error(void) { return g_last_error.c_str(); }
+
+size_t tq_workspace_bytes(const tq_config* cfg) {
+  if (!validate(cfg)) return 0;
+  return layout_of(*cfg).total;
+}
+
+size_t tq_kv_cache_bytes(const tq_config* cfg) {
+  if (!validate(cfg)) return 0;
+  return kv_bytes(*cfg);
+}
+
+tq_status tq_model_create(const tq_config* cfg, const tq_weights* w, void* workspace, void* k_cache,
+                          void* v_cache, tq_model** out) {
+  if (out == nullptr) return set_error("out is NULL"), TQ_REFUSED;
+  *out = nullptr;
+  if (!validate(cfg)) return TQ_REFUSED;
+  if (w == nullptr || w->layers == nullptr) return set_error("weights or weights->layers is NULL"), TQ_REFUSED;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return set_error("workspace must be non-NULL and 256-byte aligned"), TQ_REFUSED;
+  if (k_cache == nullptr || v_cache == nullptr || !aligned16(k_cache) || !aligned16(v_cache))
+    return set_error("k_cache and v_cache must be non-NULL and 16-byte aligned"), TQ_REFUSED;
+  if (!check_qmat(w->token_embd, "token_embd")) return TQ_REFUSED;
+  if (w->output.qs_dev != nullptr && !check_qmat(w->output, "output")) return TQ_REFUSED;
+  if (w->output_norm_dev == nullptr) return set_error("weights: output_norm is NULL"), TQ_REFUSED;
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    const tq_layer& ly = w->layers[l];
+    const tq_qmat* mats[7] = {&ly.attn_q, &ly.attn_k, &ly.attn_v, &ly.attn_output,
+                              &ly.ffn_gate, &ly.ffn_up, &ly.ffn_down};
+    for (int i = 0; i < 7; ++i) {
+      char name[64];
+      snprintf(name, sizeof(name), "blk.%d matrix %d", l, i);
+      if (!check_qmat(*mats[i], name)) return TQ_REFUSED;
+    }
+    if (!ly.attn_norm_dev || !ly.ffn_norm_dev || !ly.attn_q_norm_dev || !ly.attn_k_norm_dev)
+      return set_error("weights: a gain of blk.%d is NULL", l), TQ_REFUSED;
+    const float* gs[4] = {ly.attn_norm_dev, ly.ffn_norm_dev, ly.attn_q_norm_dev, ly.attn_k_norm_dev};
+    for (const float* gp : gs)
+      if (!aligned16(gp)) return set_error("weights: gains of blk.%d must be 16-byte aligned", l), TQ_REFUSED;
+  }
+  if (!aligned16(w->output_norm_dev)) return set_error("weights: output_norm must be 16-byte aligned"), TQ_REFUSED;
+
+  tq_model* m = new tq_model();
+  m->cfg = *cfg;
+  m->layers.assign(w->layers, w->layers + cfg->n_layers);
+  m->embd = w->token_embd;
+  m->head = w->output.qs_dev != nullptr ? w->output : w->token_embd;
+  m->out_norm = w->output_norm_dev;
+  m->ws = static_cast<uint8_t*>(workspace);
+  m->L = layout_of(*cfg);
+  m->kc = k_cache;
+  m->vc = v_cache;
+  m->layer_kv_bytes = kv_bytes(*cfg) / cfg->n_layers;
+
+  // RoPE table in double precision on the host: angle = pos * theta^(-i/half)
+  const int half = cfg->head_dim / 2;
+  std::vector<float> cs((size_t)cfg->max_ctx * half), sn((size_t)cfg->max_ctx * half);
+  for (int p = 0; p < cfg->max_ctx; ++p)
+    for (int i = 0; i < half; ++i) {
+      const double inv = 1.0 / std::pow((double)cfg->rope_theta, (double)i / (double)half);
+      const double ang = (double)p * inv;
+      cs[(size_t)p * half + i] = (float)std::cos(ang);
+      sn[(size_t)p * half + i] = (float)std::sin(ang);
+    }
+  cudaError_t e = tq::attn_prepare(cfg->kvtype, cfg->head_dim, cfg->n_heads / cfg->n_kv_heads);
+  if (e == cudaSuccess) e = cudaMemset(workspace, 0, m->L.total);
+  if (e == cudaSuccess) e = cudaMemcpy(m->cos_t(), cs.data(), cs.size() * 4, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(m->sin_t(), sn.data(), sn.size() * 4, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    fail_cuda(nullptr, e, "tq_model_create");
+    delete m;
+    return TQ_INTERNAL;
+  }
+  *out = m;
+  return TQ_OK;
+}
+
+tq_status tq_prefill(tq_model* m, int32_t seq, const int32_t* tokens, int32_t n_tokens,
+                     int32_t start_pos, const int32_t* block_table, float* logits, int32_t* argmax,
+                     void* stream) {
+  if (refuse_if_poisoned(m)) return TQ_REFUSED;
+  const tq_config& c = m->cfg;
+  if (tokens == nullptr || argmax == nullptr) return set_error("tokens and argmax must not be NULL"), TQ_REFUSED;
+  if (n_tokens < 1 || n_tokens > c.max_prefill)
+    return set_error("n_tokens=%d outside [1, max_prefill=%d]", n_tokens, c.max_prefill), TQ_REFUSED;
+  if (start_pos < 0 || (int64_t)start_pos + n_tokens > c.max_ctx)
+    return set_error("start_pos=%d + n_tokens=%d exceeds max_ctx=%d", start_pos, n_tokens, c.max_ctx),
+           TQ_REFUSED;
+  if (c.page_size > 0) {
+    if (block_table == nullptr) return set_error("paged cache: block_table must not be NULL"), TQ_REFUSED;
+    seq = 0;
+  } else if (seq < 0 || seq >= c.max_batch) {
+    return set_error("seq=%d outside [0, max_batch=%d)", seq, c.max_batch), TQ_REFUSED;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = tq::launch_embed(c.wtype, m->embd.qs_dev, m->embd.d_dev, c.vocab, c.hidden, tokens,
+                                   n_tokens, m->x(), m->status(), m->keys(), 1, s);
+  if (e == cudaSuccess) e = run_layers(m, n_tokens, nullptr, nullptr, start_pos, seq, block_table, true, s);
+  if (e == cudaSuccess) e = run_head(m, m->x() + (size_t)(n_tokens - 1) * c.hidden, 1, logits, argmax, s);
+  if (e != cudaSuccess) return fail_cuda(m, e, "tq_prefill");
+  return TQ_OK;
+}
+
+static tq_status check_decode_args(tq_model* m, int32_t batch, const int32_t* tokens,
+                                   const int32_t* positions, const int32_t* kv_lens,
+                                   const int32_t* block_table, int32_t* argmax) {
+  if (refuse_if_poisoned(m)) return TQ_REFUSED;
+  const tq_config& c = m->cfg;
+  if (batch < 1 || batch > c.max_batch)
+    return set_error("batch=%d outside [1, max_batch=%d]", batch, c.max_batch), TQ_REFUSED;
+  if (!tokens || !positions || !kv_lens || !argmax)
+    return set_error("tokens, positions, kv_lens and argmax must not be NULL"), TQ_REFUSED;
+  if (c.page_size > 0 && block_table == nullptr)
+    return set_error("paged cache: block_table must not be NULL"), TQ_REFUSED;
+  return TQ_OK;
+}
+
+tq_status tq_decode_step(tq_model* m, int32_t batch, const int32_t* tokens, const int32_t* positions,
+                         const int32_t* kv_lens, const int32_t* block_table, float* logits,
+                         int32_t* argmax, void* stream) {
+  tq_status st = check_decode_args(m, batch, tokens, positions, kv_lens, block_table, argmax);
+  if (st != TQ_OK) return st;
+  cudaError_t e = enqueue_decode(m, batch, tokens, positions, kv_lens,
+                                 m->cfg.page_size > 0 ? block_table : nullptr, logits, argmax,
+                                 static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(m, e, "tq_decode_step");
+  return TQ_OK;
+}
+
+tq_status tq_decode_step_graph(tq_model* m, int32_t batch, const int32_t* tokens,
+                               const int32_t* positions, const int32_t* kv_lens,
+                               const int32_t* block_table, float* logits, int32_t* argmax,
+                               void* stream) {
+  tq_status st = check_decode_args(m, batch, tokens, positions, kv_lens, block_table, argmax);
+  if (st != TQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* ptrs[6] = {tokens, positions, kv_lens, block_table, logits, argmax};
+  bool same = m->gexec != nullptr && m->gkey.batch == batch && m->gkey.stream == stream;
+  for (int i = 0; same && i < 6; ++i) same = m->gkey.p[i] == ptrs[i];
+  cudaError_t e;
+  if (!same) {
+    if (m->gexec != nullptr) {
+      cudaGraphExecDestroy(m->gexec);
+      m->gexec = nullptr;
+    }
+    if (s == nullptr) return set_error("graph replay needs a non-default stream"), TQ_REFUSED;
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return fail_cuda(m, e, "tq_decode_step_graph: begin capture");
+    cudaError_t le = enqueue_decode(m, batch, tokens, positions, kv_lens,
+                                    m->cfg.page_size > 0 ? block_table : nullptr, logits, argmax, s);
+    e = cudaStreamEndCapture(s, &graph);
+    if (le != cudaSuccess) e = le;
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&m->gexec, graph, 0);
+    if (graph != nullptr) cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return fail_cuda(m, e, "tq_decode_step_graph: capture");
+    m->gkey.batch = batch;
+    m->gkey.stream = stream;
+    for (int i = 0; i < 6; ++i) m->gkey.p[i] = ptrs[i];
+  }
+  e = cudaGraphLaunch(m->gexec, s);
+  if (e != cudaSuccess) return fail_cuda(m, e, "tq_decode_step_graph: launch");
+  return TQ_OK;
+}
+
+tq_status tq_model_status(tq_model* m, void* stream, uint32_t* bits) {
+  if (m == nullptr || bits == nullptr) return set_error("model and status_bits must not be NULL"), TQ_REFUSED;
+  *bits = 0;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  uint32_t v = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&v, m->status(), 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && v != 0) e = cudaMemset(m->status(), 0, 4);
+  if (e != cudaSuccess) return fail_cuda(m, e, "tq_model_status");
+  *bits = v;
+  if (v != 0) {
+    set_error("device status 0x%x (%s%s%s); the model is poisoned", v,
+              (v & TQ_DEV_BAD_TOKEN) ? "token id out of range " : "",
+              (v & TQ_DEV_KV_OVERFLOW) ? "position or cache slot out of range " : "",
+              (v & TQ_DEV_WAIT_TIMEOUT) ? "device wait timed out" : "");
+    m->poisoned = true;
+    m->poison_reason = g_last_error;
+    return TQ_INTERNAL;
+  }
+  return TQ_OK;
+}
+
+int tq_model_poisoned(const tq_model* m) { return (m != nullptr && m->poisoned) ? 1 : 0; }
+
+int32_t tq_decode_launches(const tq_model* m, int32_t batch) {
+  (void)batch;
+  if (m == nullptr) return 0;
+  return 1 + 6 * m->cfg.n_layers + 2;
+}
+
+void tq_model_free(tq_model* m) {
+  if (m == nullptr) return;
+  if (m->gexec != nullptr) cudaGraphExecDestroy(m->gexec);
+  delete m;
+}
+
+// ------------------------------------------------------------- formats --
+
+tq_status tq_repack(int32_t wtype, const void* blocks, int64_t rows, int64_t cols, void* qs,
+                    uint16_t* d, void* stream) {
+  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (rows < 0 || cols < 0 || cols % 32 != 0) return set_error("cols must be a multiple of 32"), TQ_REFUSED;
+  if (rows * cols == 0) return TQ_OK;
+  if (!blocks || !qs || !d) return set_error("pointers must not be NULL"), TQ_REFUSED;
+  if ((reinterpret_cast<uintptr_t>(blocks) & 1u) || !aligned16(qs) || (reinterpret_cast<uintptr_t>(d) & 1u))
+    return set_error("blocks must be 2-byte, qs 16-byte and d 2-byte aligned"), TQ_REFUSED;
+  cudaError_t e = tq::launch_repack(wtype, blocks, rows, cols / 32, qs, d, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(nullptr, e, "tq_repack");
+  return TQ_OK;
+}
+
+tq_status tq_quantize(int32_t wtype, const float* w, int64_t rows, int64_t cols, void* blocks, void* stream) {
+  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (rows < 0 || cols < 0 || cols % 32 != 0) return set_error("cols must be a multiple of 32"), TQ_REFUSED;
+  if (rows * cols == 0) return TQ_OK;
+  if (!w || !blocks) return set_error("pointers must not be NULL"), TQ_REFUSED;
+  cudaError_t e = tq::launch_quantize(wtype, w, rows * (cols / 32), blocks, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(nullptr, e, "tq_quantize");
+  return TQ_OK;
+}
+
+tq_status tq_dequantize(int32_t wtype, tq_qmat w, int64_t cols, int64_t row0, int64_t n_rows,
+                        float* out, void* stream) {
+  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (cols <= 0 || cols % 32 != 0 || row0 < 0 || n_rows < 0)
+    return set_error("cols must be a positive multiple of 32; rows non-negative"), TQ_REFUSED;
+  if (n_rows == 0) return TQ_OK;
+  if (!w.qs_dev || !w.d_dev || !out) return set_error("pointers must not be NULL"), TQ_REFUSED;
+  if (!aligned16(w.qs_dev) || !aligned16(out)) return set_error("qs and out must be 16-byte aligned"), TQ_REFUSED;
+  cudaError_t e = tq::launch_dequant(wtype, w.qs_dev, w.d_dev, cols / 32, row0, n_rows, out,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(nullptr, e, "tq_dequantize");
+  return TQ_OK;
+}
+
+// ------------------------------------------------------------- ops --
+
+tq_status tq_gemv(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const float* x, int32_t batch,
+                  const float* residual, float* y, void* stream) {
+  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (rows < 1 || batch < 1 || !tq::gemv_supported(cols))
+    return set_error("rows and batch must be >= 1 and cols have a GEMV mapping (got %d)", cols), TQ_REFUSED;
+  if (!w.qs_dev || !w.d_dev || !x || !y) return set_error("pointers must not be NULL"), TQ_REFUSED;
+  if (!aligned16(w.qs_dev) || !aligned16(x)) return set_error("qs and x must be 16-byte aligned"), TQ_REFUSED;
+  tq::GemvArgs g{};
+  g.seg[0] = seg_of(w, rows);
+  g.nseg = 1;
+  g.K = cols;
+  g.N = rows;
+  g.B = batch;
+  g.x = x;
+  g.y = y;
+  g.residual = residual;
+  cudaError_t e = tq::launch_gemv(wtype, tq::GEMV_STORE, g, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(nullptr, e, "tq_gemv");
+  return TQ_OK;
+}
+
+tq_status tq_swiglu_gemv(int32_t wtype, tq_qmat gate, tq_qmat up, int32_t ffn, int32_t hidden,
+                         const float* x, int32_t batch, const float* gain, float eps, float* out,
+                         void* stream) {
+  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (ffn < 1 || batch < 1 || !tq::gemv_supported(hidden))
+    return set_error("ffn and batch must be >= 1 and hidden have a GEMV mapping"), TQ_REFUSED;
+  if (!gate.qs_dev || !gate.d_dev || !up.qs_dev || !up.d_dev || !x || !out)
+    return set_error("pointers must not be NULL"), TQ_REFUSED;
+  if (!aligned16(gate.qs_dev) || !aligned16(up.qs_dev) || !aligned16(x) || (gain && !aligned16(gain)))
+    return set_error("qs, x and gain must be 16-byte aligned"), TQ_REFUSED;
+  tq::GemvArgs f{};
+  f.seg[0] = seg_of(gate, ffn);
+  f.seg[1] = seg_of(up, ffn);
+  f.nseg = 2;
+  f.K = hidden;
+  f.N = ffn;
+  f.B = batch;
+  f.x = x;
+  f.gain = gain;
+  f.eps = eps;
+  f.y = out;
+  cudaError_t e = tq::launch_gemv(wtype, tq::GEMV_SWIGLU, f, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(nullptr, e, "tq_swiglu_gemv");
+  return TQ_OK;
+}
+
+tq_status tq_lm_head(int32_t wtype, tq_qmat w, int32_t vocab, int32_t hidden, const float* x,
+                     int32_t batch, const float* gain, float eps, float* logits, int32_t* argmax,
+                     void* scratch, void* stream) {
+  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (vocab < 1 || batch < 1 || !tq::gemv_supported(hidden))
+    return set_error("vocab and batch must be >= 1 and hidden have a GEMV mapping"), TQ_REFUSED;
+  if (!w.qs_dev || !w.d_dev || !x || !gain || !argmax || !scratch)
+    return set_error("pointers must not be NULL"), TQ_REFUSED;
+  if ((reinterpret_cast<uintptr_t>(scratch) & 7u) != 0) return set_error("scratch must be 8-byte aligned"), TQ_REFUSED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned long long* keys = static_cast<unsigned long long*>(scratch);
+  cudaError_t e = cudaMemsetAsync(keys, 0, batch * sizeof(unsigned long long), s);
+  if (e == cudaSuccess) {
+    tq::GemvArgs h{};
+    h.seg[0] = seg_of(w, vocab);
+    h.nseg = 1;
+    h.K = hidden;
+    h.N = vocab;
+    h.B = batch;
+    h.x = x;
+    h.gain = gain;
+    h.eps = eps;
+    h.y = logits;
+    h.argmax_keys = keys;
+    e = tq::launch_gemv(wtype, tq::GEMV_ARGMAX, h, s);
+  }
+  if (e == cudaSuccess) e = tq::launch_argmax_finish(keys, batch, argmax, s);
+  if (e != cudaSuccess) return fail_cuda(nullptr, e, "tq_lm_head");
+  return TQ_OK;
+}
+
+}  // extern "C"

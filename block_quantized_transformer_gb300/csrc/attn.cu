@@ -1,0 +1,479 @@
+// Attention side of the decode step ("Всередині LLM: чисте виконання на
+// Python для Qwen3-0.6B на MLX", step 4 and step 5 "Вся функція уваги";
+// "Inferencia local y arquitecturas", qwen3.archdef: norm_heads before rope):
+//
+//  * rope_append: per-head RMSNorm of every Q and K head over head_dim with
+//    its gain, half-split RoPE from a host-made f32 cos/sin table, Q written
+//    back in place, K (normed, rotated) and V converted to the cache type
+//    (f16: round to nearest even) and stored at the token's cache index.
+//  * attn_decode: split-K flash-decode grouped-query attention.  One CTA per
+//    (split of the context, KV head, token); its four warps take 32-key tiles
+//    of the split in turn.  Each tile's K and V rows are contiguous in the
+//    cache and are staged into shared memory by the TMA engine (1-D bulk
+//    copies completing on an mbarrier, no multicast).  The whole query group
+//    (G heads sharing the KV head) is evaluated against each staged tile:
+//    lane l owns head_dim/32 consecutive dimensions, partial dot products are
+//    combined with a reduce-scatter butterfly that leaves lane l holding the
+//    score of (head l / (32/G), key l % (32/G)), and an online softmax in base
+//    2 keeps (max, sum, output) per head.  Warps merge in shared memory; the
+//    CTA writes its split's partial (o, m, l); the last CTA of a (token, head)
+//    to finish (atomic counter, no waiting) merges all splits and resets the
+//    counter.
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace tq {
+namespace {
+
+#define kNegInf (-__int_as_float(0x7f800000))
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+template <typename KT>
+__device__ __forceinline__ KT to_kv(float v);
+template <>
+__device__ __forceinline__ float to_kv<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __half to_kv<__half>(float v) { return __float2half_rn(v); }
+
+// Pointer to element 0 of cache row `slot` of (seq, kv head h), or null when
+// the slot or page is out of range.
+template <typename KT, int HD>
+__device__ __forceinline__ KT* cache_row(void* base, int seq, int h, int slot, const CacheView& c) {
+  if (slot < 0 || slot >= c.max_ctx) return nullptr;
+  if (c.page_size == 0) {
+    return reinterpret_cast<KT*>(base) + (((int64_t)seq * c.n_kv + h) * c.max_ctx + slot) * HD;
+  }
+  const int page = c.block_table[(int64_t)seq * c.bt_stride + slot / c.page_size];
+  if (page < 0 || page >= c.n_pages) return nullptr;
+  return reinterpret_cast<KT*>(base) +
+         (((int64_t)page * c.n_kv + h) * c.page_size + slot % c.page_size) * HD;
+}
+
+template <typename KT, int HD>
+__global__ void __launch_bounds__(128) rope_append_kernel(RopeArgs a) {
+  constexpr int DPL = HD / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hi = blockIdx.x * 4 + warp;
+  const int t = blockIdx.y;
+  if (hi >= a.nq + a.nkv) return;
+  const int pos = a.pos != nullptr ? a.pos[t] : a.pos_base + t;
+  const int slot = a.kv_len != nullptr ? a.kv_len[t] : a.pos_base + t;
+  const int seq = a.seq_fixed >= 0 ? a.seq_fixed : t;
+  const int row_stride = (a.nq + 2 * a.nkv) * HD;
+  float* row = a.qkv + (int64_t)t * row_stride;
+  const bool is_q = hi < a.nq;
+  float* src = row + (is_q ? hi * HD : a.nq * HD + (hi - a.nq) * HD);
+
+  float x[DPL];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) {
+    x[j] = src[lane + 32 * j];
+    ss = fmaf(x[j], x[j], ss);
+  }
+  ss = warp_sum(ss);
+  const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
+  const float* g = is_q ? a.gq : a.gk;
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) x[j] = x[j] * inv * g[lane + 32 * j];
+
+  if (pos >= 0 && pos < a.cache.max_ctx) {
+    constexpr int HALF = HD / 2;
+#pragma unroll
+    for (int j = 0; j < DPL / 2; ++j) {
+      const int i = lane + 32 * j;
+      const float c = a.cos_t[(int64_t)pos * HALF + i];
+      const float s = a.sin_t[(int64_t)pos * HALF + i];
+      const float x1 = x[j], x2 = x[j + DPL / 2];
+      x[j] = x1 * c - x2 * s;
+      x[j + DPL / 2] = x1 * s + x2 * c;
+    }
+  } else if (lane == 0) {
+    set_status(a.status, TQ_DEV_KV_OVERFLOW);
+  }
+
+  if (is_q) {
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) src[lane + 32 * j] = x[j];
+    return;
+  }
+  const int h = hi - a.nq;
+  KT* kd = cache_row<KT, HD>(a.kc, seq, h, slot, a.cache);
+  KT* vd = cache_row<KT, HD>(a.vc, seq, h, slot, a.cache);
+  if (kd == nullptr || vd == nullptr) {
+    if (lane == 0) set_status(a.status, TQ_DEV_KV_OVERFLOW);
+    return;
+  }
+  const float* vsrc = row + (a.nq + a.nkv) * HD + h * HD;
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) {
+    kd[lane + 32 * j] = to_kv<KT>(x[j]);
+    vd[lane + 32 * j] = to_kv<KT>(vsrc[lane + 32 * j]);
+  }
+}
+
+// ------------------------------------------------------------ attention --
+
+template <typename KT, int DPL>
+__device__ __forceinline__ void load_row(const KT* p, float (&v)[DPL]);
+template <>
+__device__ __forceinline__ void load_row<__half, 4>(const __half* p, float (&v)[4]) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+template <>
+__device__ __forceinline__ void load_row<__half, 2>(const __half* p, float (&v)[2]) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(p));
+  v[0] = a.x; v[1] = a.y;
+}
+template <>
+__device__ __forceinline__ void load_row<float, 4>(const float* p, float (&v)[4]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+template <>
+__device__ __forceinline__ void load_row<float, 2>(const float* p, float (&v)[2]) {
+  const float2 a = *reinterpret_cast<const float2*>(p);
+  v[0] = a.x; v[1] = a.y;
+}
+
+// reduce-scatter of 32 values over a full warp: lane l ends with sum of v[l]
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i < n / 2) {
+        const float send = upper ? v[i] : v[i + n / 2];
+        const float keep = upper ? v[i + n / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+  }
+  return v[0];
+}
+
+template <typename KT, int HD, int G, int NS>
+struct AttnSmem {
+  static constexpr int TILE = 32;
+  static constexpr int TILE_BYTES = TILE * HD * (int)sizeof(KT);
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int OFF_BAR = 4 * NS * STAGE_BYTES;
+  static constexpr int OFF_P = OFF_BAR + 4 * NS * 8;
+  static constexpr int OFF_ALPHA = OFF_P + 4 * G * 32 * 4;
+  static constexpr int OFF_M = OFF_ALPHA + 4 * G * 4;
+  static constexpr int OFF_L = OFF_M + 4 * G * 4;
+  static constexpr int OFF_O = OFF_L + 4 * G * 4;
+  static constexpr int OFF_FLAG = OFF_O + 4 * G * HD * 4;
+  static constexpr int BYTES = OFF_FLAG + 16;
+};
+
+template <typename KT, int HD, int G, int NS>
+__global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
+  using S = AttnSmem<KT, HD, G, NS>;
+  constexpr int DPL = HD / 32;
+  constexpr int CK = 32 / G;     // keys per score chunk
+  constexpr int NCH = 32 / CK;   // chunks per tile (= G)
+  constexpr int TILE = S::TILE;
+  extern __shared__ __align__(128) uint8_t smem[];
+
+  const int split = blockIdx.x, h = blockIdx.y, t = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  int ctx = (a.kv_len != nullptr ? a.kv_len[t] : a.pos_base + t) + 1;
+  if (ctx > a.cache.max_ctx) ctx = a.cache.max_ctx;
+  const int n_active = (ctx + a.split_keys - 1) / a.split_keys;
+  if (split >= n_active) return;
+  const int seq = a.seq_fixed >= 0 ? a.seq_fixed : t;
+  const int k0 = split * a.split_keys;
+  const int k1 = min(ctx, k0 + a.split_keys);
+  const int n_tiles = (k1 - k0 + TILE - 1) / TILE;
+  const int my_n = warp < n_tiles ? (n_tiles - warp + 3) / 4 : 0;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR) + warp * NS;
+  float* p_s = reinterpret_cast<float*>(smem + S::OFF_P) + warp * G * 32;
+  float* alpha_s = reinterpret_cast<float*>(smem + S::OFF_ALPHA) + warp * G;
+  float* m_s = reinterpret_cast<float*>(smem + S::OFF_M);
+  float* l_s = reinterpret_cast<float*>(smem + S::OFF_L);
+  float* o_s = reinterpret_cast<float*>(smem + S::OFF_O);
+  int* flag_s = reinterpret_cast<int*>(smem + S::OFF_FLAG);
+
+  // query group, pre-scaled into the base-2 softmax domain
+  float qr[G][DPL];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float* qp = a.q + (int64_t)t * a.q_stride + (h * G + g) * HD + lane * DPL;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) qr[g][d] = qp[d] * a.scale_log2;
+  }
+  const int gl = lane / CK;  // the head whose scores this lane holds
+  float m_run = kNegInf, l_run = 0.f;
+  float o[G][DPL];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) o[g][d] = 0.f;
+
+  if (lane == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
+    fence_proxy_async();
+  }
+  __syncwarp();
+
+  auto tile_key0 = [&](int k) { return k0 + (warp + 4 * k) * TILE; };
+  auto issue = [&](int k) {
+    const int key0 = tile_key0(k);
+    const int nv = min(TILE, k1 - key0);
+    const uint32_t bytes = (uint32_t)(nv * HD * sizeof(KT));
+    const KT* ks = cache_row<KT, HD>(const_cast<void*>(a.kc), seq, h, key0, a.cache);
+    const KT* vs = cache_row<KT, HD>(const_cast<void*>(a.vc), seq, h, key0, a.cache);
+    uint8_t* st = smem + ((warp * NS + k % NS) * S::STAGE_BYTES);
+    if (ks == nullptr || vs == nullptr) {
+      // unreachable for in-range slots; keep the barrier phase moving
+      set_status(a.status, TQ_DEV_KV_OVERFLOW);
+      mbar_arrive_expect_tx(&bars[k % NS], 0);
+      return;
+    }
+    mbar_arrive_expect_tx(&bars[k % NS], 2 * bytes);
+    bulk_g2s(st, ks, bytes, &bars[k % NS]);
+    bulk_g2s(st + S::TILE_BYTES, vs, bytes, &bars[k % NS]);
+  };
+  if (lane == 0)
+    for (int k = 0; k < NS && k < my_n; ++k) issue(k);
+
+  bool failed = false;
+  int consumed = 0;
+  for (int k = 0; k < my_n; ++k) {
+    const int stage = k % NS;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait_bounded(&bars[stage], (uint32_t)((k / NS) & 1), kWaitLimit) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) set_status(a.status, TQ_DEV_WAIT_TIMEOUT);
+      failed = true;
+      break;
+    }
+    consumed = k + 1;
+    const KT* Ks = reinterpret_cast<const KT*>(smem + (warp * NS + stage) * S::STAGE_BYTES);
+    const KT* Vs = reinterpret_cast<const KT*>(smem + (warp * NS + stage) * S::STAGE_BYTES + S::TILE_BYTES);
+    const int nv = min(TILE, k1 - tile_key0(k));
+
+    // scores of the whole query group against the tile's keys
+    float sc[NCH];
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < CK; ++j) {
+        float kv[DPL];
+        load_row<KT, DPL>(Ks + (c * CK + j) * HD + lane * DPL, kv);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float acc = 0.f;
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) acc = fmaf(qr[g][d], kv[d], acc);
+          v[g * CK + j] = acc;
+        }
+      }
+      const float s = reduce_scatter32(v, lane);
+      sc[c] = (c * CK + lane % CK) < nv ? s : kNegInf;
+    }
+    // online softmax for head gl
+    float mt = sc[0];
+#pragma unroll
+    for (int c = 1; c < NCH; ++c) mt = fmaxf(mt, sc[c]);
+#pragma unroll
+    for (int off = CK / 2; off >= 1; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+    const float m_new = fmaxf(m_run, mt);
+    const float alpha = exp2f(m_run - m_new);
+    float psum = 0.f;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      const float p = exp2f(sc[c] - m_new);
+      psum += p;
+      p_s[gl * 32 + c * CK + lane % CK] = p;
+    }
+    l_run = l_run * alpha + psum;
+    m_run = m_new;
+    if (lane % CK == 0) alpha_s[gl] = alpha;
+    __syncwarp();
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float al = alpha_s[g];
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) o[g][d] *= al;
+    }
+    for (int j = 0; j < nv; ++j) {
+      float vv[DPL];
+      load_row<KT, DPL>(Vs + j * HD + lane * DPL, vv);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float p = p_s[g * 32 + j];
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) o[g][d] = fmaf(p, vv[d], o[g][d]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && k + NS < my_n) {
+      fence_proxy_async();
+      issue(k + NS);
+    }
+  }
+  if (failed && lane == 0) {
+    // let copies already in flight land before the shared memory is released
+    for (int k = consumed; k < my_n && k < consumed + NS; ++k)
+      mbar_wait_bounded(&bars[k % NS], (uint32_t)((k / NS) & 1), kWaitLimit);
+  }
+
+  // ---- merge the four warps
+#pragma unroll
+  for (int off = CK / 2; off >= 1; off >>= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
+  if (lane % CK == 0) {
+    m_s[warp * G + gl] = m_run;
+    l_s[warp * G + gl] = l_run;
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) o_s[(warp * G + g) * HD + lane * DPL + d] = o[g][d];
+  __syncthreads();
+
+  const int64_t th = (int64_t)t * a.nkv + h;
+  float* part = a.part + (th * a.max_splits + split) * (G * (HD + 2));
+  for (int i = tid; i < G * HD; i += 128) {
+    const int g = i / HD, d = i % HD;
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, m_s[w * G + g]);
+    float acc = 0.f, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float f = exp2f(m_s[w * G + g] - M);
+      acc += f * o_s[(w * G + g) * HD + d];
+      L += f * l_s[w * G + g];
+    }
+    if (n_active == 1) {
+      a.o[(int64_t)t * a.nq * HD + (h * G + g) * HD + d] = acc / L;
+    } else {
+      part[g * (HD + 2) + d] = acc;
+      if (d == 0) {
+        part[g * (HD + 2) + HD] = M;
+        part[g * (HD + 2) + HD + 1] = L;
+      }
+    }
+  }
+  if (n_active == 1) return;
+
+  // ---- the last split to finish merges all splits
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) flag_s[0] = (atomicAdd(a.counters + th, 1u) == (unsigned)(n_active - 1)) ? 1 : 0;
+  __syncthreads();
+  if (flag_s[0] == 0) return;
+  __threadfence();
+  const float* base = a.part + th * a.max_splits * (G * (HD + 2));
+  for (int i = tid; i < G * HD; i += 128) {
+    const int g = i / HD, d = i % HD;
+    float M = kNegInf;
+    for (int s = 0; s < n_active; ++s) M = fmaxf(M, __ldcg(base + (s * G + g) * (HD + 2) + HD));
+    float acc = 0.f, L = 0.f;
+    for (int s = 0; s < n_active; ++s) {
+      const float* ps = base + (s * G + g) * (HD + 2);
+      const float f = exp2f(__ldcg(ps + HD) - M);
+      acc += f * __ldcg(ps + d);
+      L += f * __ldcg(ps + HD + 1);
+    }
+    a.o[(int64_t)t * a.nq * HD + (h * G + g) * HD + d] = acc / L;
+  }
+  if (tid == 0) a.counters[th] = 0u;
+}
+
+template <typename KT, int HD>
+cudaError_t rope_t(const RopeArgs& a, cudaStream_t s) {
+  dim3 grid((a.nq + a.nkv + 3) / 4, a.T);
+  rope_append_kernel<KT, HD><<<grid, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename KT, int HD, int G, int NS>
+cudaError_t attn_configure() {
+  using S = AttnSmem<KT, HD, G, NS>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<KT, HD, G, NS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  return cudaSuccess;
+}
+
+template <typename KT, int HD, int G, int NS>
+cudaError_t attn_t(const AttnArgs& a, cudaStream_t s) {
+  using S = AttnSmem<KT, HD, G, NS>;
+  cudaError_t e = attn_configure<KT, HD, G, NS>();
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.max_splits, a.nkv, a.T);
+  attn_decode_kernel<KT, HD, G, NS><<<grid, 128, S::BYTES, s>>>(a);
+  return cudaGetLastError();
+}
+
+// Two stages per warp when a warp has several tiles, except for f32 rows of
+// 128 dimensions (the second stage would not fit in shared memory).
+template <typename KT, int HD, int G>
+cudaError_t attn_g(const AttnArgs& a, cudaStream_t s) {
+  if (a.split_keys <= 4 * 32 || (sizeof(KT) == 4 && HD == 128)) return attn_t<KT, HD, G, 1>(a, s);
+  return attn_t<KT, HD, G, 2>(a, s);
+}
+
+template <typename KT, int HD>
+cudaError_t attn_h(int G, const AttnArgs& a, cudaStream_t s) {
+  switch (G) {
+    case 1: return attn_g<KT, HD, 1>(a, s);
+    case 2: return attn_g<KT, HD, 2>(a, s);
+    case 4: return attn_g<KT, HD, 4>(a, s);
+    case 8: return attn_g<KT, HD, 8>(a, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <typename KT, int HD, int G>
+cudaError_t prep_g() {
+  cudaError_t e = attn_configure<KT, HD, G, 1>();
+  if (e == cudaSuccess && !(sizeof(KT) == 4 && HD == 128)) e = attn_configure<KT, HD, G, 2>();
+  return e;
+}
+
+template <typename KT, int HD>
+cudaError_t prep_h(int G) {
+  switch (G) {
+    case 1: return prep_g<KT, HD, 1>();
+    case 2: return prep_g<KT, HD, 2>();
+    case 4: return prep_g<KT, HD, 4>();
+    case 8: return prep_g<KT, HD, 8>();
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t attn_prepare(int kvtype, int hd, int G) {
+  if (kvtype == TQ_KV_F16) return hd == 128 ? prep_h<__half, 128>(G) : prep_h<__half, 64>(G);
+  return hd == 128 ? prep_h<float, 128>(G) : prep_h<float, 64>(G);
+}
+
+cudaError_t launch_rope_append(int kvtype, int hd, const RopeArgs& a, cudaStream_t s) {
+  if (a.T <= 0) return cudaSuccess;
+  if (kvtype == TQ_KV_F16) return hd == 128 ? rope_t<__half, 128>(a, s) : rope_t<__half, 64>(a, s);
+  return hd == 128 ? rope_t<float, 128>(a, s) : rope_t<float, 64>(a, s);
+}
+
+cudaError_t launch_attn_decode(int kvtype, int hd, int G, const AttnArgs& a, cudaStream_t s) {
+  if (a.T <= 0) return cudaSuccess;
+  if (kvtype == TQ_KV_F16) return hd == 128 ? attn_h<__half, 128>(G, a, s) : attn_h<__half, 64>(G, a, s);
+  return hd == 128 ? attn_h<float, 128>(G, a, s) : attn_h<float, 64>(G, a, s);
+}
+
+}  // namespace tq

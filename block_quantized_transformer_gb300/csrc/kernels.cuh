@@ -1,0 +1,103 @@
+// Internal launchers of the tq kernels (not part of the C ABI).
+#pragma once
+
+#include "common.cuh"
+
+namespace tq {
+
+// ---- block formats (quant.cu)
+cudaError_t launch_quantize(int wtype, const float* w, int64_t n_blocks, void* out, cudaStream_t s);
+cudaError_t launch_repack(int wtype, const void* src, int64_t rows, int64_t nb, void* qs,
+                          uint16_t* d, cudaStream_t s);
+cudaError_t launch_dequant(int wtype, const void* qs, const uint16_t* d, int64_t nb, int64_t row0,
+                           int64_t n_rows, float* out, cudaStream_t s);
+cudaError_t launch_embed(int wtype, const void* qs, const uint16_t* d, int vocab, int hidden,
+                         const int32_t* tokens, int n_tokens, float* x, uint32_t* status,
+                         unsigned long long* argmax_keys, int n_keys, cudaStream_t s);
+
+// ---- decode GEMV (gemv.cu)
+enum GemvMode { GEMV_STORE = 0, GEMV_SWIGLU = 1, GEMV_ARGMAX = 2 };
+
+struct GemvSeg {
+  const uint8_t* qs;
+  const uint16_t* d;
+  int rows;
+};
+
+struct GemvArgs {
+  GemvSeg seg[3];        // STORE: row segments concatenated; SWIGLU: gate, up; ARGMAX: one
+  int nseg;
+  int K;                 // columns
+  int N;                 // output rows (SWIGLU: ffn)
+  int B;                 // tokens
+  const float* x;        // [B][K]
+  const float* gain;     // RMSNorm prologue gain [K], or null
+  float eps;
+  float* y;              // [B][N] (ARGMAX: logits, may be null)
+  const float* residual; // [B][N] or null (STORE only); may alias y
+  unsigned long long* argmax_keys;  // [B] (ARGMAX)
+};
+
+// Returns cudaErrorInvalidValue when K has no supported thread mapping.
+cudaError_t launch_gemv(int wtype, int mode, const GemvArgs& a, cudaStream_t s);
+bool gemv_supported(int K);
+
+// ---- attention side (attn.cu)
+struct CacheView {
+  int max_ctx;               // slots per sequence (contiguous) or tokens per sequence (paged)
+  int n_kv;
+  int page_size;             // 0: contiguous [seq][n_kv][max_ctx][hd]; else pages [page][n_kv][page_size][hd]
+  int n_pages;
+  const int32_t* block_table;  // [seq][bt_stride]
+  int bt_stride;
+};
+
+// Token t of a call belongs to sequence (seq_fixed >= 0 ? seq_fixed : t), is
+// rotated at position (pos ? pos[t] : pos_base + t) and stores / attends up to
+// cache index (kv_len ? kv_len[t] : pos_base + t).
+struct RopeArgs {
+  float* qkv;                // [T][(nq + 2 nkv) * hd]: q rotated in place
+  int T, nq, nkv;
+  const int32_t* pos;
+  const int32_t* kv_len;
+  int pos_base;
+  int seq_fixed;
+  void* kc;
+  void* vc;                  // this layer's caches
+  CacheView cache;
+  const float* cos_t;        // [max_ctx][hd/2]
+  const float* sin_t;
+  const float* gq;
+  const float* gk;
+  float eps;
+  uint32_t* status;
+};
+
+struct AttnArgs {
+  const float* q;            // q of token t, head h: q + t*q_stride + h*hd
+  int q_stride;
+  float* o;                  // [T][nq*hd]
+  int T, nq, nkv;
+  const int32_t* kv_len;
+  int pos_base;
+  int seq_fixed;
+  const void* kc;
+  const void* vc;
+  CacheView cache;
+  int split_keys;            // keys per split, a multiple of 32
+  int max_splits;            // >= ceil(max_ctx / split_keys)
+  float* part;               // [T][nkv][max_splits][G][hd + 2]
+  unsigned* counters;        // [T][nkv], zero between calls
+  float scale_log2;          // log2(e) / sqrt(hd)
+  uint32_t* status;
+};
+
+cudaError_t launch_rope_append(int kvtype, int hd, const RopeArgs& a, cudaStream_t s);
+cudaError_t launch_attn_decode(int kvtype, int hd, int G, const AttnArgs& a, cudaStream_t s);
+// one-time per-kernel attributes (dynamic shared memory); call outside stream capture
+cudaError_t attn_prepare(int kvtype, int hd, int G);
+
+// argmax keys -> int32 indices
+cudaError_t launch_argmax_finish(const unsigned long long* keys, int n, int32_t* out, cudaStream_t s);
+
+}  // namespace tq

@@ -1,0 +1,222 @@
+// Block formats on the GPU: encode f32 -> GGUF-order Q8_0/Q4_0 blocks,
+// repack GGUF-order blocks into the planar layout the GEMV streams, decode
+// planar rows to f32, and gather embedding rows.
+//
+// The formats are the workload descriptions' Q8_0 (fp16 d = max|w|/127,
+// int8 q = round(w/d), value d*q) and Q4_0 (fp16 d = m/-8 at the signed
+// extreme, q = clamp(round(w/d)+8, 0, 15), value d*(q-8)).  Encoding decisions
+// are taken in f32 exactly as the header tq.h states; decoding is exact.
+#include "kernels.cuh"
+
+namespace tq {
+
+// ----------------------------------------------------------------- encode --
+
+__device__ __forceinline__ float round_half_away(float v) {
+  float t = truncf(v);
+  if (fabsf(v - t) >= 0.5f) t += copysignf(1.0f, v);
+  return t;
+}
+
+// One warp per block of 32 weights; lane j holds weight j.
+template <int WT>
+__global__ void quantize_kernel(const float* __restrict__ w, int64_t n_blocks,
+                                uint8_t* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  int64_t blk = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t stride = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (; blk < n_blocks; blk += stride) {
+    const float x = w[blk * 32 + lane];
+    float d;
+    if (WT == TQ_Q8_0) {
+      const float amax = warp_max(fabsf(x));
+      d = amax / 127.0f;
+    } else {
+      // first element of largest magnitude: larger |x| wins, then lower index
+      unsigned long long key =
+          ((unsigned long long)__float_as_uint(fabsf(x)) << 32) | (unsigned)(31 - lane);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+        key = other > key ? other : key;
+      }
+      const int src = 31 - (int)(key & 0xffffffffull);
+      const float m = __shfl_sync(0xffffffffu, x, src);
+      d = m / -8.0f;
+    }
+    int q;
+    if (WT == TQ_Q8_0) {
+      q = d == 0.0f ? 0 : (int)round_half_away(x / d);
+      q = max(-127, min(127, q));
+    } else {
+      q = d == 0.0f ? 8 : (int)round_half_away(x / d) + 8;
+      q = max(0, min(15, q));
+    }
+    constexpr int BB = WT == TQ_Q8_0 ? 34 : 18;
+    uint8_t* o = out + blk * BB;
+    if (lane == 0) {
+      // blocks start at even offsets (34 and 18 are even): one 16-bit store
+      *reinterpret_cast<uint16_t*>(o) = __half_as_ushort(__float2half_rn(d));
+    }
+    if (WT == TQ_Q8_0) {
+      o[2 + lane] = (uint8_t)(int8_t)q;
+    } else {
+      const int hi = __shfl_down_sync(0xffffffffu, q, 16);
+      if (lane < 16) o[2 + lane] = (uint8_t)(q | (hi << 4));
+    }
+  }
+}
+
+// ----------------------------------------------------------------- repack --
+
+// One thread per block.  GGUF blocks start at even offsets (34 and 18 are
+// even), so they are read as 16-bit words.
+template <int WT>
+__global__ void repack_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t nb,
+                              uint8_t* __restrict__ qs, uint16_t* __restrict__ d) {
+  const int64_t n = rows * nb;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    constexpr int HW = WT == TQ_Q8_0 ? 17 : 9;  // 16-bit words per block
+    const uint16_t* b = src + i * HW;
+    d[i] = b[0];
+    uint32_t v[8];
+    if (WT == TQ_Q4_0) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = (uint32_t)b[1 + 2 * k] | ((uint32_t)b[2 + 2 * k] << 16);
+      reinterpret_cast<uint4*>(qs)[i] = make_uint4(v[0], v[1], v[2], v[3]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = (uint32_t)b[1 + 2 * k] | ((uint32_t)b[2 + 2 * k] << 16);
+      const int64_t r = i / nb, c = i % nb;
+      uint4* base = reinterpret_cast<uint4*>(qs);
+      base[(r * 2 + 0) * nb + c] = make_uint4(v[0], v[1], v[2], v[3]);
+      base[(r * 2 + 1) * nb + c] = make_uint4(v[4], v[5], v[6], v[7]);
+    }
+  }
+}
+
+// --------------------------------------------------------------- decoding --
+
+// Decode the 16 bytes of chunk `c` of a block into 16 (Q8_0) or 32 (Q4_0)
+// exact f32 values, scaled by d.
+template <int WT>
+__device__ __forceinline__ void decode_block(const uint8_t* qs, const uint16_t* dptr, int64_t row,
+                                             int64_t nb, int64_t c, float* out32) {
+  const float d = half_bits_to_float(dptr[row * nb + c]);
+  if (WT == TQ_Q4_0) {
+    const uint4 w = reinterpret_cast<const uint4*>(qs)[row * nb + c];
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint32_t byte = (ws[k >> 2] >> (8 * (k & 3))) & 0xffu;
+      out32[k] = d * (float)((int)(byte & 0xf) - 8);
+      out32[k + 16] = d * (float)((int)(byte >> 4) - 8);
+    }
+  } else {
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      const uint4 w = reinterpret_cast<const uint4*>(qs)[(row * 2 + p) * nb + c];
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int8_t q = (int8_t)((ws[k >> 2] >> (8 * (k & 3))) & 0xffu);
+        out32[16 * p + k] = d * (float)q;
+      }
+    }
+  }
+}
+
+template <int WT>
+__global__ void dequant_kernel(const uint8_t* __restrict__ qs, const uint16_t* __restrict__ d,
+                               int64_t nb, int64_t row0, int64_t n_rows, float* __restrict__ out) {
+  const int64_t n = n_rows * nb;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / nb, c = i % nb;
+    float v[32];
+    decode_block<WT>(qs, d, row0 + r, nb, c, v);
+    float4* o = reinterpret_cast<float4*>(out + (r * nb + c) * 32);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  }
+}
+
+// x[t][:] = decoded row tokens[t] of the embedding; ids out of range give
+// zeros and set TQ_DEV_BAD_TOKEN.  One CTA per token.
+template <int WT>
+__global__ void embed_kernel(const uint8_t* __restrict__ qs, const uint16_t* __restrict__ d,
+                             int vocab, int hidden, const int32_t* __restrict__ tokens,
+                             float* __restrict__ x, uint32_t* status,
+                             unsigned long long* argmax_keys, int n_keys) {
+  const int t = blockIdx.x;
+  const int nb = hidden / 32;
+  const int tok = tokens[t];
+  const bool ok = tok >= 0 && tok < vocab;
+  if (!ok && threadIdx.x == 0) set_status(status, TQ_DEV_BAD_TOKEN);
+  for (int c = threadIdx.x; c < nb; c += blockDim.x) {
+    float v[32];
+    if (ok) {
+      decode_block<WT>(qs, d, tok, nb, c, v);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] = 0.0f;
+    }
+    float4* o = reinterpret_cast<float4*>(x + (int64_t)t * hidden + c * 32);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  }
+  // the head's argmax keys are reset here, at the start of every step
+  if (argmax_keys != nullptr && t == 0)
+    for (int i = threadIdx.x; i < n_keys; i += blockDim.x) argmax_keys[i] = 0ull;
+}
+
+static unsigned grid_1d(int64_t n, int per_cta) {
+  int64_t g = (n + per_cta - 1) / per_cta;
+  if (g > (int64_t)kNumSMs * 64) g = (int64_t)kNumSMs * 64;
+  return (unsigned)(g < 1 ? 1 : g);
+}
+
+cudaError_t launch_quantize(int wtype, const float* w, int64_t n_blocks, void* out, cudaStream_t s) {
+  const unsigned g = grid_1d(n_blocks * 32, 256);
+  if (wtype == TQ_Q8_0)
+    quantize_kernel<TQ_Q8_0><<<g, 256, 0, s>>>(w, n_blocks, (uint8_t*)out);
+  else
+    quantize_kernel<TQ_Q4_0><<<g, 256, 0, s>>>(w, n_blocks, (uint8_t*)out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack(int wtype, const void* src, int64_t rows, int64_t nb, void* qs,
+                          uint16_t* d, cudaStream_t s) {
+  const unsigned g = grid_1d(rows * nb, 256);
+  if (wtype == TQ_Q8_0)
+    repack_kernel<TQ_Q8_0><<<g, 256, 0, s>>>((const uint16_t*)src, rows, nb, (uint8_t*)qs, d);
+  else
+    repack_kernel<TQ_Q4_0><<<g, 256, 0, s>>>((const uint16_t*)src, rows, nb, (uint8_t*)qs, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(int wtype, const void* qs, const uint16_t* d, int64_t nb, int64_t row0,
+                           int64_t n_rows, float* out, cudaStream_t s) {
+  const unsigned g = grid_1d(n_rows * nb, 256);
+  if (wtype == TQ_Q8_0)
+    dequant_kernel<TQ_Q8_0><<<g, 256, 0, s>>>((const uint8_t*)qs, d, nb, row0, n_rows, out);
+  else
+    dequant_kernel<TQ_Q4_0><<<g, 256, 0, s>>>((const uint8_t*)qs, d, nb, row0, n_rows, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_embed(int wtype, const void* qs, const uint16_t* d, int vocab, int hidden,
+                         const int32_t* tokens, int n_tokens, float* x, uint32_t* status,
+                         unsigned long long* argmax_keys, int n_keys, cudaStream_t s) {
+  const int threads = hidden / 32 < 128 ? 32 * ((hidden / 32 + 31) / 32) : 128;
+  if (wtype == TQ_Q8_0)
+    embed_kernel<TQ_Q8_0><<<n_tokens, threads, 0, s>>>((const uint8_t*)qs, d, vocab, hidden, tokens,
+                                                       x, status, argmax_keys, n_keys);
+  else
+    embed_kernel<TQ_Q4_0><<<n_tokens, threads, 0, s>>>((const uint8_t*)qs, d, vocab, hidden, tokens,
+                                                       x, status, argmax_keys, n_keys);
+  return cudaGetLastError();
+}
+
+}  // namespace tq

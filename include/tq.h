@@ -1,0 +1,233 @@
+/* tq -- decode step of a Qwen3-style decoder over Q8_0 / Q4_0 block-quantized
+ * weights, on one NVIDIA GB300 (sm_103a).  C ABI of libtq.so.
+ *
+ * What is computed is the forward pass of the pages "Всередині LLM: чисте
+ * виконання на Python для Qwen3-0.6B на MLX" (steps 2-9: embedding, RMSNorm,
+ * RoPE, grouped-query attention with a KV cache, SwiGLU, pre-norm block, LM
+ * head and greedy sampling, prefill then one token per step) and
+ * "Inferencia local y arquitecturas" (section "El formato": the qwen3.archdef
+ * layer graph, per-head QK-RMSNorm before RoPE, tied LM head
+ * output.weight | token_embd.weight, last(x) before the head; section "Elegir
+ * el motor": weights stay quantized and are multiplied in f32 with no
+ * activation quantization).  Handle, status and poisoning conventions follow
+ * the tessl_torch README, sections "Handle ownership, closing and errors" and
+ * "How the buffers cross".
+ *
+ * Conventions for every call:
+ *  - All memory is the caller's.  Pointers named *_dev are device pointers,
+ *    all others host pointers.  The library allocates no device memory; a
+ *    model keeps the pointers it was given, which must stay valid until
+ *    tq_model_free().
+ *  - Work is enqueued on the caller's CUDA stream (NULL = legacy default
+ *    stream) and the call returns without waiting for the GPU, except where
+ *    a call says it synchronizes.
+ *  - Return status: TQ_OK; TQ_REFUSED (an argument is invalid: nothing was
+ *    enqueued, the model stays usable); TQ_INTERNAL (a CUDA error: the model
+ *    is poisoned and refuses every later call with TQ_REFUSED; free it and
+ *    create a new one, keeping every buffer it was given alive until the
+ *    free).  tq_last_error() describes the last failure on the calling thread.
+ *  - Weight matrices are [out][in] row-major with blocks of 32 along `in`,
+ *    in the planar layout made by tq_repack() (tq_qmat).
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TQ_API __attribute__((visibility("default")))
+#else
+#define TQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { TQ_OK = 0, TQ_REFUSED = 1, TQ_INTERNAL = 2 } tq_status;
+
+/* Block formats (GGUF type ids).  Q8_0: 32 weights, fp16 d, int8 q; value
+ * d*q.  Q4_0: 32 weights, fp16 d, 4-bit q; value d*(q-8).  GGUF byte order of
+ * one block: Q8_0 = fp16 d, int8 q[32] (34 B); Q4_0 = fp16 d, uint8 qs[16],
+ * qs[j] = q[j] | q[j+16] << 4 (18 B). */
+typedef enum { TQ_Q4_0 = 2, TQ_Q8_0 = 8 } tq_wtype;
+typedef enum { TQ_KV_F32 = 0, TQ_KV_F16 = 1 } tq_kvtype;
+
+/* Bits of the device status word (tq_model_status()). */
+enum {
+  TQ_DEV_BAD_TOKEN = 1u,     /* a token id >= vocab: its embedding was read as zeros */
+  TQ_DEV_KV_OVERFLOW = 2u,   /* a position or cache slot >= capacity: the write was skipped */
+  TQ_DEV_WAIT_TIMEOUT = 4u   /* a bounded device-side wait gave up */
+};
+
+/* Model shape and capacity.  Sizes must satisfy: head_dim in {64, 128};
+ * n_heads % n_kv_heads == 0 with n_heads / n_kv_heads <= 8; hidden, ffn and
+ * n_heads*head_dim multiples of 256; max_batch >= 1.
+ * KV cache: page_size == 0 selects the contiguous layout
+ *   [n_layers][max_batch][n_kv_heads][max_ctx][head_dim]
+ * (sequence b of a decode batch uses slot b); page_size > 0 (a multiple of
+ * 32) selects the paged layout [n_layers][n_pages][n_kv_heads][page_size][head_dim]
+ * addressed through a block table [batch][max_ctx / page_size]. */
+typedef struct {
+  int32_t vocab, hidden, n_layers, n_heads, n_kv_heads, head_dim, ffn;
+  float rms_eps, rope_theta;
+  int32_t wtype;        /* tq_wtype */
+  int32_t kvtype;       /* tq_kvtype */
+  int32_t max_batch;    /* sequences in one decode step */
+  int32_t max_ctx;      /* tokens a sequence may hold (positions 0 .. max_ctx-1) */
+  int32_t max_prefill;  /* tokens one tq_prefill call may process */
+  int32_t page_size;    /* 0 = contiguous cache */
+  int32_t n_pages;      /* pages in the pool (paged cache only) */
+} tq_config;
+
+/* One quantized matrix [rows][cols] in the planar layout:
+ *  qs_dev: Q4_0 -> [rows][cols/32][16] bytes (a block's 16 nibble bytes);
+ *          Q8_0 -> [rows][2][cols/32][16] bytes (bytes 0-15 of every block of
+ *          the row, then bytes 16-31);
+ *  d_dev:  [rows][cols/32] fp16 scales.
+ * Both 16-byte aligned. */
+typedef struct {
+  const void* qs_dev;
+  const uint16_t* d_dev;
+} tq_qmat;
+
+typedef struct {
+  tq_qmat attn_q, attn_k, attn_v, attn_output, ffn_gate, ffn_up, ffn_down;
+  const float* attn_norm_dev;     /* [hidden] */
+  const float* ffn_norm_dev;      /* [hidden] */
+  const float* attn_q_norm_dev;   /* [head_dim] */
+  const float* attn_k_norm_dev;   /* [head_dim] */
+} tq_layer;
+
+typedef struct {
+  tq_qmat token_embd;             /* [vocab][hidden] */
+  tq_qmat output;                 /* [vocab][hidden]; qs_dev == NULL: tied to token_embd */
+  const float* output_norm_dev;   /* [hidden] */
+  const tq_layer* layers;         /* host array of n_layers, copied by tq_model_create */
+} tq_weights;
+
+typedef struct tq_model tq_model;
+
+/* ---------------------------------------------------------------- model -- */
+
+/* Device workspace bytes a model of this configuration needs (activations,
+ * attention partials, RoPE table, status word).  0 if the configuration is
+ * invalid (tq_last_error() says why). */
+TQ_API size_t tq_workspace_bytes(const tq_config* cfg);
+
+/* Bytes of one KV cache buffer (K or V) for this configuration. */
+TQ_API size_t tq_kv_cache_bytes(const tq_config* cfg);
+
+/* Create a model over caller-owned device memory: the weights, a workspace
+ * of tq_workspace_bytes() (256-byte aligned) and the K and V caches of
+ * tq_kv_cache_bytes() each.  Synchronizes the device once (it uploads the
+ * RoPE table, computed on the host in double precision, and clears the
+ * workspace).  The cache contents are not touched. */
+TQ_API tq_status tq_model_create(const tq_config* cfg, const tq_weights* weights, void* workspace_dev,
+                          void* k_cache_dev, void* v_cache_dev, tq_model** out);
+
+/* Prefill: run n_tokens tokens of one sequence at positions
+ * start_pos .. start_pos+n_tokens-1 (causal attention over the sequence's
+ * cached positions 0 .. start_pos-1 and the new ones), store their K/V, and
+ * produce the last position's logits and greedy token.
+ *  seq:             cache slot (contiguous cache), 0 <= seq < max_batch;
+ *                   ignored for a paged cache;
+ *  tokens_dev:      [n_tokens] int32 token ids;
+ *  block_table_dev: paged cache only: [max_ctx / page_size] int32 page ids of
+ *                   this sequence (NULL for a contiguous cache);
+ *  logits_dev:      [vocab] f32, or NULL;
+ *  argmax_dev:      [1] int32, the lowest index of the largest logit.
+ * Refused when n_tokens < 1, n_tokens > max_prefill or
+ * start_pos + n_tokens > max_ctx. */
+TQ_API tq_status tq_prefill(tq_model* m, int32_t seq, const int32_t* tokens_dev, int32_t n_tokens,
+                     int32_t start_pos, const int32_t* block_table_dev, float* logits_dev,
+                     int32_t* argmax_dev, void* stream);
+
+/* One decode step for `batch` sequences: sequence b feeds tokens_dev[b] at
+ * position positions_dev[b], appends its K/V at cache index kv_lens_dev[b]
+ * and attends over indices 0 .. kv_lens_dev[b] (kv_lens_dev[b] + 1 keys).
+ *  tokens_dev, positions_dev, kv_lens_dev: [batch] int32;
+ *  block_table_dev: paged cache: [batch][max_ctx / page_size] int32, else NULL;
+ *  logits_dev: [batch][vocab] f32, or NULL;
+ *  argmax_dev: [batch] int32.
+ * Refused when batch < 1 or batch > max_batch.  Device-side range errors
+ * (token >= vocab, kv_lens + 1 > max_ctx) set bits of the status word. */
+TQ_API tq_status tq_decode_step(tq_model* m, int32_t batch, const int32_t* tokens_dev,
+                         const int32_t* positions_dev, const int32_t* kv_lens_dev,
+                         const int32_t* block_table_dev, float* logits_dev, int32_t* argmax_dev,
+                         void* stream);
+
+/* Capture tq_decode_step(batch, ...) with these exact pointers into a CUDA
+ * graph owned by the model and replay it on `stream`: same results, fewer
+ * launch gaps.  The graph is rebuilt when any argument changes. */
+TQ_API tq_status tq_decode_step_graph(tq_model* m, int32_t batch, const int32_t* tokens_dev,
+                               const int32_t* positions_dev, const int32_t* kv_lens_dev,
+                               const int32_t* block_table_dev, float* logits_dev,
+                               int32_t* argmax_dev, void* stream);
+
+/* Wait for `stream`, then read and clear the device status word into
+ * *status_bits.  A non-zero word poisons the model and returns TQ_INTERNAL. */
+TQ_API tq_status tq_model_status(tq_model* m, void* stream, uint32_t* status_bits);
+
+/* 1 if the model is poisoned (a CUDA error or a device status bit was seen). */
+TQ_API int tq_model_poisoned(const tq_model* m);
+
+/* Number of kernel launches one tq_decode_step(batch) enqueues. */
+TQ_API int32_t tq_decode_launches(const tq_model* m, int32_t batch);
+
+/* Release the model object (not the caller's memory).  NULL is ignored. */
+TQ_API void tq_model_free(tq_model* m);
+
+/* Description of the last failure on the calling thread ("" if none). */
+TQ_API const char* tq_last_error(void);
+
+/* ------------------------------------------------------- weight formats -- */
+
+/* GGUF-order blocks -> planar layout (tq_qmat).
+ *  blocks_dev: [rows][cols/32] blocks of 34 (Q8_0) or 18 (Q4_0) bytes;
+ *  qs_dev, d_dev: outputs as described for tq_qmat.
+ * Refused when cols % 32 != 0 or a pointer is NULL or misaligned. */
+TQ_API tq_status tq_repack(int32_t wtype, const void* blocks_dev, int64_t rows, int64_t cols,
+                    void* qs_dev, uint16_t* d_dev, void* stream);
+
+/* Encode f32 weights [rows][cols] into GGUF-order Q8_0 / Q4_0 blocks
+ * (Q8_0: d = max|w|/127; Q4_0: d = m/-8 with m the first weight of largest
+ * magnitude, with its sign; q = round-half-away(w/d) in f32, clamped to
+ * [-127,127] or, plus 8, to [0,15]; the stored scale is fp16(d), round to
+ * nearest even; an all-zero block gets d = 0). */
+TQ_API tq_status tq_quantize(int32_t wtype, const float* w_dev, int64_t rows, int64_t cols,
+                      void* blocks_dev, void* stream);
+
+/* Decode planar rows [row0, row0+n_rows) of a matrix to f32 (exact). */
+TQ_API tq_status tq_dequantize(int32_t wtype, tq_qmat w, int64_t cols, int64_t row0, int64_t n_rows,
+                        float* out_dev, void* stream);
+
+/* ----------------------------------------------------------- single ops -- */
+
+/* y[b][r] = (residual ? residual[b][r] : 0) + sum_c W[r][c] * x[b][c], for
+ * b < batch, r < rows: the decode GEMV on its own (x, y, residual: f32,
+ * row-major with leading dimensions cols and rows; residual may alias y). */
+TQ_API tq_status tq_gemv(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const float* x_dev,
+                  int32_t batch, const float* residual_dev, float* y_dev, void* stream);
+
+/* RMSNorm + gate/up projections + SwiGLU on their own ("Всередині LLM ...
+ * Qwen3-0.6B на MLX", steps 3 and 6): out[b][i] = silu(g_i) * u_i with
+ * g = Wg h, u = Wu h, h = rms_norm(x[b], gain) (gain NULL: h = x[b]).
+ * x_dev [batch][hidden], out_dev [batch][ffn], f32. */
+TQ_API tq_status tq_swiglu_gemv(int32_t wtype, tq_qmat gate, tq_qmat up, int32_t ffn, int32_t hidden,
+                                const float* x_dev, int32_t batch, const float* gain_dev, float eps,
+                                float* out_dev, void* stream);
+
+/* Greedy head on its own ("Всередині LLM ... Qwen3-0.6B на MLX", step 8):
+ * logits[b] = W * rms_norm(x[b], gain) and argmax[b] = the lowest index of the
+ * largest logit.  logits_dev may be NULL; scratch_dev holds 8*batch bytes
+ * (8-byte aligned) of per-row argmax keys. */
+TQ_API tq_status tq_lm_head(int32_t wtype, tq_qmat w, int32_t vocab, int32_t hidden,
+                     const float* x_dev, int32_t batch, const float* gain_dev, float eps,
+                     float* logits_dev, int32_t* argmax_dev, void* scratch_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ_H */
