@@ -37,7 +37,8 @@ QS_BYTES = {TQ_Q4_0: 16, TQ_Q8_0: 32}
 EXPORTS = ("tq_workspace_bytes", "tq_kv_cache_bytes", "tq_model_create", "tq_prefill",
            "tq_decode_step", "tq_decode_step_graph", "tq_model_status", "tq_model_poisoned",
            "tq_decode_launches", "tq_model_free", "tq_last_error", "tq_repack", "tq_quantize",
-           "tq_dequantize", "tq_gemv", "tq_swiglu_gemv", "tq_lm_head")
+           "tq_dequantize", "tq_gemv", "tq_swiglu_gemv", "tq_lm_head", "tq_lm_head_static")
+LM_HEAD_STATIC_MAX_BATCH = 4096
 
 
 class TqError(RuntimeError):
@@ -111,6 +112,7 @@ def lib() -> ctypes.CDLL:
                 "tq_gemv": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, vp, vp]),
                 "tq_swiglu_gemv": (i32, [i32, TqQmat, TqQmat, i32, i32, vp, i32, vp, f32, vp, vp]),
                 "tq_lm_head": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, f32, vp, vp, vp, vp]),
+                "tq_lm_head_static": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, f32, vp, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -295,6 +297,28 @@ def tq_lm_head(m: QMat, x: torch.Tensor, gain: torch.Tensor, eps: float = 1e-6,
                           _dev(scratch, "scratch", torch.int64), _stream())
     _status(rc, "tq_lm_head")
     return logits, am
+
+
+def tq_lm_head_static(m: QMat, x: torch.Tensor, gain: torch.Tensor, eps: float = 1e-6,
+                      want_logits: bool = True, logits: Optional[torch.Tensor] = None,
+                      argmax: Optional[torch.Tensor] = None):
+    """tq_lm_head without caller scratch, for callers that cannot allocate
+    device memory: the argmax keys live in a static device array inside the
+    library (at most LM_HEAD_STATIC_MAX_BATCH rows).  Pass preallocated
+    `logits` / `argmax` to keep the call itself free of allocations.  Calls
+    that overlap on the GPU race on the shared array."""
+    x2 = x.reshape(-1, m.cols)
+    B = _int("batch", x2.shape[0], 1, LM_HEAD_STATIC_MAX_BATCH)
+    if logits is None and want_logits:
+        logits = torch.empty(B, m.rows, dtype=torch.float32, device=x.device)
+    if argmax is None:
+        argmax = torch.empty(B, dtype=torch.int32, device=x.device)
+    rc = lib().tq_lm_head_static(m.wtype, m.abi, m.rows, m.cols, _dev(x2, "x", torch.float32), B,
+                                 _dev(gain, "gain", torch.float32, m.cols), float(eps),
+                                 _dev(logits, "logits", torch.float32, B * m.rows),
+                                 _dev(argmax, "argmax", torch.int32, B), _stream())
+    _status(rc, "tq_lm_head_static")
+    return logits, argmax
 
 
 # ----------------------------------------------------------------------------- model

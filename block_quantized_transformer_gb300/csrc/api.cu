@@ -120,6 +120,10 @@ bool check_qmat(const tq_qmat& m, const char* name) {
 
 }  // namespace
 
+namespace tq {
+void record_error(const char* msg) { set_error("%s", msg); }
+}  // namespace tq
+
 struct tq_model {
   tq_config cfg;
   std::vector<tq_layer> layers;

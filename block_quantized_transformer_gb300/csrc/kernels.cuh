@@ -97,6 +97,9 @@ cudaError_t launch_attn_decode(int kvtype, int hd, int G, const AttnArgs& a, cud
 // one-time per-kernel attributes (dynamic shared memory); call outside stream capture
 cudaError_t attn_prepare(int kvtype, int hd, int G);
 
+// set the calling thread's tq_last_error() message (api.cu)
+void record_error(const char* msg);
+
 // argmax keys -> int32 indices
 cudaError_t launch_argmax_finish(const unsigned long long* keys, int n, int32_t* out, cudaStream_t s);
 

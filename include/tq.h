@@ -227,6 +227,28 @@ TQ_API tq_status tq_lm_head(int32_t wtype, tq_qmat w, int32_t vocab, int32_t hid
                      const float* x_dev, int32_t batch, const float* gain_dev, float eps,
                      float* logits_dev, int32_t* argmax_dev, void* scratch_dev, void* stream);
 
+/* ------------------------------------------------- allocation-free head -- */
+
+/* Largest batch of one tq_lm_head_static() call. */
+#define TQ_LM_HEAD_STATIC_MAX_BATCH 4096
+
+/* tq_lm_head() without the caller's scratch, for callers that cannot
+ * allocate device memory (a plugin inside a host framework that owns the
+ * device memory pool; a thread that must not risk the device-wide
+ * synchronization of cudaMalloc).  The pages have no counterpart: this is an
+ * integration entry point.  The argmax keys live in a static device array of
+ * TQ_LM_HEAD_STATIC_MAX_BATCH * 8 bytes (held by every GPU that loads the
+ * library until exit); batch above that maximum is refused (TQ_REFUSED).  The
+ * array is shared by all calls and keeps the last call's contents; each call
+ * clears the rows it uses.  Calls whose GPU work overlaps race on the array:
+ * serialize them.  The first call on a device looks the array up with that
+ * device current; make it before any stream capture.  Nothing is allocated
+ * (no cudaMalloc/cudaFree, no allocating library routine).  Other arguments
+ * and results are those of tq_lm_head(). */
+TQ_API tq_status tq_lm_head_static(int32_t wtype, tq_qmat w, int32_t vocab, int32_t hidden,
+                                   const float* x_dev, int32_t batch, const float* gain_dev,
+                                   float eps, float* logits_dev, int32_t* argmax_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
