@@ -219,7 +219,8 @@ cudaError_t run_layers(tq_model* m, int T, const int32_t* pos, const int32_t* kv
     g.eps = c.rms_eps;
     g.y = m->qkv();
     if ((e = tq::launch_gemv(c.wtype, tq::GEMV_STORE, g, s)) != cudaSuccess) return e;
-    // QK-norm + RoPE + KV append
+    // QK-norm + RoPE + KV append: its own kernel in prefill (every token's K/V
+    // must be stored before any token attends); inside attention in decode
     tq::RopeArgs r{};
     r.qkv = m->qkv();
     r.T = T;
@@ -238,7 +239,7 @@ cudaError_t run_layers(tq_model* m, int T, const int32_t* pos, const int32_t* kv
     r.gk = ly.attn_k_norm_dev;
     r.eps = c.rms_eps;
     r.status = m->status();
-    if ((e = tq::launch_rope_append(c.kvtype, hd, r, s)) != cudaSuccess) return e;
+    if (prefill && (e = tq::launch_rope_append(c.kvtype, hd, r, s)) != cudaSuccess) return e;
     // attention
     tq::AttnArgs a{};
     a.q = m->qkv();
@@ -259,6 +260,13 @@ cudaError_t run_layers(tq_model* m, int T, const int32_t* pos, const int32_t* kv
     a.counters = m->counters();
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
     a.status = m->status();
+    a.fused = prefill ? 0 : 1;
+    a.pos = pos;
+    a.cos_t = m->cos_t();
+    a.sin_t = m->sin_t();
+    a.gq = ly.attn_q_norm_dev;
+    a.gk = ly.attn_k_norm_dev;
+    a.eps = c.rms_eps;
     if ((e = tq::launch_attn_decode(c.kvtype, hd, G, a, s)) != cudaSuccess) return e;
     // output projection + residual
     tq::GemvArgs o{};
@@ -525,7 +533,7 @@ int tq_model_poisoned(const tq_model* m) { return (m != nullptr && m->poisoned) 
 int32_t tq_decode_launches(const tq_model* m, int32_t batch) {
   (void)batch;
   if (m == nullptr) return 0;
-  return 1 + 6 * m->cfg.n_layers + 2;
+  return 1 + 5 * m->cfg.n_layers + 2;
 }
 
 void tq_model_free(tq_model* m) {

@@ -20,6 +20,7 @@
 //    to finish (atomic counter, no waiting) merges all splits and resets the
 //    counter.
 #include "kernels.cuh"
+#include "launch.cuh"
 #include "ptx.cuh"
 
 namespace tq {
@@ -27,6 +28,7 @@ namespace {
 
 #define kNegInf (-__int_as_float(0x7f800000))
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr int kCluster = 16;  // CTAs per (token, KV head) in decode
 
 template <typename KT>
 __device__ __forceinline__ KT to_kv(float v);
@@ -52,6 +54,8 @@ __device__ __forceinline__ KT* cache_row(void* base, int seq, int h, int slot, c
 template <typename KT, int HD>
 __global__ void __launch_bounds__(128) rope_append_kernel(RopeArgs a) {
   constexpr int DPL = HD / 32;
+  grid_dep_launch();
+  grid_dep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hi = blockIdx.x * 4 + warp;
   const int t = blockIdx.y;
@@ -139,6 +143,29 @@ __device__ __forceinline__ void load_row<float, 2>(const float* p, float (&v)[2]
   v[0] = a.x; v[1] = a.y;
 }
 
+// RMSNorm over the head (gain g) and half-split RoPE at `pos` of one head held
+// as DPL consecutive dimensions per lane (lane l: dims l*DPL ..): the partner
+// of dimension i < hd/2 is i + hd/2, which lives in lane l ^ 16.
+template <int HD, int DPL>
+__device__ __forceinline__ void norm_rope_head(float (&x)[DPL], const float (&g)[DPL], float eps,
+                                               const float (&c)[DPL], const float (&sn)[DPL],
+                                               int lane, bool rope_ok) {
+  float ss = 0.f;
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) ss = fmaf(x[d], x[d], ss);
+  ss = warp_sum(ss);
+  const float inv = 1.0f / sqrtf(ss / (float)HD + eps);
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) x[d] = x[d] * inv * g[d];
+  if (!rope_ok) return;
+  const bool first = lane < 16;
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) {
+    const float other = __shfl_xor_sync(0xffffffffu, x[d], 16);
+    x[d] = first ? x[d] * c[d] - other * sn[d] : other * sn[d] + x[d] * c[d];
+  }
+}
+
 // reduce-scatter of 32 values over a full warp: lane l ends with sum of v[l]
 __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 #pragma unroll
@@ -158,6 +185,7 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 
 template <typename KT, int HD, int G, int NS>
 struct AttnSmem {
+  // res_*: this CTA's merged (m, l, o) read by the cluster's rank 0
   static constexpr int TILE = 32;
   static constexpr int TILE_BYTES = TILE * HD * (int)sizeof(KT);
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
@@ -168,10 +196,21 @@ struct AttnSmem {
   static constexpr int OFF_L = OFF_M + 4 * G * 4;
   static constexpr int OFF_O = OFF_L + 4 * G * 4;
   static constexpr int OFF_FLAG = OFF_O + 4 * G * HD * 4;
-  static constexpr int BYTES = OFF_FLAG + 16;
+  static constexpr int OFF_RES = OFF_FLAG + 16;
+  static constexpr int BYTES = OFF_RES + (2 * G + G * HD) * 4;
 };
 
-template <typename KT, int HD, int G, int NS>
+// FUSED (decode): q arrives straight from the Q/K/V projection; each CTA
+// applies QK-RMSNorm and RoPE to its query group itself, and the warp whose
+// tile holds the new position computes the new K (normed, rotated) and V,
+// stores them in the cache and only then stages that tile.  Older cache
+// positions are read-only in this step, so their tiles are staged before
+// waiting for the preceding kernel.
+// CL > 0: the CL CTAs of a cluster split the context of one (token, KV head)
+// evenly at run time and merge through distributed shared memory: no
+// partials in global memory, no counters, no fences.  CL == 0: fixed-size
+// splits merged by the last CTA to finish, through global memory.
+template <typename KT, int HD, int G, int NS, bool FUSED, int CL>
 __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
   using S = AttnSmem<KT, HD, G, NS>;
   constexpr int DPL = HD / 32;
@@ -180,16 +219,22 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
   constexpr int TILE = S::TILE;
   extern __shared__ __align__(128) uint8_t smem[];
 
+  grid_dep_launch();
   const int split = blockIdx.x, h = blockIdx.y, t = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-  int ctx = (a.kv_len != nullptr ? a.kv_len[t] : a.pos_base + t) + 1;
+  if (!FUSED) grid_dep_wait();
+  // kv_len is an input of the step, never written by a kernel of the step
+  const int new_slot = a.kv_len != nullptr ? a.kv_len[t] : a.pos_base + t;
+  int ctx = new_slot + 1;
   if (ctx > a.cache.max_ctx) ctx = a.cache.max_ctx;
-  const int n_active = (ctx + a.split_keys - 1) / a.split_keys;
-  if (split >= n_active) return;
+  // cluster: keys per CTA rounded up to whole tiles
+  const int span = CL > 0 ? ((ctx + CL * TILE - 1) / (CL * TILE)) * TILE : a.split_keys;
+  const int n_active = (ctx + span - 1) / span;
+  if (CL == 0 && split >= n_active) return;
   const int seq = a.seq_fixed >= 0 ? a.seq_fixed : t;
-  const int k0 = split * a.split_keys;
-  const int k1 = min(ctx, k0 + a.split_keys);
-  const int n_tiles = (k1 - k0 + TILE - 1) / TILE;
+  const int k0 = split * span;
+  const int k1 = min(ctx, k0 + span);
+  const int n_tiles = k1 > k0 ? (k1 - k0 + TILE - 1) / TILE : 0;
   const int my_n = warp < n_tiles ? (n_tiles - warp + 3) / 4 : 0;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR) + warp * NS;
@@ -200,14 +245,6 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
   float* o_s = reinterpret_cast<float*>(smem + S::OFF_O);
   int* flag_s = reinterpret_cast<int*>(smem + S::OFF_FLAG);
 
-  // query group, pre-scaled into the base-2 softmax domain
-  float qr[G][DPL];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const float* qp = a.q + (int64_t)t * a.q_stride + (h * G + g) * HD + lane * DPL;
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) qr[g][d] = qp[d] * a.scale_log2;
-  }
   const int gl = lane / CK;  // the head whose scores this lane holds
   float m_run = kNegInf, l_run = 0.f;
   float o[G][DPL];
@@ -240,8 +277,74 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
     bulk_g2s(st, ks, bytes, &bars[k % NS]);
     bulk_g2s(st + S::TILE_BYTES, vs, bytes, &bars[k % NS]);
   };
-  if (lane == 0)
+  // the warp whose last tile holds the new position (FUSED only)
+  const bool owns_new = FUSED && my_n > 0 && new_slot >= k0 && new_slot < k1 &&
+                        ((new_slot - k0) / TILE) % 4 == warp;
+  // Read-only inputs first (cache tiles of earlier positions, gains, the RoPE
+  // row of this position), all before waiting for the preceding kernel.
+  if (FUSED && lane == 0)
+    for (int k = 0; k < NS && k < my_n; ++k)
+      if (!(owns_new && k == my_n - 1)) issue(k);
+  const int pos = FUSED ? a.pos[t] : 0;
+  const bool rope_ok = pos >= 0 && pos < a.cache.max_ctx;
+  float gq[DPL], gk[DPL], cs[DPL], sn[DPL];
+  if (FUSED) {
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) {
+      const int i = (lane * DPL + d) % (HD / 2);
+      gq[d] = a.gq[lane * DPL + d];
+      gk[d] = a.gk[lane * DPL + d];
+      cs[d] = rope_ok ? a.cos_t[(int64_t)pos * (HD / 2) + i] : 1.f;
+      sn[d] = rope_ok ? a.sin_t[(int64_t)pos * (HD / 2) + i] : 0.f;
+    }
+    if (!rope_ok && tid == 0) set_status(a.status, TQ_DEV_KV_OVERFLOW);
+    grid_dep_wait();
+  }
+  if (!FUSED && lane == 0)
     for (int k = 0; k < NS && k < my_n; ++k) issue(k);
+
+  // query group (and the new K/V), loaded together, normed, rotated and
+  // pre-scaled into the base-2 softmax domain
+  const float* qrow = a.q + (int64_t)t * a.q_stride;
+  float qr[G][DPL], kx[DPL], vx[DPL];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float* qp = qrow + (h * G + g) * HD + lane * DPL;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) qr[g][d] = qp[d];
+  }
+  if (owns_new) {
+    const float* kp = qrow + (a.nq + h) * HD + lane * DPL;
+    const float* vp = qrow + (a.nq + a.nkv + h) * HD + lane * DPL;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) {
+      kx[d] = kp[d];
+      vx[d] = vp[d];
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    if (FUSED) norm_rope_head<HD, DPL>(qr[g], gq, a.eps, cs, sn, lane, rope_ok);
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) qr[g][d] *= a.scale_log2;
+  }
+  if (owns_new) {
+    norm_rope_head<HD, DPL>(kx, gk, a.eps, cs, sn, lane, rope_ok);
+    KT* kd = cache_row<KT, HD>(const_cast<void*>(a.kc), seq, h, new_slot, a.cache);
+    KT* vd = cache_row<KT, HD>(const_cast<void*>(a.vc), seq, h, new_slot, a.cache);
+    if (kd != nullptr && vd != nullptr) {
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) {
+        kd[lane * DPL + d] = to_kv<KT>(kx[d]);
+        vd[lane * DPL + d] = to_kv<KT>(vx[d]);
+      }
+    } else if (lane == 0) {
+      set_status(a.status, TQ_DEV_KV_OVERFLOW);
+    }
+    fence_proxy_async_global();  // the new row is read back by the TMA engine
+    __syncwarp();
+    if (lane == 0 && my_n - 1 < NS) issue(my_n - 1);
+  }
 
   bool failed = false;
   int consumed = 0;
@@ -340,6 +443,54 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
     for (int d = 0; d < DPL; ++d) o_s[(warp * G + g) * HD + lane * DPL + d] = o[g][d];
   __syncthreads();
 
+  if (CL > 0) {
+    // this CTA's (m, l, o) into shared memory, then rank 0 merges the cluster
+    float* res_m = reinterpret_cast<float*>(smem + S::OFF_RES);
+    float* res_l = res_m + G;
+    float* res_o = res_l + G;
+    for (int i = tid; i < G * HD; i += 128) {
+      const int g = i / HD, d = i % HD;
+      float M = kNegInf;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) M = fmaxf(M, m_s[w * G + g]);
+      float acc = 0.f, L = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float f = M == kNegInf ? 0.f : exp2f(m_s[w * G + g] - M);
+        acc += f * o_s[(w * G + g) * HD + d];
+        L += f * l_s[w * G + g];
+      }
+      res_o[i] = acc;
+      if (d == 0) {
+        res_m[g] = M;
+        res_l[g] = L;
+      }
+    }
+    cluster_sync_all();
+    if (split == 0) {
+      for (int i = tid; i < G * HD; i += 128) {
+        const int g = i / HD;
+        float mr[CL > 0 ? CL : 1];
+        float M = kNegInf;
+#pragma unroll
+        for (int r = 0; r < CL; ++r) {
+          mr[r] = ld_cluster_f32(map_cluster(res_m + g, r));
+          M = fmaxf(M, mr[r]);
+        }
+        float acc = 0.f, L = 0.f;
+#pragma unroll
+        for (int r = 0; r < CL; ++r) {
+          const float f = mr[r] == kNegInf ? 0.f : exp2f(mr[r] - M);
+          acc += f * ld_cluster_f32(map_cluster(res_o + i, r));
+          L += f * ld_cluster_f32(map_cluster(res_l + g, r));
+        }
+        a.o[(int64_t)t * a.nq * HD + (h * G) * HD + i] = acc / L;
+      }
+    }
+    cluster_sync_all();  // no CTA leaves while rank 0 still reads its shared memory
+    return;
+  }
+
   const int64_t th = (int64_t)t * a.nkv + h;
   float* part = a.part + (th * a.max_splits + split) * (G * (HD + 2));
   for (int i = tid; i < G * HD; i += 128) {
@@ -393,8 +544,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
 template <typename KT, int HD>
 cudaError_t rope_t(const RopeArgs& a, cudaStream_t s) {
   dim3 grid((a.nq + a.nkv + 3) / 4, a.T);
-  rope_append_kernel<KT, HD><<<grid, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(rope_append_kernel<KT, HD>, grid, dim3(128), 0, s, a);
 }
 
 template <typename KT, int HD, int G, int NS>
@@ -402,8 +552,14 @@ cudaError_t attn_configure() {
   using S = AttnSmem<KT, HD, G, NS>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<KT, HD, G, NS>,
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<KT, HD, G, NS, false, 0>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_decode_kernel<KT, HD, G, NS, true, kCluster>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_decode_kernel<KT, HD, G, NS, true, kCluster>,
+                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -415,16 +571,22 @@ cudaError_t attn_t(const AttnArgs& a, cudaStream_t s) {
   using S = AttnSmem<KT, HD, G, NS>;
   cudaError_t e = attn_configure<KT, HD, G, NS>();
   if (e != cudaSuccess) return e;
-  dim3 grid(a.max_splits, a.nkv, a.T);
-  attn_decode_kernel<KT, HD, G, NS><<<grid, 128, S::BYTES, s>>>(a);
-  return cudaGetLastError();
+  if (!a.fused) {
+    dim3 grid(a.max_splits, a.nkv, a.T);
+    return launch_k(attn_decode_kernel<KT, HD, G, NS, false, 0>, grid, dim3(128), S::BYTES, s, a);
+  }
+  // decode: one cluster of kCluster CTAs per (token, KV head)
+  return launch_cluster(attn_decode_kernel<KT, HD, G, NS, true, kCluster>, dim3(kCluster, a.nkv, a.T),
+                        dim3(128), S::BYTES, kCluster, s, a);
 }
 
-// Two stages per warp when a warp has several tiles, except for f32 rows of
-// 128 dimensions (the second stage would not fit in shared memory).
+// Two stages per warp when a warp may have several tiles, except for f32 rows
+// of 128 dimensions (the second stage would not fit in shared memory).
 template <typename KT, int HD, int G>
 cudaError_t attn_g(const AttnArgs& a, cudaStream_t s) {
-  if (a.split_keys <= 4 * 32 || (sizeof(KT) == 4 && HD == 128)) return attn_t<KT, HD, G, 1>(a, s);
+  const int keys_per_cta =
+      a.fused ? ((a.cache.max_ctx + kCluster * 32 - 1) / (kCluster * 32)) * 32 : a.split_keys;
+  if (keys_per_cta <= 4 * 32 || (sizeof(KT) == 4 && HD == 128)) return attn_t<KT, HD, G, 1>(a, s);
   return attn_t<KT, HD, G, 2>(a, s);
 }
 

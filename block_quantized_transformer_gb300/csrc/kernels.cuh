@@ -36,6 +36,7 @@ struct GemvArgs {
   float* y;              // [B][N] (ARGMAX: logits, may be null)
   const float* residual; // [B][N] or null (STORE only); may alias y
   unsigned long long* argmax_keys;  // [B] (ARGMAX)
+  uint32_t* status;      // device status word (bounded waits), or null
 };
 
 // Returns cudaErrorInvalidValue when K has no supported thread mapping.
@@ -90,6 +91,15 @@ struct AttnArgs {
   unsigned* counters;        // [T][nkv], zero between calls
   float scale_log2;          // log2(e) / sqrt(hd)
   uint32_t* status;
+  // fused decode: q, k, v come unnormalised from the Q/K/V projection (q points at
+  // the [T][(nq + 2 nkv) hd] buffer); QK-RMSNorm, RoPE and the KV append happen here
+  int fused;
+  const int32_t* pos;        // rope position per token
+  const float* cos_t;
+  const float* sin_t;
+  const float* gq;
+  const float* gk;
+  float eps;
 };
 
 cudaError_t launch_rope_append(int kvtype, int hd, const RopeArgs& a, cudaStream_t s);

@@ -7,6 +7,8 @@
 // extreme, q = clamp(round(w/d)+8, 0, 15), value d*(q-8)).  Encoding decisions
 // are taken in f32 exactly as the header tq.h states; decoding is exact.
 #include "kernels.cuh"
+#include "launch.cuh"
+#include "ptx.cuh"
 
 namespace tq {
 
@@ -149,6 +151,8 @@ __global__ void embed_kernel(const uint8_t* __restrict__ qs, const uint16_t* __r
                              int vocab, int hidden, const int32_t* __restrict__ tokens,
                              float* __restrict__ x, uint32_t* status,
                              unsigned long long* argmax_keys, int n_keys) {
+  grid_dep_launch();
+  grid_dep_wait();  // x and the argmax keys may still be read by the preceding kernel
   const int t = blockIdx.x;
   const int nb = hidden / 32;
   const int tok = tokens[t];
@@ -211,12 +215,10 @@ cudaError_t launch_embed(int wtype, const void* qs, const uint16_t* d, int vocab
                          unsigned long long* argmax_keys, int n_keys, cudaStream_t s) {
   const int threads = hidden / 32 < 128 ? 32 * ((hidden / 32 + 31) / 32) : 128;
   if (wtype == TQ_Q8_0)
-    embed_kernel<TQ_Q8_0><<<n_tokens, threads, 0, s>>>((const uint8_t*)qs, d, vocab, hidden, tokens,
-                                                       x, status, argmax_keys, n_keys);
-  else
-    embed_kernel<TQ_Q4_0><<<n_tokens, threads, 0, s>>>((const uint8_t*)qs, d, vocab, hidden, tokens,
-                                                       x, status, argmax_keys, n_keys);
-  return cudaGetLastError();
+    return launch_k(embed_kernel<TQ_Q8_0>, dim3(n_tokens), dim3(threads), 0, s, (const uint8_t*)qs, d,
+                    vocab, hidden, tokens, x, status, argmax_keys, n_keys);
+  return launch_k(embed_kernel<TQ_Q4_0>, dim3(n_tokens), dim3(threads), 0, s, (const uint8_t*)qs, d,
+                  vocab, hidden, tokens, x, status, argmax_keys, n_keys);
 }
 
 }  // namespace tq
