@@ -44,6 +44,8 @@ def parse():
                     help="profiling case: run only the fused RMSNorm + gate/up + SwiGLU GEMV over "
                          "the 36 layers' FFN weights of the 8B model (2 GB, larger than L2)")
     ap.add_argument("--reps", type=int, default=2)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling cases only: keep the first N layers of the workload")
     ap.add_argument("--workload", default="qwen3_8b_q4_0",
                     help="decode workload to time (the 8B batch-1 one by default; others for "
                          "profiling small cases)")
@@ -229,6 +231,9 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = {x.name: x for x in synth.WORKLOADS}[args.workload]
+    if args.layers:
+        import dataclasses
+        w = dataclasses.replace(w, n_layers=args.layers)
     K, W = args.steps, args.warmup
     prompt_len = w.prompt_len
     max_ctx = prompt_len + W + K + 8

@@ -350,9 +350,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
   int consumed = 0;
   for (int k = 0; k < my_n; ++k) {
     const int stage = k % NS;
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait_bounded(&bars[stage], (uint32_t)((k / NS) & 1), kWaitLimit) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
+    // every lane waits: the warp sleeps in the barrier instead of one lane spinning
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[stage], (uint32_t)((k / NS) & 1), kWaitLimit));
     if (!ok) {
       if (lane == 0) set_status(a.status, TQ_DEV_WAIT_TIMEOUT);
       failed = true;
@@ -467,27 +466,27 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
       }
     }
     cluster_sync_all();
-    if (split == 0) {
-      for (int i = tid; i < G * HD; i += 128) {
-        const int g = i / HD;
-        float mr[CL > 0 ? CL : 1];
-        float M = kNegInf;
+    // every rank merges its 1/CL share of the G*HD outputs of the cluster
+    constexpr int SHARE = (G * HD + CL - 1) / (CL > 0 ? CL : 1);
+    for (int i = split * SHARE + tid; i < (split + 1) * SHARE && i < G * HD; i += 128) {
+      const int g = i / HD;
+      float mr[CL > 0 ? CL : 1];
+      float M = kNegInf;
 #pragma unroll
-        for (int r = 0; r < CL; ++r) {
-          mr[r] = ld_cluster_f32(map_cluster(res_m + g, r));
-          M = fmaxf(M, mr[r]);
-        }
-        float acc = 0.f, L = 0.f;
-#pragma unroll
-        for (int r = 0; r < CL; ++r) {
-          const float f = mr[r] == kNegInf ? 0.f : exp2f(mr[r] - M);
-          acc += f * ld_cluster_f32(map_cluster(res_o + i, r));
-          L += f * ld_cluster_f32(map_cluster(res_l + g, r));
-        }
-        a.o[(int64_t)t * a.nq * HD + (h * G) * HD + i] = acc / L;
+      for (int r = 0; r < CL; ++r) {
+        mr[r] = ld_cluster_f32(map_cluster(res_m + g, r));
+        M = fmaxf(M, mr[r]);
       }
+      float acc = 0.f, L = 0.f;
+#pragma unroll
+      for (int r = 0; r < CL; ++r) {
+        const float f = mr[r] == kNegInf ? 0.f : exp2f(mr[r] - M);
+        acc += f * ld_cluster_f32(map_cluster(res_o + i, r));
+        L += f * ld_cluster_f32(map_cluster(res_l + g, r));
+      }
+      a.o[(int64_t)t * a.nq * HD + (h * G) * HD + i] = acc / L;
     }
-    cluster_sync_all();  // no CTA leaves while rank 0 still reads its shared memory
+    cluster_sync_all();  // no CTA leaves while another rank still reads its shared memory
     return;
   }
 
