@@ -36,7 +36,7 @@ QS_BYTES = {TQ_Q4_0: 16, TQ_Q8_0: 32}
 
 EXPORTS = ("tq_workspace_bytes", "tq_kv_cache_bytes", "tq_model_create", "tq_prefill",
            "tq_decode_step", "tq_decode_step_graph", "tq_model_status", "tq_model_poisoned",
-           "tq_decode_launches", "tq_model_free", "tq_last_error", "tq_repack", "tq_quantize",
+           "tq_decode_launches", "tq_model_free", "tq_last_error", "tq_qmat_bytes", "tq_repack", "tq_quantize",
            "tq_dequantize", "tq_gemv", "tq_swiglu_gemv", "tq_lm_head", "tq_lm_head_static")
 LM_HEAD_STATIC_MAX_BATCH = 4096
 
@@ -106,6 +106,8 @@ def lib() -> ctypes.CDLL:
                 "tq_decode_launches": (i32, [vp, i32]),
                 "tq_model_free": (None, [vp]),
                 "tq_last_error": (ctypes.c_char_p, []),
+                "tq_qmat_bytes": (i32, [i32, i64, i64, ctypes.POINTER(ctypes.c_int64),
+                                        ctypes.POINTER(ctypes.c_int64)]),
                 "tq_repack": (i32, [i32, vp, i64, i64, vp, vp, vp]),
                 "tq_quantize": (i32, [i32, vp, i64, i64, vp, vp]),
                 "tq_dequantize": (i32, [i32, TqQmat, i64, i64, i64, vp, vp]),
@@ -182,14 +184,25 @@ def tq_last_error() -> str:
     return lib().tq_last_error().decode(errors="replace")
 
 
+def tq_qmat_bytes(wtype: int, rows: int, cols: int) -> tuple:
+    """(qs bytes, d bytes) of a [rows][cols] matrix in the tiled layout."""
+    _int("rows", rows, 0, I64[1])
+    _int("cols", cols, 0, I64[1])
+    q, d = ctypes.c_int64(0), ctypes.c_int64(0)
+    _status(lib().tq_qmat_bytes(wtype, rows, cols, ctypes.byref(q), ctypes.byref(d)), "tq_qmat_bytes")
+    return q.value, d.value
+
+
 def tq_repack(wtype: int, blocks: torch.Tensor, rows: int, cols: int, qs: torch.Tensor,
               d: torch.Tensor) -> None:
+    """GGUF-order blocks -> tiled layout; qs/d hold the rows padded to a multiple of 16."""
     _int("rows", rows, 0, I64[1])
     _int("cols", cols, 0, I64[1])
     nb = cols // 32
+    qb, db = tq_qmat_bytes(wtype, rows, cols)
     rc = lib().tq_repack(wtype, _dev(blocks, "blocks", torch.uint8, rows * nb * BLOCK_BYTES[wtype]),
-                         rows, cols, _dev(qs, "qs", torch.uint8, rows * nb * QS_BYTES[wtype]),
-                         _dev(d, "d", torch.int16, rows * nb), _stream())
+                         rows, cols, _dev(qs, "qs", torch.uint8, qb),
+                         _dev(d, "d", torch.int16, db // 2), _stream())
     _status(rc, "tq_repack")
 
 
@@ -205,7 +218,7 @@ def tq_quantize(wtype: int, w: torch.Tensor, rows: int, cols: int, blocks: torch
 # ----------------------------------------------------------------------------- matrices
 
 class QMat:
-    """One planar quantized matrix [rows][cols] in device memory (torch-owned)."""
+    """One quantized matrix [rows][cols] in the tiled layout, in device memory (torch-owned)."""
 
     def __init__(self, wtype: int, rows: int, cols: int, qs: torch.Tensor, d: torch.Tensor):
         self.wtype, self.rows, self.cols, self.qs, self.d = wtype, rows, cols, qs, d
@@ -220,14 +233,14 @@ class QMat:
 
     @classmethod
     def empty(cls, wtype: int, rows: int, cols: int, device) -> "QMat":
-        nb = cols // 32
-        qs = torch.empty(rows * nb * QS_BYTES[wtype], dtype=torch.uint8, device=device)
-        d = torch.empty(rows * nb, dtype=torch.int16, device=device)
+        qb, db = tq_qmat_bytes(wtype, rows, cols)
+        qs = torch.empty(qb, dtype=torch.uint8, device=device)
+        d = torch.empty(db // 2, dtype=torch.int16, device=device)
         return cls(wtype, rows, cols, qs, d)
 
     @classmethod
     def from_blocks(cls, wtype: int, blocks: torch.Tensor, rows: int, cols: int) -> "QMat":
-        """GGUF-order block bytes (device uint8, [rows][cols/32][34|18]) -> planar."""
+        """GGUF-order block bytes (device uint8, [rows][cols/32][34|18]) -> tiled layout."""
         m = cls.empty(wtype, rows, cols, blocks.device)
         tq_repack(wtype, blocks, rows, cols, m.qs, m.d)
         return m
@@ -328,7 +341,7 @@ LAYER_GAINS = ("attn_norm", "ffn_norm", "attn_q_norm", "attn_k_norm")
 
 
 class Model:
-    """A decoder over planar quantized weights, a torch-allocated workspace and
+    """A decoder over tiled quantized weights, a torch-allocated workspace and
     KV cache.  ``mats`` maps GGUF-style names (``token_embd``,
     ``blk.{i}.attn_q`` ...; optionally ``output``) to QMat; ``gains`` maps
     ``blk.{i}.attn_norm`` ... and ``output_norm`` to f32 device tensors."""

@@ -30,7 +30,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Layout {
-  size_t x, qkv, att, act, cos_t, sin_t, part, counters, keys, status, total;
+  size_t x, qkv, att, act, cos_t, sin_t, part, counters, keys, status, chain_sync, total;
   int T;                 // rows of activation buffers
   int split_dec, splits_dec, split_pf, splits_pf;
 };
@@ -99,6 +99,7 @@ Layout layout_of(const tq_config& c) {
   L.counters = take((size_t)L.T * c.n_kv_heads * 4);
   L.keys = take((size_t)L.T * 8);
   L.status = take(16);
+  L.chain_sync = take((tq::kMaxPhases + 1) * 4);
   L.total = off;
   return L;
 }
@@ -154,6 +155,7 @@ struct tq_model {
   unsigned* counters() const { return reinterpret_cast<unsigned*>(ws + L.counters); }
   unsigned long long* keys() const { return reinterpret_cast<unsigned long long*>(ws + L.keys); }
   uint32_t* status() const { return reinterpret_cast<uint32_t*>(ws + L.status); }
+  unsigned* chain_sync() const { return reinterpret_cast<unsigned*>(ws + L.chain_sync); }
   void* kc_layer(int l) const { return static_cast<uint8_t*>(kc) + (size_t)l * layer_kv_bytes; }
   void* vc_layer(int l) const { return static_cast<uint8_t*>(vc) + (size_t)l * layer_kv_bytes; }
 };
@@ -198,27 +200,111 @@ tq::CacheView cache_view(const tq_model* m, const int32_t* block_table) {
 
 // The layer loop shared by decode (T = batch, one token per sequence) and
 // prefill (T tokens of sequence `seq` at positions pos_base..).
+// GEMV arguments of the projections of layer l over T token rows.
+tq::GemvArgs qkv_args(const tq_model* m, int l, int T) {
+  const tq_config& c = m->cfg;
+  const tq_layer& ly = m->layers[l];
+  tq::GemvArgs g{};  // RMSNorm + Q/K/V projections
+  g.seg[0] = seg_of(ly.attn_q, c.n_heads * c.head_dim);
+  g.seg[1] = seg_of(ly.attn_k, c.n_kv_heads * c.head_dim);
+  g.seg[2] = seg_of(ly.attn_v, c.n_kv_heads * c.head_dim);
+  g.nseg = 3;
+  g.K = c.hidden;
+  g.N = qkv_width(c);
+  g.B = T;
+  g.x = m->x();
+  g.gain = ly.attn_norm_dev;
+  g.eps = c.rms_eps;
+  g.y = m->qkv();
+  g.status = m->status();
+  return g;
+}
+
+tq::GemvArgs out_args(const tq_model* m, int l, int T) {
+  const tq_config& c = m->cfg;
+  tq::GemvArgs o{};  // output projection + residual
+  o.seg[0] = seg_of(m->layers[l].attn_output, c.hidden);
+  o.nseg = 1;
+  o.K = c.n_heads * c.head_dim;
+  o.N = c.hidden;
+  o.B = T;
+  o.x = m->att();
+  o.y = m->x();
+  o.residual = m->x();
+  o.status = m->status();
+  return o;
+}
+
+tq::GemvArgs ffn_args(const tq_model* m, int l, int T) {
+  const tq_config& c = m->cfg;
+  const tq_layer& ly = m->layers[l];
+  tq::GemvArgs f{};  // RMSNorm + gate/up + SwiGLU
+  f.seg[0] = seg_of(ly.ffn_gate, c.ffn);
+  f.seg[1] = seg_of(ly.ffn_up, c.ffn);
+  f.nseg = 2;
+  f.K = c.hidden;
+  f.N = c.ffn;
+  f.B = T;
+  f.x = m->x();
+  f.gain = ly.ffn_norm_dev;
+  f.eps = c.rms_eps;
+  f.y = m->act();
+  f.status = m->status();
+  return f;
+}
+
+tq::GemvArgs down_args(const tq_model* m, int l, int T) {
+  const tq_config& c = m->cfg;
+  tq::GemvArgs d{};  // down projection + residual
+  d.seg[0] = seg_of(m->layers[l].ffn_down, c.hidden);
+  d.nseg = 1;
+  d.K = c.ffn;
+  d.N = c.hidden;
+  d.B = T;
+  d.x = m->act();
+  d.y = m->x();
+  d.residual = m->x();
+  d.status = m->status();
+  return d;
+}
+
+tq::GemvArgs head_args(const tq_model* m, const float* x, int B, float* logits) {
+  const tq_config& c = m->cfg;
+  tq::GemvArgs h{};  // final RMSNorm + tied LM head + argmax
+  h.seg[0] = seg_of(m->head, c.vocab);
+  h.nseg = 1;
+  h.K = c.hidden;
+  h.N = c.vocab;
+  h.B = B;
+  h.x = x;
+  h.gain = m->out_norm;
+  h.eps = c.rms_eps;
+  h.y = logits;
+  h.argmax_keys = m->keys();
+  h.status = m->status();
+  return h;
+}
+
+// The layers and the head.  The GEMVs between two attention launches run as
+// one persistent chain: output projection, gate/up, down projection of layer
+// l and the Q/K/V projection of layer l+1 (the LM head after the last layer),
+// so the weight stream does not drain between them.  `head_x`/`head_B`: the
+// rows the head reads (all decode rows; the last prompt token in prefill).
 cudaError_t run_layers(tq_model* m, int T, const int32_t* pos, const int32_t* kv_len, int pos_base,
-                       int seq_fixed, const int32_t* block_table, bool prefill, cudaStream_t s) {
+                       int seq_fixed, const int32_t* block_table, bool prefill, const float* head_x,
+                       int head_B, float* logits, int32_t* argmax, cudaStream_t s) {
   const tq_config& c = m->cfg;
   const int hd = c.head_dim, nq = c.n_heads, nkv = c.n_kv_heads, G = nq / nkv;
   cudaError_t e;
+  {
+    tq::GemvChain ch{};
+    ch.ph[0] = qkv_args(m, 0, T);
+    ch.mode[0] = tq::GEMV_STORE;
+    ch.n = 1;
+    if ((e = tq::launch_gemv_chain(c.wtype, ch, s)) != cudaSuccess) return e;
+  }
   for (int l = 0; l < c.n_layers; ++l) {
     const tq_layer& ly = m->layers[l];
-    // RMSNorm + Q/K/V projections
-    tq::GemvArgs g{};
-    g.seg[0] = seg_of(ly.attn_q, nq * hd);
-    g.seg[1] = seg_of(ly.attn_k, nkv * hd);
-    g.seg[2] = seg_of(ly.attn_v, nkv * hd);
-    g.nseg = 3;
-    g.K = c.hidden;
-    g.N = (nq + 2 * nkv) * hd;
-    g.B = T;
-    g.x = m->x();
-    g.gain = ly.attn_norm_dev;
-    g.eps = c.rms_eps;
-    g.y = m->qkv();
-    if ((e = tq::launch_gemv(c.wtype, tq::GEMV_STORE, g, s)) != cudaSuccess) return e;
     // QK-norm + RoPE + KV append: its own kernel in prefill (every token's K/V
     // must be stored before any token attends); inside attention in decode
     tq::RopeArgs r{};
@@ -268,61 +354,26 @@ cudaError_t run_layers(tq_model* m, int T, const int32_t* pos, const int32_t* kv
     a.gk = ly.attn_k_norm_dev;
     a.eps = c.rms_eps;
     if ((e = tq::launch_attn_decode(c.kvtype, hd, G, a, s)) != cudaSuccess) return e;
-    // output projection + residual
-    tq::GemvArgs o{};
-    o.seg[0] = seg_of(ly.attn_output, c.hidden);
-    o.nseg = 1;
-    o.K = nq * hd;
-    o.N = c.hidden;
-    o.B = T;
-    o.x = m->att();
-    o.y = m->x();
-    o.residual = m->x();
-    if ((e = tq::launch_gemv(c.wtype, tq::GEMV_STORE, o, s)) != cudaSuccess) return e;
-    // RMSNorm + gate/up + SwiGLU
-    tq::GemvArgs f{};
-    f.seg[0] = seg_of(ly.ffn_gate, c.ffn);
-    f.seg[1] = seg_of(ly.ffn_up, c.ffn);
-    f.nseg = 2;
-    f.K = c.hidden;
-    f.N = c.ffn;
-    f.B = T;
-    f.x = m->x();
-    f.gain = ly.ffn_norm_dev;
-    f.eps = c.rms_eps;
-    f.y = m->act();
-    if ((e = tq::launch_gemv(c.wtype, tq::GEMV_SWIGLU, f, s)) != cudaSuccess) return e;
-    // down projection + residual
-    tq::GemvArgs d{};
-    d.seg[0] = seg_of(ly.ffn_down, c.hidden);
-    d.nseg = 1;
-    d.K = c.ffn;
-    d.N = c.hidden;
-    d.B = T;
-    d.x = m->act();
-    d.y = m->x();
-    d.residual = m->x();
-    if ((e = tq::launch_gemv(c.wtype, tq::GEMV_STORE, d, s)) != cudaSuccess) return e;
+    // output projection, FFN, and the next layer's Q/K/V (or the head)
+    tq::GemvChain ch{};
+    ch.ph[0] = out_args(m, l, T);
+    ch.mode[0] = tq::GEMV_STORE;
+    ch.ph[1] = ffn_args(m, l, T);
+    ch.mode[1] = tq::GEMV_SWIGLU;
+    ch.ph[2] = down_args(m, l, T);
+    ch.mode[2] = tq::GEMV_STORE;
+    if (l + 1 < c.n_layers) {
+      ch.ph[3] = qkv_args(m, l + 1, T);
+      ch.mode[3] = tq::GEMV_STORE;
+    } else {
+      ch.ph[3] = head_args(m, head_x, head_B, logits);
+      ch.mode[3] = tq::GEMV_ARGMAX;
+    }
+    ch.n = 4;
+    ch.sync = m->chain_sync();
+    if ((e = tq::launch_gemv_chain(c.wtype, ch, s)) != cudaSuccess) return e;
   }
-  return cudaSuccess;
-}
-
-cudaError_t run_head(tq_model* m, const float* x, int B, float* logits, int32_t* argmax, cudaStream_t s) {
-  const tq_config& c = m->cfg;
-  tq::GemvArgs h{};
-  h.seg[0] = seg_of(m->head, c.vocab);
-  h.nseg = 1;
-  h.K = c.hidden;
-  h.N = c.vocab;
-  h.B = B;
-  h.x = x;
-  h.gain = m->out_norm;
-  h.eps = c.rms_eps;
-  h.y = logits;
-  h.argmax_keys = m->keys();
-  cudaError_t e = tq::launch_gemv(c.wtype, tq::GEMV_ARGMAX, h, s);
-  if (e != cudaSuccess) return e;
-  return tq::launch_argmax_finish(m->keys(), B, argmax, s);
+  return tq::launch_argmax_finish(m->keys(), head_B, argmax, s);
 }
 
 cudaError_t enqueue_decode(tq_model* m, int batch, const int32_t* tokens, const int32_t* positions,
@@ -332,9 +383,8 @@ cudaError_t enqueue_decode(tq_model* m, int batch, const int32_t* tokens, const 
   cudaError_t e = tq::launch_embed(c.wtype, m->embd.qs_dev, m->embd.d_dev, c.vocab, c.hidden, tokens,
                                    batch, m->x(), m->status(), m->keys(), batch, s);
   if (e != cudaSuccess) return e;
-  if ((e = run_layers(m, batch, positions, kv_lens, 0, -1, block_table, false, s)) != cudaSuccess)
-    return e;
-  return run_head(m, m->x(), batch, logits, argmax, s);
+  return run_layers(m, batch, positions, kv_lens, 0, -1, block_table, false, m->x(), batch, logits,
+                    argmax, s);
 }
 
 }  // namespace
@@ -439,8 +489,9 @@ tq_status tq_prefill(tq_model* m, int32_t seq, const int32_t* tokens, int32_t n_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = tq::launch_embed(c.wtype, m->embd.qs_dev, m->embd.d_dev, c.vocab, c.hidden, tokens,
                                    n_tokens, m->x(), m->status(), m->keys(), 1, s);
-  if (e == cudaSuccess) e = run_layers(m, n_tokens, nullptr, nullptr, start_pos, seq, block_table, true, s);
-  if (e == cudaSuccess) e = run_head(m, m->x() + (size_t)(n_tokens - 1) * c.hidden, 1, logits, argmax, s);
+  if (e == cudaSuccess)
+    e = run_layers(m, n_tokens, nullptr, nullptr, start_pos, seq, block_table, true,
+                   m->x() + (size_t)(n_tokens - 1) * c.hidden, 1, logits, argmax, s);
   if (e != cudaSuccess) return fail_cuda(m, e, "tq_prefill");
   return TQ_OK;
 }
@@ -533,7 +584,7 @@ int tq_model_poisoned(const tq_model* m) { return (m != nullptr && m->poisoned) 
 int32_t tq_decode_launches(const tq_model* m, int32_t batch) {
   (void)batch;
   if (m == nullptr) return 0;
-  return 1 + 5 * m->cfg.n_layers + 2;
+  return 3 + 2 * m->cfg.n_layers;  // embed, Q/K/V of layer 0, (attention, chain) per layer, argmax
 }
 
 void tq_model_free(tq_model* m) {
@@ -544,14 +595,23 @@ void tq_model_free(tq_model* m) {
 
 // ------------------------------------------------------------- formats --
 
+tq_status tq_qmat_bytes(int32_t wtype, int64_t rows, int64_t cols, int64_t* qs_bytes, int64_t* d_bytes) {
+  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (rows < 0 || cols < 0 || cols % 256 != 0) return set_error("cols must be a multiple of 256"), TQ_REFUSED;
+  const int64_t blocks = tq::tiled_rows(rows) * (cols / 32);
+  if (qs_bytes != nullptr) *qs_bytes = blocks * (wtype == TQ_Q4_0 ? 16 : 32);
+  if (d_bytes != nullptr) *d_bytes = blocks * 2;
+  return TQ_OK;
+}
+
 tq_status tq_repack(int32_t wtype, const void* blocks, int64_t rows, int64_t cols, void* qs,
                     uint16_t* d, void* stream) {
   if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
-  if (rows < 0 || cols < 0 || cols % 32 != 0) return set_error("cols must be a multiple of 32"), TQ_REFUSED;
+  if (rows < 0 || cols < 0 || cols % 256 != 0) return set_error("cols must be a multiple of 256"), TQ_REFUSED;
   if (rows * cols == 0) return TQ_OK;
   if (!blocks || !qs || !d) return set_error("pointers must not be NULL"), TQ_REFUSED;
-  if ((reinterpret_cast<uintptr_t>(blocks) & 1u) || !aligned16(qs) || (reinterpret_cast<uintptr_t>(d) & 1u))
-    return set_error("blocks must be 2-byte, qs 16-byte and d 2-byte aligned"), TQ_REFUSED;
+  if ((reinterpret_cast<uintptr_t>(blocks) & 1u) || !aligned16(qs) || !aligned16(d))
+    return set_error("blocks must be 2-byte, qs and d 16-byte aligned"), TQ_REFUSED;
   cudaError_t e = tq::launch_repack(wtype, blocks, rows, cols / 32, qs, d, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(nullptr, e, "tq_repack");
   return TQ_OK;
@@ -570,8 +630,8 @@ tq_status tq_quantize(int32_t wtype, const float* w, int64_t rows, int64_t cols,
 tq_status tq_dequantize(int32_t wtype, tq_qmat w, int64_t cols, int64_t row0, int64_t n_rows,
                         float* out, void* stream) {
   if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
-  if (cols <= 0 || cols % 32 != 0 || row0 < 0 || n_rows < 0)
-    return set_error("cols must be a positive multiple of 32; rows non-negative"), TQ_REFUSED;
+  if (cols <= 0 || cols % 256 != 0 || row0 < 0 || n_rows < 0)
+    return set_error("cols must be a positive multiple of 256; rows non-negative"), TQ_REFUSED;
   if (n_rows == 0) return TQ_OK;
   if (!w.qs_dev || !w.d_dev || !out) return set_error("pointers must not be NULL"), TQ_REFUSED;
   if (!aligned16(w.qs_dev) || !aligned16(out)) return set_error("qs and out must be 16-byte aligned"), TQ_REFUSED;
@@ -589,7 +649,8 @@ tq_status tq_gemv(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const fl
   if (rows < 1 || batch < 1 || !tq::gemv_supported(cols))
     return set_error("rows and batch must be >= 1 and cols have a GEMV mapping (got %d)", cols), TQ_REFUSED;
   if (!w.qs_dev || !w.d_dev || !x || !y) return set_error("pointers must not be NULL"), TQ_REFUSED;
-  if (!aligned16(w.qs_dev) || !aligned16(x)) return set_error("qs and x must be 16-byte aligned"), TQ_REFUSED;
+  if (!aligned16(w.qs_dev) || !aligned16(w.d_dev) || !aligned16(x))
+    return set_error("qs, d and x must be 16-byte aligned"), TQ_REFUSED;
   tq::GemvArgs g{};
   g.seg[0] = seg_of(w, rows);
   g.nseg = 1;
@@ -612,8 +673,9 @@ tq_status tq_swiglu_gemv(int32_t wtype, tq_qmat gate, tq_qmat up, int32_t ffn, i
     return set_error("ffn and batch must be >= 1 and hidden have a GEMV mapping"), TQ_REFUSED;
   if (!gate.qs_dev || !gate.d_dev || !up.qs_dev || !up.d_dev || !x || !out)
     return set_error("pointers must not be NULL"), TQ_REFUSED;
-  if (!aligned16(gate.qs_dev) || !aligned16(up.qs_dev) || !aligned16(x) || (gain && !aligned16(gain)))
-    return set_error("qs, x and gain must be 16-byte aligned"), TQ_REFUSED;
+  if (!aligned16(gate.qs_dev) || !aligned16(up.qs_dev) || !aligned16(gate.d_dev) || !aligned16(up.d_dev) ||
+      !aligned16(x) || (gain && !aligned16(gain)))
+    return set_error("qs, d, x and gain must be 16-byte aligned"), TQ_REFUSED;
   tq::GemvArgs f{};
   f.seg[0] = seg_of(gate, ffn);
   f.seg[1] = seg_of(up, ffn);
@@ -639,6 +701,8 @@ tq_status tq_lm_head(int32_t wtype, tq_qmat w, int32_t vocab, int32_t hidden, co
   if (!w.qs_dev || !w.d_dev || !x || !gain || !argmax || !scratch)
     return set_error("pointers must not be NULL"), TQ_REFUSED;
   if ((reinterpret_cast<uintptr_t>(scratch) & 7u) != 0) return set_error("scratch must be 8-byte aligned"), TQ_REFUSED;
+  if (!aligned16(w.qs_dev) || !aligned16(w.d_dev) || !aligned16(x) || !aligned16(gain))
+    return set_error("qs, d, x and gain must be 16-byte aligned"), TQ_REFUSED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned long long* keys = static_cast<unsigned long long*>(scratch);
   cudaError_t e = cudaMemsetAsync(keys, 0, batch * sizeof(unsigned long long), s);

@@ -5,6 +5,39 @@
 
 namespace tq {
 
+// ---- tiled weight layout (tq_repack, the GEMV, decoding)
+//
+// Rows are grouped in tiles of 16 (a matrix's rows padded to a multiple of 16
+// with zero rows) and the blocks of a tile row in units of 8 blocks (256
+// inputs).  qs holds units [tile][unit] of 2048 (Q4_0) or 4096 (Q8_0) bytes,
+// d holds units [tile][unit] of 128 fp16 scales; so a tile row is
+// contiguous and a run of units is one contiguous copy.  Inside a unit, row
+// rr = 8 h + g of the tile and word i (4 bytes; Q4_0 words 0-3, Q8_0 words
+// 0-7) of block j (0-7) sit where one 16-byte load per lane of a warp hands
+// lane 4 g + c the words its mma.m16n8k16 A fragment needs (c = i mod 4):
+//   Q4_0: ((h*2 + j/4)*32 + 4g + i)*16 + (j%4)*4
+//   Q8_0: ((h*4 + j/2)*32 + 4g + i%4)*16 + (j%2)*8 + (i/4)*4
+// and the scale of (rr, j) is element (h*8 + g)*8 + j of the unit's scales.
+constexpr int kTileRows = 16;
+constexpr int kUnitBlocks = 8;
+constexpr int kUnitD = 256;  // bytes of scales per unit
+
+__host__ __device__ constexpr int unit_qs_bytes(int wt) { return wt == TQ_Q4_0 ? 2048 : 4096; }
+
+__host__ __device__ inline int64_t tiled_rows(int64_t rows) { return (rows + 15) / 16 * 16; }
+
+__host__ __device__ inline int64_t tiled_qs_offset(int wt, int64_t r, int64_t blk, int64_t nb, int i) {
+  const int64_t unit = (r >> 4) * (nb / kUnitBlocks) + (blk >> 3);
+  const int h = (int)((r >> 3) & 1), g = (int)(r & 7), j = (int)(blk & 7);
+  if (wt == TQ_Q4_0) return unit * 2048 + (int64_t)(((h * 2 + (j >> 2)) * 32 + g * 4 + i) * 16 + (j & 3) * 4);
+  return unit * 4096 + (int64_t)(((h * 4 + (j >> 1)) * 32 + g * 4 + (i & 3)) * 16 + (j & 1) * 8 + (i >> 2) * 4);
+}
+
+__host__ __device__ inline int64_t tiled_d_index(int64_t r, int64_t blk, int64_t nb) {
+  const int64_t unit = (r >> 4) * (nb / kUnitBlocks) + (blk >> 3);
+  return unit * 128 + (((r >> 3) & 1) * 8 + (r & 7)) * 8 + (blk & 7);
+}
+
 // ---- block formats (quant.cu)
 cudaError_t launch_quantize(int wtype, const float* w, int64_t n_blocks, void* out, cudaStream_t s);
 cudaError_t launch_repack(int wtype, const void* src, int64_t rows, int64_t nb, void* qs,
@@ -39,8 +72,21 @@ struct GemvArgs {
   uint32_t* status;      // device status word (bounded waits), or null
 };
 
+// Up to kMaxPhases GEMVs run by one persistent kernel; phase p+1 starts
+// after every CTA finished phase p (grid-wide counters `sync`, [kMaxPhases+1]
+// zeros between launches, which the kernel itself restores).
+constexpr int kMaxPhases = 4;
+constexpr int kMaxGrid = 256;  // CTAs of a GEMV launch at most
+struct GemvChain {
+  GemvArgs ph[kMaxPhases];
+  int mode[kMaxPhases];
+  int n;
+  unsigned* sync;
+};
+
 // Returns cudaErrorInvalidValue when K has no supported thread mapping.
 cudaError_t launch_gemv(int wtype, int mode, const GemvArgs& a, cudaStream_t s);
+cudaError_t launch_gemv_chain(int wtype, const GemvChain& c, cudaStream_t s);
 bool gemv_supported(int K);
 
 // ---- attention side (attn.cu)

@@ -69,6 +69,11 @@ extern "C" tq_status tq_lm_head_static(int32_t wtype, tq_qmat w, int32_t vocab, 
     tq::record_error("tq_lm_head_static: pointers must not be NULL");
     return TQ_REFUSED;
   }
+  if (((reinterpret_cast<uintptr_t>(w.qs_dev) | reinterpret_cast<uintptr_t>(w.d_dev) |
+        reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(gain)) & 15u) != 0) {
+    tq::record_error("tq_lm_head_static: qs, d, x and gain must be 16-byte aligned");
+    return TQ_REFUSED;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned long long* keys = nullptr;
   cudaError_t e = keys_on_current_device(&keys);

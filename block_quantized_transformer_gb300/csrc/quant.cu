@@ -1,6 +1,6 @@
 // Block formats on the GPU: encode f32 -> GGUF-order Q8_0/Q4_0 blocks,
-// repack GGUF-order blocks into the planar layout the GEMV streams, decode
-// planar rows to f32, and gather embedding rows.
+// repack GGUF-order blocks into the tiled layout the GEMV streams (see
+// kernels.cuh), decode rows of it to f32, and gather embedding rows.
 //
 // The formats are the workload descriptions' Q8_0 (fp16 d = max|w|/127,
 // int8 q = round(w/d), value d*q) and Q4_0 (fp16 d = m/-8 at the signed
@@ -71,60 +71,59 @@ __global__ void quantize_kernel(const float* __restrict__ w, int64_t n_blocks,
 
 // ----------------------------------------------------------------- repack --
 
-// One thread per block.  GGUF blocks start at even offsets (34 and 18 are
-// even), so they are read as 16-bit words.
+// One thread per (row, block) of the padded matrix.  GGUF blocks start at even
+// offsets (34 and 18 are even), so they are read as 16-bit words; rows past
+// the end of the matrix (tile padding) get zero codes and zero scales.
 template <int WT>
 __global__ void repack_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t nb,
                               uint8_t* __restrict__ qs, uint16_t* __restrict__ d) {
-  const int64_t n = rows * nb;
+  const int64_t n = tiled_rows(rows) * nb;
+  constexpr int NW = WT == TQ_Q8_0 ? 8 : 4;   // 32-bit words of codes per block
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
-    constexpr int HW = WT == TQ_Q8_0 ? 17 : 9;  // 16-bit words per block
-    const uint16_t* b = src + i * HW;
-    d[i] = b[0];
-    uint32_t v[8];
-    if (WT == TQ_Q4_0) {
+    const int64_t r = i / nb, blk = i % nb;
+    uint32_t v[NW];
+    uint16_t dv = 0;
+    if (r < rows) {
+      const uint16_t* b = src + i * (1 + 2 * NW);
+      dv = b[0];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = (uint32_t)b[1 + 2 * k] | ((uint32_t)b[2 + 2 * k] << 16);
-      reinterpret_cast<uint4*>(qs)[i] = make_uint4(v[0], v[1], v[2], v[3]);
+      for (int k = 0; k < NW; ++k) v[k] = (uint32_t)b[1 + 2 * k] | ((uint32_t)b[2 + 2 * k] << 16);
     } else {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = (uint32_t)b[1 + 2 * k] | ((uint32_t)b[2 + 2 * k] << 16);
-      const int64_t r = i / nb, c = i % nb;
-      uint4* base = reinterpret_cast<uint4*>(qs);
-      base[(r * 2 + 0) * nb + c] = make_uint4(v[0], v[1], v[2], v[3]);
-      base[(r * 2 + 1) * nb + c] = make_uint4(v[4], v[5], v[6], v[7]);
+      for (int k = 0; k < NW; ++k) v[k] = 0u;
     }
+    d[tiled_d_index(r, blk, nb)] = dv;
+#pragma unroll
+    for (int k = 0; k < NW; ++k)
+      *reinterpret_cast<uint32_t*>(qs + tiled_qs_offset(WT, r, blk, nb, k)) = v[k];
   }
 }
 
 // --------------------------------------------------------------- decoding --
 
-// Decode the 16 bytes of chunk `c` of a block into 16 (Q8_0) or 32 (Q4_0)
-// exact f32 values, scaled by d.
+// Decode block `blk` of row `row` into 32 exact f32 values d * code.
 template <int WT>
 __device__ __forceinline__ void decode_block(const uint8_t* qs, const uint16_t* dptr, int64_t row,
-                                             int64_t nb, int64_t c, float* out32) {
-  const float d = half_bits_to_float(dptr[row * nb + c]);
+                                             int64_t nb, int64_t blk, float* out32) {
+  const float d = half_bits_to_float(dptr[tiled_d_index(row, blk, nb)]);
   if (WT == TQ_Q4_0) {
-    const uint4 w = reinterpret_cast<const uint4*>(qs)[row * nb + c];
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const uint32_t byte = (ws[k >> 2] >> (8 * (k & 3))) & 0xffu;
-      out32[k] = d * (float)((int)(byte & 0xf) - 8);
-      out32[k + 16] = d * (float)((int)(byte >> 4) - 8);
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t word = *reinterpret_cast<const uint32_t*>(qs + tiled_qs_offset(WT, row, blk, nb, w));
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t byte = (word >> (8 * k)) & 0xffu;
+        out32[4 * w + k] = d * (float)((int)(byte & 0xf) - 8);
+        out32[4 * w + k + 16] = d * (float)((int)(byte >> 4) - 8);
+      }
     }
   } else {
 #pragma unroll
-    for (int p = 0; p < 2; ++p) {
-      const uint4 w = reinterpret_cast<const uint4*>(qs)[(row * 2 + p) * nb + c];
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    for (int w = 0; w < 8; ++w) {
+      const uint32_t word = *reinterpret_cast<const uint32_t*>(qs + tiled_qs_offset(WT, row, blk, nb, w));
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int8_t q = (int8_t)((ws[k >> 2] >> (8 * (k & 3))) & 0xffu);
-        out32[16 * p + k] = d * (float)q;
-      }
+      for (int k = 0; k < 4; ++k) out32[4 * w + k] = d * (float)(int8_t)((word >> (8 * k)) & 0xffu);
     }
   }
 }
@@ -192,7 +191,7 @@ cudaError_t launch_quantize(int wtype, const float* w, int64_t n_blocks, void* o
 
 cudaError_t launch_repack(int wtype, const void* src, int64_t rows, int64_t nb, void* qs,
                           uint16_t* d, cudaStream_t s) {
-  const unsigned g = grid_1d(rows * nb, 256);
+  const unsigned g = grid_1d(tiled_rows(rows) * nb, 256);
   if (wtype == TQ_Q8_0)
     repack_kernel<TQ_Q8_0><<<g, 256, 0, s>>>((const uint16_t*)src, rows, nb, (uint8_t*)qs, d);
   else

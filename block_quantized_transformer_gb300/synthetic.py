@@ -3,8 +3,8 @@
 Weights come from the shared counter-based generator (``synth``: N(0, 0.02)
 matrices, 1 + N(0, 0.02) gains) written on the GPU, are encoded to GGUF-order
 Q8_0/Q4_0 blocks by the library's own encoder (tq_quantize) and repacked to
-the planar layout (tq_repack), in row chunks of at most 2^28 weights so the
-f32 staging buffer stays at 1 GB.
+the tiled layout (tq_repack), in row chunks of at most 2^28 weights (a
+multiple of 16 rows) so the f32 staging buffer stays at 1 GB.
 """
 from __future__ import annotations
 
@@ -22,14 +22,15 @@ def build_matrix(w: "synth.Workload", name: str, device="cuda") -> QMat:
     rows, cols = w.matrix_shape(name)
     nb = cols // 32
     m = QMat.empty(wt, rows, cols, device)
-    step = max(1, min(rows, CHUNK // cols))
+    step = max(16, (CHUNK // cols) // 16 * 16)
     for r0 in range(0, rows, step):
         r1 = min(rows, r0 + step)
         f = torch.empty((r1 - r0) * cols, dtype=torch.float32, device=device)
         synth.dev_normal(f, w.seed, w.stream_of(name), first=r0 * cols)
         blocks = quantize(f.view(r1 - r0, cols), wt)
-        tq_repack(wt, blocks, r1 - r0, cols, m.qs[r0 * nb * QS_BYTES[wt]: r1 * nb * QS_BYTES[wt]],
-                  m.d[r0 * nb: r1 * nb])
+        p1 = min(r0 + step, (rows + 15) // 16 * 16)  # padded rows of this chunk
+        tq_repack(wt, blocks, r1 - r0, cols, m.qs[r0 * nb * QS_BYTES[wt]: p1 * nb * QS_BYTES[wt]],
+                  m.d[r0 * nb: p1 * nb])
         del f, blocks
     return m
 

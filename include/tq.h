@@ -26,8 +26,8 @@
  *    is poisoned and refuses every later call with TQ_REFUSED; free it and
  *    create a new one, keeping every buffer it was given alive until the
  *    free).  tq_last_error() describes the last failure on the calling thread.
- *  - Weight matrices are [out][in] row-major with blocks of 32 along `in`,
- *    in the planar layout made by tq_repack() (tq_qmat).
+ *  - Weight matrices are [out][in] with blocks of 32 along `in`, in the tiled
+ *    layout made by tq_repack() (tq_qmat).
  */
 #ifndef TQ_H
 #define TQ_H
@@ -63,7 +63,7 @@ enum {
 
 /* Model shape and capacity.  Sizes must satisfy: head_dim in {64, 128};
  * n_heads % n_kv_heads == 0 with n_heads / n_kv_heads <= 8; hidden, ffn and
- * n_heads*head_dim multiples of 256; max_batch >= 1.
+ * n_heads*head_dim multiples of 256 and at most 12288; max_batch >= 1.
  * KV cache: page_size == 0 selects the contiguous layout
  *   [n_layers][max_batch][n_kv_heads][max_ctx][head_dim]
  * (sequence b of a decode batch uses slot b); page_size > 0 (a multiple of
@@ -81,12 +81,21 @@ typedef struct {
   int32_t n_pages;      /* pages in the pool (paged cache only) */
 } tq_config;
 
-/* One quantized matrix [rows][cols] in the planar layout:
- *  qs_dev: Q4_0 -> [rows][cols/32][16] bytes (a block's 16 nibble bytes);
- *          Q8_0 -> [rows][2][cols/32][16] bytes (bytes 0-15 of every block of
- *          the row, then bytes 16-31);
- *  d_dev:  [rows][cols/32] fp16 scales.
- * Both 16-byte aligned. */
+/* One quantized matrix [rows][cols] (cols a multiple of 256) in the tiled
+ * layout.  Rows are padded with zero rows to a multiple of 16 (R rows) and
+ * grouped in tiles of 16; the 8-block runs of a tile row ("units", 16 rows x
+ * 256 inputs) are stored tile after tile:
+ *  qs_dev: R/16 * cols/256 units of 2048 (Q4_0) or 4096 (Q8_0) bytes, i.e.
+ *          R * cols/32 * 16 (Q4_0) or * 32 (Q8_0) bytes in all;
+ *  d_dev:  R/16 * cols/256 units of 128 fp16 scales (R * cols/32 scales).
+ * Inside a unit, 32-bit code word i (Q4_0: bytes 4i..4i+3 of the block's 16
+ * nibble bytes, i < 4; Q8_0: codes 4i..4i+3, i < 8) of block j (0-7) of tile
+ * row rr = 8h + g lies at byte
+ *   Q4_0: ((h*2 + j/4)*32 + 4g + i)*16 + (j%4)*4
+ *   Q8_0: ((h*4 + j/2)*32 + 4g + i%4)*16 + (j%2)*8 + (i/4)*4
+ * and its scale at element (h*8 + g)*8 + j; so each lane of a warp loads the
+ * words of its tensor-core operand fragment with one 16-byte load.
+ * tq_qmat_bytes() gives the sizes.  Both pointers 16-byte aligned. */
 typedef struct {
   const void* qs_dev;
   const uint16_t* d_dev;
@@ -184,10 +193,17 @@ TQ_API const char* tq_last_error(void);
 
 /* ------------------------------------------------------- weight formats -- */
 
-/* GGUF-order blocks -> planar layout (tq_qmat).
+/* Bytes of the qs and d arrays of a [rows][cols] matrix in the tiled layout
+ * (tq_qmat).  Refused when cols % 256 != 0 or a size is negative. */
+TQ_API tq_status tq_qmat_bytes(int32_t wtype, int64_t rows, int64_t cols, int64_t* qs_bytes,
+                               int64_t* d_bytes);
+
+/* GGUF-order blocks -> tiled layout (tq_qmat), padding rows included.
  *  blocks_dev: [rows][cols/32] blocks of 34 (Q8_0) or 18 (Q4_0) bytes;
  *  qs_dev, d_dev: outputs as described for tq_qmat.
- * Refused when cols % 32 != 0 or a pointer is NULL or misaligned. */
+ * A matrix may be repacked in row chunks whose first row is a multiple of
+ * 16, with qs_dev/d_dev advanced by that many rows' bytes.
+ * Refused when cols % 256 != 0 or a pointer is NULL or misaligned. */
 TQ_API tq_status tq_repack(int32_t wtype, const void* blocks_dev, int64_t rows, int64_t cols,
                     void* qs_dev, uint16_t* d_dev, void* stream);
 
@@ -199,7 +215,7 @@ TQ_API tq_status tq_repack(int32_t wtype, const void* blocks_dev, int64_t rows, 
 TQ_API tq_status tq_quantize(int32_t wtype, const float* w_dev, int64_t rows, int64_t cols,
                       void* blocks_dev, void* stream);
 
-/* Decode planar rows [row0, row0+n_rows) of a matrix to f32 (exact). */
+/* Decode rows [row0, row0+n_rows) of a tiled matrix to f32 (exact). */
 TQ_API tq_status tq_dequantize(int32_t wtype, tq_qmat w, int64_t cols, int64_t row0, int64_t n_rows,
                         float* out_dev, void* stream);
 

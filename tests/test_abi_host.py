@@ -84,7 +84,19 @@ def test_null_arguments_refused_without_gpu():
     L.tq_model_free(None)                               # ignored
     assert L.tq_repack(5, None, 1, 32, None, None, None) == tq.TQ_REFUSED
     assert L.tq_quantize(2, None, 1, 33, None, None) == tq.TQ_REFUSED
-    assert L.tq_repack(2, None, 0, 32, None, None, None) == tq.TQ_OK   # empty is a no-op
+    assert L.tq_repack(2, None, 0, 256, None, None, None) == tq.TQ_OK  # empty is a no-op
+    assert L.tq_repack(2, None, 1, 32, None, None, None) == tq.TQ_REFUSED  # tiles need cols % 256 == 0
+
+
+def test_tiled_matrix_sizes():
+    """Rows pad to a multiple of 16; 16 (Q4_0) or 32 (Q8_0) code bytes and one
+    fp16 scale per block."""
+    assert tq.tq_qmat_bytes(tq.TQ_Q4_0, 16, 256) == (16 * 8 * 16, 16 * 8 * 2)
+    assert tq.tq_qmat_bytes(tq.TQ_Q4_0, 17, 512) == (32 * 16 * 16, 32 * 16 * 2)
+    assert tq.tq_qmat_bytes(tq.TQ_Q8_0, 151936, 4096) == (151936 * 128 * 32, 151936 * 128 * 2)
+    assert tq.tq_qmat_bytes(tq.TQ_Q8_0, 0, 256) == (0, 0)
+    with pytest.raises(tq.TqError):
+        tq.tq_qmat_bytes(tq.TQ_Q4_0, 16, 288)
 
 
 def test_binding_range_checks_before_the_library():

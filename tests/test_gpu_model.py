@@ -1,5 +1,5 @@
 """End-to-end GPU parity of the decode step: the GPU model (device-generated
-weights, GPU encoder, planar repack, all kernels) against the oracle on the
+weights, GPU encoder, tiled repack, all kernels) against the oracle on the
 same seeded inputs, teacher-forced on the oracle's greedy tokens.  Tolerance:
 max |logit error| / oracle logit range <= 2e-3 with an f32 KV cache, 1e-2
 with f16; greedy tokens equal wherever the oracle's top-2 margin exceeds that
