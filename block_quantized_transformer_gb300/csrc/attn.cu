@@ -579,13 +579,15 @@ cudaError_t attn_t(const AttnArgs& a, cudaStream_t s) {
                         dim3(128), S::BYTES, kCluster, s, a);
 }
 
-// Two stages per warp when a warp may have several tiles, except for f32 rows
-// of 128 dimensions (the second stage would not fit in shared memory).
+// Decode (clusters of kCluster CTAs): one stage per warp, so a CTA takes
+// about a third of an SM's shared memory and every cluster of the launch
+// finds room at once (with two stages only part of the clusters fit, and
+// the rest ran as a second wave).  Prefill: two stages when a warp may have
+// several tiles, except for f32 rows of 128 dimensions (the second stage
+// would not fit in shared memory).
 template <typename KT, int HD, int G>
 cudaError_t attn_g(const AttnArgs& a, cudaStream_t s) {
-  const int keys_per_cta =
-      a.fused ? ((a.cache.max_ctx + kCluster * 32 - 1) / (kCluster * 32)) * 32 : a.split_keys;
-  if (keys_per_cta <= 4 * 32 || (sizeof(KT) == 4 && HD == 128)) return attn_t<KT, HD, G, 1>(a, s);
+  if (a.fused || a.split_keys <= 4 * 32 || (sizeof(KT) == 4 && HD == 128)) return attn_t<KT, HD, G, 1>(a, s);
   return attn_t<KT, HD, G, 2>(a, s);
 }
 
