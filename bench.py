@@ -234,6 +234,8 @@ def run_gpu(args, rank, world):
     if args.layers:
         import dataclasses
         w = dataclasses.replace(w, n_layers=args.layers)
+    if w.batch > 1:
+        return run_gpu_batched(args, rank, world, w)
     K, W = args.steps, args.warmup
     prompt_len = w.prompt_len
     max_ctx = prompt_len + W + K + 8
@@ -364,6 +366,98 @@ def run_gpu(args, rank, world):
         per_step = min(o.step() for _ in range(3))
         line["cpu_baseline"] = {"value": round(1.0 / per_step, 5), "unit": "tokens/s",
                                 "cores": o.cores, "kind": "oracle", "sample": o.desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_gpu_batched(args, rank, world, w):
+    """Batched decode over a paged f16 cache: w.batch sequences whose cached
+    lengths come from the workload's seeded length generator, their pages
+    handed out in a seeded shuffled order, the cache filled with seeded N(0, 1)
+    values (no prefill: the step's cost does not depend on what the cache
+    holds), then greedy decode steps of the whole batch, timed with CUDA events
+    around graph replays."""
+    import numpy as np
+    import torch
+    import synth
+    from block_quantized_transformer_gb300.synthetic import build_weights, build_model
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    K, W = args.steps, args.warmup
+    B, P = w.batch, w.page_size
+    lens = w.context_lengths().astype(np.int64)
+    need = lens + W + K + 1
+    per_seq = int((need.max() + P - 1) // P)
+    max_ctx = per_seq * P
+    n_pages_seq = (need + P - 1) // P
+    n_pages = int(n_pages_seq.sum())
+    keys = synth.host_normal(w.length_seed, synth.LENGTH_STREAM + 1, n_pages, sigma=1.0)
+    order = np.argsort(keys, kind="stable").astype(np.int32)        # seeded shuffle of the pool
+    table = np.zeros((B, per_seq), dtype=np.int32)
+    at = 0
+    for b in range(B):
+        table[b, :n_pages_seq[b]] = order[at:at + n_pages_seq[b]]
+        at += n_pages_seq[b]
+    mats, gains = build_weights(w, dev)
+    model = build_model(w, device=dev, max_batch=B, max_ctx=max_ctx, max_prefill=B,
+                        page_size=P, n_pages=n_pages, weights=(mats, gains))
+    chunk = 1 << 26
+    for cache, stream_id in ((model.k_cache, synth.KV_STREAM), (model.v_cache, synth.KV_STREAM + 1)):
+        for i0 in range(0, cache.numel(), chunk):
+            n = min(chunk, cache.numel() - i0)
+            f = torch.empty(n, dtype=torch.float32, device=dev)
+            synth.dev_normal(f, w.seed, stream_id, first=i0, sigma=1.0)
+            cache[i0:i0 + n].copy_(f)
+            del f
+    torch.cuda.synchronize()
+    weight_bytes = model.weight_bytes() + sum(g.numel() * 4 for g in gains.values())
+    bt = torch.tensor(table, device=dev)
+    tok = torch.tensor(synth.uniform_below(w.seed, synth.PROMPT_STREAM, B, w.vocab).astype(np.int32), device=dev)
+    pos = torch.tensor(lens.astype(np.int32), device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            model.decode_step(tok, pos, pos, block_table=bt, argmax=tok, graph=True)
+            pos.add_(1)
+        stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        clocks = Clocks(local)
+        clocks.start()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            model.decode_step(tok, pos, pos, block_table=bt, argmax=tok, graph=True)
+            pos.add_(1)
+        e1.record(stream)
+        stream.synchronize()
+        ms = e0.elapsed_time(e1)
+        clk = clocks.stop()
+        barrier(world)
+        assert model.status() == 0
+    ms_max = barrier_max(ms, world)
+    ms_step = ms_max / K
+    kv_row = 2 * w.n_kv_heads * w.head_dim * 2 * w.n_layers
+    ctx_sum = float((lens + W + 1).sum()) + B * (K - 1) / 2.0
+    step_bytes = weight_bytes + kv_row * ctx_sum + kv_row * B
+    hbm, _, peak_kind = peaks()
+    launches = model.launches_per_step * K
+    model.close()
+    line = {"metric": f"decode tokens/s (B={B}, Q4_0 Qwen3-8B shape, paged f16 KV) and achieved HBM GB/s vs peak",
+            "value": round(world * B * K / (ms_max / 1e3), 2), "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{w.name}: {B} sequences, cached lengths {int(lens.min())}..{int(lens.max())} "
+                                   f"(sum {int(lens.sum())}), pages of {P} tokens in a seeded shuffled order",
+                       "weights": "Q4_0, 4.26 GB, seeded N(0,0.02)", "kv_cache": "f16, seeded N(0,1)",
+                       "l2": "inputs exceed L2", "parallelism": f"replicas x{world}"},
+            "hbm": {"step_bytes": int(step_bytes), "achieved_gbs": round(step_bytes / (ms_step / 1e3) / 1e9, 1),
+                    "frac_of_peak": round(step_bytes / (ms_step / 1e3) / 1e9 / hbm, 4), "peak_gbs": hbm,
+                    "peak_kind": peak_kind, "roofline_tokens_per_s": round(B * hbm * 1e9 / step_bytes, 1)},
+            "gpu_launches": launches, "clocks": clk}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
