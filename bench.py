@@ -209,15 +209,24 @@ def file_hash(path):
 
 
 def traffic_from_profile(kernel_src):
-    """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source; else None."""
-    p = os.path.join(ROOT, "profiles", "gemv_q4_0_swiglu_8b.json")
+    """dram bytes per launch from the committed ncu summary of the dominant
+    GEMV phase, if it was taken on the current kernel source; else None.  The
+    summary carries two machine-readable lines: `source_sha256_16: <hex>` and
+    `dram_bytes_per_launch: <int>`."""
+    p = os.path.join(ROOT, "profiles", "gemv_chain_q4_0_swiglu_qwen3_8b.md")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p))
-    if d.get("source_sha256_16") != file_hash(kernel_src):
+    fields = {}
+    for ln in open(p):
+        if ":" in ln and ln.split(":", 1)[0].strip() in ("source_sha256_16", "dram_bytes_per_launch"):
+            k, v = ln.split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_sha256_16") != file_hash(kernel_src):
         return None
-    return d.get("dram_bytes_per_launch")
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def run_gpu(args, rank, world):
@@ -301,8 +310,8 @@ def run_gpu(args, rank, world):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4),
                 "traffic": traffic_from_profile(os.path.join(ROOT, "block_quantized_transformer_gb300",
-                                                              "csrc", "gemv.cu")),
-                "kernel": "gemv_kernel<Q4_0, SWIGLU> (RMSNorm + gate/up + SwiGLU), 2x12288x4096",
+                                                              "csrc", "gemv_impl.cuh")),
+                "kernel": "gemv_chain_kernel<Q4_0>, one RMSNorm + gate/up + SwiGLU phase, 2x12288x4096",
                 "peak_kind": peak_kind + " (burst copy, kernel timed alone)",
                 "launch_ms": round(kern_ms, 5), "bytes_per_launch": int(kern_bytes)}
 
