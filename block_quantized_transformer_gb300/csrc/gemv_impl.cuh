@@ -30,9 +30,9 @@
 // phase, which measured slower.)
 //
 // Pipeline.  Every consumer warp reads its units from its own ring of shared-
-// memory slots, which lane w of a producer warp fills with 1-D bulk copies
-// through the TMA engine (full/empty mbarriers, every wait bounded).  A
-// bulk-copy issue can stall on a full TMA queue; only the producer waits then.
+// memory slots, which a lane of one of kP producer warps fills with 1-D bulk
+// copies through the TMA engine (full/empty mbarriers, every wait bounded).
+// A bulk-copy issue can stall on a full TMA queue; only a producer waits then.
 //
 // Chains.  One launch runs up to kMaxPhases GEMVs in a row; CTAs meet at a
 // grid-wide counter between phases (the next phase reads what the previous
@@ -54,9 +54,19 @@ namespace gemv {
 
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kSyncLimit = 1u << 24;
-constexpr int kW = 8;                   // consumer warps
+#ifndef TQ_GEMV_CONSUMER_WARPS
+#define TQ_GEMV_CONSUMER_WARPS 8
+#endif
+#ifndef TQ_GEMV_SLOT_UNITS_Q4
+#define TQ_GEMV_SLOT_UNITS_Q4 4
+#endif
+constexpr int kW = TQ_GEMV_CONSUMER_WARPS;  // consumer warps
 constexpr int kCT = kW * 32;            // consumer threads
-constexpr int kThreads = kCT + 32;      // + the producer warp
+#ifndef TQ_GEMV_PRODUCER_WARPS
+#define TQ_GEMV_PRODUCER_WARPS 4  // a bulk-copy issue can stall; four issuers keep more copies in flight
+#endif
+constexpr int kP = TQ_GEMV_PRODUCER_WARPS;  // producer warps
+constexpr int kThreads = kCT + 32 * kP;
 constexpr int kSmemMax = 227 * 1024;
 constexpr int kXBlockBytes = 128;       // fp16 hi/lo fragments of one 32-input block
 constexpr int kMaxK = 12288;
@@ -70,7 +80,7 @@ template <int WT>
 struct Fmt {
   static constexpr int QU = unit_qs_bytes(WT);       // code bytes of a unit
   static constexpr int UB = QU + kUnitD;             // unit bytes
-  static constexpr int SU = WT == TQ_Q4_0 ? 4 : 2;   // units per slot
+  static constexpr int SU = WT == TQ_Q4_0 ? TQ_GEMV_SLOT_UNITS_Q4 : 2;  // units per slot (even)
   static constexpr int SLOT = SU * UB;
 };
 
@@ -419,21 +429,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
   __syncthreads();
   grid_dep_launch();
 
-  if (warp == kW) {
+  if (warp >= kW) {
     // ---------------------------------------------------------------- producer
-    // Lane w keeps consumer warp w's ring full: in a loop common to the lanes,
-    // every lane whose next stage is free (non-blocking test) issues that
-    // slot's copies, so a ring that is still being read never holds up the
-    // others, and a bulk-copy issue that stalls on a full TMA queue stalls
-    // only this warp.  Weights are read-only: nothing here waits for other
+    // Lane l of producer warp pw keeps consumer warp pw + kP l's ring full: in
+    // a loop common to the lanes, every lane whose next stage is free (non-
+    // blocking test) issues that slot's copies, so a ring that is still being
+    // read never holds up the others, and a bulk-copy issue that stalls on a
+    // full TMA queue stalls only a producer.  Weights are read-only: nothing here waits for other
     // kernels or other CTAs, so the first slots load while the consumers wait
     // for the kernel that writes this launch's activations.
-    const int w = lane < kW ? lane : 0;
+    const int pw = warp - kW;                 // producer warp pw serves rings pw, pw + kP, ...
+    const bool mine = pw + kP * lane < kW;
+    const int w = mine ? pw + kP * lane : 0;
     uint64_t* full = bars + w * 2 * depth;
     uint64_t* empty = full + depth;
     uint8_t* ring = smem + L.ring + w * depth * F::SLOT;
     Cursor cu;
-    cu.p = lane < kW ? 0 : ch.n;
+    cu.p = mine ? 0 : ch.n;
     cursor_enter<WT>(cu, ch, cta, C, w);
     int issued = 0;
     uint32_t idle = 0;
@@ -462,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
       }
     }
     // every issued copy lands before the CTA's shared memory is released
-    if (lane < kW)
+    if (mine)
       for (int k = (issued > depth ? issued - depth : 0); k < issued; ++k)
         mbar_wait_bounded(&full[k % depth], (k / depth) & 1, kWaitLimit);
     return;
