@@ -3,6 +3,7 @@
 // decode and prefill launch sequences, CUDA-graph replay of the decode step,
 // and the status / poisoning rules of the tessl_torch README ("Handle
 // ownership, closing and errors").
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -30,7 +31,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Layout {
-  size_t x, qkv, att, act, cos_t, sin_t, part, counters, keys, status, chain_sync, total;
+  size_t x, qkv, att, act, act2, xtab, xneg, inv_s, cos_t, sin_t, part, counters, keys, status, chain_sync, total;
   int T;                 // rows of activation buffers
   int split_dec, splits_dec, split_pf, splits_pf;
 };
@@ -93,6 +94,12 @@ Layout layout_of(const tq_config& c) {
   L.qkv = take((size_t)L.T * qkv_width(c) * 4);
   L.att = take((size_t)L.T * c.n_heads * c.head_dim * 4);
   L.act = take((size_t)L.T * c.ffn * 4);
+  // prefill GEMM: up-projection rows and the fragment table of the widest input
+  const int kmax = std::max(c.hidden, std::max(c.n_heads * c.head_dim, c.ffn));
+  L.act2 = take((size_t)c.max_prefill * c.ffn * 4);
+  L.xtab = take((size_t)c.max_prefill * (kmax / 32) * 128);
+  L.xneg = take((size_t)c.max_prefill * (kmax / 32) * 4);
+  L.inv_s = take((size_t)c.max_prefill * 4);
   L.cos_t = take((size_t)c.max_ctx * (c.head_dim / 2) * 4);
   L.sin_t = take((size_t)c.max_ctx * (c.head_dim / 2) * 4);
   L.part = take(part_rows * G * (c.head_dim + 2) * 4);
@@ -149,6 +156,10 @@ struct tq_model {
   float* qkv() const { return reinterpret_cast<float*>(ws + L.qkv); }
   float* att() const { return reinterpret_cast<float*>(ws + L.att); }
   float* act() const { return reinterpret_cast<float*>(ws + L.act); }
+  float* act2() const { return reinterpret_cast<float*>(ws + L.act2); }
+  uint8_t* xtab() const { return ws + L.xtab; }
+  float* xneg() const { return reinterpret_cast<float*>(ws + L.xneg); }
+  float* inv_s() const { return reinterpret_cast<float*>(ws + L.inv_s); }
   float* cos_t() const { return reinterpret_cast<float*>(ws + L.cos_t); }
   float* sin_t() const { return reinterpret_cast<float*>(ws + L.sin_t); }
   float* part() const { return reinterpret_cast<float*>(ws + L.part); }
@@ -285,6 +296,129 @@ tq::GemvArgs head_args(const tq_model* m, const float* x, int B, float* logits) 
   return h;
 }
 
+tq::RopeArgs rope_args(const tq_model* m, int l, int T, const int32_t* pos, const int32_t* kv_len, int pos_base,
+                       int seq_fixed, const int32_t* block_table) {
+  const tq_config& c = m->cfg;
+  tq::RopeArgs r{};
+  r.qkv = m->qkv();
+  r.T = T;
+  r.nq = c.n_heads;
+  r.nkv = c.n_kv_heads;
+  r.pos = pos;
+  r.kv_len = kv_len;
+  r.pos_base = pos_base;
+  r.seq_fixed = seq_fixed;
+  r.kc = m->kc_layer(l);
+  r.vc = m->vc_layer(l);
+  r.cache = cache_view(m, block_table);
+  r.cos_t = m->cos_t();
+  r.sin_t = m->sin_t();
+  r.gq = m->layers[l].attn_q_norm_dev;
+  r.gk = m->layers[l].attn_k_norm_dev;
+  r.eps = c.rms_eps;
+  r.status = m->status();
+  return r;
+}
+
+tq::AttnArgs attn_args(const tq_model* m, int l, int T, const int32_t* pos, const int32_t* kv_len, int pos_base,
+                       int seq_fixed, const int32_t* block_table, bool prefill) {
+  const tq_config& c = m->cfg;
+  const int hd = c.head_dim;
+  tq::AttnArgs a{};
+  a.q = m->qkv();
+  a.q_stride = qkv_width(c);
+  a.o = m->att();
+  a.T = T;
+  a.nq = c.n_heads;
+  a.nkv = c.n_kv_heads;
+  a.kv_len = kv_len;
+  a.pos_base = pos_base;
+  a.seq_fixed = seq_fixed;
+  a.kc = m->kc_layer(l);
+  a.vc = m->vc_layer(l);
+  a.cache = cache_view(m, block_table);
+  a.split_keys = prefill ? m->L.split_pf : m->L.split_dec;
+  a.max_splits = prefill ? m->L.splits_pf : m->L.splits_dec;
+  a.part = m->part();
+  a.counters = m->counters();
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
+  a.status = m->status();
+  a.fused = prefill ? 0 : 1;
+  a.pos = pos;
+  a.cos_t = m->cos_t();
+  a.sin_t = m->sin_t();
+  a.gq = m->layers[l].attn_q_norm_dev;
+  a.gk = m->layers[l].attn_k_norm_dev;
+  a.eps = c.rms_eps;
+  return a;
+}
+
+// Prefill of T >= 2 tokens: every projection as a GEMM over all T tokens (each
+// weight unit read once per 32 tokens), the phase input turned into the
+// fragment table by one xprep launch; attention as in decode, per query row.
+// The head runs on the last token only.
+cudaError_t run_prefill_gemm(tq_model* m, int T, int pos_base, int seq_fixed, const int32_t* block_table,
+                             float* logits, int32_t* argmax, cudaStream_t s) {
+  const tq_config& c = m->cfg;
+  const int hd = c.head_dim, nq = c.n_heads, nkv = c.n_kv_heads, G = nq / nkv;
+  cudaError_t e;
+  auto prep = [&](const float* x, const float* up, int K, const float* gain) {
+    tq::XPrepArgs p{};
+    p.x = x;
+    p.up = up;
+    p.ldx = K;
+    p.gain = gain;
+    p.eps = c.rms_eps;
+    p.K = K;
+    p.T = T;
+    p.xtab = m->xtab();
+    p.xneg = m->xneg();
+    p.inv_s = m->inv_s();
+    return tq::launch_xprep(c.wtype, p, s);
+  };
+  auto gemm = [&](const tq::GemvSeg* seg, int nseg, int K, float* y, int ldy, const float* residual) {
+    tq::QGemmArgs g{};
+    for (int i = 0; i < nseg; ++i) g.seg[i] = seg[i];
+    g.nseg = nseg;
+    g.K = K;
+    g.T = T;
+    g.xtab = m->xtab();
+    g.xneg = m->xneg();
+    g.inv_s = m->inv_s();
+    g.y = y;
+    g.ldy = ldy;
+    g.residual = residual;
+    g.status = m->status();
+    return tq::launch_qgemm(c.wtype, g, s);
+  };
+  for (int l = 0; l < c.n_layers; ++l) {
+    const tq_layer& ly = m->layers[l];
+    const tq::GemvSeg qkv[3] = {seg_of(ly.attn_q, nq * hd), seg_of(ly.attn_k, nkv * hd), seg_of(ly.attn_v, nkv * hd)};
+    if ((e = prep(m->x(), nullptr, c.hidden, ly.attn_norm_dev)) != cudaSuccess) return e;
+    if ((e = gemm(qkv, 3, c.hidden, m->qkv(), qkv_width(c), nullptr)) != cudaSuccess) return e;
+    const tq::RopeArgs r = rope_args(m, l, T, nullptr, nullptr, pos_base, seq_fixed, block_table);
+    if ((e = tq::launch_rope_append(c.kvtype, hd, r, s)) != cudaSuccess) return e;
+    const tq::AttnArgs a = attn_args(m, l, T, nullptr, nullptr, pos_base, seq_fixed, block_table, true);
+    if ((e = tq::launch_attn_decode(c.kvtype, hd, G, a, s)) != cudaSuccess) return e;
+    const tq::GemvSeg o = seg_of(ly.attn_output, c.hidden);
+    if ((e = prep(m->att(), nullptr, nq * hd, nullptr)) != cudaSuccess) return e;
+    if ((e = gemm(&o, 1, nq * hd, m->x(), c.hidden, m->x())) != cudaSuccess) return e;
+    const tq::GemvSeg gate = seg_of(ly.ffn_gate, c.ffn), up = seg_of(ly.ffn_up, c.ffn);
+    if ((e = prep(m->x(), nullptr, c.hidden, ly.ffn_norm_dev)) != cudaSuccess) return e;
+    if ((e = gemm(&gate, 1, c.hidden, m->act(), c.ffn, nullptr)) != cudaSuccess) return e;
+    if ((e = gemm(&up, 1, c.hidden, m->act2(), c.ffn, nullptr)) != cudaSuccess) return e;
+    const tq::GemvSeg down = seg_of(ly.ffn_down, c.hidden);
+    if ((e = prep(m->act(), m->act2(), c.ffn, nullptr)) != cudaSuccess) return e;
+    if ((e = gemm(&down, 1, c.ffn, m->x(), c.hidden, m->x())) != cudaSuccess) return e;
+  }
+  tq::GemvChain ch{};
+  ch.ph[0] = head_args(m, m->x() + (size_t)(T - 1) * c.hidden, 1, logits);
+  ch.mode[0] = tq::GEMV_ARGMAX;
+  ch.n = 1;
+  if ((e = tq::launch_gemv_chain(c.wtype, ch, s)) != cudaSuccess) return e;
+  return tq::launch_argmax_finish(m->keys(), 1, argmax, s);
+}
+
 // The layers and the head.  The GEMVs between two attention launches run as
 // one persistent chain: output projection, gate/up, down projection of layer
 // l and the Q/K/V projection of layer l+1 (the LM head after the last layer),
@@ -307,52 +441,11 @@ cudaError_t run_layers(tq_model* m, int T, const int32_t* pos, const int32_t* kv
     const tq_layer& ly = m->layers[l];
     // QK-norm + RoPE + KV append: its own kernel in prefill (every token's K/V
     // must be stored before any token attends); inside attention in decode
-    tq::RopeArgs r{};
-    r.qkv = m->qkv();
-    r.T = T;
-    r.nq = nq;
-    r.nkv = nkv;
-    r.pos = pos;
-    r.kv_len = kv_len;
-    r.pos_base = pos_base;
-    r.seq_fixed = seq_fixed;
-    r.kc = m->kc_layer(l);
-    r.vc = m->vc_layer(l);
-    r.cache = cache_view(m, block_table);
-    r.cos_t = m->cos_t();
-    r.sin_t = m->sin_t();
-    r.gq = ly.attn_q_norm_dev;
-    r.gk = ly.attn_k_norm_dev;
-    r.eps = c.rms_eps;
-    r.status = m->status();
-    if (prefill && (e = tq::launch_rope_append(c.kvtype, hd, r, s)) != cudaSuccess) return e;
-    // attention
-    tq::AttnArgs a{};
-    a.q = m->qkv();
-    a.q_stride = qkv_width(c);
-    a.o = m->att();
-    a.T = T;
-    a.nq = nq;
-    a.nkv = nkv;
-    a.kv_len = kv_len;
-    a.pos_base = pos_base;
-    a.seq_fixed = seq_fixed;
-    a.kc = m->kc_layer(l);
-    a.vc = m->vc_layer(l);
-    a.cache = cache_view(m, block_table);
-    a.split_keys = prefill ? m->L.split_pf : m->L.split_dec;
-    a.max_splits = prefill ? m->L.splits_pf : m->L.splits_dec;
-    a.part = m->part();
-    a.counters = m->counters();
-    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
-    a.status = m->status();
-    a.fused = prefill ? 0 : 1;
-    a.pos = pos;
-    a.cos_t = m->cos_t();
-    a.sin_t = m->sin_t();
-    a.gq = ly.attn_q_norm_dev;
-    a.gk = ly.attn_k_norm_dev;
-    a.eps = c.rms_eps;
+    if (prefill) {
+      const tq::RopeArgs r = rope_args(m, l, T, pos, kv_len, pos_base, seq_fixed, block_table);
+      if ((e = tq::launch_rope_append(c.kvtype, hd, r, s)) != cudaSuccess) return e;
+    }
+    const tq::AttnArgs a = attn_args(m, l, T, pos, kv_len, pos_base, seq_fixed, block_table, prefill);
     if ((e = tq::launch_attn_decode(c.kvtype, hd, G, a, s)) != cudaSuccess) return e;
     // output projection, FFN, and the next layer's Q/K/V (or the head)
     tq::GemvChain ch{};
@@ -490,8 +583,9 @@ tq_status tq_prefill(tq_model* m, int32_t seq, const int32_t* tokens, int32_t n_
   cudaError_t e = tq::launch_embed(c.wtype, m->embd.qs_dev, m->embd.d_dev, c.vocab, c.hidden, tokens,
                                    n_tokens, m->x(), m->status(), m->keys(), 1, s);
   if (e == cudaSuccess)
-    e = run_layers(m, n_tokens, nullptr, nullptr, start_pos, seq, block_table, true,
-                   m->x() + (size_t)(n_tokens - 1) * c.hidden, 1, logits, argmax, s);
+    e = n_tokens >= 2 ? run_prefill_gemm(m, n_tokens, start_pos, seq, block_table, logits, argmax, s)
+                      : run_layers(m, n_tokens, nullptr, nullptr, start_pos, seq, block_table, true,
+                                   m->x() + (size_t)(n_tokens - 1) * c.hidden, 1, logits, argmax, s);
   if (e != cudaSuccess) return fail_cuda(m, e, "tq_prefill");
   return TQ_OK;
 }

@@ -89,6 +89,36 @@ cudaError_t launch_gemv(int wtype, int mode, const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_gemv_chain(int wtype, const GemvChain& c, cudaStream_t s);
 bool gemv_supported(int K);
 
+// ---- prefill GEMM (qgemm.cu)
+// Input rows of a phase -> fragment table (see qgemm.cu): x [T][ldx] f32, up
+// (optional: the input is silu(x) * up), gain (optional RMSNorm gain, eps).
+struct XPrepArgs {
+  const float* x;
+  const float* up;
+  int ldx;
+  const float* gain;
+  float eps;
+  int K, T;
+  uint8_t* xtab;   // [K/256][T][8][128 B]
+  float* xneg;     // [K/256][T][8]
+  float* inv_s;    // [T]
+};
+// Y[t][r] (+)= sum_k W[r][k] X[t][k] over the concatenated segments.
+struct QGemmArgs {
+  GemvSeg seg[3];
+  int nseg;
+  int K, T;
+  const uint8_t* xtab;
+  const float* xneg;
+  const float* inv_s;
+  float* y;                // [T][ldy]
+  int ldy;
+  const float* residual;   // [T][ldy] or null; may alias y
+  uint32_t* status;
+};
+cudaError_t launch_xprep(int wtype, const XPrepArgs& a, cudaStream_t s);
+cudaError_t launch_qgemm(int wtype, const QGemmArgs& a, cudaStream_t s);
+
 // ---- attention side (attn.cu)
 struct CacheView {
   int max_ctx;               // slots per sequence (contiguous) or tokens per sequence (paged)
