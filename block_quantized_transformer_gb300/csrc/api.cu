@@ -31,7 +31,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Layout {
-  size_t x, qkv, att, act, act2, xtab, xneg, inv_s, cos_t, sin_t, part, counters, keys, status, chain_sync, total;
+  size_t x, qkv, att, act, act2, xtab, xneg, inv_s, logits, cos_t, sin_t, part, counters, keys, status, chain_sync, total;
   int T;                 // rows of activation buffers
   int split_dec, splits_dec, split_pf, splits_pf;
 };
@@ -96,10 +96,11 @@ Layout layout_of(const tq_config& c) {
   L.act = take((size_t)L.T * c.ffn * 4);
   // prefill GEMM: up-projection rows and the fragment table of the widest input
   const int kmax = std::max(c.hidden, std::max(c.n_heads * c.head_dim, c.ffn));
-  L.act2 = take((size_t)c.max_prefill * c.ffn * 4);
-  L.xtab = take((size_t)c.max_prefill * (kmax / 32) * 128);
-  L.xneg = take((size_t)c.max_prefill * (kmax / 32) * 4);
-  L.inv_s = take((size_t)c.max_prefill * 4);
+  L.act2 = take((size_t)L.T * c.ffn * 4);
+  L.xtab = take((size_t)L.T * (kmax / 32) * 128);
+  L.xneg = take((size_t)L.T * (kmax / 32) * 4);
+  L.inv_s = take((size_t)L.T * 4);
+  L.logits = c.max_batch > 1 ? take((size_t)c.max_batch * c.vocab * 4) : 0;
   L.cos_t = take((size_t)c.max_ctx * (c.head_dim / 2) * 4);
   L.sin_t = take((size_t)c.max_ctx * (c.head_dim / 2) * 4);
   L.part = take(part_rows * G * (c.head_dim + 2) * 4);
@@ -160,6 +161,7 @@ struct tq_model {
   uint8_t* xtab() const { return ws + L.xtab; }
   float* xneg() const { return reinterpret_cast<float*>(ws + L.xneg); }
   float* inv_s() const { return reinterpret_cast<float*>(ws + L.inv_s); }
+  float* logits_ws() const { return reinterpret_cast<float*>(ws + L.logits); }
   float* cos_t() const { return reinterpret_cast<float*>(ws + L.cos_t); }
   float* sin_t() const { return reinterpret_cast<float*>(ws + L.sin_t); }
   float* part() const { return reinterpret_cast<float*>(ws + L.part); }
@@ -353,70 +355,96 @@ tq::AttnArgs attn_args(const tq_model* m, int l, int T, const int32_t* pos, cons
   return a;
 }
 
-// Prefill of T >= 2 tokens: every projection as a GEMM over all T tokens (each
-// weight unit read once per 32 tokens), the phase input turned into the
-// fragment table by one xprep launch; attention as in decode, per query row.
-// The head runs on the last token only.
-cudaError_t run_prefill_gemm(tq_model* m, int T, int pos_base, int seq_fixed, const int32_t* block_table,
-                             float* logits, int32_t* argmax, cudaStream_t s) {
+cudaError_t gemm_prep(tq_model* m, int T, const float* x, const float* up, int K, const float* gain, cudaStream_t s) {
+  tq::XPrepArgs p{};
+  p.x = x;
+  p.up = up;
+  p.ldx = K;
+  p.gain = gain;
+  p.eps = m->cfg.rms_eps;
+  p.K = K;
+  p.T = T;
+  p.xtab = m->xtab();
+  p.xneg = m->xneg();
+  p.inv_s = m->inv_s();
+  return tq::launch_xprep(m->cfg.wtype, p, s);
+}
+
+cudaError_t gemm_run(tq_model* m, int T, const tq::GemvSeg* seg, int nseg, int K, float* y, int ldy,
+                     const float* residual, cudaStream_t s) {
+  tq::QGemmArgs g{};
+  for (int i = 0; i < nseg; ++i) g.seg[i] = seg[i];
+  g.nseg = nseg;
+  g.K = K;
+  g.T = T;
+  g.xtab = m->xtab();
+  g.xneg = m->xneg();
+  g.inv_s = m->inv_s();
+  g.y = y;
+  g.ldy = ldy;
+  g.residual = residual;
+  g.status = m->status();
+  return tq::launch_qgemm(m->cfg.wtype, g, s);
+}
+
+// The layers for T >= 2 token rows with every projection as a GEMM over all
+// rows (each weight unit read once per 32 rows), each phase's input turned
+// into the fragment table by one xprep launch.  Prefill (pos == nullptr): the
+// K/V of all rows are appended first, then each row attends over its causal
+// prefix.  Batched decode: row b is sequence b at positions[b]; QK-norm, RoPE
+// and the append happen inside the fused attention.
+cudaError_t run_layers_gemm(tq_model* m, int T, const int32_t* pos, const int32_t* kv_len, int pos_base,
+                            int seq_fixed, const int32_t* block_table, cudaStream_t s) {
   const tq_config& c = m->cfg;
   const int hd = c.head_dim, nq = c.n_heads, nkv = c.n_kv_heads, G = nq / nkv;
+  const bool prefill = pos == nullptr;
   cudaError_t e;
-  auto prep = [&](const float* x, const float* up, int K, const float* gain) {
-    tq::XPrepArgs p{};
-    p.x = x;
-    p.up = up;
-    p.ldx = K;
-    p.gain = gain;
-    p.eps = c.rms_eps;
-    p.K = K;
-    p.T = T;
-    p.xtab = m->xtab();
-    p.xneg = m->xneg();
-    p.inv_s = m->inv_s();
-    return tq::launch_xprep(c.wtype, p, s);
-  };
-  auto gemm = [&](const tq::GemvSeg* seg, int nseg, int K, float* y, int ldy, const float* residual) {
-    tq::QGemmArgs g{};
-    for (int i = 0; i < nseg; ++i) g.seg[i] = seg[i];
-    g.nseg = nseg;
-    g.K = K;
-    g.T = T;
-    g.xtab = m->xtab();
-    g.xneg = m->xneg();
-    g.inv_s = m->inv_s();
-    g.y = y;
-    g.ldy = ldy;
-    g.residual = residual;
-    g.status = m->status();
-    return tq::launch_qgemm(c.wtype, g, s);
-  };
   for (int l = 0; l < c.n_layers; ++l) {
     const tq_layer& ly = m->layers[l];
     const tq::GemvSeg qkv[3] = {seg_of(ly.attn_q, nq * hd), seg_of(ly.attn_k, nkv * hd), seg_of(ly.attn_v, nkv * hd)};
-    if ((e = prep(m->x(), nullptr, c.hidden, ly.attn_norm_dev)) != cudaSuccess) return e;
-    if ((e = gemm(qkv, 3, c.hidden, m->qkv(), qkv_width(c), nullptr)) != cudaSuccess) return e;
-    const tq::RopeArgs r = rope_args(m, l, T, nullptr, nullptr, pos_base, seq_fixed, block_table);
-    if ((e = tq::launch_rope_append(c.kvtype, hd, r, s)) != cudaSuccess) return e;
-    const tq::AttnArgs a = attn_args(m, l, T, nullptr, nullptr, pos_base, seq_fixed, block_table, true);
+    if ((e = gemm_prep(m, T, m->x(), nullptr, c.hidden, ly.attn_norm_dev, s)) != cudaSuccess) return e;
+    if ((e = gemm_run(m, T, qkv, 3, c.hidden, m->qkv(), qkv_width(c), nullptr, s)) != cudaSuccess) return e;
+    if (prefill) {
+      const tq::RopeArgs r = rope_args(m, l, T, pos, kv_len, pos_base, seq_fixed, block_table);
+      if ((e = tq::launch_rope_append(c.kvtype, hd, r, s)) != cudaSuccess) return e;
+    }
+    const tq::AttnArgs a = attn_args(m, l, T, pos, kv_len, pos_base, seq_fixed, block_table, prefill);
     if ((e = tq::launch_attn_decode(c.kvtype, hd, G, a, s)) != cudaSuccess) return e;
     const tq::GemvSeg o = seg_of(ly.attn_output, c.hidden);
-    if ((e = prep(m->att(), nullptr, nq * hd, nullptr)) != cudaSuccess) return e;
-    if ((e = gemm(&o, 1, nq * hd, m->x(), c.hidden, m->x())) != cudaSuccess) return e;
+    if ((e = gemm_prep(m, T, m->att(), nullptr, nq * hd, nullptr, s)) != cudaSuccess) return e;
+    if ((e = gemm_run(m, T, &o, 1, nq * hd, m->x(), c.hidden, m->x(), s)) != cudaSuccess) return e;
     const tq::GemvSeg gate = seg_of(ly.ffn_gate, c.ffn), up = seg_of(ly.ffn_up, c.ffn);
-    if ((e = prep(m->x(), nullptr, c.hidden, ly.ffn_norm_dev)) != cudaSuccess) return e;
-    if ((e = gemm(&gate, 1, c.hidden, m->act(), c.ffn, nullptr)) != cudaSuccess) return e;
-    if ((e = gemm(&up, 1, c.hidden, m->act2(), c.ffn, nullptr)) != cudaSuccess) return e;
+    if ((e = gemm_prep(m, T, m->x(), nullptr, c.hidden, ly.ffn_norm_dev, s)) != cudaSuccess) return e;
+    if ((e = gemm_run(m, T, &gate, 1, c.hidden, m->act(), c.ffn, nullptr, s)) != cudaSuccess) return e;
+    if ((e = gemm_run(m, T, &up, 1, c.hidden, m->act2(), c.ffn, nullptr, s)) != cudaSuccess) return e;
     const tq::GemvSeg down = seg_of(ly.ffn_down, c.hidden);
-    if ((e = prep(m->act(), m->act2(), c.ffn, nullptr)) != cudaSuccess) return e;
-    if ((e = gemm(&down, 1, c.ffn, m->x(), c.hidden, m->x())) != cudaSuccess) return e;
+    if ((e = gemm_prep(m, T, m->act(), m->act2(), c.ffn, nullptr, s)) != cudaSuccess) return e;
+    if ((e = gemm_run(m, T, &down, 1, c.ffn, m->x(), c.hidden, m->x(), s)) != cudaSuccess) return e;
   }
+  return cudaSuccess;
+}
+
+// Greedy head on one row: the one-phase GEMV chain with the argmax epilogue.
+cudaError_t run_head_one(tq_model* m, const float* x, float* logits, int32_t* argmax, cudaStream_t s) {
   tq::GemvChain ch{};
-  ch.ph[0] = head_args(m, m->x() + (size_t)(T - 1) * c.hidden, 1, logits);
+  ch.ph[0] = head_args(m, x, 1, logits);
   ch.mode[0] = tq::GEMV_ARGMAX;
   ch.n = 1;
-  if ((e = tq::launch_gemv_chain(c.wtype, ch, s)) != cudaSuccess) return e;
+  cudaError_t e = tq::launch_gemv_chain(m->cfg.wtype, ch, s);
+  if (e != cudaSuccess) return e;
   return tq::launch_argmax_finish(m->keys(), 1, argmax, s);
+}
+
+// Greedy head on B >= 2 rows: final RMSNorm + LM head as a GEMM into the
+// logits (the caller's, or the workspace's), then a row argmax.
+cudaError_t run_head_gemm(tq_model* m, int B, float* logits, int32_t* argmax, cudaStream_t s) {
+  const tq_config& c = m->cfg;
+  float* lg = logits != nullptr ? logits : m->logits_ws();
+  const tq::GemvSeg h = seg_of(m->head, c.vocab);
+  cudaError_t e = gemm_prep(m, B, m->x(), nullptr, c.hidden, m->out_norm, s);
+  if (e == cudaSuccess) e = gemm_run(m, B, &h, 1, c.hidden, lg, c.vocab, nullptr, s);
+  if (e == cudaSuccess) e = tq::launch_argmax_rows(lg, B, c.vocab, argmax, s);
+  return e;
 }
 
 // The layers and the head.  The GEMVs between two attention launches run as
@@ -476,6 +504,10 @@ cudaError_t enqueue_decode(tq_model* m, int batch, const int32_t* tokens, const 
   cudaError_t e = tq::launch_embed(c.wtype, m->embd.qs_dev, m->embd.d_dev, c.vocab, c.hidden, tokens,
                                    batch, m->x(), m->status(), m->keys(), batch, s);
   if (e != cudaSuccess) return e;
+  if (batch >= 2) {  // batched: weights read once per 32 sequences
+    e = run_layers_gemm(m, batch, positions, kv_lens, 0, -1, block_table, s);
+    return e == cudaSuccess ? run_head_gemm(m, batch, logits, argmax, s) : e;
+  }
   return run_layers(m, batch, positions, kv_lens, 0, -1, block_table, false, m->x(), batch, logits,
                     argmax, s);
 }
@@ -582,10 +614,13 @@ tq_status tq_prefill(tq_model* m, int32_t seq, const int32_t* tokens, int32_t n_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = tq::launch_embed(c.wtype, m->embd.qs_dev, m->embd.d_dev, c.vocab, c.hidden, tokens,
                                    n_tokens, m->x(), m->status(), m->keys(), 1, s);
-  if (e == cudaSuccess)
-    e = n_tokens >= 2 ? run_prefill_gemm(m, n_tokens, start_pos, seq, block_table, logits, argmax, s)
-                      : run_layers(m, n_tokens, nullptr, nullptr, start_pos, seq, block_table, true,
-                                   m->x() + (size_t)(n_tokens - 1) * c.hidden, 1, logits, argmax, s);
+  if (e == cudaSuccess && n_tokens >= 2) {
+    e = run_layers_gemm(m, n_tokens, nullptr, nullptr, start_pos, seq, block_table, s);
+    if (e == cudaSuccess) e = run_head_one(m, m->x() + (size_t)(n_tokens - 1) * c.hidden, logits, argmax, s);
+  } else if (e == cudaSuccess) {
+    e = run_layers(m, n_tokens, nullptr, nullptr, start_pos, seq, block_table, true,
+                   m->x() + (size_t)(n_tokens - 1) * c.hidden, 1, logits, argmax, s);
+  }
   if (e != cudaSuccess) return fail_cuda(m, e, "tq_prefill");
   return TQ_OK;
 }
@@ -676,9 +711,10 @@ tq_status tq_model_status(tq_model* m, void* stream, uint32_t* bits) {
 int tq_model_poisoned(const tq_model* m) { return (m != nullptr && m->poisoned) ? 1 : 0; }
 
 int32_t tq_decode_launches(const tq_model* m, int32_t batch) {
-  (void)batch;
   if (m == nullptr) return 0;
-  return 3 + 2 * m->cfg.n_layers;  // embed, Q/K/V of layer 0, (attention, chain) per layer, argmax
+  // batch 1: embed, Q/K/V of layer 0, (attention, chain) per layer, argmax finish;
+  // batch >= 2: embed, 10 per layer (5 fragment tables, 5 GEMMs with attention), head table + GEMM + argmax
+  return batch >= 2 ? 4 + 10 * m->cfg.n_layers : 3 + 2 * m->cfg.n_layers;
 }
 
 void tq_model_free(tq_model* m) {

@@ -18,6 +18,32 @@ __global__ void argmax_finish_kernel(const unsigned long long* keys, int n, int3
   if (i < n) out[i] = (int32_t)argmax_key_index(keys[i]);
 }
 
+// out[b] = index of the largest of logits[b][0..V), the lowest index on ties
+// (the same 64-bit keys as the GEMV's argmax epilogue).  One CTA per row.
+__global__ void __launch_bounds__(256) argmax_rows_kernel(const float* logits, int V, int32_t* out) {
+  grid_dep_launch();
+  grid_dep_wait();
+  const float* row = logits + (int64_t)blockIdx.x * V;
+  unsigned long long best = 0ull;
+  for (int i = threadIdx.x; i < V; i += 256) {
+    const unsigned long long k = argmax_key(row[i], (uint32_t)i);
+    best = k > best ? k : best;
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+    best = other > best ? other : best;
+  }
+  __shared__ unsigned long long sh[8];
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long m = sh[0];
+    for (int w = 1; w < 8; ++w) m = sh[w] > m ? sh[w] : m;
+    out[blockIdx.x] = (int32_t)argmax_key_index(m);
+  }
+}
+
 // Any K that is a multiple of 256 (whole 16-byte rows of fp16 scales) whose
 // activations and pipeline stages fit in shared memory.
 bool pick_mapping(int K) { return K > 0 && K % 256 == 0 && K <= 12288; }
@@ -42,6 +68,11 @@ cudaError_t launch_gemv(int wtype, int mode, const GemvArgs& a, cudaStream_t s) 
   c.mode[0] = mode;
   c.n = 1;
   return launch_gemv_chain(wtype, c, s);
+}
+
+cudaError_t launch_argmax_rows(const float* logits, int n, int V, int32_t* out, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  return launch_k(argmax_rows_kernel, dim3(n), dim3(256), 0, s, logits, V, out);
 }
 
 cudaError_t launch_argmax_finish(const unsigned long long* keys, int n, int32_t* out, cudaStream_t s) {

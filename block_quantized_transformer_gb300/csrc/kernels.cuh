@@ -188,5 +188,7 @@ void record_error(const char* msg);
 
 // argmax keys -> int32 indices
 cudaError_t launch_argmax_finish(const unsigned long long* keys, int n, int32_t* out, cudaStream_t s);
+// logits [n][V] -> per-row argmax, ties to the lowest index
+cudaError_t launch_argmax_rows(const float* logits, int n, int V, int32_t* out, cudaStream_t s);
 
 }  // namespace tq
