@@ -540,6 +540,390 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
   if (tid == 0) a.counters[th] = 0u;
 }
 
+// ------------------------------------------------- tensor-core decode path --
+//
+// Fused decode over an f16 cache with the products on the tensor cores.  Same
+// split of work, prologue (QK-norm, RoPE, append) and cluster merge as
+// attn_decode_kernel<__half, .., FUSED, kCluster>; per 32-key tile:
+//  * the warp stages K and V with 16-byte cp.async copies into shared memory
+//    whose 16-byte chunks are XOR-swizzled by the key's low three bits, so
+//    ldmatrix reads of eight keys hit eight different banks;
+//  * scores S^T = K Q^T with mma.m16n8k16: A = K rows (exact f16), B = the
+//    query group, every head as an unevaluated sum hi + lo of two fp16 values
+//    after a per-head power-of-two scale (columns 2h, 2h+1), f32 sums;
+//  * online base-2 softmax per head on the score fragments (a thread holds
+//    four keys of one head; three shuffles finish a tile);
+//  * O^T += V^T P^T: A = V read with ldmatrix.trans, B = the probabilities,
+//    again as hi + lo fp16 pairs of p * 2^14, f32 accumulators.
+// Products are exact and sums f32, so the result matches the scalar path to
+// f32 rounding.
+
+template <int HD, int G>
+struct TcSmem {
+  static constexpr int TILE = 32;
+  static constexpr int TILE_BYTES = TILE * HD * 2;       // one K or V tile
+  static constexpr int WARP_BYTES = 2 * TILE_BYTES;
+  static constexpr int OFF_P = 4 * WARP_BYTES;           // [warp][G][32] probabilities
+  static constexpr int OFF_Q = OFF_P + 4 * G * 32 * 4;   // [G][HD] scaled q
+  static constexpr int OFF_QS = OFF_Q + G * HD * 4;      // [G] 1 / (q scale)
+  static constexpr int OFF_M = OFF_QS + ((G * 4 + 15) / 16) * 16;
+  static constexpr int OFF_L = OFF_M + 4 * G * 4;
+  static constexpr int OFF_O = OFF_L + 4 * G * 4;
+  static constexpr int OFF_RES = OFF_O + 4 * G * HD * 4;
+  static constexpr int BYTES = OFF_RES + (2 * G + G * HD) * 4;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// all but the most recent group of this thread's copies have landed
+__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+               "{%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// hi = x with its low 13 mantissa bits cleared (exact in fp16 for |x| >= 2^-14),
+// lo = fp16(x - hi); packs (hi or lo of a, of b) into an fp16 pair.
+__device__ __forceinline__ uint32_t split_pair(float a, float b, bool lo_part) {
+  const float ha = __uint_as_float(__float_as_uint(a) & 0xFFFFE000u);
+  const float hb = __uint_as_float(__float_as_uint(b) & 0xFFFFE000u);
+  const __half2 v = lo_part ? __floats2half2_rn(a - ha, b - hb) : __floats2half2_rn(ha, hb);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int HD, int G>
+__global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
+  using S = TcSmem<HD, G>;
+  constexpr int CL = kCluster;
+  constexpr int DPL = HD / 32;
+  constexpr int TILE = S::TILE;
+  constexpr int NT = G > 4 ? 2 : 1;        // n-tiles of 4 heads (8 columns: hi, lo)
+  constexpr int KS = HD / 16;              // k-steps of the score MMA
+  constexpr int CH = HD / 8;               // 16-byte chunks per key row
+  extern __shared__ __align__(128) uint8_t smem[];
+
+  grid_dep_launch();
+  const int split = blockIdx.x, h = blockIdx.y, t = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int g = lane >> 2, c = lane & 3;
+  const int new_slot = a.kv_len != nullptr ? a.kv_len[t] : a.pos_base + t;
+  int ctx = new_slot + 1;
+  if (ctx > a.cache.max_ctx) ctx = a.cache.max_ctx;
+  const int span = ((ctx + CL * TILE - 1) / (CL * TILE)) * TILE;
+  const int seq = a.seq_fixed >= 0 ? a.seq_fixed : t;
+  const int k0 = split * span;
+  const int k1 = min(ctx, k0 + span);
+  const int n_tiles = k1 > k0 ? (k1 - k0 + TILE - 1) / TILE : 0;
+  const int my_n = warp < n_tiles ? (n_tiles - warp + 3) / 4 : 0;
+
+  uint8_t* kt = smem + warp * S::WARP_BYTES;
+  uint8_t* vt = kt + S::TILE_BYTES;
+  const uint32_t kt_s = smem_addr(kt), vt_s = smem_addr(vt);
+  float* p_s = reinterpret_cast<float*>(smem + S::OFF_P) + warp * G * 32;
+  float* q_s = reinterpret_cast<float*>(smem + S::OFF_Q);
+  float* qs_s = reinterpret_cast<float*>(smem + S::OFF_QS);
+  float* m_s = reinterpret_cast<float*>(smem + S::OFF_M);
+  float* l_s = reinterpret_cast<float*>(smem + S::OFF_L);
+  float* o_s = reinterpret_cast<float*>(smem + S::OFF_O);
+
+  auto tile_key0 = [&](int k) { return k0 + (warp + 4 * k) * TILE; };
+  // stage tile k: cp.async of the valid keys' rows into swizzled chunks, zeros
+  // for the keys past the end (so that p = 0 meets finite V)
+  // stage the K (V) rows of tile k: cp.async of the valid keys' rows into
+  // swizzled chunks, zeros for the keys past the end (so that p = 0 meets
+  // finite V), then one commit group.  A tile's 32 keys are consecutive rows
+  // of one page (pages hold a multiple of 32 keys, tiles start at multiples of 32).
+  auto stage_one = [&](int k, bool is_v) {
+    const int key0 = tile_key0(k);
+    const int nv = min(TILE, k1 - key0);
+    const __half* base = cache_row<__half, HD>(const_cast<void*>(is_v ? a.vc : a.kc), seq, h, key0, a.cache);
+    uint8_t* dst = is_v ? vt : kt;
+    const uint32_t dst_s = is_v ? vt_s : kt_s;
+    for (int i = lane; i < TILE * CH; i += 32) {
+      const int key = i / CH, ch = i % CH;
+      const uint32_t off = (uint32_t)(key * HD * 2 + ((ch ^ (key & 7)) * 16));
+      if (key < nv && base != nullptr)
+        cp_async16(dst_s + off, base + key * HD + ch * 8);
+      else
+        *reinterpret_cast<uint4*>(dst + off) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    cp_async_commit();
+  };
+  auto stage = [&](int k) {
+    stage_one(k, false);
+    stage_one(k, true);
+  };
+  const bool owns_new = my_n > 0 && new_slot >= k0 && new_slot < k1 && ((new_slot - k0) / TILE) % 4 == warp;
+  // the first tile of earlier positions is read-only: staged before waiting
+  if (my_n > 0 && !(owns_new && my_n == 1)) stage(0);
+  const int pos = a.pos[t];
+  const bool rope_ok = pos >= 0 && pos < a.cache.max_ctx;
+  float gq[DPL], gk[DPL], cs[DPL], sn[DPL];
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) {
+    const int i = (lane * DPL + d) % (HD / 2);
+    gq[d] = a.gq[lane * DPL + d];
+    gk[d] = a.gk[lane * DPL + d];
+    cs[d] = rope_ok ? a.cos_t[(int64_t)pos * (HD / 2) + i] : 1.f;
+    sn[d] = rope_ok ? a.sin_t[(int64_t)pos * (HD / 2) + i] : 0.f;
+  }
+  if (!rope_ok && tid == 0) set_status(a.status, TQ_DEV_KV_OVERFLOW);
+  grid_dep_wait();
+
+  // query group: warp w normalises, rotates and scales heads w, w+4 into q_s
+  const float* qrow = a.q + (int64_t)t * a.q_stride;
+  for (int gg = warp; gg < G; gg += 4) {
+    float qr[DPL];
+    const float* qp = qrow + (h * G + gg) * HD + lane * DPL;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) qr[d] = qp[d];
+    norm_rope_head<HD, DPL>(qr, gq, a.eps, cs, sn, lane, rope_ok);
+    float mx = 0.f;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) {
+      qr[d] *= a.scale_log2;
+      mx = fmaxf(mx, fabsf(qr[d]));
+    }
+    mx = warp_max(mx);
+    int e2 = 0;  // scale the head so its largest |q| lies in [2^14, 2^15)
+    if (mx > 0.f && mx <= 3.4e38f) e2 = 14 - (int)((__float_as_uint(mx) >> 23) & 0xffu) + 127;
+    e2 = max(-100, min(100, e2));
+    const float sc = __uint_as_float((uint32_t)(e2 + 127) << 23);
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) q_s[gg * HD + lane * DPL + d] = qr[d] * sc;
+    if (lane == 0) qs_s[gg] = __uint_as_float((uint32_t)(127 - e2) << 23);
+  }
+  if (owns_new) {
+    float kx[DPL], vx[DPL];
+    const float* kp = qrow + (a.nq + h) * HD + lane * DPL;
+    const float* vp = qrow + (a.nq + a.nkv + h) * HD + lane * DPL;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) {
+      kx[d] = kp[d];
+      vx[d] = vp[d];
+    }
+    norm_rope_head<HD, DPL>(kx, gk, a.eps, cs, sn, lane, rope_ok);
+    __half* kd = cache_row<__half, HD>(const_cast<void*>(a.kc), seq, h, new_slot, a.cache);
+    __half* vd = cache_row<__half, HD>(const_cast<void*>(a.vc), seq, h, new_slot, a.cache);
+    if (kd != nullptr && vd != nullptr) {
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) {
+        kd[lane * DPL + d] = __float2half_rn(kx[d]);
+        vd[lane * DPL + d] = __float2half_rn(vx[d]);
+      }
+    } else if (lane == 0) {
+      set_status(a.status, TQ_DEV_KV_OVERFLOW);
+    }
+    __threadfence();  // the new row is read back by this warp's copies
+    __syncwarp();
+    if (my_n == 1) stage(0);
+  }
+  __syncthreads();  // q_s, qs_s
+
+  // B fragments of the query group: column 2j + part of n-tile nt is head 4 nt + j
+  uint32_t qb[NT][KS][2];
+  float inv_q[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hh = nt * 4 + (g >> 1);
+    const bool lo = (g & 1) != 0;
+    inv_q[nt] = (nt * 4 + c) < G ? qs_s[nt * 4 + c] : 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      if (hh < G) {
+        const float* qv = q_s + hh * HD + ks * 16 + 2 * c;
+        qb[nt][ks][0] = split_pair(qv[0], qv[1], lo);
+        qb[nt][ks][1] = split_pair(qv[8], qv[9], lo);
+      } else {
+        qb[nt][ks][0] = qb[nt][ks][1] = 0u;
+      }
+    }
+  }
+
+  float m_run[NT], l_run[NT], o[NT][KS][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m_run[nt] = kNegInf;
+    l_run[nt] = 0.f;
+#pragma unroll
+    for (int md = 0; md < KS; ++md) o[nt][md][0] = o[nt][md][1] = o[nt][md][2] = o[nt][md][3] = 0.f;
+  }
+  // copy groups in flight at the top of iteration k: K(k), V(k)
+  for (int k = 0; k < my_n; ++k) {
+    cp_async_wait_prev();  // K(k)
+    __syncwarp();
+    const int nv = min(TILE, k1 - tile_key0(k));
+    // scores of the tile: two m-tiles of 16 keys
+    float sc[NT][2][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) sc[nt][mt][0] = sc[nt][mt][1] = sc[nt][mt][2] = sc[nt][mt][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int key = mt * 16 + (lane & 15), ch = 2 * ks + (lane >> 4);
+        uint32_t af[4];
+        ldsm_x4(kt_s + key * HD * 2 + ((ch ^ (key & 7)) * 16), af[0], af[1], af[2], af[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_f16(sc[nt][mt], af, qb[nt][ks][0], qb[nt][ks][1]);
+      }
+    }
+    __syncwarp();  // every lane is done with K(k): load K(k+1) behind the rest of this tile
+    if (k + 1 < my_n) stage_one(k + 1, false);
+    else cp_async_commit();
+    // online softmax per head (this thread: head 4 nt + c, keys g, g+8, 16+g, 24+g)
+    float alpha[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float s4[4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        s4[2 * mt] = (mt * 16 + g) < nv ? (sc[nt][mt][0] + sc[nt][mt][1]) * inv_q[nt] : kNegInf;
+        s4[2 * mt + 1] = (mt * 16 + g + 8) < nv ? (sc[nt][mt][2] + sc[nt][mt][3]) * inv_q[nt] : kNegInf;
+      }
+      float mt_ = fmaxf(fmaxf(s4[0], s4[1]), fmaxf(s4[2], s4[3]));
+      mt_ = fmaxf(mt_, __shfl_xor_sync(0xffffffffu, mt_, 4));
+      mt_ = fmaxf(mt_, __shfl_xor_sync(0xffffffffu, mt_, 8));
+      mt_ = fmaxf(mt_, __shfl_xor_sync(0xffffffffu, mt_, 16));
+      const float m_new = fmaxf(m_run[nt], mt_);
+      alpha[nt] = m_run[nt] == kNegInf ? 0.f : exp2f(m_run[nt] - m_new);
+      float ps = 0.f;
+      const int hh = nt * 4 + c;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float p = m_new == kNegInf ? 0.f : exp2f(s4[i] - m_new);
+        ps += p;
+        if (hh < G) p_s[hh * 32 + (i >> 1) * 16 + g + (i & 1) * 8] = p;
+      }
+      ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+      ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+      ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+      l_run[nt] = l_run[nt] * alpha[nt] + ps;
+      m_run[nt] = m_new;
+#pragma unroll
+      for (int md = 0; md < KS; ++md)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) o[nt][md][r] *= alpha[nt];
+    }
+    cp_async_wait_prev();  // V(k)
+    __syncwarp();
+    // O^T += V^T P^T: two k-steps of 16 keys
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int hh = nt * 4 + (g >> 1);
+        const bool lo = (g & 1) != 0;
+        if (hh < G) {
+          const float* pv = p_s + hh * 32 + kk * 16 + 2 * c;
+          pb[nt][0] = split_pair(pv[0] * 16384.f, pv[1] * 16384.f, lo);
+          pb[nt][1] = split_pair(pv[8] * 16384.f, pv[9] * 16384.f, lo);
+        } else {
+          pb[nt][0] = pb[nt][1] = 0u;
+        }
+      }
+#pragma unroll
+      for (int md = 0; md < KS; ++md) {
+        const int mi = lane >> 3;
+        const int key = kk * 16 + (lane & 7) + ((mi >> 1) & 1) * 8, ch = 2 * md + (mi & 1);
+        uint32_t af[4];
+        ldsm_x4_t(vt_s + key * HD * 2 + ((ch ^ (key & 7)) * 16), af[0], af[1], af[2], af[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_f16(o[nt][md], af, pb[nt][0], pb[nt][1]);
+      }
+    }
+    __syncwarp();  // p_s and the V buffer are rewritten next
+    if (k + 1 < my_n) stage_one(k + 1, true);
+    else cp_async_commit();
+  }
+
+  // ---- this warp's (m, l, o) per head into shared memory, then merge as the
+  // scalar path does
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hh = nt * 4 + c;
+    if (hh < G) {
+      if (g == 0) {
+        m_s[warp * G + hh] = m_run[nt];
+        l_s[warp * G + hh] = l_run[nt];
+      }
+#pragma unroll
+      for (int md = 0; md < KS; ++md) {
+        o_s[(warp * G + hh) * HD + md * 16 + g] = (o[nt][md][0] + o[nt][md][1]) * (1.0f / 16384.f);
+        o_s[(warp * G + hh) * HD + md * 16 + g + 8] = (o[nt][md][2] + o[nt][md][3]) * (1.0f / 16384.f);
+      }
+    }
+  }
+  __syncthreads();
+  float* res_m = reinterpret_cast<float*>(smem + S::OFF_RES);
+  float* res_l = res_m + G;
+  float* res_o = res_l + G;
+  for (int i = tid; i < G * HD; i += 128) {
+    const int gg = i / HD, d = i % HD;
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, m_s[w * G + gg]);
+    float acc = 0.f, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float f = M == kNegInf ? 0.f : exp2f(m_s[w * G + gg] - M);
+      acc += f * o_s[(w * G + gg) * HD + d];
+      L += f * l_s[w * G + gg];
+    }
+    res_o[i] = acc;
+    if (d == 0) {
+      res_m[gg] = M;
+      res_l[gg] = L;
+    }
+  }
+  cluster_sync_all();
+  constexpr int SHARE = (G * HD + CL - 1) / CL;
+  for (int i = split * SHARE + tid; i < (split + 1) * SHARE && i < G * HD; i += 128) {
+    const int gg = i / HD;
+    float mr[CL];
+    float M = kNegInf;
+#pragma unroll
+    for (int r = 0; r < CL; ++r) {
+      mr[r] = ld_cluster_f32(map_cluster(res_m + gg, r));
+      M = fmaxf(M, mr[r]);
+    }
+    float acc = 0.f, L = 0.f;
+#pragma unroll
+    for (int r = 0; r < CL; ++r) {
+      const float f = mr[r] == kNegInf ? 0.f : exp2f(mr[r] - M);
+      acc += f * ld_cluster_f32(map_cluster(res_o + i, r));
+      L += f * ld_cluster_f32(map_cluster(res_l + gg, r));
+    }
+    a.o[(int64_t)t * a.nq * HD + (h * G) * HD + i] = acc / L;
+  }
+  cluster_sync_all();  // no CTA leaves while another rank still reads its shared memory
+}
+
+template <int HD, int G>
+cudaError_t attn_tc_t(const AttnArgs& a, cudaStream_t s) {
+  using S = TcSmem<HD, G>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tc_kernel<HD, G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  return launch_cluster(attn_tc_kernel<HD, G>, dim3(kCluster, a.nkv, a.T), dim3(128), S::BYTES, kCluster, s, a);
+}
+
 template <typename KT, int HD>
 cudaError_t rope_t(const RopeArgs& a, cudaStream_t s) {
   dim3 grid((a.nq + a.nkv + 3) / 4, a.T);
@@ -587,6 +971,7 @@ cudaError_t attn_t(const AttnArgs& a, cudaStream_t s) {
 // would not fit in shared memory).
 template <typename KT, int HD, int G>
 cudaError_t attn_g(const AttnArgs& a, cudaStream_t s) {
+  if (sizeof(KT) == 2 && a.fused) return attn_tc_t<HD, G>(a, s);
   if (a.fused || a.split_keys <= 4 * 32 || (sizeof(KT) == 4 && HD == 128)) return attn_t<KT, HD, G, 1>(a, s);
   return attn_t<KT, HD, G, 2>(a, s);
 }
