@@ -37,7 +37,8 @@ QS_BYTES = {TQ_Q4_0: 16, TQ_Q8_0: 32}
 EXPORTS = ("tq_workspace_bytes", "tq_kv_cache_bytes", "tq_model_create", "tq_prefill",
            "tq_decode_step", "tq_decode_step_graph", "tq_model_status", "tq_model_poisoned",
            "tq_decode_launches", "tq_model_free", "tq_last_error", "tq_qmat_bytes", "tq_repack", "tq_quantize",
-           "tq_dequantize", "tq_gemv", "tq_swiglu_gemv", "tq_lm_head", "tq_lm_head_static")
+           "tq_dequantize", "tq_gemv", "tq_gemm_scratch_bytes", "tq_gemm", "tq_swiglu_gemv", "tq_lm_head",
+           "tq_lm_head_static")
 LM_HEAD_STATIC_MAX_BATCH = 4096
 
 
@@ -112,6 +113,8 @@ def lib() -> ctypes.CDLL:
                 "tq_quantize": (i32, [i32, vp, i64, i64, vp, vp]),
                 "tq_dequantize": (i32, [i32, TqQmat, i64, i64, i64, vp, vp]),
                 "tq_gemv": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, vp, vp]),
+                "tq_gemm_scratch_bytes": (ctypes.c_size_t, [i32, i32]),
+                "tq_gemm": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, vp, vp, vp]),
                 "tq_swiglu_gemv": (i32, [i32, TqQmat, TqQmat, i32, i32, vp, i32, vp, f32, vp, vp]),
                 "tq_lm_head": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, f32, vp, vp, vp, vp]),
                 "tq_lm_head_static": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, f32, vp, vp, vp]),
@@ -278,6 +281,26 @@ def tq_gemv(m: QMat, x: torch.Tensor, residual: Optional[torch.Tensor] = None,
                        _dev(residual, "residual", torch.float32, B * m.rows),
                        _dev(out, "y", torch.float32, B * m.rows), _stream())
     _status(rc, "tq_gemv")
+    return out
+
+
+def tq_gemm(m: QMat, x: torch.Tensor, residual: Optional[torch.Tensor] = None,
+            out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """y[t] = residual[t] + W x[t] for x [n_rows][cols] f32: the prefill GEMM."""
+    x2 = x.reshape(-1, m.cols)
+    T = _int("n_rows", x2.shape[0], 1, I32[1])
+    nb = int(lib().tq_gemm_scratch_bytes(T, m.cols))
+    if nb == 0:
+        raise TqError(f"tq_gemm: unsupported shape ({T}, {m.cols})")
+    scratch = torch.empty(nb + 256, dtype=torch.uint8, device=x.device)
+    off = (-scratch.data_ptr()) % 256
+    if out is None:
+        out = torch.empty(T, m.rows, dtype=torch.float32, device=x.device)
+    rc = lib().tq_gemm(m.wtype, m.abi, m.rows, m.cols, _dev(x2, "x", torch.float32, T * m.cols), T,
+                       _dev(residual, "residual", torch.float32, T * m.rows),
+                       _dev(out, "y", torch.float32, T * m.rows),
+                       ctypes.c_void_p(scratch.data_ptr() + off), _stream())
+    _status(rc, "tq_gemm")
     return out
 
 

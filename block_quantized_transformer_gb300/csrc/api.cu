@@ -795,6 +795,70 @@ tq_status tq_gemv(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const fl
   return TQ_OK;
 }
 
+namespace {
+struct GemmScratch {
+  size_t xtab, xneg, inv_s, total;
+};
+GemmScratch gemm_scratch(int32_t n_rows, int32_t cols) {
+  GemmScratch g{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  g.xtab = take((size_t)n_rows * (cols / 32) * 128);
+  g.xneg = take((size_t)n_rows * (cols / 32) * 4);
+  g.inv_s = take((size_t)n_rows * 4);
+  g.total = off;
+  return g;
+}
+}  // namespace
+
+size_t tq_gemm_scratch_bytes(int32_t n_rows, int32_t cols) {
+  if (n_rows < 1 || cols < 256 || cols % 256 != 0 || cols > 12288) return 0;
+  return gemm_scratch(n_rows, cols).total;
+}
+
+tq_status tq_gemm(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const float* x, int32_t n_rows,
+                  const float* residual, float* y, void* scratch, void* stream) {
+  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (rows < 1 || n_rows < 1 || cols < 256 || cols % 256 != 0 || cols > 12288)
+    return set_error("rows, n_rows must be >= 1 and cols a multiple of 256 up to 12288"), TQ_REFUSED;
+  if (!w.qs_dev || !w.d_dev || !x || !y || !scratch) return set_error("pointers must not be NULL"), TQ_REFUSED;
+  if (!aligned16(w.qs_dev) || !aligned16(w.d_dev) || !aligned16(x) || (residual && !aligned16(residual)) ||
+      (reinterpret_cast<uintptr_t>(scratch) & 255u) != 0)
+    return set_error("qs, d, x, residual must be 16-byte and scratch 256-byte aligned"), TQ_REFUSED;
+  const GemmScratch g = gemm_scratch(n_rows, cols);
+  uint8_t* sb = static_cast<uint8_t*>(scratch);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  tq::XPrepArgs p{};
+  p.x = x;
+  p.ldx = cols;
+  p.K = cols;
+  p.T = n_rows;
+  p.xtab = sb + g.xtab;
+  p.xneg = reinterpret_cast<float*>(sb + g.xneg);
+  p.inv_s = reinterpret_cast<float*>(sb + g.inv_s);
+  cudaError_t e = tq::launch_xprep(wtype, p, s);
+  if (e == cudaSuccess) {
+    tq::QGemmArgs q{};
+    q.seg[0] = seg_of(w, rows);
+    q.nseg = 1;
+    q.K = cols;
+    q.T = n_rows;
+    q.xtab = p.xtab;
+    q.xneg = p.xneg;
+    q.inv_s = p.inv_s;
+    q.y = y;
+    q.ldy = rows;
+    q.residual = residual;
+    e = tq::launch_qgemm(wtype, q, s);
+  }
+  if (e != cudaSuccess) return fail_cuda(nullptr, e, "tq_gemm");
+  return TQ_OK;
+}
+
 tq_status tq_swiglu_gemv(int32_t wtype, tq_qmat gate, tq_qmat up, int32_t ffn, int32_t hidden,
                          const float* x, int32_t batch, const float* gain, float eps, float* out,
                          void* stream) {

@@ -227,6 +227,22 @@ TQ_API tq_status tq_dequantize(int32_t wtype, tq_qmat w, int64_t cols, int64_t r
 TQ_API tq_status tq_gemv(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const float* x_dev,
                   int32_t batch, const float* residual_dev, float* y_dev, void* stream);
 
+/* Bytes of scratch tq_gemm needs for n_rows rows of cols inputs (0 when the
+ * sizes are invalid). */
+TQ_API size_t tq_gemm_scratch_bytes(int32_t n_rows, int32_t cols);
+
+/* The prefill GEMM on its own: y[t][r] = (residual ? residual[t][r] : 0) +
+ * sum_c W[r][c] * x[t][c] for t < n_rows, r < rows, each weight unit read once
+ * per 32 rows of x (x, y, residual: f32 row-major with leading dimensions cols
+ * and rows; residual may alias y; all 16-byte aligned).  scratch_dev: at least
+ * tq_gemm_scratch_bytes(n_rows, cols) bytes of device memory, 256-byte aligned,
+ * owned by the caller; the call must not overlap another use of it.  Refused
+ * when cols % 256 != 0 or cols > 12288, a size is < 1 or a pointer NULL or
+ * misaligned. */
+TQ_API tq_status tq_gemm(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const float* x_dev,
+                         int32_t n_rows, const float* residual_dev, float* y_dev, void* scratch_dev,
+                         void* stream);
+
 /* RMSNorm + gate/up projections + SwiGLU on their own ("Всередині LLM ...
  * Qwen3-0.6B на MLX", steps 3 and 6): out[b][i] = silu(g_i) * u_i with
  * g = Wg h, u = Wu h, h = rms_norm(x[b], gain) (gain NULL: h = x[b]).

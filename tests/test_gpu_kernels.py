@@ -95,6 +95,37 @@ def test_gemv_batched_with_residual(batch):
     _gemv_case("q8_0", 200, 1024, batch, True, 12)
 
 
+def _gemm_case(wtype, rows, cols, n, residual, seed):
+    w = synth.host_normal(seed, 1, rows * cols).reshape(rows, cols)
+    blocks = quant.quantize(w, wtype)
+    m = tq.QMat.from_blocks(WT[wtype], torch.from_numpy(blocks).to(DEV), rows, cols)
+    x = synth.host_normal(seed, 2, n * cols, sigma=1.0).reshape(n, cols)
+    x[0, :] *= 1e-3                                   # rows of very different scales
+    r = synth.host_normal(seed, 3, n * rows, sigma=1.0).reshape(n, rows) if residual else None
+    y = tq.tq_gemm(m, torch.from_numpy(x).to(DEV),
+                   residual=None if r is None else torch.from_numpy(r).to(DEV)).cpu().numpy()
+    W = quant.dequantize(blocks, wtype)
+    ref = x.astype(np.float64) @ W.T
+    bound = np.abs(x.astype(np.float64)) @ np.abs(W).T
+    if r is not None:
+        ref = ref + r
+        bound = bound + np.abs(r)
+    err = np.abs(y - ref)
+    assert np.all(err <= 2e-6 * bound + 1e-30), float(np.max(err / bound))
+
+
+@pytest.mark.parametrize("wtype,rows,cols,n", [
+    ("q4_0", 4096 + 5, 4096, 37), ("q4_0", 77, 3072, 33), ("q4_0", 1003, 12288, 5),
+    ("q4_0", 130, 256, 2), ("q8_0", 300, 1024, 64), ("q8_0", 50, 768, 31), ("q8_0", 1, 4096, 3)])
+def test_gemm_matches_oracle(wtype, rows, cols, n):
+    _gemm_case(wtype, rows, cols, n, False, rows + cols + n)
+
+
+def test_gemm_with_residual():
+    _gemm_case("q4_0", 515, 2048, 70, True, 13)
+    _gemm_case("q8_0", 200, 1024, 9, True, 14)
+
+
 @pytest.mark.parametrize("wtype", ["q8_0", "q4_0"])
 def test_lm_head_logits_and_argmax_ties(wtype):
     vocab, hidden = 20011, 1024
