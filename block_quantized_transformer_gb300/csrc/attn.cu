@@ -570,7 +570,9 @@ struct TcSmem {
   static constexpr int OFF_L = OFF_M + 4 * G * 4;
   static constexpr int OFF_O = OFF_L + 4 * G * 4;
   static constexpr int OFF_RES = OFF_O + 4 * G * HD * 4;
-  static constexpr int BYTES = OFF_RES + (2 * G + G * HD) * 4;
+  static constexpr int SHARE = G * HD / kCluster;        // outputs each cluster rank finishes
+  static constexpr int OFF_IN = OFF_RES + (2 * G + G * HD) * 4;  // [rank][SHARE + 2G] pushed to this rank
+  static constexpr int BYTES = OFF_IN + kCluster * (SHARE + 2 * G) * 4;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -617,7 +619,9 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
   const int split = blockIdx.x, h = blockIdx.y, t = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int g = lane >> 2, c = lane & 3;
+  // step inputs, never written by a kernel of the step: load both at once
   const int new_slot = a.kv_len != nullptr ? a.kv_len[t] : a.pos_base + t;
+  const int pos = a.pos[t];
   int ctx = new_slot + 1;
   if (ctx > a.cache.max_ctx) ctx = a.cache.max_ctx;
   const int span = ((ctx + CL * TILE - 1) / (CL * TILE)) * TILE;
@@ -667,7 +671,6 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
   const bool owns_new = my_n > 0 && new_slot >= k0 && new_slot < k1 && ((new_slot - k0) / TILE) % 4 == warp;
   // the first tile of earlier positions is read-only: staged before waiting
   if (my_n > 0 && !(owns_new && my_n == 1)) stage(0);
-  const int pos = a.pos[t];
   const bool rope_ok = pos >= 0 && pos < a.cache.max_ctx;
   float gq[DPL], gk[DPL], cs[DPL], sn[DPL];
 #pragma unroll
@@ -888,27 +891,34 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
       res_l[gg] = L;
     }
   }
+  // push: rank q finishes outputs [q SHARE, (q+1) SHARE); every rank writes
+  // its partial of that range and its (m, l) into rank q's inbox, then one
+  // cluster barrier, then each rank merges from its own shared memory
+  constexpr int SHARE = S::SHARE;
+  constexpr int ROW = SHARE + 2 * G;
+  float* inbox = reinterpret_cast<float*>(smem + S::OFF_IN);
+  __syncthreads();  // res_* complete
+  for (int i = tid; i < CL * ROW; i += 128) {
+    const int q = i / ROW, j = i % ROW;
+    const float v = j < SHARE ? res_o[q * SHARE + j] : j < SHARE + G ? res_m[j - SHARE] : res_l[j - SHARE - G];
+    st_cluster_f32(map_cluster(inbox + split * ROW + j, q), v);
+  }
   cluster_sync_all();
-  constexpr int SHARE = (G * HD + CL - 1) / CL;
-  for (int i = split * SHARE + tid; i < (split + 1) * SHARE && i < G * HD; i += 128) {
-    const int gg = i / HD;
-    float mr[CL];
+  for (int i = tid; i < SHARE; i += 128) {
+    const int o_idx = split * SHARE + i, gg = o_idx / HD;
     float M = kNegInf;
 #pragma unroll
-    for (int r = 0; r < CL; ++r) {
-      mr[r] = ld_cluster_f32(map_cluster(res_m + gg, r));
-      M = fmaxf(M, mr[r]);
-    }
+    for (int r = 0; r < CL; ++r) M = fmaxf(M, inbox[r * ROW + SHARE + gg]);
     float acc = 0.f, L = 0.f;
 #pragma unroll
     for (int r = 0; r < CL; ++r) {
-      const float f = mr[r] == kNegInf ? 0.f : exp2f(mr[r] - M);
-      acc += f * ld_cluster_f32(map_cluster(res_o + i, r));
-      L += f * ld_cluster_f32(map_cluster(res_l + gg, r));
+      const float mr = inbox[r * ROW + SHARE + gg];
+      const float f = mr == kNegInf ? 0.f : exp2f(mr - M);
+      acc += f * inbox[r * ROW + i];
+      L += f * inbox[r * ROW + SHARE + G + gg];
     }
-    a.o[(int64_t)t * a.nq * HD + (h * G) * HD + i] = acc / L;
+    a.o[(int64_t)t * a.nq * HD + (h * G) * HD + o_idx] = acc / L;
   }
-  cluster_sync_all();  // no CTA leaves while another rank still reads its shared memory
 }
 
 template <int HD, int G>
