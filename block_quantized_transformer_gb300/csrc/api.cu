@@ -30,8 +30,12 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+constexpr int64_t kGemmPartFloats = 4 << 20;  // 16 MB of split-K partial sums
+constexpr int kGemmCounters = 4096;
+
 struct Layout {
-  size_t x, qkv, att, act, act2, xtab, xneg, inv_s, logits, cos_t, sin_t, part, counters, keys, status, chain_sync, total;
+  size_t x, qkv, att, act, act2, xtab, xneg, inv_s, logits, cos_t, sin_t, part, counters, keys, status, chain_sync,
+      gemm_part, gemm_ctr, total;
   int T;                 // rows of activation buffers
   int split_dec, splits_dec, split_pf, splits_pf;
 };
@@ -108,6 +112,9 @@ Layout layout_of(const tq_config& c) {
   L.keys = take((size_t)L.T * 8);
   L.status = take(16);
   L.chain_sync = take((tq::kMaxPhases + 1) * 4);
+  // split-K partial sums of the GEMMs over few rows (batched decode)
+  L.gemm_part = L.T > 1 ? take((size_t)kGemmPartFloats * 4) : 0;
+  L.gemm_ctr = L.T > 1 ? take((size_t)kGemmCounters * 4) : 0;
   L.total = off;
   return L;
 }
@@ -169,6 +176,8 @@ struct tq_model {
   unsigned long long* keys() const { return reinterpret_cast<unsigned long long*>(ws + L.keys); }
   uint32_t* status() const { return reinterpret_cast<uint32_t*>(ws + L.status); }
   unsigned* chain_sync() const { return reinterpret_cast<unsigned*>(ws + L.chain_sync); }
+  float* gemm_part() const { return L.T > 1 ? reinterpret_cast<float*>(ws + L.gemm_part) : nullptr; }
+  unsigned* gemm_ctr() const { return L.T > 1 ? reinterpret_cast<unsigned*>(ws + L.gemm_ctr) : nullptr; }
   void* kc_layer(int l) const { return static_cast<uint8_t*>(kc) + (size_t)l * layer_kv_bytes; }
   void* vc_layer(int l) const { return static_cast<uint8_t*>(vc) + (size_t)l * layer_kv_bytes; }
 };
@@ -384,6 +393,10 @@ cudaError_t gemm_run(tq_model* m, int T, const tq::GemvSeg* seg, int nseg, int K
   g.ldy = ldy;
   g.residual = residual;
   g.status = m->status();
+  g.part = m->gemm_part();
+  g.part_cap = kGemmPartFloats;
+  g.counters = m->gemm_ctr();
+  g.n_counters = kGemmCounters;
   return tq::launch_qgemm(m->cfg.wtype, g, s);
 }
 

@@ -115,6 +115,12 @@ struct QGemmArgs {
   int ldy;
   const float* residual;   // [T][ldy] or null; may alias y
   uint32_t* status;
+  // split over K (few token rows): part holds part_cap floats of partial sums,
+  // counters n_counters zeros between launches; null part keeps one split
+  float* part;
+  int64_t part_cap;
+  unsigned* counters;
+  int n_counters;
 };
 cudaError_t launch_xprep(int wtype, const XPrepArgs& a, cudaStream_t s);
 cudaError_t launch_qgemm(int wtype, const QGemmArgs& a, cudaStream_t s);

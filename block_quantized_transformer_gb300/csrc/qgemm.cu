@@ -11,7 +11,9 @@
 // makes the 32 tokens of a CTA one contiguous copy per unit.
 //
 // qgemm_kernel: a CTA takes 8 tiles (128 rows) x 32 tokens and walks the K
-// units; thread 0 streams each unit's 8 weight units, the tokens' fragments and
+// units (with few tokens, a 1/ks share of them: ks CTAs per tile group store
+// partial sums and the last of them to finish adds the ks partials in split
+// order); thread 0 streams each unit's 8 weight units, the tokens' fragments and
 // bias sums into one of two shared-memory stages with 1-D bulk copies (bounded
 // mbarrier waits).  Warp w multiplies tile w by the 32 tokens: per block the A
 // fragment (rows g, g+8) is decoded once and used for the 8 groups of 4 tokens
@@ -211,6 +213,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) qgemm_kernel(const __grid_consta
   const int G = a.K / 256;
   const int tb = blockIdx.x * kTiles, t0 = blockIdx.y * kTok;
   const int ntok = min(kTok, a.T - t0);
+  const int ks = gridDim.z, z = blockIdx.z;
+  const int ub = G * z / ks, ue = G * (z + 1) / ks;  // this CTA's K units
   if (tid == 0) {
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
@@ -221,8 +225,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) qgemm_kernel(const __grid_consta
   // weights are read-only; the fragment table is written by the preceding kernel
   grid_dep_wait();
   if (tid == 0) {
-    issue_stage<WT>(a, m, tb, t0, ntok, 0, G, smem, &full[0]);
-    if (G > 1) issue_stage<WT>(a, m, tb, t0, ntok, 1, G, smem + F::STAGE, &full[1]);
+    issue_stage<WT>(a, m, tb, t0, ntok, ub, G, smem, &full[0]);
+    if (ub + 1 < ue) issue_stage<WT>(a, m, tb, t0, ntok, ub + 1, G, smem + F::STAGE, &full[1]);
   }
   constexpr int NS = WT == TQ_Q4_0 ? 2 : 4;  // 16-byte code loads per row half
   const uint32_t sb = smem_addr(smem);
@@ -231,9 +235,9 @@ __global__ void __launch_bounds__(kThreadsG, 1) qgemm_kernel(const __grid_consta
   for (int q = 0; q < 8; ++q) acc[q][0] = acc[q][1] = 0.f;
   bool failed = false;
   const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int u = 0; u < G; ++u) {
-    const int sidx = u & 1;
-    const bool ok = failed || mbar_wait_bounded(&full[sidx], (uint32_t)((u >> 1) & 1), kWaitLimitG);
+  for (int u = ub; u < ue; ++u) {
+    const int sidx = (u - ub) & 1;
+    const bool ok = failed || mbar_wait_bounded(&full[sidx], (uint32_t)(((u - ub) >> 1) & 1), kWaitLimitG);
     if (!__all_sync(0xffffffffu, ok) && !failed) {
       if (lane == 0) set_status(a.status, TQ_DEV_WAIT_TIMEOUT);
       failed = true;
@@ -285,13 +289,60 @@ __global__ void __launch_bounds__(kThreadsG, 1) qgemm_kernel(const __grid_consta
       }
     }
     __syncthreads();  // every warp is done with this stage
-    if (tid == 0 && u + 2 < G && !failed) issue_stage<WT>(a, m, tb, t0, ntok, u + 2, G, smem + sidx * F::STAGE, &full[sidx]);
+    if (tid == 0 && u + 2 < ue && !failed) issue_stage<WT>(a, m, tb, t0, ntok, u + 2, G, smem + sidx * F::STAGE, &full[sidx]);
   }
   // epilogue: lane (g, c) holds rows g, g+8 of tile tb + warp for tokens t0 + 4q + c
   const int t = tb + warp;
-  if (t < m.T) {
-    const int s = seg_of(m, t);
-    const int rows = a.seg[s].rows;
+  const bool tile_ok = t < m.T;
+  const int s = tile_ok ? seg_of(m, t) : 0;
+  const int rows = a.seg[s].rows;
+  if (ks > 1) {
+    // this split's scaled sums, then the last split CTA of the tile group adds
+    // all of them in split order
+    if (tile_ok) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int tok = t0 + 4 * q + c;
+        if (tok >= a.T) continue;
+        const float is = a.inv_s[tok];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int local = (t - sel3(m.tile0, s)) * kTileRows + g + 8 * h;
+          if (local < rows)
+            a.part[((int64_t)z * a.T + tok) * a.ldy + sel3r(m.row0, s) + local] = acc[q][h] * is;
+        }
+      }
+    }
+    __shared__ int last_split;
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      unsigned* ctr = a.counters + blockIdx.y * gridDim.x + blockIdx.x;
+      last_split = atomicAdd(ctr, 1u) == (unsigned)(ks - 1);
+      if (last_split) {
+        *ctr = 0u;  // zero for the next launch
+        __threadfence();
+      }
+    }
+    __syncthreads();
+    if (!last_split || !tile_ok) return;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int tok = t0 + 4 * q + c;
+      if (tok >= a.T) continue;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int local = (t - sel3(m.tile0, s)) * kTileRows + g + 8 * h;
+        if (local >= rows) continue;
+        const int64_t o = (int64_t)tok * a.ldy + sel3r(m.row0, s) + local;
+        float v = 0.f;
+        for (int zz = 0; zz < ks; ++zz) v += __ldcg(a.part + (int64_t)zz * a.T * a.ldy + o);
+        a.y[o] = a.residual != nullptr ? a.residual[o] + v : v;
+      }
+    }
+    return;
+  }
+  if (tile_ok) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int tok = t0 + 4 * q + c;
@@ -320,8 +371,29 @@ cudaError_t launch_qgemm_t(const QGemmArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = kNumSMs;
+  }
   const TileMap m = tile_map(a);
-  dim3 grid((m.T + kTiles - 1) / kTiles, (a.T + kTok - 1) / kTok);
+  dim3 grid((m.T + kTiles - 1) / kTiles, (a.T + kTok - 1) / kTok, 1);
+  // Few tokens leave most SMs idle: split K so that waves x units per split
+  // (plus a small cost per split for the partial sums) is least.  One CTA per SM.
+  const int G = a.K / 256, base = (int)(grid.x * grid.y);
+  if (a.part != nullptr && a.counters != nullptr && base <= a.n_counters && base < 2 * sms) {
+    double best = 1e30;
+    for (int k = 1; k <= 16 && k <= G; ++k) {
+      if (k > 1 && (int64_t)k * a.T * a.ldy > a.part_cap) break;
+      const double cost = (double)((base * k + sms - 1) / sms) * ((G + k - 1) / k) + (k > 1 ? 0.1 * k : 0.0);
+      if (cost < best) {
+        best = cost;
+        grid.z = k;
+      }
+    }
+  }
   return launch_k(qgemm_kernel<WT>, grid, dim3(kThreadsG), F::SMEM, s, a);
 }
 

@@ -79,3 +79,11 @@ def test_batched_decode_paged_ragged():
 def test_batched_decode_paged_f16_q4_0():
     w = dataclasses.replace(synth.TINY, wtype="q4_0", kv="f16")
     _batched_case(w, [33, 7], steps=8, page_size=32, n_pages=5, seed=3)
+
+
+def test_batched_decode_split_k_projections():
+    # hidden 1024 / ffn 3072: every projection has 4-12 K units and few CTAs
+    # at 4 rows, so the GEMMs split K across CTAs and add the partial sums
+    w = dataclasses.replace(synth.TINY, name="split_k_q4_0", hidden=1024, ffn=3072, n_heads=8,
+                            n_kv_heads=4, head_dim=128, wtype="q4_0", kv="f16")
+    _batched_case(w, [9, 4, 17, 12], steps=4, page_size=32, n_pages=9, seed=5)
