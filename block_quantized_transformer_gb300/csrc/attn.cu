@@ -558,7 +558,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
 // Products are exact and sums f32, so the result matches the scalar path to
 // f32 rounding.
 
-template <int HD, int G>
+template <int HD, int G, int CL>
 struct TcSmem {
   static constexpr int TILE = 32;
   static constexpr int TILE_BYTES = TILE * HD * 2;       // one K or V tile
@@ -570,9 +570,9 @@ struct TcSmem {
   static constexpr int OFF_L = OFF_M + 4 * G * 4;
   static constexpr int OFF_O = OFF_L + 4 * G * 4;
   static constexpr int OFF_RES = OFF_O + 4 * G * HD * 4;
-  static constexpr int SHARE = G * HD / kCluster;        // outputs each cluster rank finishes
+  static constexpr int SHARE = G * HD / CL;              // outputs each cluster rank finishes
   static constexpr int OFF_IN = OFF_RES + (2 * G + G * HD) * 4;  // [rank][SHARE + 2G] pushed to this rank
-  static constexpr int BYTES = OFF_IN + kCluster * (SHARE + 2 * G) * 4;
+  static constexpr int BYTES = OFF_IN + CL * (SHARE + 2 * G) * 4;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -604,10 +604,9 @@ __device__ __forceinline__ uint32_t split_pair(float a, float b, bool lo_part) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int HD, int G>
+template <int HD, int G, int CL>
 __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
-  using S = TcSmem<HD, G>;
-  constexpr int CL = kCluster;
+  using S = TcSmem<HD, G, CL>;
   constexpr int DPL = HD / 32;
   constexpr int TILE = S::TILE;
   constexpr int NT = G > 4 ? 2 : 1;        // n-tiles of 4 heads (8 columns: hi, lo)
@@ -921,17 +920,28 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
   }
 }
 
-template <int HD, int G>
-cudaError_t attn_tc_t(const AttnArgs& a, cudaStream_t s) {
-  using S = TcSmem<HD, G>;
+template <int HD, int G, int CL>
+cudaError_t attn_tc_cl(const AttnArgs& a, cudaStream_t s) {
+  using S = TcSmem<HD, G, CL>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_tc_kernel<HD, G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, G, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         S::BYTES);
+    if (e == cudaSuccess && CL > 8)
+      e = cudaFuncSetAttribute(attn_tc_kernel<HD, G, CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_cluster(attn_tc_kernel<HD, G>, dim3(kCluster, a.nkv, a.T), dim3(128), S::BYTES, kCluster, s, a);
+  return launch_cluster(attn_tc_kernel<HD, G, CL>, dim3(CL, a.nkv, a.T), dim3(128), S::BYTES, CL, s, a);
+}
+
+// One token: 16 CTAs per KV head share its context (parallelism for one
+// sequence).  Several tokens (batched decode): 4 CTAs per (token, KV head),
+// so every warp has several tiles to pipeline and the launch still has
+// thousands of CTAs.
+template <int HD, int G>
+cudaError_t attn_tc_t(const AttnArgs& a, cudaStream_t s) {
+  return a.T == 1 ? attn_tc_cl<HD, G, kCluster>(a, s) : attn_tc_cl<HD, G, 4>(a, s);
 }
 
 template <typename KT, int HD>
