@@ -604,7 +604,13 @@ __device__ __forceinline__ uint32_t split_pair(float a, float b, bool lo_part) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int HD, int G, int CL>
+// FUSED (decode): q, k, v come unnormalised from the projection; QK-norm,
+// RoPE and the append of the new row happen here, and the rows of earlier
+// positions are staged before waiting for the projection.  Not FUSED
+// (prefill): the append kernel already normalised and rotated q and stored
+// every row's K/V, so nothing is staged before the wait; rows are taken
+// longest prefix first.
+template <int HD, int G, int CL, bool FUSED>
 __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
   using S = TcSmem<HD, G, CL>;
   constexpr int DPL = HD / 32;
@@ -615,12 +621,12 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
 
   grid_dep_launch();
-  const int split = blockIdx.x, h = blockIdx.y, t = blockIdx.z;
+  const int split = blockIdx.x, h = blockIdx.y, t = FUSED ? blockIdx.z : gridDim.z - 1 - blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int g = lane >> 2, c = lane & 3;
   // step inputs, never written by a kernel of the step: load both at once
   const int new_slot = a.kv_len != nullptr ? a.kv_len[t] : a.pos_base + t;
-  const int pos = a.pos[t];
+  const int pos = FUSED ? a.pos[t] : 0;
   int ctx = new_slot + 1;
   if (ctx > a.cache.max_ctx) ctx = a.cache.max_ctx;
   const int span = ((ctx + CL * TILE - 1) / (CL * TILE)) * TILE;
@@ -667,21 +673,23 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
     stage_one(k, false);
     stage_one(k, true);
   };
-  const bool owns_new = my_n > 0 && new_slot >= k0 && new_slot < k1 && ((new_slot - k0) / TILE) % 4 == warp;
-  // the first tile of earlier positions is read-only: staged before waiting
-  if (my_n > 0 && !(owns_new && my_n == 1)) stage(0);
+  const bool owns_new =
+      FUSED && my_n > 0 && new_slot >= k0 && new_slot < k1 && ((new_slot - k0) / TILE) % 4 == warp;
+  // decode: the first tile of earlier positions is read-only: staged before waiting
+  if (FUSED && my_n > 0 && !(owns_new && my_n == 1)) stage(0);
   const bool rope_ok = pos >= 0 && pos < a.cache.max_ctx;
   float gq[DPL], gk[DPL], cs[DPL], sn[DPL];
 #pragma unroll
   for (int d = 0; d < DPL; ++d) {
     const int i = (lane * DPL + d) % (HD / 2);
-    gq[d] = a.gq[lane * DPL + d];
-    gk[d] = a.gk[lane * DPL + d];
-    cs[d] = rope_ok ? a.cos_t[(int64_t)pos * (HD / 2) + i] : 1.f;
-    sn[d] = rope_ok ? a.sin_t[(int64_t)pos * (HD / 2) + i] : 0.f;
+    gq[d] = FUSED ? a.gq[lane * DPL + d] : 1.f;
+    gk[d] = FUSED ? a.gk[lane * DPL + d] : 1.f;
+    cs[d] = FUSED && rope_ok ? a.cos_t[(int64_t)pos * (HD / 2) + i] : 1.f;
+    sn[d] = FUSED && rope_ok ? a.sin_t[(int64_t)pos * (HD / 2) + i] : 0.f;
   }
-  if (!rope_ok && tid == 0) set_status(a.status, TQ_DEV_KV_OVERFLOW);
+  if (FUSED && !rope_ok && tid == 0) set_status(a.status, TQ_DEV_KV_OVERFLOW);
   grid_dep_wait();
+  if (!FUSED && my_n > 0) stage(0);  // prefill: the rows were written by the preceding kernel
 
   // query group: warp w normalises, rotates and scales heads w, w+4 into q_s
   const float* qrow = a.q + (int64_t)t * a.q_stride;
@@ -690,7 +698,7 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
     const float* qp = qrow + (h * G + gg) * HD + lane * DPL;
 #pragma unroll
     for (int d = 0; d < DPL; ++d) qr[d] = qp[d];
-    norm_rope_head<HD, DPL>(qr, gq, a.eps, cs, sn, lane, rope_ok);
+    if (FUSED) norm_rope_head<HD, DPL>(qr, gq, a.eps, cs, sn, lane, rope_ok);
     float mx = 0.f;
 #pragma unroll
     for (int d = 0; d < DPL; ++d) {
@@ -920,19 +928,19 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
   }
 }
 
-template <int HD, int G, int CL>
+template <int HD, int G, int CL, bool FUSED>
 cudaError_t attn_tc_cl(const AttnArgs& a, cudaStream_t s) {
   using S = TcSmem<HD, G, CL>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, G, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         S::BYTES);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, G, CL, FUSED>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
     if (e == cudaSuccess && CL > 8)
-      e = cudaFuncSetAttribute(attn_tc_kernel<HD, G, CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      e = cudaFuncSetAttribute(attn_tc_kernel<HD, G, CL, FUSED>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_cluster(attn_tc_kernel<HD, G, CL>, dim3(CL, a.nkv, a.T), dim3(128), S::BYTES, CL, s, a);
+  return launch_cluster(attn_tc_kernel<HD, G, CL, FUSED>, dim3(CL, a.nkv, a.T), dim3(128), S::BYTES, CL, s, a);
 }
 
 // One token: 16 CTAs per KV head share its context (parallelism for one
@@ -941,7 +949,7 @@ cudaError_t attn_tc_cl(const AttnArgs& a, cudaStream_t s) {
 // thousands of CTAs.
 template <int HD, int G>
 cudaError_t attn_tc_t(const AttnArgs& a, cudaStream_t s) {
-  return a.T == 1 ? attn_tc_cl<HD, G, kCluster>(a, s) : attn_tc_cl<HD, G, 4>(a, s);
+  return a.T == 1 ? attn_tc_cl<HD, G, kCluster, true>(a, s) : attn_tc_cl<HD, G, 4, true>(a, s);
 }
 
 template <typename KT, int HD>
@@ -992,6 +1000,9 @@ cudaError_t attn_t(const AttnArgs& a, cudaStream_t s) {
 template <typename KT, int HD, int G>
 cudaError_t attn_g(const AttnArgs& a, cudaStream_t s) {
   if (sizeof(KT) == 2 && a.fused) return attn_tc_t<HD, G>(a, s);
+  // prefill over an f16 cache: one CTA per (query row, KV head), its whole
+  // causal prefix (rows are many; the K/V of the prompt stay in L2)
+  if (sizeof(KT) == 2) return attn_tc_cl<HD, G, 1, false>(a, s);
   if (a.fused || a.split_keys <= 4 * 32 || (sizeof(KT) == 4 && HD == 128)) return attn_t<KT, HD, G, 1>(a, s);
   return attn_t<KT, HD, G, 2>(a, s);
 }

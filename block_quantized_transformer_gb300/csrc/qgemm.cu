@@ -202,8 +202,10 @@ __device__ __forceinline__ void issue_stage(const QGemmArgs& a, const TileMap& m
   bulk_g2s(st + F::W + F::X, a.xneg + ent, (uint32_t)(ntok * kUnitBlocks * 4), bar);
 }
 
+// Q4_0: two CTAs per SM (128 registers; the two stages fit twice in shared
+// memory), so each scheduler has four warps to hide latency with
 template <int WT>
-__global__ void __launch_bounds__(kThreadsG, 1) qgemm_kernel(const __grid_constant__ QGemmArgs a) {
+__global__ void __launch_bounds__(kThreadsG, WT == TQ_Q4_0 ? 2 : 1) qgemm_kernel(const __grid_constant__ QGemmArgs a) {
   using F = QF<WT>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + 2 * F::STAGE);
@@ -371,17 +373,21 @@ cudaError_t launch_qgemm_t(const QGemmArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  static int sms = 0;
+  static int sms = 0;  // CTA slots: SMs x resident CTAs per SM
   if (sms == 0) {
-    int dev = 0;
+    int dev = 0, per = 1;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = kNumSMs;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, qgemm_kernel<WT>, kThreadsG, F::SMEM) != cudaSuccess ||
+        per < 1)
+      per = 1;
+    sms *= per;
   }
   const TileMap m = tile_map(a);
   dim3 grid((m.T + kTiles - 1) / kTiles, (a.T + kTok - 1) / kTok, 1);
   // Few tokens leave most SMs idle: split K so that waves x units per split
-  // (plus a small cost per split for the partial sums) is least.  One CTA per SM.
+  // (plus a small cost per split for the partial sums) is least.
   const int G = a.K / 256, base = (int)(grid.x * grid.y);
   if (a.part != nullptr && a.counters != nullptr && base <= a.n_counters && base < 2 * sms) {
     double best = 1e30;
