@@ -453,7 +453,7 @@ def run_gpu_batched(args, rank, world, w):
     ctx_sum = float((lens + W + 1).sum()) + B * (K - 1) / 2.0
     step_bytes = weight_bytes + kv_row * ctx_sum + kv_row * B
     hbm, _, peak_kind = peaks()
-    launches = model.launches_per_step * K
+    launches = model.decode_launches(B) * K
     model.close()
     line = {"metric": f"decode tokens/s (B={B}, Q4_0 Qwen3-8B shape, paged f16 KV) and achieved HBM GB/s vs peak",
             "value": round(world * B * K / (ms_max / 1e3), 2), "unit": "tokens/s", "n_gpus": world,

@@ -467,6 +467,10 @@ class Model:
     def launches_per_step(self) -> int:
         return int(lib().tq_decode_launches(self._h(), 1))
 
+    def decode_launches(self, batch: int) -> int:
+        """Kernel launches of one decode step of `batch` sequences."""
+        return int(lib().tq_decode_launches(self._h(), batch))
+
     def prefill(self, tokens: torch.Tensor, start_pos: int = 0, seq: int = 0,
                 block_table: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
                 argmax: Optional[torch.Tensor] = None) -> torch.Tensor:

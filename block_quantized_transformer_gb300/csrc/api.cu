@@ -100,7 +100,7 @@ Layout layout_of(const tq_config& c) {
   L.act = take((size_t)L.T * c.ffn * 4);
   // prefill GEMM: up-projection rows and the fragment table of the widest input
   const int kmax = std::max(c.hidden, std::max(c.n_heads * c.head_dim, c.ffn));
-  L.act2 = take((size_t)L.T * c.ffn * 4);
+  L.act2 = take((size_t)L.T * 2 * c.ffn * 4);  // GEMM path: rows of [gate | up]
   L.xtab = take((size_t)L.T * (kmax / 32) * 128);
   L.xneg = take((size_t)L.T * (kmax / 32) * 4);
   L.inv_s = take((size_t)L.T * 4);
@@ -364,11 +364,12 @@ tq::AttnArgs attn_args(const tq_model* m, int l, int T, const int32_t* pos, cons
   return a;
 }
 
-cudaError_t gemm_prep(tq_model* m, int T, const float* x, const float* up, int K, const float* gain, cudaStream_t s) {
+cudaError_t gemm_prep(tq_model* m, int T, const float* x, const float* up, int K, const float* gain, cudaStream_t s,
+                      int ldx = 0) {
   tq::XPrepArgs p{};
   p.x = x;
   p.up = up;
-  p.ldx = K;
+  p.ldx = ldx > 0 ? ldx : K;
   p.gain = gain;
   p.eps = m->cfg.rms_eps;
   p.K = K;
@@ -428,10 +429,11 @@ cudaError_t run_layers_gemm(tq_model* m, int T, const int32_t* pos, const int32_
     if ((e = gemm_run(m, T, &o, 1, nq * hd, m->x(), c.hidden, m->x(), s)) != cudaSuccess) return e;
     const tq::GemvSeg gate = seg_of(ly.ffn_gate, c.ffn), up = seg_of(ly.ffn_up, c.ffn);
     if ((e = gemm_prep(m, T, m->x(), nullptr, c.hidden, ly.ffn_norm_dev, s)) != cudaSuccess) return e;
-    if ((e = gemm_run(m, T, &gate, 1, c.hidden, m->act(), c.ffn, nullptr, s)) != cudaSuccess) return e;
-    if ((e = gemm_run(m, T, &up, 1, c.hidden, m->act2(), c.ffn, nullptr, s)) != cudaSuccess) return e;
+    // gate and up in one GEMM: row t of act2 holds [gate | up]
+    const tq::GemvSeg gu[2] = {gate, up};
+    if ((e = gemm_run(m, T, gu, 2, c.hidden, m->act2(), 2 * c.ffn, nullptr, s)) != cudaSuccess) return e;
     const tq::GemvSeg down = seg_of(ly.ffn_down, c.hidden);
-    if ((e = gemm_prep(m, T, m->act(), m->act2(), c.ffn, nullptr, s)) != cudaSuccess) return e;
+    if ((e = gemm_prep(m, T, m->act2(), m->act2() + c.ffn, c.ffn, nullptr, s, 2 * c.ffn)) != cudaSuccess) return e;
     if ((e = gemm_run(m, T, &down, 1, c.ffn, m->x(), c.hidden, m->x(), s)) != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -726,8 +728,8 @@ int tq_model_poisoned(const tq_model* m) { return (m != nullptr && m->poisoned) 
 int32_t tq_decode_launches(const tq_model* m, int32_t batch) {
   if (m == nullptr) return 0;
   // batch 1: embed, Q/K/V of layer 0, (attention, chain) per layer, argmax finish;
-  // batch >= 2: embed, 10 per layer (5 fragment tables, 5 GEMMs with attention), head table + GEMM + argmax
-  return batch >= 2 ? 4 + 10 * m->cfg.n_layers : 3 + 2 * m->cfg.n_layers;
+  // batch >= 2: embed, 9 per layer (4 fragment tables, 4 GEMMs, attention), head table + GEMM + argmax
+  return batch >= 2 ? 4 + 9 * m->cfg.n_layers : 3 + 2 * m->cfg.n_layers;
 }
 
 void tq_model_free(tq_model* m) {
