@@ -180,9 +180,12 @@ __device__ __forceinline__ int seg_of(const TileMap& m, int t) {
 __device__ __forceinline__ int sel3(const int (&v)[4], int s) { return s == 0 ? v[0] : s == 1 ? v[1] : v[2]; }
 __device__ __forceinline__ int sel3r(const int (&v)[3], int s) { return s == 0 ? v[0] : s == 1 ? v[1] : v[2]; }
 
+// Stage of K unit u: the weight units of the CTA's tiles (read-only: may be
+// issued before the preceding kernel is done) and the tokens' fragments and
+// bias sums; issue_weights arms the stage's barrier for both parts.
 template <int WT>
-__device__ __forceinline__ void issue_stage(const QGemmArgs& a, const TileMap& m, int tb, int t0, int ntok, int u,
-                                            int G, uint8_t* st, uint64_t* bar) {
+__device__ __forceinline__ void issue_weights(const QGemmArgs& a, const TileMap& m, int tb, int ntok, int u, int G,
+                                              uint8_t* st, uint64_t* bar) {
   using F = QF<WT>;
   uint32_t bytes = (uint32_t)(ntok * kUnitBlocks * (128 + 4));
   int nt = 0;
@@ -197,9 +200,21 @@ __device__ __forceinline__ void issue_stage(const QGemmArgs& a, const TileMap& m
     bulk_g2s(st + i * F::QU, gs.qs + off * F::QU, F::QU, bar);
     bulk_g2s(st + kTiles * F::QU + i * kUnitD, reinterpret_cast<const uint8_t*>(gs.d) + off * kUnitD, kUnitD, bar);
   }
+}
+
+template <int WT>
+__device__ __forceinline__ void issue_x(const QGemmArgs& a, int t0, int ntok, int u, uint8_t* st, uint64_t* bar) {
+  using F = QF<WT>;
   const int64_t ent = ((int64_t)u * a.T + t0) * kUnitBlocks;
   bulk_g2s(st + F::W, a.xtab + ent * 128, (uint32_t)(ntok * kUnitBlocks * 128), bar);
   bulk_g2s(st + F::W + F::X, a.xneg + ent, (uint32_t)(ntok * kUnitBlocks * 4), bar);
+}
+
+template <int WT>
+__device__ __forceinline__ void issue_stage(const QGemmArgs& a, const TileMap& m, int tb, int t0, int ntok, int u,
+                                            int G, uint8_t* st, uint64_t* bar) {
+  issue_weights<WT>(a, m, tb, ntok, u, G, st, bar);
+  issue_x<WT>(a, t0, ntok, u, st, bar);
 }
 
 // Q4_0: two CTAs per SM (128 registers; the two stages fit twice in shared
@@ -224,11 +239,16 @@ __global__ void __launch_bounds__(kThreadsG, WT == TQ_Q4_0 ? 2 : 1) qgemm_kernel
   }
   __syncthreads();
   grid_dep_launch();
-  // weights are read-only; the fragment table is written by the preceding kernel
+  // weights are read-only: the first two stages' units load while the
+  // preceding kernel writes the fragment table
+  if (tid == 0) {
+    issue_weights<WT>(a, m, tb, ntok, ub, G, smem, &full[0]);
+    if (ub + 1 < ue) issue_weights<WT>(a, m, tb, ntok, ub + 1, G, smem + F::STAGE, &full[1]);
+  }
   grid_dep_wait();
   if (tid == 0) {
-    issue_stage<WT>(a, m, tb, t0, ntok, ub, G, smem, &full[0]);
-    if (ub + 1 < ue) issue_stage<WT>(a, m, tb, t0, ntok, ub + 1, G, smem + F::STAGE, &full[1]);
+    issue_x<WT>(a, t0, ntok, ub, smem, &full[0]);
+    if (ub + 1 < ue) issue_x<WT>(a, t0, ntok, ub + 1, smem + F::STAGE, &full[1]);
   }
   constexpr int NS = WT == TQ_Q4_0 ? 2 : 4;  // 16-byte code loads per row half
   const uint32_t sb = smem_addr(smem);
