@@ -427,7 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
     fence_proxy_async();
   }
   __syncthreads();
-  grid_dep_launch();
+  // A chain's CTAs meet at grid-wide counters, so every CTA must be resident
+  // before a later kernel may take an SM: with several phases the dependent
+  // launch is released only after the first counter is full (every CTA is
+  // running); a single GEMV releases it at once.
+  if (ch.n == 1) grid_dep_launch();
 
   if (warp >= kW) {
     // ---------------------------------------------------------------- producer
@@ -508,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
           }
           if (it > 32) __nanosleep(64);
         }
+        if (p == 1) grid_dep_launch();
       }
       consumer_sync();
     }
@@ -717,29 +722,26 @@ cudaError_t launch_chain(const GemvChain& c, cudaStream_t s) {
     return launch_k(gemv_chain_kernel<WT>, dim3(q.Cp), dim3(kThreads), L.bytes, s, c, depth, max_k);
   }
   // several phases: every CTA must be resident at once (grid-wide counters).
-  // With programmatic dependent launch too when the driver takes the pair:
-  // the CTAs then start (and fetch weights) while the previous kernel drains.
-  static int coop_pdl = 1;
+  // The grid is one CTA per SM (a CTA fits an SM), the CTAs start as the
+  // previous kernel's CTAs exit, and the kernel releases its dependent launch
+  // only when all of them are running.
+  // Without programmatic dependent launch (TQ_PDL=0) a cooperative launch.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = L.bytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = (coop_pdl && pdl_enabled()) ? 2 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_chain_kernel<WT>, c, depth, max_k);
-  if (e != cudaSuccess && cfg.numAttrs == 2) {
-    (void)cudaGetLastError();
-    coop_pdl = 0;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gemv_chain_kernel<WT>, c, depth, max_k);
+  cudaLaunchAttribute attr[1];
+  if (pdl_enabled()) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
   }
-  return e;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_chain_kernel<WT>, c, depth, max_k);
 }
 
 }  // namespace gemv
