@@ -87,3 +87,10 @@ def test_batched_decode_split_k_projections():
     w = dataclasses.replace(synth.TINY, name="split_k_q4_0", hidden=1024, ffn=3072, n_heads=8,
                             n_kv_heads=4, head_dim=128, wtype="q4_0", kv="f16")
     _batched_case(w, [9, 4, 17, 12], steps=4, page_size=32, n_pages=9, seed=5)
+
+
+def test_batched_decode_split_k_q8_0():
+    # the split-K GEMM of the Q8_0 kernel (one CTA per SM), contiguous f32 cache
+    w = dataclasses.replace(synth.TINY, name="split_k_q8_0", hidden=1024, ffn=3072, n_heads=8,
+                            n_kv_heads=4, head_dim=128, wtype="q8_0", kv="f32")
+    _batched_case(w, [6, 15, 3], steps=3)

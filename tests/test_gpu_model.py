@@ -131,3 +131,13 @@ def test_qwen3_0p6b_q8_0_full_workload():
 def test_qwen3_0p6b_q4_0_long_context():
     w = synth.QWEN3_0P6B_Q4_LONG
     run_case(w, w.prompt_len, 64)
+
+
+def test_gqa_group_sizes_f16_cache():
+    # the tensor-core attention (decode, and prefill in its non-fused mode) for
+    # groups of 1, 8 and 4 query heads per KV head, head_dim 64
+    import dataclasses
+    for nq, nkv in [(4, 4), (8, 1), (8, 2)]:
+        w = dataclasses.replace(synth.TINY, name=f"tiny_f16_g{nq // nkv}", n_heads=nq, n_kv_heads=nkv,
+                                hidden=512, kv="f16")
+        run_case(w, 11, 5)
