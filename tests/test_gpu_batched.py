@@ -94,3 +94,9 @@ def test_batched_decode_split_k_q8_0():
     w = dataclasses.replace(synth.TINY, name="split_k_q8_0", hidden=1024, ffn=3072, n_heads=8,
                             n_kv_heads=4, head_dim=128, wtype="q8_0", kv="f32")
     _batched_case(w, [6, 15, 3], steps=3)
+
+
+def test_batched_decode_paged_f16_group_of_8():
+    # 4-CTA tensor-core attention clusters with two n-tiles (8 query heads per KV head)
+    w = dataclasses.replace(synth.TINY, name="batched_g8", hidden=512, n_heads=8, n_kv_heads=1, kv="f16")
+    _batched_case(w, [18, 41, 7], steps=5, page_size=32, n_pages=7, seed=11)

@@ -141,3 +141,18 @@ def test_gqa_group_sizes_f16_cache():
         w = dataclasses.replace(synth.TINY, name=f"tiny_f16_g{nq // nkv}", n_heads=nq, n_kv_heads=nkv,
                                 hidden=512, kv="f16")
         run_case(w, 11, 5)
+
+
+def test_prefill_in_chunks_equals_one_shot_f16_cache():
+    # the tensor-core prefill attention continues from a nonzero position
+    import dataclasses
+    w = dataclasses.replace(synth.TINY, name="tiny_f16_chunks", kv="f16")
+    prompt = torch.tensor(w.prompt(n=40), dtype=torch.int32, device=DEV)
+    a = build_model(w, device=DEV, max_ctx=64, max_prefill=40)
+    la = torch.empty(w.vocab, device=DEV)
+    a.prefill(prompt, logits=la)
+    b = build_model(w, device=DEV, max_ctx=64, max_prefill=40)
+    lb = torch.empty(w.vocab, device=DEV)
+    b.prefill(prompt[:17], logits=lb)
+    b.prefill(prompt[17:], start_pos=17, logits=lb)
+    assert torch.allclose(la, lb, rtol=0, atol=1e-4 * float(la.max() - la.min()))
