@@ -19,7 +19,7 @@ reordering beyond the definitions:
   ("last(x)") feeds the head
 * greedy sampling and the prefill-then-decode loop ... same page, steps 8-9
 
-Readings where the pages leave a step open (listed in the design doc): the mask is
+Readings where the pages leave a step open: the mask is
 "key position <= query position" (adding -1e9 above the diagonal gives
 exactly the same softmax in f64); an f16 KV cache rounds K (after QK-norm and
 RoPE) and V to f16 when they are stored; argmax ties go to the lowest index.

@@ -11,7 +11,7 @@ neither block format.  The workload descriptions define both:
   magnitude taken with its sign; 4-bit q = clamp(round(w / d) + 8, 0, 15);
   value d * (q - 8).
 
-Readings where the definition is open (each one is listed in the design doc):
+Readings where the definition is open:
 
 * d is computed in f32, w / d is an f32 division by that f32 d, and the
   stored scale is fp16(d) rounded to nearest even.

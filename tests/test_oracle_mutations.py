@@ -97,3 +97,64 @@ def test_planted_unsigned_q4_extreme_is_caught(monkeypatch):
     monkeypatch.setattr(quant, "quantize_q4_0", unsigned)
     with pytest.raises(AssertionError):
         pins.test_hand_worked_block("q4_0_block.txt", "q4_0")
+
+
+def test_planted_embed_off_by_one_row_is_caught(monkeypatch):
+    real = om.OracleModel.embed
+
+    def shifted(self, tokens):
+        t = (np.asarray(tokens, dtype=np.int64) + 1) % self.w.vocab   # planted: next row
+        return real(self, t)
+    monkeypatch.setattr(om.OracleModel, "embed", shifted)
+    for wtype in ("q8_0", "q4_0"):
+        with pytest.raises(AssertionError):
+            pins.test_embed_gathers_the_token_rows(wtype)
+
+
+def _attn_block_variant(round_k_before_rope=False, round_q=False):
+    """The oracle's attention block with one planted change to where the f16
+    cache rounds."""
+    def attn_block(self, i, h, cache, positions):
+        w = self.w
+        p = f"blk.{i}"
+        T = h.shape[0]
+        q = self.linear(h, f"{p}.attn_q").reshape(T, w.n_heads, w.head_dim).transpose(1, 0, 2)
+        k = self.linear(h, f"{p}.attn_k").reshape(T, w.n_kv_heads, w.head_dim).transpose(1, 0, 2)
+        v = self.linear(h, f"{p}.attn_v").reshape(T, w.n_kv_heads, w.head_dim).transpose(1, 0, 2)
+        q = om.rms_norm(q, self.gain(f"{p}.attn_q_norm"), w.rms_eps)
+        k = om.rms_norm(k, self.gain(f"{p}.attn_k_norm"), w.rms_eps)
+        if round_k_before_rope:
+            k = self.store_kv(k)
+        q = om.rope(q, positions, w.rope_theta)
+        k = om.rope(k, positions, w.rope_theta)
+        if round_q:
+            q = self.store_kv(q)
+        if not round_k_before_rope:
+            k = self.store_kv(k)
+        v = self.store_kv(v)
+        if cache[i] is not None:
+            ck, cv = cache[i]
+            k = np.concatenate([ck, k], axis=1)
+            v = np.concatenate([cv, v], axis=1)
+        cache[i] = (k, v)
+        o = om.attention(q, k, v, positions)
+        o = o.transpose(1, 0, 2).reshape(T, w.n_heads * w.head_dim)
+        return self.linear(o, f"{p}.attn_output")
+    return attn_block
+
+
+def test_unplanted_variant_passes_the_store_pin(monkeypatch):
+    monkeypatch.setattr(om.OracleModel, "attn_block", _attn_block_variant())
+    pins.test_f16_kv_store_point_matches_torch_recomposition()
+
+
+def test_planted_rounding_before_rope_is_caught(monkeypatch):
+    monkeypatch.setattr(om.OracleModel, "attn_block", _attn_block_variant(round_k_before_rope=True))
+    with pytest.raises(AssertionError):
+        pins.test_f16_kv_store_point_matches_torch_recomposition()
+
+
+def test_planted_rounding_of_q_is_caught(monkeypatch):
+    monkeypatch.setattr(om.OracleModel, "attn_block", _attn_block_variant(round_q=True))
+    with pytest.raises(AssertionError):
+        pins.test_f16_kv_store_point_matches_torch_recomposition()

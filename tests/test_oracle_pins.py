@@ -286,3 +286,89 @@ def test_model_matches_torch_library_composition():
     xl = F.rms_norm(x[-1], (w.hidden,), weight=g("output_norm"), eps=w.rms_eps)
     ref = (xl @ W("token_embd").T).numpy()
     assert np.allclose(m.forward_nocache(prompt), ref, rtol=1e-11, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- embedding, KV store
+
+def _decode_row_by_hand(raw_row: np.ndarray, wtype: str) -> list:
+    """One row of GGUF-order blocks decoded byte by byte in plain Python,
+    independently of oracle.quant: fp16 scale, then int8 codes (Q8_0) or
+    nibble pairs, low nibble = element j, high nibble = element j + 16 (Q4_0)."""
+    import struct
+    out = []
+    for blk in raw_row:
+        b = bytes(int(v) for v in blk)
+        d = struct.unpack("<e", b[:2])[0]
+        if wtype == "q8_0":
+            out += [d * struct.unpack("<b", b[2 + j:3 + j])[0] for j in range(32)]
+        else:
+            lo = [(b[2 + j] & 15) - 8 for j in range(16)]
+            hi = [(b[2 + j] >> 4) - 8 for j in range(16)]
+            out += [d * q for q in lo + hi]
+    return out
+
+
+@pytest.mark.parametrize("wtype", ["q8_0", "q4_0"])
+def test_embed_gathers_the_token_rows(wtype):
+    """embed(t) is row t of token_embd, decoded: checked against a byte-by-byte
+    decode of that row and against the generator's f32 row t (within one
+    quantization step: half a step of rounding, the fp16 rounding of the scale,
+    and Q4_0's clamp of +8 steps to +7), which rows t - 1 and t + 1 are not."""
+    w = synth.Workload("pin_embed", vocab=300, hidden=64, n_layers=1, n_heads=2, n_kv_heads=1,
+                       head_dim=32, ffn=64, wtype=wtype, kv="f32", seed=4)
+    m = om.OracleModel(w, om.synth_weights(w))
+    tokens = [0, 1, 299, 150, 150, 7]
+    x = m.embed(tokens)
+    assert x.shape == (len(tokens), w.hidden)
+    f32 = synth.host_tensor(w, "token_embd").astype(np.float64)
+    raw = m.weights["token_embd"]
+    for i, t in enumerate(tokens):
+        assert x[i].tolist() == _decode_row_by_hand(raw[t], wtype), (i, t)
+        err = np.abs(x[i] - f32[t]).reshape(-1, 32).max(axis=1)
+        step = np.abs(f32[t]).reshape(-1, 32).max(axis=1) / (127.0 if wtype == "q8_0" else 8.0)
+        assert np.all(err <= 1.01 * step), (t, err / step)
+        for nb in (t - 1, t + 1):
+            if 0 <= nb < w.vocab:
+                assert np.abs(x[i] - f32[nb]).max() > 4 * step.max()
+
+
+def test_f16_kv_store_point_matches_torch_recomposition():
+    """With an f16 cache, K is rounded to f16 after QK-RMSNorm and RoPE, V after
+    its projection, and q is not rounded.  Recomposed with torch (f64
+    F.rms_norm, rotation as a complex multiply, Tensor.half) from the oracle's
+    decoded weights: the cache holds exactly the recomposed K/V, and the
+    layer's attention output equals SDPA over unrounded q and rounded K/V."""
+    w, m = _tiny("f16")
+    prompt = list(w.prompt(n=6))
+    T, hd, half = len(prompt), w.head_dim, w.head_dim // 2
+    x = m.embed(prompt)
+    p = "blk.0"
+    h = om.rms_norm(x, m.gain(f"{p}.attn_norm"), w.rms_eps)
+    cache = m.new_cache()
+    out = m.attn_block(0, h, cache, np.arange(T))
+
+    def W(n):
+        return torch.from_numpy(m.matrix(n))
+
+    th = torch.from_numpy(h)
+    ang = torch.from_numpy(om.rope_angles(np.arange(T), hd, w.rope_theta))
+    turn = torch.polar(torch.ones_like(ang), ang)                      # e^{i angle}
+
+    def rot(t):
+        z = torch.complex(t[..., :half], t[..., half:]) * turn
+        return torch.cat([z.real, z.imag], -1)
+
+    q = (th @ W(f"{p}.attn_q").T).view(T, w.n_heads, hd).transpose(0, 1)
+    k = (th @ W(f"{p}.attn_k").T).view(T, w.n_kv_heads, hd).transpose(0, 1)
+    v = (th @ W(f"{p}.attn_v").T).view(T, w.n_kv_heads, hd).transpose(0, 1)
+    gq = torch.from_numpy(m.gain(f"{p}.attn_q_norm"))
+    gk = torch.from_numpy(m.gain(f"{p}.attn_k_norm"))
+    q = rot(F.rms_norm(q, (hd,), weight=gq, eps=w.rms_eps))
+    k16 = rot(F.rms_norm(k, (hd,), weight=gk, eps=w.rms_eps)).half().double()
+    v16 = v.half().double()
+    ck, cv = cache[0]
+    assert np.array_equal(ck, k16.numpy()) and np.array_equal(cv, v16.numpy())
+    o = F.scaled_dot_product_attention(q, k16.repeat_interleave(w.group, 0),
+                                       v16.repeat_interleave(w.group, 0), is_causal=True)
+    ref = (o.transpose(0, 1).reshape(T, -1) @ W(f"{p}.attn_output").T).numpy()
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-13)
