@@ -35,7 +35,8 @@ BLOCK_BYTES = {TQ_Q4_0: 18, TQ_Q8_0: 34}
 QS_BYTES = {TQ_Q4_0: 16, TQ_Q8_0: 32}
 
 EXPORTS = ("tq_workspace_bytes", "tq_kv_cache_bytes", "tq_model_create", "tq_prefill",
-           "tq_decode_step", "tq_decode_step_graph", "tq_model_status", "tq_model_poisoned",
+           "tq_decode_step", "tq_decode_step_graph", "tq_model_status", "tq_model_set_wait_limit",
+           "tq_model_poisoned",
            "tq_decode_launches", "tq_model_free", "tq_last_error", "tq_qmat_bytes", "tq_repack", "tq_quantize",
            "tq_dequantize", "tq_gemv", "tq_gemm_scratch_bytes", "tq_gemm", "tq_swiglu_gemv", "tq_lm_head",
            "tq_lm_head_static")
@@ -103,6 +104,7 @@ def lib() -> ctypes.CDLL:
                 "tq_decode_step": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
                 "tq_decode_step_graph": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
                 "tq_model_status": (i32, [vp, vp, ctypes.POINTER(ctypes.c_uint32)]),
+                "tq_model_set_wait_limit": (i32, [vp, ctypes.c_uint32]),
                 "tq_model_poisoned": (ctypes.c_int, [vp]),
                 "tq_decode_launches": (i32, [vp, i32]),
                 "tq_model_free": (None, [vp]),
@@ -151,6 +153,10 @@ def _dev(t: Optional[torch.Tensor], name: str, dtype=None, min_numel: int = 0):
         return None
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TqError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        # the library works on the current device: another GPU's memory would fault
+        raise TqError(f"{name} is on {t.device}, but the current device is "
+                      f"cuda:{torch.cuda.current_device()}")
     if not t.is_contiguous():
         raise TqError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -386,6 +392,11 @@ class Model:
         self.cfg = TqConfig(rms_eps=float(rms_eps), rope_theta=float(rope_theta), wtype=wt,
                             kvtype=kvt, **vals)
         self.device = torch.device(device)
+        if self.device.type != "cuda" or (self.device.index is not None and
+                                          self.device.index != torch.cuda.current_device()):
+            raise TqError(f"the model's device {self.device} must be the current CUDA device "
+                          f"(cuda:{torch.cuda.current_device()})")
+        self.device = torch.device("cuda", torch.cuda.current_device())
         ws = tq_workspace_bytes(self.cfg)
         if ws == 0:
             raise TqError(f"invalid configuration: {tq_last_error()}")
@@ -500,6 +511,12 @@ class Model:
                 _dev(argmax, "argmax", torch.int32, B), _stream(self.device))
         self._after(rc, "tq_decode_step_graph" if graph else "tq_decode_step")
         return argmax
+
+    def set_wait_limit(self, polls: int) -> None:
+        """Polls after which a GEMV chain's grid-wide waits give up (0: the
+        default); a tiny limit exercises the timeout path (tq_model_set_wait_limit)."""
+        _int("polls", polls, 0, 2**32 - 1)
+        self._after(lib().tq_model_set_wait_limit(self._h(), polls), "tq_model_set_wait_limit")
 
     def status(self) -> int:
         bits = ctypes.c_uint32(0)

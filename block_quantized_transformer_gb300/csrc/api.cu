@@ -152,6 +152,7 @@ struct tq_model {
   size_t layer_kv_bytes;
   bool poisoned = false;
   std::string poison_reason;
+  unsigned chain_wait_limit = 0;  // polls of a chain's grid-wide waits (0: the kernel's default)
   // decode-step graph
   cudaGraphExec_t gexec = nullptr;
   struct {
@@ -507,6 +508,7 @@ cudaError_t run_layers(tq_model* m, int T, const int32_t* pos, const int32_t* kv
     }
     ch.n = 4;
     ch.sync = m->chain_sync();
+    ch.sync_limit = m->chain_wait_limit;
     if ((e = tq::launch_gemv_chain(c.wtype, ch, s)) != cudaSuccess) return e;
   }
   return tq::launch_argmax_finish(m->keys(), head_B, argmax, s);
@@ -720,6 +722,16 @@ tq_status tq_model_status(tq_model* m, void* stream, uint32_t* bits) {
     m->poison_reason = g_last_error;
     return TQ_INTERNAL;
   }
+  return TQ_OK;
+}
+
+tq_status tq_model_set_wait_limit(tq_model* m, uint32_t polls) {
+  if (refuse_if_poisoned(m)) return TQ_REFUSED;
+  if (m->chain_wait_limit != polls && m->gexec != nullptr) {  // a captured step keeps the old value
+    cudaGraphExecDestroy(m->gexec);
+    m->gexec = nullptr;
+  }
+  m->chain_wait_limit = polls;
   return TQ_OK;
 }
 

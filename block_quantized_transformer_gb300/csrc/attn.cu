@@ -931,15 +931,15 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
 template <int HD, int G, int CL, bool FUSED>
 cudaError_t attn_tc_cl(const AttnArgs& a, cudaStream_t s) {
   using S = TcSmem<HD, G, CL>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, G, CL, FUSED>,
+  static PerDevice setup;
+  cudaError_t e = per_device(setup, nullptr, [](int, int&) {
+    cudaError_t r = cudaFuncSetAttribute(attn_tc_kernel<HD, G, CL, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
-    if (e == cudaSuccess && CL > 8)
-      e = cudaFuncSetAttribute(attn_tc_kernel<HD, G, CL, FUSED>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+    if (r == cudaSuccess && CL > 8)
+      r = cudaFuncSetAttribute(attn_tc_kernel<HD, G, CL, FUSED>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return r;
+  });
+  if (e != cudaSuccess) return e;
   return launch_cluster(attn_tc_kernel<HD, G, CL, FUSED>, dim3(CL, a.nkv, a.T), dim3(128), S::BYTES, CL, s, a);
 }
 
@@ -961,8 +961,8 @@ cudaError_t rope_t(const RopeArgs& a, cudaStream_t s) {
 template <typename KT, int HD, int G, int NS>
 cudaError_t attn_configure() {
   using S = AttnSmem<KT, HD, G, NS>;
-  static bool configured = false;
-  if (!configured) {
+  static PerDevice setup;
+  return per_device(setup, nullptr, [](int, int&) {
     cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<KT, HD, G, NS, false, 0>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
     if (e == cudaSuccess)
@@ -971,10 +971,8 @@ cudaError_t attn_configure() {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_decode_kernel<KT, HD, G, NS, true, kCluster>,
                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  return cudaSuccess;
+    return e;
+  });
 }
 
 template <typename KT, int HD, int G, int NS>

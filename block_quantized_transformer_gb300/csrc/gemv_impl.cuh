@@ -503,9 +503,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
       grid_dep_wait();
     } else {
       if (tid == 0 && !*abort_flag) {
+        const uint32_t limit = ch.sync_limit != 0u ? ch.sync_limit : kSyncLimit;
         uint32_t it = 0;
         while (ld_acquire(ch.sync + (p - 1)) < (unsigned)C) {
-          if (++it > kSyncLimit) {
+          if (++it > limit) {
             set_status(status, TQ_DEV_WAIT_TIMEOUT);
             *abort_flag = 1;
             break;
@@ -700,17 +701,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
 template <int WT>
 cudaError_t launch_chain(const GemvChain& c, cudaStream_t s) {
   using F = Fmt<WT>;
-  static int sms = 0;
-  if (sms == 0) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_chain_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static PerDevice setup;
+  int sms = 0;
+  cudaError_t e = per_device(setup, &sms, [](int dev, int& n) {
+    cudaError_t r = cudaFuncSetAttribute(gemv_chain_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemMax);
-    if (e != cudaSuccess) return e;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = kNumSMs;
-    if (sms > kMaxGrid) sms = kMaxGrid;
-  }
+    if (r != cudaSuccess) return r;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = kNumSMs;
+    if (n > kMaxGrid) n = kMaxGrid;
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   int max_k = 0;
   for (int p = 0; p < c.n; ++p) max_k = c.ph[p].K > max_k ? c.ph[p].K : max_k;
   int depth = 8;

@@ -82,6 +82,7 @@ struct GemvChain {
   int mode[kMaxPhases];
   int n;
   unsigned* sync;
+  unsigned sync_limit;   // polls before a wait between phases gives up (0: the default)
 };
 
 // Returns cudaErrorInvalidValue when K has no supported thread mapping.

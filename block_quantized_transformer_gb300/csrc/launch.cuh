@@ -6,7 +6,42 @@
 #include <cuda_runtime.h>
 #include <stdlib.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace tq {
+
+// One-time set-up of a kernel per device (its shared-memory attribute, the
+// device's SM count ...), done for the device current at the call and kept
+// for that device; safe when several threads launch at once.
+constexpr int kMaxDevices = 64;
+struct PerDevice {
+  std::atomic<int> ready[kMaxDevices];
+  int value[kMaxDevices];
+  std::mutex mu;
+};
+
+// Runs setup(dev, value) once per device; *out (if not null) receives the
+// value it stored.
+template <typename F>
+cudaError_t per_device(PerDevice& pd, int* out, F&& setup) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!pd.ready[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(pd.mu);
+    if (!pd.ready[dev].load(std::memory_order_relaxed)) {
+      int v = 0;
+      e = setup(dev, v);
+      if (e != cudaSuccess) return e;
+      pd.value[dev] = v;
+      pd.ready[dev].store(1, std::memory_order_release);
+    }
+  }
+  if (out != nullptr) *out = pd.value[dev];
+  return cudaSuccess;
+}
 
 inline bool pdl_enabled() {
   // TQ_PDL=0 turns programmatic dependent launch off (for A/B timing)

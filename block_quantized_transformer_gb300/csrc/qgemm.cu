@@ -387,23 +387,20 @@ __global__ void __launch_bounds__(kThreadsG, WT == TQ_Q4_0 ? 2 : 1) qgemm_kernel
 template <int WT>
 cudaError_t launch_qgemm_t(const QGemmArgs& a, cudaStream_t s) {
   using F = QF<WT>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(qgemm_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, F::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  static int sms = 0;  // CTA slots: SMs x resident CTAs per SM
-  if (sms == 0) {
-    int dev = 0, per = 1;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = kNumSMs;
+  static PerDevice setup;
+  int sms = 0;  // CTA slots: SMs x resident CTAs per SM
+  cudaError_t e = per_device(setup, &sms, [](int dev, int& n) {
+    cudaError_t r = cudaFuncSetAttribute(qgemm_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, F::SMEM);
+    if (r != cudaSuccess) return r;
+    int per = 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = kNumSMs;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, qgemm_kernel<WT>, kThreadsG, F::SMEM) != cudaSuccess ||
         per < 1)
       per = 1;
-    sms *= per;
-  }
+    n *= per;
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   const TileMap m = tile_map(a);
   dim3 grid((m.T + kTiles - 1) / kTiles, (a.T + kTok - 1) / kTok, 1);
   // Few tokens leave most SMs idle: split K so that waves x units per split

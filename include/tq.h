@@ -179,6 +179,19 @@ TQ_API tq_status tq_decode_step_graph(tq_model* m, int32_t batch, const int32_t*
  * *status_bits.  A non-zero word poisons the model and returns TQ_INTERNAL. */
 TQ_API tq_status tq_model_status(tq_model* m, void* stream, uint32_t* status_bits);
 
+/* Polls after which each grid-wide wait between the phases of the decode
+ * GEMV chains gives up (0 restores the default of 2^24 polls, far longer than
+ * any step).  A wait that gives up sets TQ_DEV_WAIT_TIMEOUT in the status
+ * word, and the launch runs on without waiting (no wait is left unbounded
+ * and every bulk copy it issued lands before it exits), so its results are
+ * meaningless; tq_model_status() then reports the bit and poisons the model.
+ * For tests of that failure path: a limit of one or two polls is shorter than
+ * the CTAs of a chain take to meet.  Applies to steps enqueued afterwards (a
+ * captured decode graph is dropped and re-captured).  The tessl_torch README,
+ * "Handle ownership, closing and errors", sets the rule that a failed wait
+ * poisons the handle rather than hanging. */
+TQ_API tq_status tq_model_set_wait_limit(tq_model* m, uint32_t polls);
+
 /* 1 if the model is poisoned (a CUDA error or a device status bit was seen). */
 TQ_API int tq_model_poisoned(const tq_model* m);
 
@@ -274,7 +287,9 @@ TQ_API tq_status tq_lm_head(int32_t wtype, tq_qmat w, int32_t vocab, int32_t hid
  * array is shared by all calls and keeps the last call's contents; each call
  * clears the rows it uses.  Calls whose GPU work overlaps race on the array:
  * serialize them.  The first call on a device looks the array up with that
- * device current; make it before any stream capture.  Nothing is allocated
+ * device current; make it before any stream capture.  The looked-up address is
+ * kept for the life of the process: after cudaDeviceReset() on that device it
+ * is stale, so do not call this entry point on a device that was reset.  Nothing is allocated
  * (no cudaMalloc/cudaFree, no allocating library routine).  Other arguments
  * and results are those of tq_lm_head(). */
 TQ_API tq_status tq_lm_head_static(int32_t wtype, tq_qmat w, int32_t vocab, int32_t hidden,

@@ -129,8 +129,10 @@ def test_qwen3_0p6b_q8_0_full_workload():
 
 
 def test_qwen3_0p6b_q4_0_long_context():
+    # the whole workload: 4096-token prompt, then all 256 decode steps
     w = synth.QWEN3_0P6B_Q4_LONG
-    run_case(w, w.prompt_len, 64)
+    errs = run_case(w, w.prompt_len, w.decode_steps)
+    print(f"0.6B Q4_0 long context: max rel logit err {max(errs):.3e} over {len(errs)} steps")
 
 
 def test_gqa_group_sizes_f16_cache():
@@ -156,3 +158,23 @@ def test_prefill_in_chunks_equals_one_shot_f16_cache():
     b.prefill(prompt[:17], logits=lb)
     b.prefill(prompt[17:], start_pos=17, logits=lb)
     assert torch.allclose(la, lb, rtol=0, atol=1e-4 * float(la.max() - la.min()))
+
+
+def test_chain_wait_timeout_sets_status_poisons_and_context_stays_usable():
+    # A one-poll limit on the grid-wide waits between chain phases is shorter
+    # than the chain's CTAs take to meet: a wait gives up, sets the status bit
+    # and the launch runs on; the model is poisoned, the context is not.
+    import block_quantized_transformer_gb300 as tq
+    w = synth.TINY
+    m = build_model(w, device=DEV, max_ctx=64)
+    m.set_wait_limit(1)
+    tok = torch.tensor([3], dtype=torch.int32, device=DEV)
+    for s in range(12):
+        p = torch.tensor([s], dtype=torch.int32, device=DEV)
+        m.decode_step(tok, p, p)
+    with pytest.raises(tq.TqPoisoned, match="device wait timed out"):
+        m.status()
+    with pytest.raises(tq.TqError, match="closed"):
+        m.decode_step(tok, p, p)
+    torch.cuda.synchronize()
+    run_case(w, w.prompt_len, 4)          # a fresh model on the same device is exact again
