@@ -34,7 +34,7 @@ constexpr int64_t kGemmPartFloats = 4 << 20;  // 16 MB of split-K partial sums
 constexpr int kGemmCounters = 4096;
 
 struct Layout {
-  size_t x, qkv, att, act, act2, xtab, xneg, inv_s, logits, cos_t, sin_t, part, counters, keys, status, chain_sync,
+  size_t x, qkv, att, act, act2, x16, inv_s, logits, cos_t, sin_t, part, counters, keys, status, chain_sync,
       gemm_part, gemm_ctr, total;
   int T;                 // rows of activation buffers
   int split_dec, splits_dec, split_pf, splits_pf;
@@ -98,11 +98,11 @@ Layout layout_of(const tq_config& c) {
   L.qkv = take((size_t)L.T * qkv_width(c) * 4);
   L.att = take((size_t)L.T * c.n_heads * c.head_dim * 4);
   L.act = take((size_t)L.T * c.ffn * 4);
-  // prefill GEMM: up-projection rows and the fragment table of the widest input
+  // GEMM path (prefill, batched decode): rows of [gate | up], and the fp16
+  // rows of the widest GEMM input with their scales
   const int kmax = std::max(c.hidden, std::max(c.n_heads * c.head_dim, c.ffn));
-  L.act2 = take((size_t)L.T * 2 * c.ffn * 4);  // GEMM path: rows of [gate | up]
-  L.xtab = take((size_t)L.T * (kmax / 32) * 128);
-  L.xneg = take((size_t)L.T * (kmax / 32) * 4);
+  L.act2 = take((size_t)L.T * 2 * c.ffn * 4);
+  L.x16 = take((size_t)L.T * kmax * 2);
   L.inv_s = take((size_t)L.T * 4);
   L.logits = c.max_batch > 1 ? take((size_t)c.max_batch * c.vocab * 4) : 0;
   L.cos_t = take((size_t)c.max_ctx * (c.head_dim / 2) * 4);
@@ -166,8 +166,7 @@ struct tq_model {
   float* att() const { return reinterpret_cast<float*>(ws + L.att); }
   float* act() const { return reinterpret_cast<float*>(ws + L.act); }
   float* act2() const { return reinterpret_cast<float*>(ws + L.act2); }
-  uint8_t* xtab() const { return ws + L.xtab; }
-  float* xneg() const { return reinterpret_cast<float*>(ws + L.xneg); }
+  __half* x16() const { return reinterpret_cast<__half*>(ws + L.x16); }
   float* inv_s() const { return reinterpret_cast<float*>(ws + L.inv_s); }
   float* logits_ws() const { return reinterpret_cast<float*>(ws + L.logits); }
   float* cos_t() const { return reinterpret_cast<float*>(ws + L.cos_t); }
@@ -367,7 +366,7 @@ tq::AttnArgs attn_args(const tq_model* m, int l, int T, const int32_t* pos, cons
 
 cudaError_t gemm_prep(tq_model* m, int T, const float* x, const float* up, int K, const float* gain, cudaStream_t s,
                       int ldx = 0) {
-  tq::XPrepArgs p{};
+  tq::XPrep16Args p{};
   p.x = x;
   p.up = up;
   p.ldx = ldx > 0 ? ldx : K;
@@ -375,21 +374,19 @@ cudaError_t gemm_prep(tq_model* m, int T, const float* x, const float* up, int K
   p.eps = m->cfg.rms_eps;
   p.K = K;
   p.T = T;
-  p.xtab = m->xtab();
-  p.xneg = m->xneg();
+  p.x16 = m->x16();
   p.inv_s = m->inv_s();
-  return tq::launch_xprep(m->cfg.wtype, p, s);
+  return tq::launch_xprep16(p, s);
 }
 
 cudaError_t gemm_run(tq_model* m, int T, const tq::GemvSeg* seg, int nseg, int K, float* y, int ldy,
                      const float* residual, cudaStream_t s) {
-  tq::QGemmArgs g{};
+  tq::TcGemmArgs g{};
   for (int i = 0; i < nseg; ++i) g.seg[i] = seg[i];
   g.nseg = nseg;
   g.K = K;
   g.T = T;
-  g.xtab = m->xtab();
-  g.xneg = m->xneg();
+  g.x16 = m->x16();
   g.inv_s = m->inv_s();
   g.y = y;
   g.ldy = ldy;
@@ -399,12 +396,12 @@ cudaError_t gemm_run(tq_model* m, int T, const tq::GemvSeg* seg, int nseg, int K
   g.part_cap = kGemmPartFloats;
   g.counters = m->gemm_ctr();
   g.n_counters = kGemmCounters;
-  return tq::launch_qgemm(m->cfg.wtype, g, s);
+  return tq::launch_tcgemm(m->cfg.wtype, g, s);
 }
 
-// The layers for T >= 2 token rows with every projection as a GEMM over all
-// rows (each weight unit read once per 32 rows), each phase's input turned
-// into the fragment table by one xprep launch.  Prefill (pos == nullptr): the
+// The layers for T >= 2 token rows with every projection as a tensor-core
+// GEMM over all rows (each weight tile decoded once per CTA of up to 256
+// rows), each phase's input turned into fp16 rows by one xprep16 launch.  Prefill (pos == nullptr): the
 // K/V of all rows are appended first, then each row attends over its causal
 // prefix.  Batched decode: row b is sequence b at positions[b]; QK-norm, RoPE
 // and the append happen inside the fused attention.
@@ -824,7 +821,7 @@ tq_status tq_gemv(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const fl
 
 namespace {
 struct GemmScratch {
-  size_t xtab, xneg, inv_s, total;
+  size_t x16, inv_s, total;
 };
 GemmScratch gemm_scratch(int32_t n_rows, int32_t cols) {
   GemmScratch g{};
@@ -834,8 +831,7 @@ GemmScratch gemm_scratch(int32_t n_rows, int32_t cols) {
     off = align_up(off + bytes, 256);
     return o;
   };
-  g.xtab = take((size_t)n_rows * (cols / 32) * 128);
-  g.xneg = take((size_t)n_rows * (cols / 32) * 4);
+  g.x16 = take((size_t)n_rows * cols * 2);
   g.inv_s = take((size_t)n_rows * 4);
   g.total = off;
   return g;
@@ -859,28 +855,26 @@ tq_status tq_gemm(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const fl
   const GemmScratch g = gemm_scratch(n_rows, cols);
   uint8_t* sb = static_cast<uint8_t*>(scratch);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  tq::XPrepArgs p{};
+  tq::XPrep16Args p{};
   p.x = x;
   p.ldx = cols;
   p.K = cols;
   p.T = n_rows;
-  p.xtab = sb + g.xtab;
-  p.xneg = reinterpret_cast<float*>(sb + g.xneg);
+  p.x16 = reinterpret_cast<__half*>(sb + g.x16);
   p.inv_s = reinterpret_cast<float*>(sb + g.inv_s);
-  cudaError_t e = tq::launch_xprep(wtype, p, s);
+  cudaError_t e = tq::launch_xprep16(p, s);
   if (e == cudaSuccess) {
-    tq::QGemmArgs q{};
+    tq::TcGemmArgs q{};
     q.seg[0] = seg_of(w, rows);
     q.nseg = 1;
     q.K = cols;
     q.T = n_rows;
-    q.xtab = p.xtab;
-    q.xneg = p.xneg;
+    q.x16 = p.x16;
     q.inv_s = p.inv_s;
     q.y = y;
     q.ldy = rows;
     q.residual = residual;
-    e = tq::launch_qgemm(wtype, q, s);
+    e = tq::launch_tcgemm(wtype, q, s);
   }
   if (e != cudaSuccess) return fail_cuda(nullptr, e, "tq_gemm");
   return TQ_OK;

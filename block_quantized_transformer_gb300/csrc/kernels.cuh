@@ -90,41 +90,38 @@ cudaError_t launch_gemv(int wtype, int mode, const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_gemv_chain(int wtype, const GemvChain& c, cudaStream_t s);
 bool gemv_supported(int K);
 
-// ---- prefill GEMM (qgemm.cu)
-// Input rows of a phase -> fragment table (see qgemm.cu): x [T][ldx] f32, up
-// (optional: the input is silu(x) * up), gain (optional RMSNorm gain, eps).
-struct XPrepArgs {
+// ---- tensor-core GEMM for prefill and batched decode (tcgemm.cu)
+// Phase input rows -> fp16 rows after a power-of-two scale per row.
+struct XPrep16Args {
   const float* x;
-  const float* up;
+  const float* up;       // optional: the input is silu(x) * up
   int ldx;
-  const float* gain;
+  const float* gain;     // optional RMSNorm gain
   float eps;
   int K, T;
-  uint8_t* xtab;   // [K/256][T][8][128 B]
-  float* xneg;     // [K/256][T][8]
-  float* inv_s;    // [T]
+  __half* x16;           // [T][K]
+  float* inv_s;          // [T]: 2^-e of row t
 };
-// Y[t][r] (+)= sum_k W[r][k] X[t][k] over the concatenated segments.
-struct QGemmArgs {
+// Y[t][r] (+)= sum_k W[r][k] X[t][k] over the concatenated segments, on tcgen05.
+struct TcGemmArgs {
   GemvSeg seg[3];
   int nseg;
   int K, T;
-  const uint8_t* xtab;
-  const float* xneg;
-  const float* inv_s;
+  const __half* x16;       // [T][K], 16-byte aligned
+  const float* inv_s;      // [T]
   float* y;                // [T][ldy]
   int ldy;
   const float* residual;   // [T][ldy] or null; may alias y
   uint32_t* status;
-  // split over K (few token rows): part holds part_cap floats of partial sums,
-  // counters n_counters zeros between launches; null part keeps one split
+  // split over K (few token rows): part_cap floats of partial sums, n_counters
+  // zero counters between launches; null part keeps one split
   float* part;
   int64_t part_cap;
   unsigned* counters;
   int n_counters;
 };
-cudaError_t launch_xprep(int wtype, const XPrepArgs& a, cudaStream_t s);
-cudaError_t launch_qgemm(int wtype, const QGemmArgs& a, cudaStream_t s);
+cudaError_t launch_xprep16(const XPrep16Args& a, cudaStream_t s);
+cudaError_t launch_tcgemm(int wtype, const TcGemmArgs& a, cudaStream_t s);
 
 // ---- attention side (attn.cu)
 struct CacheView {

@@ -1,0 +1,537 @@
+// Tensor-core (tcgen05 / TMEM) GEMM over the tiled Q4_0 / Q8_0 weights, for
+// the projections of prefill and of batched decode, where many token rows
+// share each weight: Y[t][r] = sum_k W[r][k] X[t][k] (+ residual).  The
+// prompt pass of "Всередині LLM: чисте виконання на Python для Qwen3-0.6B на
+// MLX" (steps 3-7 over all positions, step 9: prefill, then one token at a
+// time) is the same set of dense contractions over T rows.
+//
+// Operands.  The weights are decoded to fp16 in shared memory, one rounding
+// of the exact product d * (q - 8) (Q4_0) or d * q (Q8_0); the activation
+// rows are turned into fp16 after a power-of-two scale per row (xprep16),
+// so that the row's largest magnitude lies in [2^14, 2^15); the tensor core
+// multiplies fp16 x fp16 and sums in f32 (TMEM), and the epilogue undoes the
+// row scale exactly.  Each operand is rounded once to 11 significant bits,
+// so an output differs from the exact sum by at most about 2^-10 * sum|x w|.
+//
+// CTA work item: 128 weight rows (8 tiles of 16) x BN token rows over a
+// range of K (the whole K, or a 1/ks share when few CTAs would be busy: the
+// ks partial sums are then added by the last CTA of the group, in split
+// order).  K advances in stages of 128 inputs (half a unit of the tiled
+// layout), NS stages in flight:
+//  - 8 decode warps: read the stage's codes and scales from global memory
+//    (one 16-byte load per lane, 512 contiguous bytes per warp), decode them
+//    to fp16 and store them in the 128-byte swizzled K-major layout (two
+//    64-input atoms of 128 rows);
+//  - warp 8: allocates the TMEM accumulator, and its lane 0 loads the
+//    stage's activations with two TMA tile loads (64 inputs x BN rows each,
+//    128-byte swizzle) from the fp16 activation matrix;
+//  - warp 9, lane 0: issues the stage's 8 tcgen05.mma (M 128, N BN, K 16)
+//    and commits them to the stage's "empty" barrier, and after the last
+//    stage to the accumulator barrier;
+//  - epilogue (the decode warps, 32 TMEM lanes each): TMEM -> registers,
+//    times the row scale, plus the residual, to global memory.
+// Every wait is bounded; a wait that gives up sets TQ_DEV_WAIT_TIMEOUT and
+// the CTA runs on without waiting, then waits (bounded) for its MMAs before
+// it frees TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kernels.cuh"
+#include "launch.cuh"
+#include "ptx.cuh"
+#include "umma.cuh"
+
+namespace tq {
+namespace tc {
+
+constexpr int kBM = 128;          // weight rows per CTA
+constexpr int kBK = 128;          // inputs per stage
+constexpr int kDQ = 8;            // decode warps
+constexpr int kThreads = (kDQ + 2) * 32;
+constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait here
+constexpr int kAtomBytes = kBM * 128;  // one 64-input atom of the weight operand
+
+template <int BN>
+struct Cfg {
+  static constexpr int A = kBM * kBK * 2;   // 32 KB
+  static constexpr int B = BN * kBK * 2;    // BN * 256 bytes
+  static constexpr int STAGE = A + B;
+  static constexpr int NS = (200 * 1024) / STAGE > 8 ? 8 : (200 * 1024) / STAGE;
+  static constexpr int BAR = 1024;          // barriers, TMEM address, flags
+  static constexpr int SMEM = 1024 + NS * STAGE + BAR;  // + alignment slack
+  static constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+};
+
+struct TileMap {
+  int T;
+  int tile0[4];
+  int row0[3];
+};
+
+__host__ __device__ inline TileMap tile_map(const TcGemmArgs& a) {
+  TileMap m;
+  int t = 0, r = 0;
+  for (int s = 0; s < 3; ++s) {
+    m.tile0[s] = t;
+    m.row0[s] = r;
+    if (s < a.nseg) {
+      t += (a.seg[s].rows + kTileRows - 1) / kTileRows;
+      r += a.seg[s].rows;
+    }
+  }
+  m.tile0[3] = t;
+  m.T = t;
+  return m;
+}
+
+__device__ __forceinline__ int seg_of(const TileMap& m, int t) {
+  return t >= m.tile0[2] ? 2 : t >= m.tile0[1] ? 1 : 0;
+}
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             uint32_t* status) {
+  if (*abort_flag) return false;
+  if (mbar_wait_timed(bar, parity, kWaitNs)) return true;
+  set_status(status, TQ_DEV_WAIT_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
+__device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ uint32_t h2bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// Four codes held as bytes of `w` (byte b: 1024 + value in fp16 after the
+// byte interleave with 0x64) -> fp16 (code - bias) * d, two pairs.
+__device__ __forceinline__ void decode4(uint32_t w, __half2 bias2, __half2 d2, uint32_t& p01, uint32_t& p23) {
+  const uint32_t a = __byte_perm(w, 0x64646464u, 0x5150);  // fp16 pair 1024 + byte0, 1024 + byte1
+  const uint32_t b = __byte_perm(w, 0x64646464u, 0x5352);  // bytes 2, 3
+  p01 = h2bits(__hmul2(__hsub2(*reinterpret_cast<const __half2*>(&a), bias2), d2));
+  p23 = h2bits(__hmul2(__hsub2(*reinterpret_cast<const __half2*>(&b), bias2), d2));
+}
+
+// Shared address of inputs e..e+3 (e a multiple of 4, < 64) of row r in a
+// 64-input atom of the swizzled layout.
+__device__ __forceinline__ uint32_t a_addr(uint32_t atom, int r, int e) {
+  const int c = e >> 3;
+  return atom + r * 128 + ((c ^ (r & 7)) << 4) + (e & 4) * 2;
+}
+
+// Decode stage `st` (inputs 128 st .. 128 st + 127) of the CTA's 128 rows
+// into the weight operand at `A`.  Warp w decodes tile w of the CTA.
+template <int WT>
+__device__ __forceinline__ void decode_stage(const TcGemmArgs& a, const TileMap& m, int tile, int G, int st,
+                                             uint32_t A, int lane, int w) {
+  const int g = lane >> 2, i = lane & 3;
+  const int u = st >> 1, sh = st & 1;  // unit, half of the unit
+  const int t = tile + w;
+  const __half2 zero2 = __float2half2_rn(0.f);
+  if (t >= m.T) {  // rows past the last tile: zeros
+    for (int h = 0; h < 2; ++h) {
+      const int r = w * 16 + h * 8 + g;
+      for (int jj = 0; jj < 4; ++jj) {
+        const uint32_t atom = A + (jj >> 1) * kAtomBytes;
+        const int e = (jj & 1) * 32 + 4 * i;
+        sts64(a_addr(atom, r, e), h2bits(zero2), h2bits(zero2));
+        sts64(a_addr(atom, r, e + 16), h2bits(zero2), h2bits(zero2));
+      }
+    }
+    return;
+  }
+  const int s = seg_of(m, t);
+  const GemvSeg& gs = a.seg[s];
+  const int64_t unit = (int64_t)(t - m.tile0[s]) * G + u;
+  const uint8_t* qs = gs.qs + unit * unit_qs_bytes(WT);
+  const uint16_t* dd = gs.d + unit * 128;
+  if (WT == TQ_Q4_0) {
+    const __half2 bias2 = __float2half2_rn(1032.f);  // 1024 + 8
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 pc = ldg_stream(qs + ((h * 2 + sh) * 32 + lane) * 16);
+      const uint2 dv = __ldg(reinterpret_cast<const uint2*>(dd + (h * 8 + g) * 8 + 4 * sh));
+      const int r = w * 16 + h * 8 + g;
+      const uint32_t words[4] = {pc.x, pc.y, pc.z, pc.w};
+      const uint32_t dw[2] = {dv.x, dv.y};
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {  // block 4 sh + jj: word i = inputs 4i..4i+3 (low), +16 (high)
+        const uint32_t dbits = (dw[jj >> 1] >> ((jj & 1) * 16)) & 0xffffu;
+        const __half2 d2 = __halves2half2(__ushort_as_half((uint16_t)dbits), __ushort_as_half((uint16_t)dbits));
+        const uint32_t wd = words[jj];
+        uint32_t l01, l23, h01, h23;
+        decode4(wd & 0x0F0F0F0Fu, bias2, d2, l01, l23);
+        decode4((wd >> 4) & 0x0F0F0F0Fu, bias2, d2, h01, h23);
+        const uint32_t atom = A + (jj >> 1) * kAtomBytes;
+        const int e = (jj & 1) * 32 + 4 * i;
+        sts64(a_addr(atom, r, e), l01, l23);
+        sts64(a_addr(atom, r, e + 16), h01, h23);
+      }
+    }
+  } else {
+    const __half2 bias2 = __float2half2_rn(1152.f);  // 1024 + 128
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int jp = 0; jp < 2; ++jp) {  // block pair 2 sh + jp of the unit
+        const uint4 pc = ldg_stream(qs + ((h * 4 + 2 * sh + jp) * 32 + lane) * 16);
+        const uint32_t dv = __ldg(reinterpret_cast<const uint32_t*>(dd + (h * 8 + g) * 8 + 4 * sh + 2 * jp));
+        const int r = w * 16 + h * 8 + g;
+        const uint32_t words[4] = {pc.x, pc.y, pc.z, pc.w};
+#pragma unroll
+        for (int jb = 0; jb < 2; ++jb) {  // block 4 sh + 2 jp + jb
+          const uint32_t dbits = (dv >> (jb * 16)) & 0xffffu;
+          const __half2 d2 = __halves2half2(__ushort_as_half((uint16_t)dbits), __ushort_as_half((uint16_t)dbits));
+          uint32_t l01, l23, h01, h23;  // code words i (inputs 4i..) and i + 4 (inputs 16 + 4i..)
+          decode4(words[jb * 2] ^ 0x80808080u, bias2, d2, l01, l23);
+          decode4(words[jb * 2 + 1] ^ 0x80808080u, bias2, d2, h01, h23);
+          const int jj = 2 * jp + jb;
+          const uint32_t atom = A + (jj >> 1) * kAtomBytes;
+          const int e = (jj & 1) * 32 + 4 * i;
+          sts64(a_addr(atom, r, e), l01, l23);
+          sts64(a_addr(atom, r, e + 16), h01, h23);
+        }
+      }
+    }
+  }
+}
+
+template <int WT, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    tcgemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ TcGemmArgs a) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw);
+  uint8_t* misc = sbase + C::NS * C::STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(misc);
+  uint64_t* empty = full + C::NS;
+  uint64_t* acc_bar = empty + C::NS;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* last_flag = const_cast<int*>(reinterpret_cast<volatile int*>(abort_flag + 1));
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const TileMap m = tile_map(a);
+  const int G = a.K / 256;
+  const int nst_all = a.K / kBK;
+  const int ks = gridDim.z, z = blockIdx.z;
+  const int sb = nst_all * z / ks, se = nst_all * (z + 1) / ks;
+  const int nst = se - sb;
+  const int tile = blockIdx.x * (kBM / kTileRows);
+  const int n0 = blockIdx.y * BN;
+
+  if (tid == 0) {
+    for (int k = 0; k < C::NS; ++k) {
+      mbar_init(&full[k], kDQ + 1);
+      mbar_init(&empty[k], 1);
+    }
+    mbar_init(acc_bar, 1);
+    *abort_flag = 0;
+    fence_proxy_async();
+  }
+  if (warp == kDQ) umma::tmem_alloc(tmem_holder, C::TMEM_COLS);
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = *tmem_holder;
+  grid_dep_launch();
+
+  if (warp < kDQ) {
+    // ------------------------------------------------------------ decode
+    for (int s = 0; s < nst; ++s) {
+      const int slot = s % C::NS;
+      if (s >= C::NS) {
+        const bool ok = wait_bounded(&empty[slot], (uint32_t)(((s / C::NS) - 1) & 1), abort_flag, a.status);
+        (void)ok;
+      }
+      decode_stage<WT>(a, m, tile, G, sb + s, base + slot * C::STAGE, lane, warp);
+      fence_proxy_async();  // the generic-proxy stores, before the tensor core reads them
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[slot]);
+    }
+    // ---------------------------------------------------------- epilogue
+    grid_dep_wait();
+    wait_bounded(acc_bar, 0u, abort_flag, a.status);
+    umma::fence_after_sync();
+    const int q = warp & 3;                 // TMEM lanes 32 q .. 32 q + 31
+    const int row = 32 * q + lane;          // weight row within the CTA
+    const int t = tile + row / kTileRows;
+    const bool row_ok = t < m.T;
+    const int s = row_ok ? seg_of(m, t) : 0;
+    const int local = row_ok ? (t - m.tile0[s]) * kTileRows + row % kTileRows : 0;
+    const bool valid = row_ok && local < a.seg[s].rows;
+    const int col = (s == 0 ? m.row0[0] : s == 1 ? m.row0[1] : m.row0[2]) + local;
+    constexpr int CW = BN >= 64 ? BN / 2 : BN;  // columns per warp
+    const int c0 = BN >= 64 ? (warp >> 2) * CW : 0;
+    if (BN >= 64 || warp < 4) {
+      for (int cc = 0; cc < CW; cc += 32) {
+        float v[32];
+        umma::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(c0 + cc), v);
+        if (!valid) continue;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int tok = n0 + c0 + cc + j;
+          if (tok >= a.T) continue;
+          const float val = v[j] * __ldg(a.inv_s + tok);
+          const int64_t o = (int64_t)tok * a.ldy + col;
+          if (ks > 1) {
+            __stcg(a.part + (int64_t)z * a.T * a.ldy + o, val);
+          } else {
+            a.y[o] = a.residual != nullptr ? a.residual[o] + val : val;
+          }
+        }
+      }
+    }
+  } else if (warp == kDQ) {
+    // ------------------------------------------------- activations (TMA)
+    if (lane == 0) {
+      umma::prefetch_tmap(&xmap);
+      grid_dep_wait();
+      for (int s = 0; s < nst; ++s) {
+        const int slot = s % C::NS;
+        if (s >= C::NS) wait_bounded(&empty[slot], (uint32_t)(((s / C::NS) - 1) & 1), abort_flag, a.status);
+        if (*abort_flag) {
+          mbar_arrive(&full[slot]);  // keep the phase count; nothing is loaded
+          continue;
+        }
+        uint8_t* bdst = sbase + slot * C::STAGE + C::A;
+        mbar_arrive_expect_tx(&full[slot], (uint32_t)C::B);
+        const int k0 = (sb + s) * kBK;
+        umma::tma_load_2d(bdst, &xmap, k0, n0, &full[slot]);
+        umma::tma_load_2d(bdst + BN * 128, &xmap, k0 + 64, n0, &full[slot]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma::idesc_f16_f32(kBM, BN);
+      for (int s = 0; s < nst; ++s) {
+        const int slot = s % C::NS;
+        const bool ok = wait_bounded(&full[slot], (uint32_t)((s / C::NS) & 1), abort_flag, a.status);
+        umma::fence_after_sync();
+        const uint32_t A = base + slot * C::STAGE, B = A + C::A;
+        if (ok) {
+#pragma unroll
+          for (int at = 0; at < 2; ++at)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma::mma_f16(tmem, umma::desc_sw128(A + at * kAtomBytes + kk * 32),
+                            umma::desc_sw128(B + at * (BN * 128) + kk * 32), idesc,
+                            (s > 0 || at > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma::commit(&empty[slot]);  // the stage is free once these MMAs are done
+      }
+      umma::commit(acc_bar);
+    }
+  }
+
+  if (ks > 1) __threadfence();  // this thread's partial sums, before the split counter
+  // every TMEM load and every MMA is done before the columns are freed
+  umma::fence_before_sync();
+  __syncthreads();
+  if (warp == kDQ) {
+    umma::fence_after_sync();
+    if (*abort_flag) mbar_wait_timed(acc_bar, 0u, kWaitNs);
+    umma::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (ks == 1) return;
+
+  // ---------------------------------------------- split K: the last CTA adds
+  if (tid == 0) {
+    __threadfence();
+    unsigned* ctr = a.counters + blockIdx.y * gridDim.x + blockIdx.x;
+    const int last = atomicAdd(ctr, 1u) == (unsigned)(ks - 1);
+    if (last) {
+      *ctr = 0u;  // zero for the next launch
+      __threadfence();
+    }
+    *last_flag = last;
+  }
+  __syncthreads();
+  if (!*last_flag || warp >= 4) return;
+  {
+    const int row = 32 * warp + lane;
+    const int t = tile + row / kTileRows;
+    if (t >= m.T) return;
+    const int s = seg_of(m, t);
+    const int local = (t - m.tile0[s]) * kTileRows + row % kTileRows;
+    if (local >= a.seg[s].rows) return;
+    const int col = (s == 0 ? m.row0[0] : s == 1 ? m.row0[1] : m.row0[2]) + local;
+    for (int j = 0; j < BN; ++j) {
+      const int tok = n0 + j;
+      if (tok >= a.T) break;
+      const int64_t o = (int64_t)tok * a.ldy + col;
+      float v = 0.f;
+      for (int zz = 0; zz < ks; ++zz) v += __ldcg(a.part + (int64_t)zz * a.T * a.ldy + o);
+      a.y[o] = a.residual != nullptr ? a.residual[o] + v : v;
+    }
+  }
+}
+
+// ------------------------------------------------------------ xprep16 --
+
+// Row t of the phase input (x, RMS-normalised with `gain`, or silu(x) * up)
+// -> fp16 row t of x16 after the power-of-two scale 2^e that puts its largest
+// magnitude in [2^14, 2^15); inv_s[t] = 2^-e.
+__global__ void __launch_bounds__(256) xprep16_kernel(const XPrep16Args a) {
+  grid_dep_launch();
+  grid_dep_wait();
+  constexpr int CPT = 12288 / 8 / 256;  // 8-input chunks per thread at the largest K
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ float sum_sh[8], max_sh[8];
+  const int nch = a.K / 8;
+  const float* xr = a.x + (int64_t)t * a.ldx;
+  const float* ur = a.up != nullptr ? a.up + (int64_t)t * a.ldx : nullptr;
+  float4 v0[CPT], v1[CPT];
+  float ss = 0.f, mx = 0.f;
+#pragma unroll
+  for (int r = 0; r < CPT; ++r) {
+    const int c = tid + r * 256;
+    if (c < nch) {
+      float4 p0 = *reinterpret_cast<const float4*>(xr + 8 * c);
+      float4 p1 = *reinterpret_cast<const float4*>(xr + 8 * c + 4);
+      if (ur != nullptr) {  // silu(gate) * up
+        const float4 u0 = *reinterpret_cast<const float4*>(ur + 8 * c);
+        const float4 u1 = *reinterpret_cast<const float4*>(ur + 8 * c + 4);
+        p0 = make_float4(p0.x / (1.f + __expf(-p0.x)) * u0.x, p0.y / (1.f + __expf(-p0.y)) * u0.y,
+                         p0.z / (1.f + __expf(-p0.z)) * u0.z, p0.w / (1.f + __expf(-p0.w)) * u0.w);
+        p1 = make_float4(p1.x / (1.f + __expf(-p1.x)) * u1.x, p1.y / (1.f + __expf(-p1.y)) * u1.y,
+                         p1.z / (1.f + __expf(-p1.z)) * u1.z, p1.w / (1.f + __expf(-p1.w)) * u1.w);
+      }
+      if (a.gain != nullptr) {
+        ss = fmaf(p0.x, p0.x, fmaf(p0.y, p0.y, fmaf(p0.z, p0.z, fmaf(p0.w, p0.w, ss))));
+        ss = fmaf(p1.x, p1.x, fmaf(p1.y, p1.y, fmaf(p1.z, p1.z, fmaf(p1.w, p1.w, ss))));
+        const float4 g0 = *reinterpret_cast<const float4*>(a.gain + 8 * c);
+        const float4 g1 = *reinterpret_cast<const float4*>(a.gain + 8 * c + 4);
+        p0 = make_float4(p0.x * g0.x, p0.y * g0.y, p0.z * g0.z, p0.w * g0.w);
+        p1 = make_float4(p1.x * g1.x, p1.y * g1.y, p1.z * g1.z, p1.w * g1.w);
+      }
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(p0.x), fabsf(p0.y)), fmaxf(fabsf(p0.z), fabsf(p0.w))));
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(p1.x), fabsf(p1.y)), fmaxf(fabsf(p1.z), fabsf(p1.w))));
+      v0[r] = p0;
+      v1[r] = p1;
+    }
+  }
+  ss = warp_sum(ss);
+  mx = warp_max(mx);
+  if (lane == 0) {
+    sum_sh[warp] = ss;
+    max_sh[warp] = mx;
+  }
+  __syncthreads();
+  ss = 0.f;
+  mx = 0.f;
+  for (int w = 0; w < 8; ++w) {
+    ss += sum_sh[w];
+    mx = fmaxf(mx, max_sh[w]);
+  }
+  const float scale = a.gain != nullptr ? 1.0f / sqrtf(ss / (float)a.K + a.eps) : 1.0f;
+  mx *= scale;
+  int e2 = 0;  // 2^e2 puts the largest |value| in [2^14, 2^15)
+  if (mx > 0.f && mx <= 3.4e38f) e2 = 14 - (int)((__float_as_uint(mx) >> 23) & 0xffu) + 127;
+  e2 = max(-100, min(100, e2));
+  const float f = scale * __uint_as_float((uint32_t)(e2 + 127) << 23);
+  if (tid == 0) a.inv_s[t] = __uint_as_float((uint32_t)(127 - e2) << 23);
+  __half* out = a.x16 + (int64_t)t * a.K;
+#pragma unroll
+  for (int r = 0; r < CPT; ++r) {
+    const int c = tid + r * 256;
+    if (c < nch) {
+      const __half2 h0 = __floats2half2_rn(v0[r].x * f, v0[r].y * f);
+      const __half2 h1 = __floats2half2_rn(v0[r].z * f, v0[r].w * f);
+      const __half2 h2 = __floats2half2_rn(v1[r].x * f, v1[r].y * f);
+      const __half2 h3 = __floats2half2_rn(v1[r].z * f, v1[r].w * f);
+      *reinterpret_cast<uint4*>(out + 8 * c) = make_uint4(h2bits(h0), h2bits(h1), h2bits(h2), h2bits(h3));
+    }
+  }
+}
+
+// ------------------------------------------------------------ launch --
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// Tensor map of the fp16 activations [T][K]: boxes of 64 inputs x BN rows,
+// 128-byte swizzle; rows past T read as zeros.
+cudaError_t encode_x(CUtensorMap* map, const __half* x16, int K, int T, int BN) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)T};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)BN};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(x16), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int WT, int BN>
+cudaError_t launch_bn(const TcGemmArgs& a, cudaStream_t s) {
+  using C = Cfg<BN>;
+  static PerDevice setup;
+  int sms = 0;
+  cudaError_t e = per_device(setup, &sms, [](int dev, int& n) {
+    cudaError_t r = cudaFuncSetAttribute(tcgemm_kernel<WT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (r != cudaSuccess) return r;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = kNumSMs;
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
+  CUtensorMap map;
+  if ((e = encode_x(&map, a.x16, a.K, a.T, BN)) != cudaSuccess) return e;
+  const TileMap m = tile_map(a);
+  dim3 grid((m.T + kBM / kTileRows - 1) / (kBM / kTileRows), (a.T + BN - 1) / BN, 1);
+  // Few CTAs would leave most SMs idle: split K so that waves x stages per
+  // split (plus a small cost per split for the partial sums) is least.
+  const int nst = a.K / kBK, base = (int)(grid.x * grid.y);
+  if (a.part != nullptr && a.counters != nullptr && base <= a.n_counters && base < sms) {
+    double best = 1e30;
+    for (int k = 1; k <= 16 && k <= nst; ++k) {
+      if (k > 1 && (int64_t)k * a.T * a.ldy > a.part_cap) break;
+      const double cost = (double)((base * k + sms - 1) / sms) * ((nst + k - 1) / k) + (k > 1 ? 0.5 * k : 0.0);
+      if (cost < best) {
+        best = cost;
+        grid.z = k;
+      }
+    }
+  }
+  return launch_k(tcgemm_kernel<WT, BN>, grid, dim3(kThreads), C::SMEM, s, map, a);
+}
+
+template <int WT>
+cudaError_t launch_wt(const TcGemmArgs& a, cudaStream_t s) {
+  if (a.T <= 32) return launch_bn<WT, 32>(a, s);
+  if (a.T <= 64) return launch_bn<WT, 64>(a, s);
+  if (a.T <= 128) return launch_bn<WT, 128>(a, s);
+  return launch_bn<WT, 256>(a, s);
+}
+
+}  // namespace tc
+
+cudaError_t launch_xprep16(const XPrep16Args& a, cudaStream_t s) {
+  if (a.T <= 0) return cudaSuccess;
+  if (a.K % 256 != 0 || a.K > 12288) return cudaErrorInvalidValue;
+  return launch_k(tc::xprep16_kernel, dim3(a.T), dim3(256), 0, s, a);
+}
+
+cudaError_t launch_tcgemm(int wtype, const TcGemmArgs& a, cudaStream_t s) {
+  if (a.T <= 0) return cudaSuccess;
+  if (a.K % 256 != 0 || a.K > 12288 || a.nseg < 1 || a.nseg > 3) return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(a.x16) & 15u) != 0) return cudaErrorInvalidValue;
+  return wtype == TQ_Q4_0 ? tc::launch_wt<TQ_Q4_0>(a, s) : tc::launch_wt<TQ_Q8_0>(a, s);
+}
+
+}  // namespace tq

@@ -244,10 +244,16 @@ TQ_API tq_status tq_gemv(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, c
  * sizes are invalid). */
 TQ_API size_t tq_gemm_scratch_bytes(int32_t n_rows, int32_t cols);
 
-/* The prefill GEMM on its own: y[t][r] = (residual ? residual[t][r] : 0) +
- * sum_c W[r][c] * x[t][c] for t < n_rows, r < rows, each weight unit read once
- * per 32 rows of x (x, y, residual: f32 row-major with leading dimensions cols
- * and rows; residual may alias y; all 16-byte aligned).  scratch_dev: at least
+/* The GEMM of prefill and batched decode on its own ("Всередині LLM ...
+ * Qwen3-0.6B на MLX", step 9: the prompt's positions through the same
+ * projections): y[t][r] = (residual ? residual[t][r] : 0) +
+ * sum_c W[r][c] * x[t][c] for t < n_rows, r < rows, on the tcgen05 tensor
+ * cores: the weights decoded to fp16 in shared memory (d * (q - 8) or d * q
+ * rounded once), each row of x scaled by a power of two and rounded to fp16,
+ * products summed in f32, so |error| <= about 2^-10 * sum_c |W[r][c] x[t][c]|;
+ * each weight tile is decoded once per 256 rows of x (x, y, residual: f32
+ * row-major with leading dimensions cols and rows; residual may alias y; all
+ * 16-byte aligned).  scratch_dev: at least
  * tq_gemm_scratch_bytes(n_rows, cols) bytes of device memory, 256-byte aligned,
  * owned by the caller; the call must not overlap another use of it.  Refused
  * when cols % 256 != 0 or cols > 12288, a size is < 1 or a pointer NULL or

@@ -128,13 +128,12 @@ def test_model_handle_discipline_without_gpu():
 
 
 def test_gemm_scratch_bytes():
-    """Fragment table (128 B per row and block of 32 inputs), negated bias sums
-    (4 B per row and block) and one output scale per row, each 256-byte aligned;
-    0 for shapes the GEMM does not take."""
+    """fp16 activation rows (2 B per row and input) and one output scale per
+    row, each 256-byte aligned; 0 for shapes the GEMM does not take."""
     L = tq.lib()
     up = lambda n: (n + 255) // 256 * 256
     for n_rows, cols in [(1, 256), (32, 4096), (2048, 12288), (7, 768)]:
-        want = up(n_rows * cols // 32 * 128) + up(n_rows * cols // 32 * 4) + up(n_rows * 4)
+        want = up(n_rows * cols * 2) + up(n_rows * 4)
         assert L.tq_gemm_scratch_bytes(n_rows, cols) == want
     for n_rows, cols in [(0, 256), (4, 0), (4, 288), (4, 12544)]:
         assert L.tq_gemm_scratch_bytes(n_rows, cols) == 0

@@ -74,11 +74,16 @@ def _gemv_case(wtype, rows, cols, batch, residual, seed):
     W = quant.dequantize(blocks, wtype)
     ref = x.astype(np.float64) @ W.T
     bound = np.abs(x.astype(np.float64)) @ np.abs(W).T
+    # fp16 operands: weight and activation each rounded once to 11 significant
+    # bits (2^-10 of |x w| together), weights below 2^-14 rounded to a multiple
+    # of 2^-24, and an allowance of 2^-23 per input for the f32 sums
+    tol = (2.0 ** -10 + cols * 2.0 ** -23) * bound + 2.0 ** -25 * np.abs(x).sum(1, keepdims=True)
     if r is not None:
         ref = ref + r
-        bound = bound + np.abs(r)
+        tol = tol + 2.0 ** -23 * np.abs(r)
     err = np.abs(y - ref)
-    assert np.all(err <= 2e-6 * bound + 1e-30), float(np.max(err / bound))
+    assert np.all(err <= tol), float(np.max(err / tol))
+    return float(np.max(err / np.maximum(bound, 1e-30)))
 
 
 @pytest.mark.parametrize("wtype,rows,cols", [
@@ -107,16 +112,23 @@ def _gemm_case(wtype, rows, cols, n, residual, seed):
     W = quant.dequantize(blocks, wtype)
     ref = x.astype(np.float64) @ W.T
     bound = np.abs(x.astype(np.float64)) @ np.abs(W).T
+    # fp16 operands: weight and activation each rounded once to 11 significant
+    # bits (2^-10 of |x w| together), weights below 2^-14 rounded to a multiple
+    # of 2^-24, and an allowance of 2^-23 per input for the f32 sums
+    tol = (2.0 ** -10 + cols * 2.0 ** -23) * bound + 2.0 ** -25 * np.abs(x).sum(1, keepdims=True)
     if r is not None:
         ref = ref + r
-        bound = bound + np.abs(r)
+        tol = tol + 2.0 ** -23 * np.abs(r)
     err = np.abs(y - ref)
-    assert np.all(err <= 2e-6 * bound + 1e-30), float(np.max(err / bound))
+    assert np.all(err <= tol), float(np.max(err / tol))
+    return float(np.max(err / np.maximum(bound, 1e-30)))
 
 
 @pytest.mark.parametrize("wtype,rows,cols,n", [
     ("q4_0", 4096 + 5, 4096, 37), ("q4_0", 77, 3072, 33), ("q4_0", 1003, 12288, 5),
-    ("q4_0", 130, 256, 2), ("q8_0", 300, 1024, 64), ("q8_0", 50, 768, 31), ("q8_0", 1, 4096, 3)])
+    ("q4_0", 130, 256, 2), ("q8_0", 300, 1024, 64), ("q8_0", 50, 768, 31), ("q8_0", 1, 4096, 3),
+    ("q4_0", 1024 + 16, 4096, 300), ("q8_0", 384, 1024, 257), ("q4_0", 6144, 4096, 2048),
+    ("q4_0", 256, 12288, 96), ("q8_0", 200, 512, 128)])
 def test_gemm_matches_oracle(wtype, rows, cols, n):
     _gemm_case(wtype, rows, cols, n, False, rows + cols + n)
 
