@@ -14,25 +14,27 @@
 // so an output differs from the exact sum by at most about 2^-10 * sum|x w|.
 //
 // CTA work item: 128 weight rows (8 tiles of 16) x BN token rows over a
-// range of K (the whole K, or a 1/ks share when few CTAs would be busy: the
-// ks partial sums are then added by the last CTA of the group, in split
-// order).  K advances in stages of 128 inputs (half a unit of the tiled
-// layout), NS stages in flight:
-//  - 8 decode warps: read the stage's codes and scales from global memory
-//    (one 16-byte load per lane, 512 contiguous bytes per warp), decode them
-//    to fp16 and store them in the 128-byte swizzled K-major layout (two
-//    64-input atoms of 128 rows);
-//  - warp 8: allocates the TMEM accumulator, and its lane 0 loads the
-//    stage's activations with two TMA tile loads (64 inputs x BN rows each,
+// range of K units (the whole K, or a 1/ks share when few CTAs would be busy:
+// the ks partial sums are then added by the last CTA of the group, in split
+// order).  Roles:
+//  - warp 10, lane 0: streams the CTA's weight units (codes and scales of
+//    its 8 tiles, 256 inputs each) into a ring of R raw slots with 1-D bulk
+//    copies (TMA engine); weights are read-only, so this starts before the
+//    preceding kernel is done;
+//  - 8 decode warps: per stage of 64 inputs, decode tile w's codes from the
+//    raw slot to fp16 and store them in the 128-byte swizzled K-major layout
+//    (one 64-input atom of 128 rows) of one of NS operand stages;
+//  - warp 8: allocates the TMEM accumulator, and its lane 0 loads each
+//    stage's activations with one TMA tile load (64 inputs x BN rows,
 //    128-byte swizzle) from the fp16 activation matrix;
-//  - warp 9, lane 0: issues the stage's 8 tcgen05.mma (M 128, N BN, K 16)
+//  - warp 9, lane 0: issues the stage's 4 tcgen05.mma (M 128, N BN, K 16)
 //    and commits them to the stage's "empty" barrier, and after the last
 //    stage to the accumulator barrier;
 //  - epilogue (the decode warps, 32 TMEM lanes each): TMEM -> registers,
 //    times the row scale, plus the residual, to global memory.
-// Every wait is bounded; a wait that gives up sets TQ_DEV_WAIT_TIMEOUT and
-// the CTA runs on without waiting, then waits (bounded) for its MMAs before
-// it frees TMEM.
+// Every wait is bounded in time; a wait that gives up sets
+// TQ_DEV_WAIT_TIMEOUT and the CTA runs on without waiting, then waits
+// (bounded) for its MMAs and copies before it frees TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -45,21 +47,29 @@ namespace tq {
 namespace tc {
 
 constexpr int kBM = 128;          // weight rows per CTA
-constexpr int kBK = 128;          // inputs per stage
-constexpr int kDQ = 8;            // decode warps
-constexpr int kThreads = (kDQ + 2) * 32;
+constexpr int kBK = 64;           // inputs per operand stage (one swizzle atom)
+constexpr int kTiles = kBM / kTileRows;
+constexpr int kDQ = 8;            // decode warps, warp w <-> tile w
+constexpr int kWarpB = kDQ, kWarpMMA = kDQ + 1, kWarpRaw = kDQ + 2;
+constexpr int kThreads = (kDQ + 3) * 32;
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait here
-constexpr int kAtomBytes = kBM * 128;  // one 64-input atom of the weight operand
+constexpr int kSmemBudget = 212 * 1024;
 
-template <int BN>
+template <int WT, int BN>
 struct Cfg {
-  static constexpr int A = kBM * kBK * 2;   // 32 KB
-  static constexpr int B = BN * kBK * 2;    // BN * 256 bytes
+  static constexpr int A = kBM * kBK * 2;                      // 16 KB
+  static constexpr int B = BN * kBK * 2;                       // BN * 128 bytes
   static constexpr int STAGE = A + B;
-  static constexpr int NS = (200 * 1024) / STAGE > 8 ? 8 : (200 * 1024) / STAGE;
-  static constexpr int BAR = 1024;          // barriers, TMEM address, flags
-  static constexpr int SMEM = 1024 + NS * STAGE + BAR;  // + alignment slack
+  static constexpr int NS = BN >= 128 ? 3 : 4;                 // operand stages
+  static constexpr int UQ = unit_qs_bytes(WT);                 // codes of one tile's unit
+  static constexpr int RAW = kTiles * (UQ + kUnitD);           // one raw slot: the CTA's 8 units
+  static constexpr int R0 = (kSmemBudget - NS * STAGE) / RAW;
+  static constexpr int R = R0 > 6 ? 6 : R0;                    // raw slots
+  static constexpr int MISC = 512;                             // barriers, TMEM address, flags
+  static constexpr int SMEM = 1024 + NS * STAGE + R * RAW + MISC;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+  static_assert(R >= 2, "shared memory too small for two raw slots");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 struct TileMap {
@@ -101,15 +111,40 @@ __device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
   asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t h2bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
-// Four codes held as bytes of `w` (byte b: 1024 + value in fp16 after the
-// byte interleave with 0x64) -> fp16 (code - bias) * d, two pairs.
+// Four codes held as the bytes of `w` -> fp16 (code - bias) * d, as two
+// pairs: each byte b is interleaved with 0x64, which reads as the fp16 value
+// 1024 + b; subtracting bias (1024 + the code offset) is exact, and the
+// product with the block scale is the one rounding.
 __device__ __forceinline__ void decode4(uint32_t w, __half2 bias2, __half2 d2, uint32_t& p01, uint32_t& p23) {
   const uint32_t a = __byte_perm(w, 0x64646464u, 0x5150);  // fp16 pair 1024 + byte0, 1024 + byte1
   const uint32_t b = __byte_perm(w, 0x64646464u, 0x5352);  // bytes 2, 3
   p01 = h2bits(__hmul2(__hsub2(*reinterpret_cast<const __half2*>(&a), bias2), d2));
   p23 = h2bits(__hmul2(__hsub2(*reinterpret_cast<const __half2*>(&b), bias2), d2));
+}
+
+__device__ __forceinline__ __half2 scale2(uint32_t bits) {
+  const __half h = __ushort_as_half((uint16_t)(bits & 0xffffu));
+  return __halves2half2(h, h);
 }
 
 // Shared address of inputs e..e+3 (e a multiple of 4, < 64) of row r in a
@@ -119,79 +154,59 @@ __device__ __forceinline__ uint32_t a_addr(uint32_t atom, int r, int e) {
   return atom + r * 128 + ((c ^ (r & 7)) << 4) + (e & 4) * 2;
 }
 
-// Decode stage `st` (inputs 128 st .. 128 st + 127) of the CTA's 128 rows
-// into the weight operand at `A`.  Warp w decodes tile w of the CTA.
+// Stage q (inputs 64 q .. 64 q + 63, blocks 2q and 2q + 1) of the unit in raw
+// slot `rs` -> the fp16 operand atom `A`, tile w of the CTA (rows 16 w ..).
+// Raw slot: the 8 tiles' codes (UQ bytes each), then their scales (256 B each).
 template <int WT>
-__device__ __forceinline__ void decode_stage(const TcGemmArgs& a, const TileMap& m, int tile, int G, int st,
-                                             uint32_t A, int lane, int w) {
+__device__ __forceinline__ void decode_stage(uint32_t rs, int q, uint32_t A, int lane, int w, bool tile_ok) {
   const int g = lane >> 2, i = lane & 3;
-  const int u = st >> 1, sh = st & 1;  // unit, half of the unit
-  const int t = tile + w;
-  const __half2 zero2 = __float2half2_rn(0.f);
-  if (t >= m.T) {  // rows past the last tile: zeros
+  if (!tile_ok) {  // rows past the last tile: zeros
+#pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int r = w * 16 + h * 8 + g;
-      for (int jj = 0; jj < 4; ++jj) {
-        const uint32_t atom = A + (jj >> 1) * kAtomBytes;
-        const int e = (jj & 1) * 32 + 4 * i;
-        sts64(a_addr(atom, r, e), h2bits(zero2), h2bits(zero2));
-        sts64(a_addr(atom, r, e + 16), h2bits(zero2), h2bits(zero2));
+#pragma unroll
+      for (int jb = 0; jb < 2; ++jb) {
+        const int e = jb * 32 + 4 * i;
+        sts64(a_addr(A, r, e), 0u, 0u);
+        sts64(a_addr(A, r, e + 16), 0u, 0u);
       }
     }
     return;
   }
-  const int s = seg_of(m, t);
-  const GemvSeg& gs = a.seg[s];
-  const int64_t unit = (int64_t)(t - m.tile0[s]) * G + u;
-  const uint8_t* qs = gs.qs + unit * unit_qs_bytes(WT);
-  const uint16_t* dd = gs.d + unit * 128;
-  if (WT == TQ_Q4_0) {
-    const __half2 bias2 = __float2half2_rn(1032.f);  // 1024 + 8
+  constexpr int UQ = unit_qs_bytes(WT);
+  const uint32_t qs = rs + w * UQ;
+  const uint32_t dd = rs + kTiles * UQ + w * kUnitD;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint4 pc = ldg_stream(qs + ((h * 2 + sh) * 32 + lane) * 16);
-      const uint2 dv = __ldg(reinterpret_cast<const uint2*>(dd + (h * 8 + g) * 8 + 4 * sh));
-      const int r = w * 16 + h * 8 + g;
-      const uint32_t words[4] = {pc.x, pc.y, pc.z, pc.w};
-      const uint32_t dw[2] = {dv.x, dv.y};
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {  // block 4 sh + jj: word i = inputs 4i..4i+3 (low), +16 (high)
-        const uint32_t dbits = (dw[jj >> 1] >> ((jj & 1) * 16)) & 0xffffu;
-        const __half2 d2 = __halves2half2(__ushort_as_half((uint16_t)dbits), __ushort_as_half((uint16_t)dbits));
-        const uint32_t wd = words[jj];
-        uint32_t l01, l23, h01, h23;
-        decode4(wd & 0x0F0F0F0Fu, bias2, d2, l01, l23);
-        decode4((wd >> 4) & 0x0F0F0F0Fu, bias2, d2, h01, h23);
-        const uint32_t atom = A + (jj >> 1) * kAtomBytes;
-        const int e = (jj & 1) * 32 + 4 * i;
-        sts64(a_addr(atom, r, e), l01, l23);
-        sts64(a_addr(atom, r, e + 16), h01, h23);
-      }
+  for (int h = 0; h < 2; ++h) {
+    const int r = w * 16 + h * 8 + g;
+    // scales of blocks 2q, 2q + 1 of row 8h + g
+    const uint32_t dw = lds32(dd + ((h * 8 + g) * 8 + 2 * q) * 2);
+    uint32_t wlo[2], whi[2];  // per block jb: inputs 4i..4i+3 and 16+4i..16+4i+3
+    if (WT == TQ_Q4_0) {
+      // piece (h, q/2) of lane 4g + i holds word i of blocks 4(q/2) .. 4(q/2)+3
+      const uint2 v = lds64(qs + ((h * 2 + (q >> 1)) * 32 + lane) * 16 + (q & 1) * 8);
+      wlo[0] = v.x & 0x0F0F0F0Fu;
+      whi[0] = (v.x >> 4) & 0x0F0F0F0Fu;
+      wlo[1] = v.y & 0x0F0F0F0Fu;
+      whi[1] = (v.y >> 4) & 0x0F0F0F0Fu;
+    } else {
+      // piece (h, q) of lane 4g + i: code words i, i + 4 of blocks 2q, 2q + 1
+      const uint4 v = lds128(qs + ((h * 4 + q) * 32 + lane) * 16);
+      wlo[0] = v.x ^ 0x80808080u;
+      whi[0] = v.y ^ 0x80808080u;
+      wlo[1] = v.z ^ 0x80808080u;
+      whi[1] = v.w ^ 0x80808080u;
     }
-  } else {
-    const __half2 bias2 = __float2half2_rn(1152.f);  // 1024 + 128
+    const __half2 bias2 = __float2half2_rn(WT == TQ_Q4_0 ? 1032.f : 1152.f);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-#pragma unroll
-      for (int jp = 0; jp < 2; ++jp) {  // block pair 2 sh + jp of the unit
-        const uint4 pc = ldg_stream(qs + ((h * 4 + 2 * sh + jp) * 32 + lane) * 16);
-        const uint32_t dv = __ldg(reinterpret_cast<const uint32_t*>(dd + (h * 8 + g) * 8 + 4 * sh + 2 * jp));
-        const int r = w * 16 + h * 8 + g;
-        const uint32_t words[4] = {pc.x, pc.y, pc.z, pc.w};
-#pragma unroll
-        for (int jb = 0; jb < 2; ++jb) {  // block 4 sh + 2 jp + jb
-          const uint32_t dbits = (dv >> (jb * 16)) & 0xffffu;
-          const __half2 d2 = __halves2half2(__ushort_as_half((uint16_t)dbits), __ushort_as_half((uint16_t)dbits));
-          uint32_t l01, l23, h01, h23;  // code words i (inputs 4i..) and i + 4 (inputs 16 + 4i..)
-          decode4(words[jb * 2] ^ 0x80808080u, bias2, d2, l01, l23);
-          decode4(words[jb * 2 + 1] ^ 0x80808080u, bias2, d2, h01, h23);
-          const int jj = 2 * jp + jb;
-          const uint32_t atom = A + (jj >> 1) * kAtomBytes;
-          const int e = (jj & 1) * 32 + 4 * i;
-          sts64(a_addr(atom, r, e), l01, l23);
-          sts64(a_addr(atom, r, e + 16), h01, h23);
-        }
-      }
+    for (int jb = 0; jb < 2; ++jb) {
+      const __half2 d2 = scale2(dw >> (16 * jb));
+      uint32_t l01, l23, h01, h23;
+      decode4(wlo[jb], bias2, d2, l01, l23);
+      decode4(whi[jb], bias2, d2, h01, h23);
+      const int e = jb * 32 + 4 * i;
+      sts64(a_addr(A, r, e), l01, l23);
+      sts64(a_addr(A, r, e + 16), h01, h23);
     }
   }
 }
@@ -199,27 +214,29 @@ __device__ __forceinline__ void decode_stage(const TcGemmArgs& a, const TileMap&
 template <int WT, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     tcgemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ TcGemmArgs a) {
-  using C = Cfg<BN>;
+  using C = Cfg<WT, BN>;
   extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* sbase = smem_raw + (base - raw);
-  uint8_t* misc = sbase + C::NS * C::STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(misc);
-  uint64_t* empty = full + C::NS;
-  uint64_t* acc_bar = empty + C::NS;
+  const uint32_t raw0 = smem_addr(smem_raw);
+  const uint32_t base = (raw0 + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw0);
+  const uint32_t rbase = base + C::NS * C::STAGE;               // raw slots
+  uint8_t* misc = sbase + C::NS * C::STAGE + C::R * C::RAW;
+  uint64_t* full = reinterpret_cast<uint64_t*>(misc);          // [NS] operand stage ready
+  uint64_t* empty = full + C::NS;                               // [NS] operand stage consumed
+  uint64_t* rfull = empty + C::NS;                              // [R] raw slot landed
+  uint64_t* rempty = rfull + C::R;                              // [R] raw slot decoded
+  uint64_t* acc_bar = rempty + C::R;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* last_flag = const_cast<int*>(reinterpret_cast<volatile int*>(abort_flag + 1));
+  volatile int* last_flag = abort_flag + 1;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const TileMap m = tile_map(a);
   const int G = a.K / 256;
-  const int nst_all = a.K / kBK;
   const int ks = gridDim.z, z = blockIdx.z;
-  const int sb = nst_all * z / ks, se = nst_all * (z + 1) / ks;
-  const int nst = se - sb;
-  const int tile = blockIdx.x * (kBM / kTileRows);
+  const int ub = G * z / ks, ue = G * (z + 1) / ks;  // this CTA's K units
+  const int nu = ue - ub, nst = 4 * nu;
+  const int tile = blockIdx.x * kTiles;
   const int n0 = blockIdx.y * BN;
 
   if (tid == 0) {
@@ -227,11 +244,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[k], kDQ + 1);
       mbar_init(&empty[k], 1);
     }
+    for (int k = 0; k < C::R; ++k) {
+      mbar_init(&rfull[k], 1);
+      mbar_init(&rempty[k], kDQ);
+    }
     mbar_init(acc_bar, 1);
     *abort_flag = 0;
     fence_proxy_async();
   }
-  if (warp == kDQ) umma::tmem_alloc(tmem_holder, C::TMEM_COLS);
+  if (warp == kWarpB) umma::tmem_alloc(tmem_holder, C::TMEM_COLS);
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
@@ -240,35 +261,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kDQ) {
     // ------------------------------------------------------------ decode
-    for (int s = 0; s < nst; ++s) {
-      const int slot = s % C::NS;
-      if (s >= C::NS) {
-        const bool ok = wait_bounded(&empty[slot], (uint32_t)(((s / C::NS) - 1) & 1), abort_flag, a.status);
-        (void)ok;
+    const bool tile_ok = tile + warp < m.T;
+    for (int u = 0; u < nu; ++u) {
+      const int rsl = u % C::R;
+      wait_bounded(&rfull[rsl], (uint32_t)((u / C::R) & 1), abort_flag, a.status);
+      for (int q = 0; q < 4; ++q) {
+        const int s = 4 * u + q, slot = s % C::NS;
+        if (s >= C::NS) wait_bounded(&empty[slot], (uint32_t)(((s / C::NS) - 1) & 1), abort_flag, a.status);
+        decode_stage<WT>(rbase + rsl * C::RAW, q, base + slot * C::STAGE, lane, warp, tile_ok);
+        fence_proxy_async();  // the generic-proxy stores, before the tensor core reads them
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[slot]);
       }
-      decode_stage<WT>(a, m, tile, G, sb + s, base + slot * C::STAGE, lane, warp);
-      fence_proxy_async();  // the generic-proxy stores, before the tensor core reads them
       __syncwarp();
-      if (lane == 0) mbar_arrive(&full[slot]);
+      if (lane == 0) mbar_arrive(&rempty[rsl]);
     }
     // ---------------------------------------------------------- epilogue
     grid_dep_wait();
     wait_bounded(acc_bar, 0u, abort_flag, a.status);
     umma::fence_after_sync();
-    const int q = warp & 3;                 // TMEM lanes 32 q .. 32 q + 31
-    const int row = 32 * q + lane;          // weight row within the CTA
+    const int qd = warp & 3;                // TMEM lanes 32 qd .. 32 qd + 31
+    const int row = 32 * qd + lane;         // weight row within the CTA
     const int t = tile + row / kTileRows;
     const bool row_ok = t < m.T;
-    const int s = row_ok ? seg_of(m, t) : 0;
-    const int local = row_ok ? (t - m.tile0[s]) * kTileRows + row % kTileRows : 0;
-    const bool valid = row_ok && local < a.seg[s].rows;
-    const int col = (s == 0 ? m.row0[0] : s == 1 ? m.row0[1] : m.row0[2]) + local;
+    const int sg = row_ok ? seg_of(m, t) : 0;
+    const int local = row_ok ? (t - m.tile0[sg]) * kTileRows + row % kTileRows : 0;
+    const bool valid = row_ok && local < a.seg[sg].rows;
+    const int col = (sg == 0 ? m.row0[0] : sg == 1 ? m.row0[1] : m.row0[2]) + local;
     constexpr int CW = BN >= 64 ? BN / 2 : BN;  // columns per warp
     const int c0 = BN >= 64 ? (warp >> 2) * CW : 0;
     if (BN >= 64 || warp < 4) {
       for (int cc = 0; cc < CW; cc += 32) {
         float v[32];
-        umma::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(c0 + cc), v);
+        umma::tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(c0 + cc), v);
         if (!valid) continue;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -284,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == kDQ) {
+  } else if (warp == kWarpB) {
     // ------------------------------------------------- activations (TMA)
     if (lane == 0) {
       umma::prefetch_tmap(&xmap);
@@ -296,14 +321,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&full[slot]);  // keep the phase count; nothing is loaded
           continue;
         }
-        uint8_t* bdst = sbase + slot * C::STAGE + C::A;
         mbar_arrive_expect_tx(&full[slot], (uint32_t)C::B);
-        const int k0 = (sb + s) * kBK;
-        umma::tma_load_2d(bdst, &xmap, k0, n0, &full[slot]);
-        umma::tma_load_2d(bdst + BN * 128, &xmap, k0 + 64, n0, &full[slot]);
+        umma::tma_load_2d(sbase + slot * C::STAGE + C::A, &xmap, (4 * ub + s) * kBK, n0, &full[slot]);
       }
     }
-  } else {
+  } else if (warp == kWarpMMA) {
     // ------------------------------------------------------- MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc = umma::idesc_f16_f32(kBM, BN);
@@ -314,16 +336,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t A = base + slot * C::STAGE, B = A + C::A;
         if (ok) {
 #pragma unroll
-          for (int at = 0; at < 2; ++at)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma::mma_f16(tmem, umma::desc_sw128(A + at * kAtomBytes + kk * 32),
-                            umma::desc_sw128(B + at * (BN * 128) + kk * 32), idesc,
-                            (s > 0 || at > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)
+            umma::mma_f16(tmem, umma::desc_sw128(A + kk * 32), umma::desc_sw128(B + kk * 32), idesc,
+                          (s > 0 || kk > 0) ? 1u : 0u);
         }
         umma::commit(&empty[slot]);  // the stage is free once these MMAs are done
       }
       umma::commit(acc_bar);
+    }
+  } else if (warp == kWarpRaw) {
+    // ------------------------------------------------- weight units (bulk)
+    if (lane == 0) {
+      int nt = 0;  // the CTA's tiles that exist
+      for (int i = 0; i < kTiles; ++i)
+        if (tile + i < m.T) ++nt;
+      int issued = 0;
+      for (int u = 0; u < nu; ++u) {
+        const int rsl = u % C::R;
+        if (u >= C::R && !wait_bounded(&rempty[rsl], (uint32_t)(((u / C::R) - 1) & 1), abort_flag, a.status))
+          break;
+        if (*abort_flag) break;
+        const uint32_t dst = rbase + rsl * C::RAW;
+        mbar_arrive_expect_tx(&rfull[rsl], (uint32_t)(nt * (C::UQ + kUnitD)));
+        for (int i = 0; i < nt; ++i) {
+          const int t = tile + i, sg = seg_of(m, t);
+          const GemvSeg& gs = a.seg[sg];
+          const int64_t unit = (int64_t)(t - m.tile0[sg]) * G + ub + u;
+          bulk_g2s(sbase + (dst - base) + i * C::UQ, gs.qs + unit * C::UQ, C::UQ, &rfull[rsl]);
+          bulk_g2s(sbase + (dst - base) + kTiles * C::UQ + i * kUnitD,
+                   reinterpret_cast<const uint8_t*>(gs.d) + unit * kUnitD, kUnitD, &rfull[rsl]);
+        }
+        ++issued;
+      }
+      // every issued copy lands before the CTA's shared memory is released
+      for (int u = (issued > C::R ? issued - C::R : 0); u < issued; ++u)
+        mbar_wait_timed(&rfull[u % C::R], (uint32_t)((u / C::R) & 1), kWaitNs);
     }
   }
 
@@ -331,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // every TMEM load and every MMA is done before the columns are freed
   umma::fence_before_sync();
   __syncthreads();
-  if (warp == kDQ) {
+  if (warp == kWarpB) {
     umma::fence_after_sync();
     if (*abort_flag) mbar_wait_timed(acc_bar, 0u, kWaitNs);
     umma::tmem_dealloc(tmem, C::TMEM_COLS);
@@ -355,10 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = 32 * warp + lane;
     const int t = tile + row / kTileRows;
     if (t >= m.T) return;
-    const int s = seg_of(m, t);
-    const int local = (t - m.tile0[s]) * kTileRows + row % kTileRows;
-    if (local >= a.seg[s].rows) return;
-    const int col = (s == 0 ? m.row0[0] : s == 1 ? m.row0[1] : m.row0[2]) + local;
+    const int sg = seg_of(m, t);
+    const int local = (t - m.tile0[sg]) * kTileRows + row % kTileRows;
+    if (local >= a.seg[sg].rows) return;
+    const int col = (sg == 0 ? m.row0[0] : sg == 1 ? m.row0[1] : m.row0[2]) + local;
     for (int j = 0; j < BN; ++j) {
       const int tok = n0 + j;
       if (tok >= a.T) break;
@@ -480,7 +527,7 @@ cudaError_t encode_x(CUtensorMap* map, const __half* x16, int K, int T, int BN) 
 
 template <int WT, int BN>
 cudaError_t launch_bn(const TcGemmArgs& a, cudaStream_t s) {
-  using C = Cfg<BN>;
+  using C = Cfg<WT, BN>;
   static PerDevice setup;
   int sms = 0;
   cudaError_t e = per_device(setup, &sms, [](int dev, int& n) {
@@ -493,15 +540,15 @@ cudaError_t launch_bn(const TcGemmArgs& a, cudaStream_t s) {
   CUtensorMap map;
   if ((e = encode_x(&map, a.x16, a.K, a.T, BN)) != cudaSuccess) return e;
   const TileMap m = tile_map(a);
-  dim3 grid((m.T + kBM / kTileRows - 1) / (kBM / kTileRows), (a.T + BN - 1) / BN, 1);
+  dim3 grid((m.T + kTiles - 1) / kTiles, (a.T + BN - 1) / BN, 1);
   // Few CTAs would leave most SMs idle: split K so that waves x stages per
   // split (plus a small cost per split for the partial sums) is least.
-  const int nst = a.K / kBK, base = (int)(grid.x * grid.y);
+  const int G = a.K / 256, base = (int)(grid.x * grid.y);
   if (a.part != nullptr && a.counters != nullptr && base <= a.n_counters && base < sms) {
     double best = 1e30;
-    for (int k = 1; k <= 16 && k <= nst; ++k) {
+    for (int k = 1; k <= 16 && k <= G; ++k) {
       if (k > 1 && (int64_t)k * a.T * a.ldy > a.part_cap) break;
-      const double cost = (double)((base * k + sms - 1) / sms) * ((nst + k - 1) / k) + (k > 1 ? 0.5 * k : 0.0);
+      const double cost = (double)((base * k + sms - 1) / sms) * ((G + k - 1) / k) + (k > 1 ? 0.25 * k : 0.0);
       if (cost < best) {
         best = cost;
         grid.z = k;
