@@ -17,26 +17,30 @@
 // range of K units (the whole K, or a 1/ks share when few CTAs would be busy:
 // the ks partial sums are then added by the last CTA of the group, in split
 // order).  Roles:
-//  - warp 10, lane 0: streams the CTA's weight units (codes and scales of
+//  - warp 18, lane 0: streams the CTA's weight units (codes and scales of
 //    its 8 tiles, 256 inputs each) into a ring of R raw slots with 1-D bulk
 //    copies (TMA engine); weights are read-only, so this starts before the
 //    preceding kernel is done;
-//  - 8 decode warps: per stage of 64 inputs, decode tile w's codes from the
-//    raw slot to fp16 and store them in the 128-byte swizzled K-major layout
-//    (one 64-input atom of 128 rows) of one of NS operand stages;
-//  - warp 8: allocates the TMEM accumulator, and its lane 0 loads each
+//  - 16 decode warps (8 rows of a tile each): per stage of 64 inputs, decode
+//    the codes from the raw slot to fp16 and store them in the 128-byte
+//    swizzled K-major layout (one 64-input atom of 128 rows) of one of NS
+//    operand stages;
+//  - warp 16: allocates the TMEM accumulator, and its lane 0 loads each
 //    stage's activations with one TMA tile load (64 inputs x BN rows,
 //    128-byte swizzle) from the fp16 activation matrix;
-//  - warp 9, lane 0: issues the stage's 4 tcgen05.mma (M 128, N BN, K 16)
+//  - warp 17, lane 0: issues the stage's 4 tcgen05.mma (M 128, N BN, K 16)
 //    and commits them to the stage's "empty" barrier, and after the last
 //    stage to the accumulator barrier;
-//  - epilogue (the decode warps, 32 TMEM lanes each): TMEM -> registers,
-//    times the row scale, plus the residual, to global memory.
+//  - epilogue (decode warps 0-7, or 0-3 for 32 columns; 32 TMEM lanes
+//    each): TMEM -> registers, times the row scale, plus the residual (all
+//    loads of a chunk before its stores), to global memory.
 // Every wait is bounded in time; a wait that gives up sets
 // TQ_DEV_WAIT_TIMEOUT and the CTA runs on without waiting, then waits
 // (bounded) for its MMAs and copies before it frees TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <type_traits>
 
 #include "kernels.cuh"
 #include "launch.cuh"
@@ -49,7 +53,7 @@ namespace tc {
 constexpr int kBM = 128;          // weight rows per CTA
 constexpr int kBK = 64;           // inputs per operand stage (one swizzle atom)
 constexpr int kTiles = kBM / kTileRows;
-constexpr int kDQ = 8;            // decode warps, warp w <-> tile w
+constexpr int kDQ = 16;           // decode warps, warp w <-> rows 8 (w % 2) .. of tile w / 2
 constexpr int kWarpB = kDQ, kWarpMMA = kDQ + 1, kWarpRaw = kDQ + 2;
 constexpr int kThreads = (kDQ + 3) * 32;
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait here
@@ -154,60 +158,68 @@ __device__ __forceinline__ uint32_t a_addr(uint32_t atom, int r, int e) {
   return atom + r * 128 + ((c ^ (r & 7)) << 4) + (e & 4) * 2;
 }
 
-// Stage q (inputs 64 q .. 64 q + 63, blocks 2q and 2q + 1) of the unit in raw
-// slot `rs` -> the fp16 operand atom `A`, tile w of the CTA (rows 16 w ..).
-// Raw slot: the 8 tiles' codes (UQ bytes each), then their scales (256 B each).
+// Per-thread constants of the decode: lane 4g + i of decode warp w handles
+// row 8h + g of tile w / 2 (h = w % 2) and code word i of each block.
+struct DecodeLane {
+  uint32_t st[4];   // operand offsets of inputs 4i, 16 + 4i, 32 + 4i, 48 + 4i of the row
+  uint32_t qs;      // raw-slot offset of the lane's first code piece
+  uint32_t dd;      // raw-slot offset of the row's scales
+  bool ok;          // the tile exists
+};
+
 template <int WT>
-__device__ __forceinline__ void decode_stage(uint32_t rs, int q, uint32_t A, int lane, int w, bool tile_ok) {
-  const int g = lane >> 2, i = lane & 3;
-  if (!tile_ok) {  // rows past the last tile: zeros
+__device__ __forceinline__ DecodeLane decode_lane(int lane, int w, bool tile_ok) {
+  constexpr int UQ = unit_qs_bytes(WT);
+  const int g = lane >> 2, i = lane & 3, tw = w >> 1, h = w & 1;
+  const int r = tw * 16 + h * 8 + g;
+  DecodeLane d;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = w * 16 + h * 8 + g;
+  for (int k = 0; k < 4; ++k) {
+    const int e = k * 16 + 4 * i;
+    d.st[k] = (uint32_t)(r * 128 + (((e >> 3) ^ g) << 4) + (e & 4) * 2);
+  }
+  d.qs = (uint32_t)(tw * UQ + ((WT == TQ_Q4_0 ? h * 2 : h * 4) * 32 + lane) * 16);
+  d.dd = (uint32_t)(kTiles * UQ + tw * kUnitD + (h * 8 + g) * 16);
+  d.ok = tile_ok;
+  return d;
+}
+
+// Stage q (inputs 64 q .. 64 q + 63, blocks 2q and 2q + 1) of the unit in raw
+// slot `rs` -> this lane's 16 inputs of the fp16 operand atom `A`.  Raw slot:
+// the 8 tiles' codes (UQ bytes each), then their scales (256 B each).
+template <int WT, int Q>
+__device__ __forceinline__ void decode_stage(uint32_t rs, uint32_t A, const DecodeLane& L) {
+  if (!L.ok) {  // rows past the last tile: zeros
 #pragma unroll
-      for (int jb = 0; jb < 2; ++jb) {
-        const int e = jb * 32 + 4 * i;
-        sts64(a_addr(A, r, e), 0u, 0u);
-        sts64(a_addr(A, r, e + 16), 0u, 0u);
-      }
-    }
+    for (int k = 0; k < 4; ++k) sts64(A + L.st[k], 0u, 0u);
     return;
   }
-  constexpr int UQ = unit_qs_bytes(WT);
-  const uint32_t qs = rs + w * UQ;
-  const uint32_t dd = rs + kTiles * UQ + w * kUnitD;
+  const uint32_t dw = lds32(rs + L.dd + 4 * Q);  // scales of blocks 2Q, 2Q + 1
+  uint32_t wlo[2], whi[2];  // per block jb: inputs 4i..4i+3 and 16+4i..16+4i+3
+  if (WT == TQ_Q4_0) {
+    // piece (h, Q/2) of the lane holds word i of blocks 4(Q/2) .. 4(Q/2)+3
+    const uint2 v = lds64(rs + L.qs + (Q >> 1) * 512 + (Q & 1) * 8);
+    wlo[0] = v.x & 0x0F0F0F0Fu;
+    whi[0] = (v.x >> 4) & 0x0F0F0F0Fu;
+    wlo[1] = v.y & 0x0F0F0F0Fu;
+    whi[1] = (v.y >> 4) & 0x0F0F0F0Fu;
+  } else {
+    // piece (h, Q) of the lane: code words i, i + 4 of blocks 2Q, 2Q + 1
+    const uint4 v = lds128(rs + L.qs + Q * 512);
+    wlo[0] = v.x ^ 0x80808080u;
+    whi[0] = v.y ^ 0x80808080u;
+    wlo[1] = v.z ^ 0x80808080u;
+    whi[1] = v.w ^ 0x80808080u;
+  }
+  const __half2 bias2 = __float2half2_rn(WT == TQ_Q4_0 ? 1032.f : 1152.f);
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = w * 16 + h * 8 + g;
-    // scales of blocks 2q, 2q + 1 of row 8h + g
-    const uint32_t dw = lds32(dd + ((h * 8 + g) * 8 + 2 * q) * 2);
-    uint32_t wlo[2], whi[2];  // per block jb: inputs 4i..4i+3 and 16+4i..16+4i+3
-    if (WT == TQ_Q4_0) {
-      // piece (h, q/2) of lane 4g + i holds word i of blocks 4(q/2) .. 4(q/2)+3
-      const uint2 v = lds64(qs + ((h * 2 + (q >> 1)) * 32 + lane) * 16 + (q & 1) * 8);
-      wlo[0] = v.x & 0x0F0F0F0Fu;
-      whi[0] = (v.x >> 4) & 0x0F0F0F0Fu;
-      wlo[1] = v.y & 0x0F0F0F0Fu;
-      whi[1] = (v.y >> 4) & 0x0F0F0F0Fu;
-    } else {
-      // piece (h, q) of lane 4g + i: code words i, i + 4 of blocks 2q, 2q + 1
-      const uint4 v = lds128(qs + ((h * 4 + q) * 32 + lane) * 16);
-      wlo[0] = v.x ^ 0x80808080u;
-      whi[0] = v.y ^ 0x80808080u;
-      wlo[1] = v.z ^ 0x80808080u;
-      whi[1] = v.w ^ 0x80808080u;
-    }
-    const __half2 bias2 = __float2half2_rn(WT == TQ_Q4_0 ? 1032.f : 1152.f);
-#pragma unroll
-    for (int jb = 0; jb < 2; ++jb) {
-      const __half2 d2 = scale2(dw >> (16 * jb));
-      uint32_t l01, l23, h01, h23;
-      decode4(wlo[jb], bias2, d2, l01, l23);
-      decode4(whi[jb], bias2, d2, h01, h23);
-      const int e = jb * 32 + 4 * i;
-      sts64(a_addr(A, r, e), l01, l23);
-      sts64(a_addr(A, r, e + 16), h01, h23);
-    }
+  for (int jb = 0; jb < 2; ++jb) {
+    const __half2 d2 = scale2(dw >> (16 * jb));
+    uint32_t l01, l23, h01, h23;
+    decode4(wlo[jb], bias2, d2, l01, l23);
+    decode4(whi[jb], bias2, d2, h01, h23);
+    sts64(A + L.st[2 * jb], l01, l23);
+    sts64(A + L.st[2 * jb + 1], h01, h23);
   }
 }
 
@@ -261,51 +273,68 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kDQ) {
     // ------------------------------------------------------------ decode
-    const bool tile_ok = tile + warp < m.T;
+    const DecodeLane L = decode_lane<WT>(lane, warp, tile + (warp >> 1) < m.T);
+    auto stage = [&](auto qc, int u, uint32_t rs) {
+      constexpr int Q = decltype(qc)::value;
+      const int s = 4 * u + Q, slot = s % C::NS;
+      if (s >= C::NS) wait_bounded(&empty[slot], (uint32_t)(((s / C::NS) - 1) & 1), abort_flag, a.status);
+      decode_stage<WT, Q>(rs, base + slot * C::STAGE, L);
+      fence_proxy_async();  // the generic-proxy stores, before the tensor core reads them
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[slot]);
+    };
     for (int u = 0; u < nu; ++u) {
       const int rsl = u % C::R;
       wait_bounded(&rfull[rsl], (uint32_t)((u / C::R) & 1), abort_flag, a.status);
-      for (int q = 0; q < 4; ++q) {
-        const int s = 4 * u + q, slot = s % C::NS;
-        if (s >= C::NS) wait_bounded(&empty[slot], (uint32_t)(((s / C::NS) - 1) & 1), abort_flag, a.status);
-        decode_stage<WT>(rbase + rsl * C::RAW, q, base + slot * C::STAGE, lane, warp, tile_ok);
-        fence_proxy_async();  // the generic-proxy stores, before the tensor core reads them
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[slot]);
-      }
+      const uint32_t rs = rbase + rsl * C::RAW;
+      stage(std::integral_constant<int, 0>{}, u, rs);
+      stage(std::integral_constant<int, 1>{}, u, rs);
+      stage(std::integral_constant<int, 2>{}, u, rs);
+      stage(std::integral_constant<int, 3>{}, u, rs);
       __syncwarp();
       if (lane == 0) mbar_arrive(&rempty[rsl]);
     }
     // ---------------------------------------------------------- epilogue
-    grid_dep_wait();
-    wait_bounded(acc_bar, 0u, abort_flag, a.status);
-    umma::fence_after_sync();
-    const int qd = warp & 3;                // TMEM lanes 32 qd .. 32 qd + 31
-    const int row = 32 * qd + lane;         // weight row within the CTA
-    const int t = tile + row / kTileRows;
-    const bool row_ok = t < m.T;
-    const int sg = row_ok ? seg_of(m, t) : 0;
-    const int local = row_ok ? (t - m.tile0[sg]) * kTileRows + row % kTileRows : 0;
-    const bool valid = row_ok && local < a.seg[sg].rows;
-    const int col = (sg == 0 ? m.row0[0] : sg == 1 ? m.row0[1] : m.row0[2]) + local;
-    constexpr int CW = BN >= 64 ? BN / 2 : BN;  // columns per warp
-    const int c0 = BN >= 64 ? (warp >> 2) * CW : 0;
-    if (BN >= 64 || warp < 4) {
-      for (int cc = 0; cc < CW; cc += 32) {
-        float v[32];
-        umma::tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(c0 + cc), v);
+    constexpr int EW = BN >= 64 ? 8 : 4;        // epilogue warps
+    constexpr int CW = BN >= 64 ? BN / 2 : BN;  // columns per epilogue warp
+    if (warp < EW) {
+      grid_dep_wait();
+      wait_bounded(acc_bar, 0u, abort_flag, a.status);
+      umma::fence_after_sync();
+      const int qd = warp & 3;                // TMEM lanes 32 qd .. 32 qd + 31
+      const int row = 32 * qd + lane;         // weight row within the CTA
+      const int t = tile + row / kTileRows;
+      const bool row_ok = t < m.T;
+      const int sg = row_ok ? seg_of(m, t) : 0;
+      const int local = row_ok ? (t - m.tile0[sg]) * kTileRows + row % kTileRows : 0;
+      const bool valid = row_ok && local < a.seg[sg].rows;
+      const int col = (sg == 0 ? m.row0[0] : sg == 1 ? m.row0[1] : m.row0[2]) + local;
+      const int c0 = (warp >> 2) * CW;
+      for (int cc = 0; cc < CW; cc += 16) {
+        float v[16];
+        umma::tmem_ld16(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(c0 + cc), v);
         if (!valid) continue;
+        const int tk0 = n0 + c0 + cc;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int tok = n0 + c0 + cc + j;
-          if (tok >= a.T) continue;
-          const float val = v[j] * __ldg(a.inv_s + tok);
-          const int64_t o = (int64_t)tok * a.ldy + col;
-          if (ks > 1) {
-            __stcg(a.part + (int64_t)z * a.T * a.ldy + o, val);
-          } else {
-            a.y[o] = a.residual != nullptr ? a.residual[o] + val : val;
-          }
+        for (int j = 0; j < 16; ++j) v[j] *= tk0 + j < a.T ? __ldg(a.inv_s + tk0 + j) : 0.f;
+        if (ks > 1) {
+          float* dst = a.part + (int64_t)z * a.T * a.ldy + col;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (tk0 + j < a.T) __stcg(dst + (int64_t)(tk0 + j) * a.ldy, v[j]);
+        } else if (a.residual != nullptr) {
+          // every residual load before any store (the residual may alias y)
+          float r[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            r[j] = tk0 + j < a.T ? __ldcg(a.residual + (int64_t)(tk0 + j) * a.ldy + col) : 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (tk0 + j < a.T) a.y[(int64_t)(tk0 + j) * a.ldy + col] = r[j] + v[j];
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (tk0 + j < a.T) a.y[(int64_t)(tk0 + j) * a.ldy + col] = v[j];
         }
       }
     }
@@ -397,23 +426,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     *last_flag = last;
   }
   __syncthreads();
-  if (!*last_flag || warp >= 4) return;
-  {
-    const int row = 32 * warp + lane;
+  if (!*last_flag) return;
+  // element (row, token) -> thread; consecutive threads take consecutive rows
+  for (int e = tid; e < kBM * BN; e += kThreads) {
+    const int row = e % kBM, tok = n0 + e / kBM;
     const int t = tile + row / kTileRows;
-    if (t >= m.T) return;
+    if (t >= m.T || tok >= a.T) continue;
     const int sg = seg_of(m, t);
     const int local = (t - m.tile0[sg]) * kTileRows + row % kTileRows;
-    if (local >= a.seg[sg].rows) return;
+    if (local >= a.seg[sg].rows) continue;
     const int col = (sg == 0 ? m.row0[0] : sg == 1 ? m.row0[1] : m.row0[2]) + local;
-    for (int j = 0; j < BN; ++j) {
-      const int tok = n0 + j;
-      if (tok >= a.T) break;
-      const int64_t o = (int64_t)tok * a.ldy + col;
-      float v = 0.f;
-      for (int zz = 0; zz < ks; ++zz) v += __ldcg(a.part + (int64_t)zz * a.T * a.ldy + o);
-      a.y[o] = a.residual != nullptr ? a.residual[o] + v : v;
-    }
+    const int64_t o = (int64_t)tok * a.ldy + col;
+    float p[16];
+#pragma unroll
+    for (int zz = 0; zz < 16; ++zz) p[zz] = zz < ks ? __ldcg(a.part + (int64_t)zz * a.T * a.ldy + o) : 0.f;
+    const float r = a.residual != nullptr ? __ldcg(a.residual + o) : 0.f;
+    float v = 0.f;
+#pragma unroll
+    for (int zz = 0; zz < 16; ++zz) v += p[zz];  // split order
+    a.y[o] = r + v;
   }
 }
 
@@ -541,14 +572,16 @@ cudaError_t launch_bn(const TcGemmArgs& a, cudaStream_t s) {
   if ((e = encode_x(&map, a.x16, a.K, a.T, BN)) != cudaSuccess) return e;
   const TileMap m = tile_map(a);
   dim3 grid((m.T + kTiles - 1) / kTiles, (a.T + BN - 1) / BN, 1);
-  // Few CTAs would leave most SMs idle: split K so that waves x stages per
-  // split (plus a small cost per split for the partial sums) is least.
+  // Few CTAs, or a last wave that leaves most SMs idle: split K so that
+  // waves x (units per split + about one unit of pipeline fill), plus a small
+  // cost per split for the partial sums, is least.
   const int G = a.K / 256, base = (int)(grid.x * grid.y);
-  if (a.part != nullptr && a.counters != nullptr && base <= a.n_counters && base < sms) {
+  if (a.part != nullptr && a.counters != nullptr && base <= a.n_counters) {
     double best = 1e30;
     for (int k = 1; k <= 16 && k <= G; ++k) {
       if (k > 1 && (int64_t)k * a.T * a.ldy > a.part_cap) break;
-      const double cost = (double)((base * k + sms - 1) / sms) * ((G + k - 1) / k) + (k > 1 ? 0.25 * k : 0.0);
+      const double cost =
+          (double)((base * k + sms - 1) / sms) * ((G + k - 1) / k + 1) + (k > 1 ? 0.25 * k : 0.0);
       if (cost < best) {
         best = cost;
         grid.z = k;
