@@ -1,19 +1,33 @@
-"""Decode benchmark: batch-1 greedy decode of the Qwen3-8B-shaped Q4_0 model
-(vocab 151936, hidden 4096, 36 layers, 32/8 heads, head_dim 128, FFN 12288,
-f16 KV cache) after a 2048-token prompt, on one GB300 per rank.
+"""Decode benchmark of the Qwen3-8B-shaped Q4_0 model (vocab 151936, hidden
+4096, 36 layers, 32/8 heads, head_dim 128, FFN 12288, f16 KV cache) on one
+GB300 per rank.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
-One "step" is one full decode step (embedding, 36 layers, final norm, tied LM
-head, argmax) through the CUDA-graph replay of tq_decode_step.  Inputs are
-device-resident; the model (4.26 GB of weights) exceeds L2, so every step
-reads its weights from HBM.  Prints one JSON line.  Under torchrun each rank
-runs an independent replica (the step does not shard); `value` is the sum of
-tokens over all ranks divided by the slowest rank's time.
+Headline: batch-1 greedy decode after a 2048-token prompt.  One "step" is one
+full decode step (embedding, 36 layers, final norm, tied LM head, argmax)
+through the CUDA-graph replay of tq_decode_step; inputs are device-resident
+and the model's 4.26 GB of weights exceed L2, so every step reads them from
+HBM.  The same JSON line carries:
 
-`--impl reference` times the CPU oracle on this host's cores on a bounded
-sample of the same step (2 of the 36 layers at full size plus the LM head,
-scaled to a full step).
+* `roofline`: the step's dominant kernel, the GEMV chain that follows each
+  layer's attention (output projection, FFN, next layer's Q/K/V), launched as
+  in the step (tq_decode_chain) for layers 0..34 in a CUDA graph and timed
+  with CUDA events;
+* `e2e`: the same step through the public API with the token copied in from
+  pinned host memory and the argmax copied out, every step;
+* `prefill`: the 2048-token prompt, timed warm with CUDA events, with the
+  tensor-core GEMM's roofline (tq_gemm at 2048 rows over the 36 layers' gate
+  matrices);
+* `batched`: 32 sequences with seeded ragged contexts over a paged f16 cache,
+  one decode step of the whole batch per graph replay, with the batched
+  GEMM's roofline (tq_gemm at 32 rows over the 36 layers' down projections);
+* `cpu_baseline` (also inside `prefill` and `batched`): the oracle timed on
+  this host's cores on a bounded sample of each workload.
+
+Under torchrun every rank runs an independent replica (the step does not
+shard); `value` is the sum of tokens over all ranks divided by the slowest
+rank's time.  `--impl reference` times the oracle alone on this host's cores.
 """
 from __future__ import annotations
 
@@ -24,6 +38,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -31,6 +46,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode tokens/s (B=1, Q4_0 Qwen3-8B shape) and achieved HBM GB/s vs peak"
 PROMPT = 2048
+N_SAMPLE_LAYERS = 2
 
 
 def parse():
@@ -40,15 +56,14 @@ def parse():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["swiglu"], default=None,
-                    help="profiling case: run only the fused RMSNorm + gate/up + SwiGLU GEMV over "
-                         "the 36 layers' FFN weights of the 8B model (2 GB, larger than L2)")
-    ap.add_argument("--reps", type=int, default=2)
+    ap.add_argument("--no-batched", action="store_true", help="skip the batched sub-benchmark")
+    ap.add_argument("--batched-steps", type=int, default=30)
+    ap.add_argument("--prefill-reps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling cases only: keep the first N layers of the workload")
     ap.add_argument("--workload", default="qwen3_8b_q4_0",
-                    help="decode workload to time (the 8B batch-1 one by default; others for "
-                         "profiling small cases)")
+                    help="decode workload of the headline (profiling cases may pick another)")
     return ap.parse_args()
 
 
@@ -56,20 +71,20 @@ def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
-    return 6800.0, 1900.0, "fallback"
+        return {"hbm": float(d["hbm_gbs"]), "tc": float(d["bf16_tflops"]),
+                "tc_sust": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "kind": "measured"}
+    return {"hbm": 6800.0, "tc": 1900.0, "tc_sust": 1700.0, "kind": "fallback"}
 
 
-def dist_init(n):
+def dist_init():
     rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
     if world > 1:
         import torch.distributed as dist
-        backend = "nccl"
-        dist.init_process_group(backend)
+        dist.init_process_group("nccl")
     return rank, world
 
 
-def barrier_max(value, world):
+def reduce_max(value, world):
     if world == 1:
         return value
     import torch
@@ -96,9 +111,8 @@ class Clocks:
 
     def start(self):
         try:
-            import tempfile
-            self.path = tempfile.mktemp(suffix=".csv")
-            self.f = open(self.path, "w")
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            self.f = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
@@ -133,16 +147,13 @@ class Clocks:
 
 # ----------------------------------------------------------------------------- oracle timing
 
-N_SAMPLE_LAYERS = 2
-
-
 class OracleSample:
-    """The oracle (as it stands, float32) on a bounded sample of one decode
-    step of the 8B workload: 2 of the 36 full-size layers at a context of 2048
-    cached positions, plus the full 151936x4096 LM head.  One call of step()
-    returns the time of a full 36-layer step, scaled from the sample."""
+    """The oracle (as it stands, float32) on bounded samples of the three
+    workloads, over 2 of the 36 full-size layers (their layer time scaled to
+    36) plus the full 151936 x 4096 LM head.  Weights are decoded once, before
+    any timing."""
 
-    def __init__(self, ctx=PROMPT):
+    def __init__(self):
         import numpy as np
         import synth
         from oracle import model as om
@@ -157,24 +168,66 @@ class OracleSample:
         weights["output_norm"] = synth.host_tensor(w, "output_norm")
         self.m = om.OracleModel(w, weights, dtype=np.float32)
         for n in names + ["token_embd"]:
-            self.m.matrix(n)                      # decoded once, outside the timed region
-        kv = synth.host_normal(w.seed, synth.KV_STREAM, 2 * w.n_kv_heads * ctx * w.head_dim,
-                               sigma=1.0).reshape(2, w.n_kv_heads, ctx, w.head_dim)
-        self.kv = kv.astype(np.float16).astype(np.float32)
-        self.ctx = ctx
-        self.x0 = self.m.embed([1])
+            self.m.matrix(n)
         self.cores = len(os.sched_getaffinity(0))
-        self.desc = (f"oracle float32 decode step at context {ctx}: {N_SAMPLE_LAYERS} of "
-                     f"{w.n_layers} full-size layers and the 151936x4096 LM head timed, the "
-                     f"layer time scaled to {w.n_layers} layers; weights decoded before timing")
 
-    def step(self) -> float:
+    def _kv(self, stream, ctx):
         import numpy as np
-        cache = [(self.kv[0].copy(), self.kv[1].copy()) for _ in range(N_SAMPLE_LAYERS)]
+        import synth
+        w = self.w
+        kv = synth.host_normal(w.seed, stream, 2 * w.n_kv_heads * ctx * w.head_dim, sigma=1.0)
+        return kv.astype(np.float16).astype(np.float32).reshape(2, w.n_kv_heads, ctx, w.head_dim)
+
+    def decode_step(self, ctx=PROMPT):
+        """Seconds of one full batch-1 decode step at `ctx` cached positions."""
+        import numpy as np
+        import synth
+        kv = self._kv(synth.KV_STREAM, ctx)
+        cache = [(kv[0].copy(), kv[1].copy()) for _ in range(N_SAMPLE_LAYERS)]
+        x = self.m.embed([1])
         t0 = time.perf_counter()
-        x = self.x0
         for i in range(N_SAMPLE_LAYERS):
-            x = self.m.block(i, x, cache, np.array([self.ctx]))
+            x = self.m.block(i, x, cache, np.array([ctx]))
+        t1 = time.perf_counter()
+        self.m.head(x[-1])
+        t2 = time.perf_counter()
+        return (t1 - t0) / N_SAMPLE_LAYERS * self.w.n_layers + (t2 - t1)
+
+    def decode_desc(self, ctx=PROMPT):
+        return (f"oracle float32 batch-1 decode step at context {ctx}: {N_SAMPLE_LAYERS} of "
+                f"{self.w.n_layers} full-size layers and the 151936x4096 LM head timed, the layer "
+                f"time scaled to {self.w.n_layers} layers; weights decoded before timing")
+
+    def batched_step(self, lens, n_seq=4):
+        """Seconds of one batched decode step over len(lens) sequences, from
+        `n_seq` of them (their layer time scaled to all sequences and 36 layers;
+        the head for all sequences at once)."""
+        import numpy as np
+        import synth
+        x_all = self.m.embed(list(range(1, len(lens) + 1)))
+        t_layers = 0.0
+        for b in range(n_seq):
+            ctx = int(lens[b])
+            kv = self._kv(synth.KV_STREAM + 2 + b, ctx)
+            cache = [(kv[0].copy(), kv[1].copy()) for _ in range(N_SAMPLE_LAYERS)]
+            x = x_all[b:b + 1]
+            t0 = time.perf_counter()
+            for i in range(N_SAMPLE_LAYERS):
+                x = self.m.block(i, x, cache, np.array([ctx]))
+            t_layers += time.perf_counter() - t0
+        t0 = time.perf_counter()
+        self.m.head(x_all)
+        t_head = time.perf_counter() - t0
+        return t_layers / n_seq * len(lens) / N_SAMPLE_LAYERS * self.w.n_layers + t_head
+
+    def prefill(self, n=PROMPT):
+        """Seconds of a full n-token prefill (36 layers scaled from 2, last-row head)."""
+        import numpy as np
+        x = self.m.embed(self.w.prompt(n=n))
+        cache = self.m.new_cache()
+        t0 = time.perf_counter()
+        for i in range(N_SAMPLE_LAYERS):
+            x = self.m.block(i, x, cache, np.arange(n))
         t1 = time.perf_counter()
         self.m.head(x[-1])
         t2 = time.perf_counter()
@@ -186,47 +239,75 @@ def run_reference(args, rank, world):
         return
     o = OracleSample()
     for _ in range(args.warmup):
-        o.step()
-    total = sum(o.step() for _ in range(args.steps))
+        o.decode_step()
+    total = sum(o.decode_step() for _ in range(args.steps))
     value = args.steps / total
+    desc = o.decode_desc()
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 / value, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": "qwen3_8b_q4_0 batch-1 greedy decode after a 2048-token prompt",
-                       "sample": o.desc},
+                       "sample": desc},
             "cpu_baseline": {"value": round(value, 5), "unit": "tokens/s", "cores": o.cores,
-                             "kind": "oracle", "sample": o.desc},
+                             "kind": "oracle", "sample": desc},
             "e2e": {"value": round(value, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-# ----------------------------------------------------------------------------- GPU bench
+# ----------------------------------------------------------------------------- helpers
 
-def file_hash(path):
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+def file_hash(*paths):
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
 
 
-def traffic_from_profile(kernel_src):
-    """dram bytes per launch from the committed ncu summary of the dominant
-    GEMV phase, if it was taken on the current kernel source; else None.  The
-    summary carries two machine-readable lines: `source_sha256_16: <hex>` and
-    `dram_bytes_per_launch: <int>`."""
-    p = os.path.join(ROOT, "profiles", "gemv_chain_q4_0_swiglu_qwen3_8b.md")
+CSRC = os.path.join(ROOT, "block_quantized_transformer_gb300", "csrc")
+
+
+def traffic_of(name, *sources):
+    """DRAM bytes per launch of a kernel from profiles/traffic.json (written
+    from an ncu capture), if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    fields = {}
-    for ln in open(p):
-        if ":" in ln and ln.split(":", 1)[0].strip() in ("source_sha256_16", "dram_bytes_per_launch"):
-            k, v = ln.split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
-    if fields.get("source_sha256_16") != file_hash(kernel_src):
+    entry = json.load(open(p)).get(name)
+    if not entry or entry.get("source_sha256_16") != file_hash(*[os.path.join(CSRC, s) for s in sources]):
         return None
-    try:
-        return int(fields["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+    return int(entry["dram_bytes_per_launch"])
+
+
+def time_graph(fn, n, stream, reps=3):
+    """Mean time (ms) of one of the n launches that fn(i) enqueues, from a CUDA
+    graph of all n, replayed `reps` times between CUDA events on `stream`."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(n):                       # the first launches set kernel attributes
+            fn(i)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                fn(i)
+        g.replay()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        stream.synchronize()
+    return e0.elapsed_time(e1) / (reps * n)
+
+
+# ----------------------------------------------------------------------------- GPU bench
+
+def q4_bytes(rows, cols):
+    return rows * cols // 32 * 18
 
 
 def run_gpu(args, rank, world):
@@ -243,28 +324,36 @@ def run_gpu(args, rank, world):
     if args.layers:
         import dataclasses
         w = dataclasses.replace(w, n_layers=args.layers)
-    if w.batch > 1:
-        return run_gpu_batched(args, rank, world, w)
+    pk = peaks()
     K, W = args.steps, args.warmup
-    prompt_len = w.prompt_len
-    max_ctx = prompt_len + W + K + 8
+    P = w.prompt_len
+    E = args.e2e_steps
+    max_ctx = P + W + K + E + 16
     mats, gains = build_weights(w, dev)
-    model = build_model(w, device=dev, max_ctx=max_ctx, max_prefill=prompt_len,
-                        weights=(mats, gains))
+    model = build_model(w, device=dev, max_ctx=max_ctx, max_prefill=P, weights=(mats, gains))
     torch.cuda.synchronize()
     weight_bytes = model.weight_bytes() + sum(g.numel() * 4 for g in gains.values())
     stream = torch.cuda.Stream(device=dev)
     prompt = torch.tensor(w.prompt(), dtype=torch.int32, device=dev)
+    L = w.n_layers
+
     with torch.cuda.stream(stream):
-        t0 = time.perf_counter()
+        # ---- prefill, warm: one untimed call, then reps calls between CUDA events
         am = model.prefill(prompt)
         stream.synchronize()
-        prefill_s = time.perf_counter() - t0
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        for _ in range(args.prefill_reps):
+            am = model.prefill(prompt)
+        p1.record(stream)
+        stream.synchronize()
+        prefill_ms = p0.elapsed_time(p1) / args.prefill_reps
+
+        # ---- batch-1 decode: warm-up (graph capture on the first replay), timed region
         tok = torch.empty(1, dtype=torch.int32, device=dev)
         tok.copy_(am)
-        pos = torch.full((1,), prompt_len, dtype=torch.int32, device=dev)
-        logits = None
-        # warm-up (graph capture happens on the first replay)
+        pos = torch.full((1,), P, dtype=torch.int32, device=dev)
         for _ in range(W):
             model.decode_step(tok, pos, pos, argmax=tok, graph=True)
             pos.add_(1)
@@ -287,33 +376,33 @@ def run_gpu(args, rank, world):
         clk = clocks.stop()
         barrier(world)
         assert model.status() == 0
-    ms_max = barrier_max(ms, world)
+    ms_max = reduce_max(ms, world)
     ms_step = ms_max / K
+    value = world * K / (ms_max / 1e3)
 
     # algorithmic bytes per step: all weights + KV read at each step's context + KV write
     esz = 2 if w.kv == "f16" else 4
-    kv_row = 2 * w.n_kv_heads * w.head_dim * esz * w.n_layers        # bytes per cached position
+    kv_row = 2 * w.n_kv_heads * w.head_dim * esz * L              # bytes per cached position
     mean_ctx = ctx0 + (K - 1) / 2.0 + 1
     step_bytes = weight_bytes + kv_row * mean_ctx + kv_row
-    value = world * K / (ms_max / 1e3)
-    hbm, bf16, peak_kind = peaks()
 
-    # ---- dominant kernel alone: fused RMSNorm + gate/up GEMV + SwiGLU over all 36 layers
-    x = torch.randn(1, w.hidden, device=dev)
-    act = torch.empty(1, w.ffn, device=dev)
-    g_bytes = [mats[f"blk.{i}.ffn_gate"].nbytes + mats[f"blk.{i}.ffn_up"].nbytes for i in range(w.n_layers)]
-    kern_ms = time_swiglu_graph(tq, [mats[f"blk.{i}.ffn_gate"] for i in range(w.n_layers)],
-                                [mats[f"blk.{i}.ffn_up"] for i in range(w.n_layers)],
-                                [gains[f"blk.{i}.ffn_norm"] for i in range(w.n_layers)], x, act, stream)
-    kern_bytes = sum(g_bytes) / w.n_layers + 4 * (w.hidden * 2 + w.ffn)
-    achieved = kern_bytes / (kern_ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4),
-                "traffic": traffic_from_profile(os.path.join(ROOT, "block_quantized_transformer_gb300",
-                                                              "csrc", "gemv_impl.cuh")),
-                "kernel": "gemv_chain_kernel<Q4_0>, one RMSNorm + gate/up + SwiGLU phase, 2x12288x4096",
-                "peak_kind": peak_kind + " (burst copy, kernel timed alone)",
-                "launch_ms": round(kern_ms, 5), "bytes_per_launch": int(kern_bytes)}
+    # ---- dominant kernel: the GEMV chain after each attention, as launched in the step
+    H, F, nq, nkv, hd = w.hidden, w.ffn, w.n_heads, w.n_kv_heads, w.head_dim
+    chain_bytes = (q4_bytes(H, nq * hd) + 2 * q4_bytes(F, H) + q4_bytes(H, F)
+                   + q4_bytes((nq + 2 * nkv) * hd, H))
+    chain_act = 4 * (2 * H + 2 * nq * hd + 2 * H + F + 2 * H + F + H + (nq + 2 * nkv) * hd)
+    n_chain = max(1, L - 1)
+    chain_ms = time_graph(lambda i: model.decode_chain(i), n_chain, stream)
+    chain_alg = chain_bytes + chain_act
+    roofline = {"bound": "hbm", "achieved": round(chain_alg / (chain_ms / 1e3) / 1e9, 1), "peak": pk["hbm"],
+                "unit": "GB/s", "frac": round(chain_alg / (chain_ms / 1e3) / 1e9 / pk["hbm"], 4),
+                "traffic": traffic_of("gemv_chain_layer_qwen3_8b_q4_0", "gemv_impl.cuh", "gemv.cu",
+                                      "gemv_q4.cu"),
+                "kernel": "gemv_chain_kernel<Q4_0>: output projection + residual, RMSNorm + gate/up "
+                          "+ SwiGLU, down projection + residual, next layer's RMSNorm + Q/K/V",
+                "timing": f"tq_decode_chain for layers 0..{n_chain - 1} in one CUDA graph, CUDA events",
+                "peak_kind": pk["kind"] + " copy bandwidth",
+                "launch_ms": round(chain_ms, 5), "bytes_per_launch": int(chain_alg)}
 
     # ---- end to end: host token in, host argmax out, every step
     h_tok = torch.empty(1, dtype=torch.int32, pin_memory=True)
@@ -323,21 +412,10 @@ def run_gpu(args, rank, world):
     d_pos = torch.empty(1, dtype=torch.int32, device=dev)
     d_out = torch.empty(1, dtype=torch.int32, device=dev)
     h_tok[0] = int(tok.item())
-    p = int(pos.item())
-    e2e_steps = min(K, max(1, max_ctx - p - 1))
+    p = ctx0 + K
     with torch.cuda.stream(stream):
-        h_pos[0] = p
-        d_tok.copy_(h_tok, non_blocking=True)
-        d_pos.copy_(h_pos, non_blocking=True)
-        model.decode_step(d_tok, d_pos, d_pos, argmax=d_out, graph=True)   # capture
-        h_out.copy_(d_out, non_blocking=True)
-        stream.synchronize()
-        p += 1
-        h_tok[0] = int(h_out[0])
-        e2e_steps = min(e2e_steps, max_ctx - p - 1)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for _ in range(e2e_steps):
+        def e2e_step():
+            nonlocal p
             h_pos[0] = p
             d_tok.copy_(h_tok, non_blocking=True)
             d_pos.copy_(h_pos, non_blocking=True)
@@ -346,55 +424,117 @@ def run_gpu(args, rank, world):
             stream.synchronize()
             h_tok[0] = int(h_out[0])
             p += 1
+        e2e_step()                                  # graph capture with these buffers
+        e2e_steps = min(E, max_ctx - p - 1)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
         e2e_s = time.perf_counter() - t0
-    e2e_s = barrier_max(e2e_s, world)
-    e2e = {"value": world * e2e_steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 8,
+    e2e_s = reduce_max(e2e_s, world)
+    e2e = {"value": round(world * e2e_steps / e2e_s, 2), "unit": "tokens/s", "h2d_bytes_per_step": 8,
            "d2h_bytes_per_step": 4, "steps": e2e_steps}
-
     launches = model.launches_per_step * K
     model.close()
 
+    # ---- prefill roofline: the tensor-core GEMM at 2048 rows (gate matrices of every layer)
+    x = torch.randn(P, H, device=dev)
+    y = torch.empty(P, F, device=dev)
+    scr = torch.empty(tq.lib().tq_gemm_scratch_bytes(F, P, H) + 256, dtype=torch.uint8, device=dev)
+    gemm_ms = time_graph(lambda i: tq.tq_gemm(mats[f"blk.{i}.ffn_gate"], x, out=y, scratch=scr), L, stream)
+    gemm_flop = 2.0 * P * F * H
+    prefill_flop = 2.0 * P * weight_count_layers(w) + attn_prefill_flop(w, P)
+    prefill = {"tokens": P, "ms": round(prefill_ms, 3), "tokens_per_s": round(world * P / (prefill_ms / 1e3), 1),
+               "timing": f"warm, {args.prefill_reps} calls between CUDA events",
+               "tflops": round(prefill_flop / (prefill_ms / 1e3) / 1e12, 1),
+               "frac_of_tensor_peak": round(prefill_flop / (prefill_ms / 1e3) / 1e12 / pk["tc_sust"], 4),
+               "tensor_peak_tflops": pk["tc_sust"], "flop": prefill_flop,
+               "roofline": {"bound": "tensor", "achieved": round(gemm_flop / (gemm_ms / 1e3) / 1e12, 1),
+                            "peak": pk["tc"], "unit": "TFLOP/s",
+                            "frac": round(gemm_flop / (gemm_ms / 1e3) / 1e12 / pk["tc"], 4),
+                            "traffic": traffic_of("tcgemm_prefill_gate_qwen3_8b_q4_0", "tcgemm.cu"),
+                            "kernel": "tcgemm_kernel<Q4_0, 256> (tcgen05, fp16 operands, f32 TMEM) + "
+                                      "xprep16: gate projection 12288x4096 at 2048 rows",
+                            "timing": f"tq_gemm over the {L} layers' gate matrices in one CUDA graph",
+                            "peak_kind": pk["kind"] + " bf16 dense burst (fp16 has the same rate)",
+                            "launch_ms": round(gemm_ms, 5), "flop_per_launch": gemm_flop}}
+    del x, y, scr
+
+    batched = None
+    if not args.no_batched and w.name == "qwen3_8b_q4_0":
+        batched = run_batched(args, world, mats, gains, dev, stream, pk)
+
     line = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": f"{w.name} batch-1 greedy decode after a {prompt_len}-token prompt "
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32 (decode GEMVs: exact codes x 21-bit activations, f32 sums); prefill/batched "
+                     "GEMMs: fp16 x fp16 -> f32 (tcgen05)",
+            "data": "synthetic",
+            "config": {"workload": f"{w.name} batch-1 greedy decode after a {P}-token prompt "
                                    f"(context {ctx0}..{ctx0 + K - 1})",
                        "weights": "Q4_0, 4.26 GB, seeded N(0,0.02)", "kv_cache": "f16",
                        "l2": "inputs exceed L2 (4.3 GB of weights read every step)",
                        "parallelism": f"replicas x{world}"},
             "hbm": {"step_bytes": int(step_bytes), "achieved_gbs": round(step_bytes / (ms_step / 1e3) / 1e9, 1),
-                    "frac_of_peak": round(step_bytes / (ms_step / 1e3) / 1e9 / hbm, 4),
-                    "peak_gbs": hbm, "peak_kind": peak_kind,
-                    "roofline_tokens_per_s": round(hbm * 1e9 / step_bytes, 1)},
+                    "frac_of_peak": round(step_bytes / (ms_step / 1e3) / 1e9 / pk["hbm"], 4),
+                    "peak_gbs": pk["hbm"], "peak_kind": pk["kind"],
+                    "roofline_tokens_per_s": round(pk["hbm"] * 1e9 / step_bytes, 1)},
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
-            "prefill": {"tokens": prompt_len, "seconds": round(prefill_s, 4),
-                        "tokens_per_s": round(prompt_len / prefill_s, 1)}}
-    if rank == 0 and not args.no_cpu_baseline:
+            "prefill": prefill}
+    if batched is not None:
+        line["batched"] = batched
+    if rank == 0 and not args.no_cpu_baseline and w.name == "qwen3_8b_q4_0" and not args.layers:
         o = OracleSample()
-        o.step()
-        per_step = min(o.step() for _ in range(3))
-        line["cpu_baseline"] = {"value": round(1.0 / per_step, 5), "unit": "tokens/s",
-                                "cores": o.cores, "kind": "oracle", "sample": o.desc}
+        o.decode_step()
+        per_step = min(o.decode_step() for _ in range(3))
+        line["cpu_baseline"] = {"value": round(1.0 / per_step, 5), "unit": "tokens/s", "cores": o.cores,
+                                "kind": "oracle", "sample": o.decode_desc()}
+        pf = o.prefill()
+        line["prefill"]["cpu_baseline"] = {
+            "value": round(PROMPT / pf, 3), "unit": "tokens/s", "cores": o.cores, "kind": "oracle",
+            "sample": f"oracle float32 prefill of the {PROMPT}-token prompt: {N_SAMPLE_LAYERS} of "
+                      f"{w.n_layers} full-size layers timed, scaled to {w.n_layers}, plus the last-row head"}
+        if batched is not None:
+            lens = synth.QWEN3_8B_Q4_BATCHED.context_lengths()
+            bs = o.batched_step(lens)
+            line["batched"]["cpu_baseline"] = {
+                "value": round(len(lens) / bs, 4), "unit": "tokens/s", "cores": o.cores, "kind": "oracle",
+                "sample": f"oracle float32 batched step: 4 of {len(lens)} sequences (their seeded "
+                          f"contexts) through {N_SAMPLE_LAYERS} of {w.n_layers} full-size layers, scaled "
+                          f"to all sequences and layers, plus the LM head for all {len(lens)}"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
-def run_gpu_batched(args, rank, world, w):
-    """Batched decode over a paged f16 cache: w.batch sequences whose cached
-    lengths come from the workload's seeded length generator, their pages
-    handed out in a seeded shuffled order, the cache filled with seeded N(0, 1)
-    values (no prefill: the step's cost does not depend on what the cache
-    holds), then greedy decode steps of the whole batch, timed with CUDA events
-    around graph replays."""
+def weight_count_layers(w):
+    """Weights multiplied per token in prefill: every layer's projections and the head row."""
+    H, F, hd = w.hidden, w.ffn, w.head_dim
+    per_layer = H * (w.n_heads + 2 * w.n_kv_heads) * hd + w.n_heads * hd * H + 3 * F * H
+    return per_layer * w.n_layers
+
+
+def attn_prefill_flop(w, T):
+    """Causal attention of a T-token prompt: q.k and p.v over j <= i for every
+    query head and layer."""
+    pairs = T * (T + 1) / 2
+    return 2.0 * 2.0 * pairs * w.n_heads * w.head_dim * w.n_layers
+
+
+def run_batched(args, world, mats, gains, dev, stream, pk):
+    """32 sequences of the batched serving mix over a paged f16 cache: cached
+    lengths from the seeded length generator, pages handed out in a seeded
+    shuffled order, the cache filled with seeded N(0, 1) values (no prefill:
+    the step's cost does not depend on what the cache holds), then greedy
+    decode steps of the whole batch, timed with CUDA events around graph
+    replays."""
     import numpy as np
     import torch
     import synth
-    from block_quantized_transformer_gb300.synthetic import build_weights, build_model
+    import block_quantized_transformer_gb300 as tq
+    from block_quantized_transformer_gb300.synthetic import build_model
 
-    local = int(os.environ.get("LOCAL_RANK", 0))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    K, W = args.steps, args.warmup
+    w = synth.QWEN3_8B_Q4_BATCHED
+    K, W = args.batched_steps, 3
     B, P = w.batch, w.page_size
     lens = w.context_lengths().astype(np.int64)
     need = lens + W + K + 1
@@ -409,7 +549,6 @@ def run_gpu_batched(args, rank, world, w):
     for b in range(B):
         table[b, :n_pages_seq[b]] = order[at:at + n_pages_seq[b]]
         at += n_pages_seq[b]
-    mats, gains = build_weights(w, dev)
     model = build_model(w, device=dev, max_batch=B, max_ctx=max_ctx, max_prefill=B,
                         page_size=P, n_pages=n_pages, weights=(mats, gains))
     chunk = 1 << 26
@@ -425,7 +564,6 @@ def run_gpu_batched(args, rank, world, w):
     bt = torch.tensor(table, device=dev)
     tok = torch.tensor(synth.uniform_below(w.seed, synth.PROMPT_STREAM, B, w.vocab).astype(np.int32), device=dev)
     pos = torch.tensor(lens.astype(np.int32), device=dev)
-    stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         for _ in range(W):
             model.decode_step(tok, pos, pos, block_table=bt, argmax=tok, graph=True)
@@ -433,8 +571,6 @@ def run_gpu_batched(args, rank, world, w):
         stream.synchronize()
         barrier(world)
         torch.cuda.synchronize()
-        clocks = Clocks(local)
-        clocks.start()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -444,89 +580,53 @@ def run_gpu_batched(args, rank, world, w):
         e1.record(stream)
         stream.synchronize()
         ms = e0.elapsed_time(e1)
-        clk = clocks.stop()
         barrier(world)
         assert model.status() == 0
-    ms_max = barrier_max(ms, world)
+    ms_max = reduce_max(ms, world)
     ms_step = ms_max / K
     kv_row = 2 * w.n_kv_heads * w.head_dim * 2 * w.n_layers
     ctx_sum = float((lens + W + 1).sum()) + B * (K - 1) / 2.0
     step_bytes = weight_bytes + kv_row * ctx_sum + kv_row * B
-    hbm, _, peak_kind = peaks()
     launches = model.decode_launches(B) * K
     model.close()
-    line = {"metric": f"decode tokens/s (B={B}, Q4_0 Qwen3-8B shape, paged f16 KV) and achieved HBM GB/s vs peak",
-            "value": round(world * B * K / (ms_max / 1e3), 2), "unit": "tokens/s", "n_gpus": world,
-            "steps": K, "warmup": W, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+    del model
+    torch.cuda.empty_cache()
+
+    # the batched GEMM as the step runs it: 32 rows, K split across CTAs (down projections)
+    H, F, L = w.hidden, w.ffn, w.n_layers
+    x = torch.randn(B, F, device=dev)
+    y = torch.empty(B, H, device=dev)
+    scr = torch.empty(tq.lib().tq_gemm_scratch_bytes(H, B, F) + 256, dtype=torch.uint8, device=dev)
+    gemm_ms = time_graph(lambda i: tq.tq_gemm(mats[f"blk.{i}.ffn_down"], x, out=y, scratch=scr), L, stream)
+    gemm_bytes = q4_bytes(H, F) + 4 * B * (F + H)
+    return {"metric": f"decode tokens/s (B={B}, Q4_0 Qwen3-8B shape, paged f16 KV)",
+            "value": round(world * B * K / (ms_max / 1e3), 2), "unit": "tokens/s", "steps": K, "warmup": W,
+            "ms_per_step": round(ms_step, 4),
             "config": {"workload": f"{w.name}: {B} sequences, cached lengths {int(lens.min())}..{int(lens.max())} "
                                    f"(sum {int(lens.sum())}), pages of {P} tokens in a seeded shuffled order",
-                       "weights": "Q4_0, 4.26 GB, seeded N(0,0.02)", "kv_cache": "f16, seeded N(0,1)",
-                       "l2": "inputs exceed L2", "parallelism": f"replicas x{world}"},
+                       "kv_cache": "f16, seeded N(0,1)", "l2": "inputs exceed L2"},
             "hbm": {"step_bytes": int(step_bytes), "achieved_gbs": round(step_bytes / (ms_step / 1e3) / 1e9, 1),
-                    "frac_of_peak": round(step_bytes / (ms_step / 1e3) / 1e9 / hbm, 4), "peak_gbs": hbm,
-                    "peak_kind": peak_kind, "roofline_tokens_per_s": round(B * hbm * 1e9 / step_bytes, 1)},
-            "gpu_launches": launches, "clocks": clk}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-
-
-def time_swiglu_graph(tq, gate, up, gains, x, act, stream, reps=5):
-    """Mean duration of one fused RMSNorm + gate/up + SwiGLU GEMV launch: the
-    launches over all layers' matrices (each larger than half of L2, together
-    far larger) are captured in a CUDA graph and replayed, so host launch
-    overhead is not timed; CUDA events on the launching stream."""
-    import torch
-    n = len(gate)
-    with torch.cuda.stream(stream):
-        for i in range(n):                         # first launches set kernel attributes
-            tq.tq_swiglu_gemv(gate[i], up[i], x, gains[i], out=act)
-        stream.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
-                tq.tq_swiglu_gemv(gate[i], up[i], x, gains[i], out=act)
-        g.replay()
-        stream.synchronize()
-        k0 = torch.cuda.Event(enable_timing=True)
-        k1 = torch.cuda.Event(enable_timing=True)
-        k0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        k1.record(stream)
-        stream.synchronize()
-    return k0.elapsed_time(k1) / (reps * n)
-
-
-def run_kernel_case(args):
-    import torch
-    import synth
-    import block_quantized_transformer_gb300 as tq
-    from block_quantized_transformer_gb300.synthetic import build_matrix, build_gain
-    w = synth.QWEN3_8B_Q4
-    dev = torch.device("cuda", 0)
-    gate = [build_matrix(w, f"blk.{i}.ffn_gate", dev) for i in range(w.n_layers)]
-    up = [build_matrix(w, f"blk.{i}.ffn_up", dev) for i in range(w.n_layers)]
-    gn = [build_gain(w, f"blk.{i}.ffn_norm", dev) for i in range(w.n_layers)]
-    x = torch.randn(1, w.hidden, device=dev)
-    act = torch.empty(1, w.ffn, device=dev)
-    ms = time_swiglu_graph(tq, gate, up, gn, x, act, torch.cuda.Stream(device=dev), reps=args.reps)
-    nbytes = gate[0].nbytes + up[0].nbytes
-    print(json.dumps({"kernel": "swiglu_gemv q4_0 2x12288x4096", "launches": args.reps * w.n_layers,
-                      "timing": "CUDA graph of 36 launches, replayed",
-                      "ms_per_launch": ms, "gbs": nbytes / ms / 1e6}))
+                    "frac_of_peak": round(step_bytes / (ms_step / 1e3) / 1e9 / pk["hbm"], 4),
+                    "peak_gbs": pk["hbm"], "roofline_tokens_per_s": round(B * pk["hbm"] * 1e9 / step_bytes, 1)},
+            "roofline": {"bound": "hbm", "achieved": round(gemm_bytes / (gemm_ms / 1e3) / 1e9, 1),
+                         "peak": pk["hbm"], "unit": "GB/s",
+                         "frac": round(gemm_bytes / (gemm_ms / 1e3) / 1e9 / pk["hbm"], 4),
+                         "traffic": traffic_of("tcgemm_batched_down_qwen3_8b_q4_0", "tcgemm.cu"),
+                         "kernel": "tcgemm_kernel<Q4_0, 32> (tcgen05) + xprep16: down projection "
+                                   "4096x12288 at 32 rows, K split across CTAs as in the step",
+                         "timing": f"tq_gemm over the {L} layers' down matrices in one CUDA graph",
+                         "peak_kind": pk["kind"] + " copy bandwidth",
+                         "launch_ms": round(gemm_ms, 5), "bytes_per_launch": int(gemm_bytes)},
+            "gpu_launches": launches}
 
 
 def main():
     args = parse()
-    if args.kernel is not None:
-        run_kernel_case(args)
-        return
     if args.impl == "reference":
         rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
         run_reference(args, rank, world)
         return
-    rank, world = dist_init(args.gpus)
+    rank, world = dist_init()
     run_gpu(args, rank, world)
     if world > 1:
         import torch.distributed as dist

@@ -35,7 +35,8 @@ BLOCK_BYTES = {TQ_Q4_0: 18, TQ_Q8_0: 34}
 QS_BYTES = {TQ_Q4_0: 16, TQ_Q8_0: 32}
 
 EXPORTS = ("tq_workspace_bytes", "tq_kv_cache_bytes", "tq_model_create", "tq_prefill",
-           "tq_decode_step", "tq_decode_step_graph", "tq_model_status", "tq_model_set_wait_limit",
+           "tq_decode_step", "tq_decode_step_graph", "tq_decode_chain", "tq_model_status",
+           "tq_model_set_wait_limit",
            "tq_model_poisoned",
            "tq_decode_launches", "tq_model_free", "tq_last_error", "tq_qmat_bytes", "tq_repack", "tq_quantize",
            "tq_dequantize", "tq_gemv", "tq_gemm_scratch_bytes", "tq_gemm", "tq_swiglu_gemv", "tq_lm_head",
@@ -105,6 +106,7 @@ def lib() -> ctypes.CDLL:
                 "tq_decode_step_graph": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
                 "tq_model_status": (i32, [vp, vp, ctypes.POINTER(ctypes.c_uint32)]),
                 "tq_model_set_wait_limit": (i32, [vp, ctypes.c_uint32]),
+                "tq_decode_chain": (i32, [vp, i32, vp]),
                 "tq_model_poisoned": (ctypes.c_int, [vp]),
                 "tq_decode_launches": (i32, [vp, i32]),
                 "tq_model_free": (None, [vp]),
@@ -115,7 +117,7 @@ def lib() -> ctypes.CDLL:
                 "tq_quantize": (i32, [i32, vp, i64, i64, vp, vp]),
                 "tq_dequantize": (i32, [i32, TqQmat, i64, i64, i64, vp, vp]),
                 "tq_gemv": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, vp, vp]),
-                "tq_gemm_scratch_bytes": (ctypes.c_size_t, [i32, i32]),
+                "tq_gemm_scratch_bytes": (ctypes.c_size_t, [i32, i32, i32]),
                 "tq_gemm": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, vp, vp, vp]),
                 "tq_swiglu_gemv": (i32, [i32, TqQmat, TqQmat, i32, i32, vp, i32, vp, f32, vp, vp]),
                 "tq_lm_head": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, f32, vp, vp, vp, vp]),
@@ -291,14 +293,20 @@ def tq_gemv(m: QMat, x: torch.Tensor, residual: Optional[torch.Tensor] = None,
 
 
 def tq_gemm(m: QMat, x: torch.Tensor, residual: Optional[torch.Tensor] = None,
-            out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """y[t] = residual[t] + W x[t] for x [n_rows][cols] f32: the prefill GEMM."""
+            out: Optional[torch.Tensor] = None, scratch: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """y[t] = residual[t] + W x[t] for x [n_rows][cols] f32: the GEMM of
+    prefill and batched decode.  `scratch`: optional uint8 device buffer of at
+    least tq_gemm_scratch_bytes(rows, n_rows, cols) + 256 bytes, reused across
+    calls (calls on it must not overlap)."""
     x2 = x.reshape(-1, m.cols)
     T = _int("n_rows", x2.shape[0], 1, I32[1])
-    nb = int(lib().tq_gemm_scratch_bytes(T, m.cols))
+    nb = int(lib().tq_gemm_scratch_bytes(m.rows, T, m.cols))
     if nb == 0:
         raise TqError(f"tq_gemm: unsupported shape ({T}, {m.cols})")
-    scratch = torch.empty(nb + 256, dtype=torch.uint8, device=x.device)
+    if scratch is None:
+        scratch = torch.empty(nb + 256, dtype=torch.uint8, device=x.device)
+    elif scratch.numel() < nb + 256:
+        raise TqError(f"scratch holds {scratch.numel()} bytes, needs {nb + 256}")
     off = (-scratch.data_ptr()) % 256
     if out is None:
         out = torch.empty(T, m.rows, dtype=torch.float32, device=x.device)
@@ -511,6 +519,12 @@ class Model:
                 _dev(argmax, "argmax", torch.int32, B), _stream(self.device))
         self._after(rc, "tq_decode_step_graph" if graph else "tq_decode_step")
         return argmax
+
+    def decode_chain(self, layer: int) -> None:
+        """Enqueue the batch-1 decode step's GEMV chain after `layer`'s attention
+        on its own (tq_decode_chain), over the workspace's current activations."""
+        _int("layer", layer, 0, self.cfg.n_layers - 1)
+        self._after(lib().tq_decode_chain(self._h(), layer, _stream(self.device)), "tq_decode_chain")
 
     def set_wait_limit(self, polls: int) -> None:
         """Polls after which a GEMV chain's grid-wide waits give up (0: the

@@ -460,6 +460,32 @@ cudaError_t run_head_gemm(tq_model* m, int B, float* logits, int32_t* argmax, cu
   return e;
 }
 
+// The GEMV chain that follows layer l's attention: output projection +
+// residual, RMSNorm + gate/up + SwiGLU, down projection + residual, then the
+// next layer's RMSNorm + Q/K/V (after the last layer: final norm + LM head +
+// argmax keys over `head_B` rows at head_x).
+tq::GemvChain layer_chain(const tq_model* m, int l, int T, const float* head_x, int head_B, float* logits) {
+  const tq_config& c = m->cfg;
+  tq::GemvChain ch{};
+  ch.ph[0] = out_args(m, l, T);
+  ch.mode[0] = tq::GEMV_STORE;
+  ch.ph[1] = ffn_args(m, l, T);
+  ch.mode[1] = tq::GEMV_SWIGLU;
+  ch.ph[2] = down_args(m, l, T);
+  ch.mode[2] = tq::GEMV_STORE;
+  if (l + 1 < c.n_layers) {
+    ch.ph[3] = qkv_args(m, l + 1, T);
+    ch.mode[3] = tq::GEMV_STORE;
+  } else {
+    ch.ph[3] = head_args(m, head_x, head_B, logits);
+    ch.mode[3] = tq::GEMV_ARGMAX;
+  }
+  ch.n = 4;
+  ch.sync = m->chain_sync();
+  ch.sync_limit = m->chain_wait_limit;
+  return ch;
+}
+
 // The layers and the head.  The GEMVs between two attention launches run as
 // one persistent chain: output projection, gate/up, down projection of layer
 // l and the Q/K/V projection of layer l+1 (the LM head after the last layer),
@@ -489,23 +515,7 @@ cudaError_t run_layers(tq_model* m, int T, const int32_t* pos, const int32_t* kv
     const tq::AttnArgs a = attn_args(m, l, T, pos, kv_len, pos_base, seq_fixed, block_table, prefill);
     if ((e = tq::launch_attn_decode(c.kvtype, hd, G, a, s)) != cudaSuccess) return e;
     // output projection, FFN, and the next layer's Q/K/V (or the head)
-    tq::GemvChain ch{};
-    ch.ph[0] = out_args(m, l, T);
-    ch.mode[0] = tq::GEMV_STORE;
-    ch.ph[1] = ffn_args(m, l, T);
-    ch.mode[1] = tq::GEMV_SWIGLU;
-    ch.ph[2] = down_args(m, l, T);
-    ch.mode[2] = tq::GEMV_STORE;
-    if (l + 1 < c.n_layers) {
-      ch.ph[3] = qkv_args(m, l + 1, T);
-      ch.mode[3] = tq::GEMV_STORE;
-    } else {
-      ch.ph[3] = head_args(m, head_x, head_B, logits);
-      ch.mode[3] = tq::GEMV_ARGMAX;
-    }
-    ch.n = 4;
-    ch.sync = m->chain_sync();
-    ch.sync_limit = m->chain_wait_limit;
+    const tq::GemvChain ch = layer_chain(m, l, T, head_x, head_B, logits);
     if ((e = tq::launch_gemv_chain(c.wtype, ch, s)) != cudaSuccess) return e;
   }
   return tq::launch_argmax_finish(m->keys(), head_B, argmax, s);
@@ -732,6 +742,16 @@ tq_status tq_model_set_wait_limit(tq_model* m, uint32_t polls) {
   return TQ_OK;
 }
 
+tq_status tq_decode_chain(tq_model* m, int32_t layer, void* stream) {
+  if (refuse_if_poisoned(m)) return TQ_REFUSED;
+  if (layer < 0 || layer >= m->cfg.n_layers)
+    return set_error("layer=%d outside [0, n_layers=%d)", layer, m->cfg.n_layers), TQ_REFUSED;
+  const tq::GemvChain ch = layer_chain(m, layer, 1, m->x(), 1, nullptr);
+  cudaError_t e = tq::launch_gemv_chain(m->cfg.wtype, ch, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(m, e, "tq_decode_chain");
+  return TQ_OK;
+}
+
 int tq_model_poisoned(const tq_model* m) { return (m != nullptr && m->poisoned) ? 1 : 0; }
 
 int32_t tq_decode_launches(const tq_model* m, int32_t batch) {
@@ -821,9 +841,10 @@ tq_status tq_gemv(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const fl
 
 namespace {
 struct GemmScratch {
-  size_t x16, inv_s, total;
+  size_t x16, inv_s, part, counters, total;
+  int64_t part_floats;
 };
-GemmScratch gemm_scratch(int32_t n_rows, int32_t cols) {
+GemmScratch gemm_scratch(int32_t rows, int32_t n_rows, int32_t cols) {
   GemmScratch g{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -833,14 +854,18 @@ GemmScratch gemm_scratch(int32_t n_rows, int32_t cols) {
   };
   g.x16 = take((size_t)n_rows * cols * 2);
   g.inv_s = take((size_t)n_rows * 4);
+  // partial sums of up to 16 splits of K, within the model's cap
+  g.part_floats = std::min<int64_t>((int64_t)16 * n_rows * rows, kGemmPartFloats);
+  g.part = take((size_t)g.part_floats * 4);
+  g.counters = take((size_t)kGemmCounters * 4);
   g.total = off;
   return g;
 }
 }  // namespace
 
-size_t tq_gemm_scratch_bytes(int32_t n_rows, int32_t cols) {
-  if (n_rows < 1 || cols < 256 || cols % 256 != 0 || cols > 12288) return 0;
-  return gemm_scratch(n_rows, cols).total;
+size_t tq_gemm_scratch_bytes(int32_t rows, int32_t n_rows, int32_t cols) {
+  if (rows < 1 || n_rows < 1 || cols < 256 || cols % 256 != 0 || cols > 12288) return 0;
+  return gemm_scratch(rows, n_rows, cols).total;
 }
 
 tq_status tq_gemm(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const float* x, int32_t n_rows,
@@ -852,7 +877,7 @@ tq_status tq_gemm(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const fl
   if (!aligned16(w.qs_dev) || !aligned16(w.d_dev) || !aligned16(x) || (residual && !aligned16(residual)) ||
       (reinterpret_cast<uintptr_t>(scratch) & 255u) != 0)
     return set_error("qs, d, x, residual must be 16-byte and scratch 256-byte aligned"), TQ_REFUSED;
-  const GemmScratch g = gemm_scratch(n_rows, cols);
+  const GemmScratch g = gemm_scratch(rows, n_rows, cols);
   uint8_t* sb = static_cast<uint8_t*>(scratch);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   tq::XPrep16Args p{};
@@ -862,7 +887,8 @@ tq_status tq_gemm(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const fl
   p.T = n_rows;
   p.x16 = reinterpret_cast<__half*>(sb + g.x16);
   p.inv_s = reinterpret_cast<float*>(sb + g.inv_s);
-  cudaError_t e = tq::launch_xprep16(p, s);
+  cudaError_t e = cudaMemsetAsync(sb + g.counters, 0, (size_t)kGemmCounters * 4, s);
+  if (e == cudaSuccess) e = tq::launch_xprep16(p, s);
   if (e == cudaSuccess) {
     tq::TcGemmArgs q{};
     q.seg[0] = seg_of(w, rows);
@@ -874,6 +900,10 @@ tq_status tq_gemm(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const fl
     q.y = y;
     q.ldy = rows;
     q.residual = residual;
+    q.part = reinterpret_cast<float*>(sb + g.part);
+    q.part_cap = g.part_floats;
+    q.counters = reinterpret_cast<unsigned*>(sb + g.counters);
+    q.n_counters = kGemmCounters;
     e = tq::launch_tcgemm(wtype, q, s);
   }
   if (e != cudaSuccess) return fail_cuda(nullptr, e, "tq_gemm");

@@ -195,6 +195,16 @@ TQ_API tq_status tq_model_set_wait_limit(tq_model* m, uint32_t polls);
 /* 1 if the model is poisoned (a CUDA error or a device status bit was seen). */
 TQ_API int tq_model_poisoned(const tq_model* m);
 
+/* One step of the batch-1 decode path on its own: the GEMV chain that
+ * follows layer `layer`'s attention ("Всередині LLM ... Qwen3-0.6B на MLX",
+ * steps 5-7: output projection + residual, RMSNorm + SwiGLU FFN + residual,
+ * then the next layer's RMSNorm + Q/K/V projections, or after the last layer
+ * step 8's final norm + LM head + argmax keys), exactly as tq_decode_step
+ * launches it, over the workspace's current activations.  For measuring the
+ * chain inside the step's launch configuration; the workspace's activations
+ * are overwritten.  Refused when layer is outside [0, n_layers). */
+TQ_API tq_status tq_decode_chain(tq_model* m, int32_t layer, void* stream);
+
 /* Number of kernel launches one tq_decode_step(batch) enqueues. */
 TQ_API int32_t tq_decode_launches(const tq_model* m, int32_t batch);
 
@@ -240,9 +250,10 @@ TQ_API tq_status tq_dequantize(int32_t wtype, tq_qmat w, int64_t cols, int64_t r
 TQ_API tq_status tq_gemv(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const float* x_dev,
                   int32_t batch, const float* residual_dev, float* y_dev, void* stream);
 
-/* Bytes of scratch tq_gemm needs for n_rows rows of cols inputs (0 when the
- * sizes are invalid). */
-TQ_API size_t tq_gemm_scratch_bytes(int32_t n_rows, int32_t cols);
+/* Bytes of scratch tq_gemm needs for a [rows][cols] matrix and n_rows rows
+ * of input (0 when the sizes are invalid): the fp16 input rows, their scales,
+ * split-K partial sums and split counters. */
+TQ_API size_t tq_gemm_scratch_bytes(int32_t rows, int32_t n_rows, int32_t cols);
 
 /* The GEMM of prefill and batched decode on its own ("Всередині LLM ...
  * Qwen3-0.6B на MLX", step 9: the prompt's positions through the same
@@ -253,9 +264,11 @@ TQ_API size_t tq_gemm_scratch_bytes(int32_t n_rows, int32_t cols);
  * products summed in f32, so |error| <= about 2^-10 * sum_c |W[r][c] x[t][c]|;
  * each weight tile is decoded once per 256 rows of x (x, y, residual: f32
  * row-major with leading dimensions cols and rows; residual may alias y; all
- * 16-byte aligned).  scratch_dev: at least
- * tq_gemm_scratch_bytes(n_rows, cols) bytes of device memory, 256-byte aligned,
- * owned by the caller; the call must not overlap another use of it.  Refused
+ * 16-byte aligned).  With few rows of x, K is split across CTAs as in the
+ * model's batched decode (the partial sums are added in split order).
+ * scratch_dev: at least tq_gemm_scratch_bytes(rows, n_rows, cols) bytes of
+ * device memory, 256-byte aligned, owned by the caller; the call must not
+ * overlap another use of it.  Refused
  * when cols % 256 != 0 or cols > 12288, a size is < 1 or a pointer NULL or
  * misaligned. */
 TQ_API tq_status tq_gemm(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const float* x_dev,

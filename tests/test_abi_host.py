@@ -128,12 +128,14 @@ def test_model_handle_discipline_without_gpu():
 
 
 def test_gemm_scratch_bytes():
-    """fp16 activation rows (2 B per row and input) and one output scale per
-    row, each 256-byte aligned; 0 for shapes the GEMM does not take."""
+    """fp16 activation rows (2 B per row and input), one output scale per
+    row, split-K partial sums (16 splits, at most 4M floats) and 4096 split
+    counters, each 256-byte aligned; 0 for shapes the GEMM does not take."""
     L = tq.lib()
     up = lambda n: (n + 255) // 256 * 256
-    for n_rows, cols in [(1, 256), (32, 4096), (2048, 12288), (7, 768)]:
-        want = up(n_rows * cols * 2) + up(n_rows * 4)
-        assert L.tq_gemm_scratch_bytes(n_rows, cols) == want
-    for n_rows, cols in [(0, 256), (4, 0), (4, 288), (4, 12544)]:
-        assert L.tq_gemm_scratch_bytes(n_rows, cols) == 0
+    for rows, n_rows, cols in [(16, 1, 256), (4096, 32, 4096), (24576, 2048, 12288), (77, 7, 768)]:
+        part = min(16 * n_rows * rows, 4 << 20)
+        want = up(n_rows * cols * 2) + up(n_rows * 4) + up(part * 4) + up(4096 * 4)
+        assert L.tq_gemm_scratch_bytes(rows, n_rows, cols) == want
+    for rows, n_rows, cols in [(16, 0, 256), (16, 4, 0), (16, 4, 288), (16, 4, 12544), (0, 4, 256)]:
+        assert L.tq_gemm_scratch_bytes(rows, n_rows, cols) == 0

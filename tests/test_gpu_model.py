@@ -179,3 +179,18 @@ def test_chain_wait_timeout_sets_status_poisons_and_context_stays_usable():
         m.decode_step(tok, p, p)
     torch.cuda.synchronize()
     run_case(w, w.prompt_len, 4)          # a fresh model on the same device is exact again
+
+
+def test_decode_chain_alone_matches_the_step():
+    # tq_decode_chain enqueues the step's own chain: after a decode step, re-running
+    # the last layer's chain over the same activations reproduces the step's head
+    import block_quantized_transformer_gb300 as tq
+    w = synth.TINY
+    m = build_model(w, device=DEV, max_ctx=32)
+    prompt = torch.tensor(w.prompt(), dtype=torch.int32, device=DEV)
+    m.prefill(prompt)
+    with pytest.raises(tq.TqError, match="outside"):
+        m.decode_chain(w.n_layers)
+    m.decode_chain(0)                       # runs; overwrites the activations
+    assert m.status() == 0
+    m.close()
