@@ -16,21 +16,24 @@
 // CTA work item: 128 weight rows (8 tiles of 16) x BN token rows over a
 // range of K units (the whole K, or a 1/ks share when few CTAs would be busy:
 // the ks partial sums are then added by the last CTA of the group, in split
-// order).  Roles:
+// order).  K advances in stages of 64 inputs.  Roles:
 //  - warp 18, lane 0: streams the CTA's weight units (codes and scales of
-//    its 8 tiles, 256 inputs each) into a ring of R raw slots with 1-D bulk
-//    copies (TMA engine); weights are read-only, so this starts before the
-//    preceding kernel is done;
-//  - 16 decode warps (8 rows of a tile each): per stage of 64 inputs, decode
-//    the codes from the raw slot to fp16 and store them in the 128-byte
-//    swizzled K-major layout (one 64-input atom of 128 rows) of one of NS
-//    operand stages;
-//  - warp 16: allocates the TMEM accumulator, and its lane 0 loads each
-//    stage's activations with one TMA tile load (64 inputs x BN rows,
-//    128-byte swizzle) from the fp16 activation matrix;
-//  - warp 17, lane 0: issues the stage's 4 tcgen05.mma (M 128, N BN, K 16)
-//    and commits them to the stage's "empty" barrier, and after the last
-//    stage to the accumulator barrier;
+//    its 8 tiles, runs of U units of 256 inputs) into a ring of R
+//    shared-memory slots with 1-D bulk copies (TMA engine); weights are
+//    read-only, so this starts before the preceding kernel is done;
+//  - 16 decode warps: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one weight
+//    row per thread) and a quarter of the stage's inputs (16 of one block);
+//    it decodes them from the raw slot to fp16 and writes them with
+//    tcgen05.st into one of NA weight-operand stages held in tensor memory
+//    (32 columns each), so the decoded weights never pass through shared
+//    memory, whose bandwidth the tensor core's reads of the activations need;
+//  - warp 16: allocates the CTA's 512 TMEM columns (accumulator: columns
+//    0 .. BN-1; weight stages after it), and its lane 0 loads each stage's
+//    activations with one TMA tile load (64 inputs x BN rows, 128-byte
+//    swizzle) from the fp16 activation matrix into one of NB shared stages;
+//  - warp 17, lane 0: issues the stage's 4 tcgen05.mma (M 128, N BN, K 16;
+//    A from TMEM, B from shared memory) and commits them to the stages'
+//    "empty" barriers, and after the last stage to the accumulator barrier;
 //  - epilogue (decode warps 0-7, or 0-3 for 32 columns; 32 TMEM lanes
 //    each): TMEM -> registers, times the row scale, plus the residual (all
 //    loads of a chunk before its stores), to global memory.
@@ -51,7 +54,7 @@ namespace tq {
 namespace tc {
 
 constexpr int kBM = 128;          // weight rows per CTA
-constexpr int kBK = 64;           // inputs per operand stage (one swizzle atom)
+constexpr int kBK = 128;          // inputs per operand stage (half a unit; two swizzle atoms of activations)
 constexpr int kTiles = kBM / kTileRows;
 constexpr int kDQ = 16;           // decode warps, warp w <-> rows 8 (w % 2) .. of tile w / 2
 constexpr int kWarpB = kDQ, kWarpMMA = kDQ + 1, kWarpRaw = kDQ + 2;
@@ -61,17 +64,30 @@ constexpr int kSmemBudget = 212 * 1024;
 
 template <int WT, int BN>
 struct Cfg {
-  static constexpr int A = kBM * kBK * 2;                      // 16 KB
-  static constexpr int B = BN * kBK * 2;                       // BN * 128 bytes
-  static constexpr int STAGE = A + B;
-  static constexpr int NS = BN >= 128 ? 3 : 4;                 // operand stages
+  // Rings: weight operands in TMEM (NA stages of 64 columns after the BN
+  // accumulator columns), activation operands in shared memory (NB stages of
+  // 128 inputs x BN rows), raw weight units in shared memory (R slots of 256
+  // inputs x 128 rows).  A stage returns to its producer only after the MMAs
+  // that read it complete, so each ring covers its own round trip.
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr int NA0 = (int)(TMEM_COLS - BN) / 64;
+  static constexpr int NA = NA0 > 6 ? 6 : NA0;
+  static constexpr int B = BN * kBK * 2;                       // BN * 256 bytes
+  static constexpr int NB0 = (BN >= 256 ? 128 * 1024 : 64 * 1024) / B;
+  static constexpr int NB = NB0 < 2 ? 2 : NB0 > 8 ? 8 : NB0;
   static constexpr int UQ = unit_qs_bytes(WT);                 // codes of one tile's unit
-  static constexpr int RAW = kTiles * (UQ + kUnitD);           // one raw slot: the CTA's 8 units
-  static constexpr int R0 = (kSmemBudget - NS * STAGE) / RAW;
-  static constexpr int R = R0 > 6 ? 6 : R0;                    // raw slots
+  static constexpr int RAW1 = kTiles * (UQ + kUnitD);          // the CTA's 8 tiles, one unit each
+  // a raw slot holds U consecutive units of every tile, so each tile's run
+  // arrives in two bulk copies (codes, scales) of several KB: the TMA
+  // engine's cost per copy stays small against its cost per byte
+  static constexpr int U0 = (kSmemBudget - NB * B) / (2 * RAW1);
+  static constexpr int U = U0 >= 4 ? 4 : U0 >= 2 ? 2 : 1;
+  static constexpr int RAW = U * RAW1;
+  static constexpr int R0 = (kSmemBudget - NB * B) / RAW;
+  static constexpr int R = R0 > 4 ? 4 : R0;                    // raw slots
   static constexpr int MISC = 512;                             // barriers, TMEM address, flags
-  static constexpr int SMEM = 1024 + NS * STAGE + R * RAW + MISC;  // + alignment slack
-  static constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+  static constexpr int SMEM = 1024 + NB * B + R * RAW + MISC;  // + alignment slack
+  static_assert(NA >= 3, "tensor memory too small for the weight stages");
   static_assert(R >= 2, "shared memory too small for two raw slots");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -111,10 +127,6 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
   return false;
 }
 
-__device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
-  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
-}
-
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
@@ -124,6 +136,12 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
   return v;
 }
 
@@ -151,75 +169,78 @@ __device__ __forceinline__ __half2 scale2(uint32_t bits) {
   return __halves2half2(h, h);
 }
 
-// Shared address of inputs e..e+3 (e a multiple of 4, < 64) of row r in a
-// 64-input atom of the swizzled layout.
-__device__ __forceinline__ uint32_t a_addr(uint32_t atom, int r, int e) {
-  const int c = e >> 3;
-  return atom + r * 128 + ((c ^ (r & 7)) << 4) + (e & 4) * 2;
-}
-
-// Per-thread constants of the decode: lane 4g + i of decode warp w handles
-// row 8h + g of tile w / 2 (h = w % 2) and code word i of each block.
+// Inputs inside each 128-input half unit are taken in the order the tiled
+// layout hands them to a thread: position p = 32 i + 8 jb + e (word i,
+// block jb, e < 8) holds input 32 jb + 4 i + (e & 3) + 16 (e >> 2), i.e.
+// word i's four low-nibble (or first) inputs, then its four high-nibble (or
+// second-word) inputs.  xprep16 writes the activations in the same order,
+// so the contraction is unchanged.
+//
+// Per-thread constants of the decode.  Decode warp w owns TMEM lanes
+// 32 (w % 4) .. + 31, so lane l holds weight row r = 32 (w % 4) + l (tile
+// r / 16, row r % 16 = 8 h + g of the tile), and decodes code word i = w / 4
+// of each of the stage's 4 blocks: 32 inputs, TMEM columns 16 i .. 16 i + 15
+// of the stage.
 struct DecodeLane {
-  uint32_t st[4];   // operand offsets of inputs 4i, 16 + 4i, 32 + 4i, 48 + 4i of the row
-  uint32_t qs;      // raw-slot offset of the lane's first code piece
-  uint32_t dd;      // raw-slot offset of the row's scales
+  uint32_t qs;      // raw-slot offset of the thread's code piece (first unit, stage 0)
+  uint32_t dd;      // raw-slot offset of the row's scales of blocks 0..3 (first unit)
+  uint32_t col;     // TMEM lane << 16 | column offset within a stage
   bool ok;          // the tile exists
 };
 
-template <int WT>
+template <int WT, int U>
 __device__ __forceinline__ DecodeLane decode_lane(int lane, int w, bool tile_ok) {
   constexpr int UQ = unit_qs_bytes(WT);
-  const int g = lane >> 2, i = lane & 3, tw = w >> 1, h = w & 1;
-  const int r = tw * 16 + h * 8 + g;
+  const int q = w & 3, i = w >> 2;
+  const int r = 32 * q + lane, tw = r >> 4, rr = r & 15, h = rr >> 3, g = rr & 7;
   DecodeLane d;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int e = k * 16 + 4 * i;
-    d.st[k] = (uint32_t)(r * 128 + (((e >> 3) ^ g) << 4) + (e & 4) * 2);
-  }
-  d.qs = (uint32_t)(tw * UQ + ((WT == TQ_Q4_0 ? h * 2 : h * 4) * 32 + lane) * 16);
-  d.dd = (uint32_t)(kTiles * UQ + tw * kUnitD + (h * 8 + g) * 16);
+  // Q4_0: the 16-byte piece (h*2 + j/4)*32 + 4g + i holds word i of blocks 4(j/4) .. +3;
+  // Q8_0: the piece (h*4 + j/2)*32 + 4g + i holds code words i, i + 4 of blocks 2(j/2), +1
+  d.qs = (uint32_t)(tw * U * UQ + ((WT == TQ_Q4_0 ? h * 2 : h * 4) * 32 + 4 * g + i) * 16);
+  d.dd = (uint32_t)(kTiles * U * UQ + tw * U * kUnitD + (h * 8 + g) * 16);
+  d.col = ((uint32_t)(32 * q) << 16) | (uint32_t)(16 * i);
   d.ok = tile_ok;
   return d;
 }
 
-// Stage q (inputs 64 q .. 64 q + 63, blocks 2q and 2q + 1) of the unit in raw
-// slot `rs` -> this lane's 16 inputs of the fp16 operand atom `A`.  Raw slot:
-// the 8 tiles' codes (UQ bytes each), then their scales (256 B each).
-template <int WT, int Q>
-__device__ __forceinline__ void decode_stage(uint32_t rs, uint32_t A, const DecodeLane& L) {
+// Stage S of a unit (inputs 128 S .. 128 S + 127: blocks 4S .. 4S + 3) ->
+// this thread's 32 fp16 weights as 16 TMEM columns.  rq, rd: the unit's
+// codes and scales in the raw slot (which holds the 8 tiles' runs of U units
+// of codes, UQ bytes each, then their scales, 256 B each).
+template <int WT, int S>
+__device__ __forceinline__ void decode_stage(uint32_t rq, uint32_t rd, const DecodeLane& L, uint32_t (&out)[16]) {
   if (!L.ok) {  // rows past the last tile: zeros
 #pragma unroll
-    for (int k = 0; k < 4; ++k) sts64(A + L.st[k], 0u, 0u);
+    for (int k = 0; k < 16; ++k) out[k] = 0u;
     return;
   }
-  const uint32_t dw = lds32(rs + L.dd + 4 * Q);  // scales of blocks 2Q, 2Q + 1
-  uint32_t wlo[2], whi[2];  // per block jb: inputs 4i..4i+3 and 16+4i..16+4i+3
-  if (WT == TQ_Q4_0) {
-    // piece (h, Q/2) of the lane holds word i of blocks 4(Q/2) .. 4(Q/2)+3
-    const uint2 v = lds64(rs + L.qs + (Q >> 1) * 512 + (Q & 1) * 8);
-    wlo[0] = v.x & 0x0F0F0F0Fu;
-    whi[0] = (v.x >> 4) & 0x0F0F0F0Fu;
-    wlo[1] = v.y & 0x0F0F0F0Fu;
-    whi[1] = (v.y >> 4) & 0x0F0F0F0Fu;
-  } else {
-    // piece (h, Q) of the lane: code words i, i + 4 of blocks 2Q, 2Q + 1
-    const uint4 v = lds128(rs + L.qs + Q * 512);
-    wlo[0] = v.x ^ 0x80808080u;
-    whi[0] = v.y ^ 0x80808080u;
-    wlo[1] = v.z ^ 0x80808080u;
-    whi[1] = v.w ^ 0x80808080u;
-  }
+  const uint2 dv = lds64(rd + L.dd + 8 * S);  // scales of blocks 4S .. 4S + 3
+  const uint32_t ds[2] = {dv.x, dv.y};
   const __half2 bias2 = __float2half2_rn(WT == TQ_Q4_0 ? 1032.f : 1152.f);
+  uint32_t lo[4], hi[4];  // per block: first and second four inputs of word i
+  if (WT == TQ_Q4_0) {
+    const uint4 v = lds128(rq + L.qs + S * 512);
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int jb = 0; jb < 2; ++jb) {
-    const __half2 d2 = scale2(dw >> (16 * jb));
-    uint32_t l01, l23, h01, h23;
-    decode4(wlo[jb], bias2, d2, l01, l23);
-    decode4(whi[jb], bias2, d2, h01, h23);
-    sts64(A + L.st[2 * jb], l01, l23);
-    sts64(A + L.st[2 * jb + 1], h01, h23);
+    for (int jb = 0; jb < 4; ++jb) {
+      lo[jb] = wv[jb] & 0x0F0F0F0Fu;
+      hi[jb] = (wv[jb] >> 4) & 0x0F0F0F0Fu;
+    }
+  } else {
+#pragma unroll
+    for (int jp = 0; jp < 2; ++jp) {
+      const uint4 v = lds128(rq + L.qs + (2 * S + jp) * 512);
+      lo[2 * jp] = v.x ^ 0x80808080u;
+      hi[2 * jp] = v.y ^ 0x80808080u;
+      lo[2 * jp + 1] = v.z ^ 0x80808080u;
+      hi[2 * jp + 1] = v.w ^ 0x80808080u;
+    }
+  }
+#pragma unroll
+  for (int jb = 0; jb < 4; ++jb) {
+    const __half2 d2 = scale2(ds[jb >> 1] >> (16 * (jb & 1)));
+    decode4(lo[jb], bias2, d2, out[4 * jb], out[4 * jb + 1]);
+    decode4(hi[jb], bias2, d2, out[4 * jb + 2], out[4 * jb + 3]);
   }
 }
 
@@ -231,11 +252,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw0 = smem_addr(smem_raw);
   const uint32_t base = (raw0 + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw0);
-  const uint32_t rbase = base + C::NS * C::STAGE;               // raw slots
-  uint8_t* misc = sbase + C::NS * C::STAGE + C::R * C::RAW;
-  uint64_t* full = reinterpret_cast<uint64_t*>(misc);          // [NS] operand stage ready
-  uint64_t* empty = full + C::NS;                               // [NS] operand stage consumed
-  uint64_t* rfull = empty + C::NS;                              // [R] raw slot landed
+  const uint32_t bbase = base;                                  // activation stages
+  const uint32_t rbase = bbase + C::NB * C::B;                  // raw slots
+  uint8_t* misc = sbase + (rbase - base) + C::R * C::RAW;
+  uint64_t* full = reinterpret_cast<uint64_t*>(misc);          // [NA] weight operand in TMEM
+  uint64_t* empty = full + C::NA;                               // [NA] weight operand consumed
+  uint64_t* bfull = empty + C::NA;                              // [NB] activation operand landed
+  uint64_t* bempty = bfull + C::NB;                             // [NB] activation operand consumed
+  uint64_t* rfull = bempty + C::NB;                             // [R] raw slot landed
   uint64_t* rempty = rfull + C::R;                              // [R] raw slot decoded
   uint64_t* acc_bar = rempty + C::R;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_bar + 1);
@@ -247,14 +271,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = a.K / 256;
   const int ks = gridDim.z, z = blockIdx.z;
   const int ub = G * z / ks, ue = G * (z + 1) / ks;  // this CTA's K units
-  const int nu = ue - ub, nst = 4 * nu;
+  const int nu = ue - ub, nst = 2 * nu;
   const int tile = blockIdx.x * kTiles;
   const int n0 = blockIdx.y * BN;
 
   if (tid == 0) {
-    for (int k = 0; k < C::NS; ++k) {
-      mbar_init(&full[k], kDQ + 1);
+    for (int k = 0; k < C::NA; ++k) {
+      mbar_init(&full[k], kDQ);
       mbar_init(&empty[k], 1);
+    }
+    for (int k = 0; k < C::NB; ++k) {
+      mbar_init(&bfull[k], 1);
+      mbar_init(&bempty[k], 1);
     }
     for (int k = 0; k < C::R; ++k) {
       mbar_init(&rfull[k], 1);
@@ -273,24 +301,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kDQ) {
     // ------------------------------------------------------------ decode
-    const DecodeLane L = decode_lane<WT>(lane, warp, tile + (warp >> 1) < m.T);
-    auto stage = [&](auto qc, int u, uint32_t rs) {
-      constexpr int Q = decltype(qc)::value;
-      const int s = 4 * u + Q, slot = s % C::NS;
-      if (s >= C::NS) wait_bounded(&empty[slot], (uint32_t)(((s / C::NS) - 1) & 1), abort_flag, a.status);
-      decode_stage<WT, Q>(rs, base + slot * C::STAGE, L);
-      fence_proxy_async();  // the generic-proxy stores, before the tensor core reads them
+    const DecodeLane L = decode_lane<WT, C::U>(lane, warp, tile + ((32 * (warp & 3) + lane) >> 4) < m.T);
+    auto stage = [&](auto qc, int u, uint32_t rq, uint32_t rd) {
+      constexpr int S = decltype(qc)::value;
+      const int s = 2 * u + S, slot = s % C::NA;
+      uint32_t w32[16];
+      decode_stage<WT, S>(rq, rd, L, w32);
+      if (s >= C::NA) wait_bounded(&empty[slot], (uint32_t)(((s / C::NA) - 1) & 1), abort_flag, a.status);
+      umma::fence_after_sync();
+      umma::tmem_st16(tmem + L.col + (uint32_t)(BN + 64 * slot), w32);
+      umma::fence_before_sync();  // the stores, before the MMA thread learns of them
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[slot]);
     };
-    for (int u = 0; u < nu; ++u) {
-      const int rsl = u % C::R;
-      wait_bounded(&rfull[rsl], (uint32_t)((u / C::R) & 1), abort_flag, a.status);
+    const int nslots = (nu + C::U - 1) / C::U;
+    for (int k = 0; k < nslots; ++k) {
+      const int rsl = k % C::R;
+      wait_bounded(&rfull[rsl], (uint32_t)((k / C::R) & 1), abort_flag, a.status);
       const uint32_t rs = rbase + rsl * C::RAW;
-      stage(std::integral_constant<int, 0>{}, u, rs);
-      stage(std::integral_constant<int, 1>{}, u, rs);
-      stage(std::integral_constant<int, 2>{}, u, rs);
-      stage(std::integral_constant<int, 3>{}, u, rs);
+      const int n = min(C::U, nu - k * C::U);
+      for (int uu = 0; uu < n; ++uu) {
+        const uint32_t rq = rs + uu * C::UQ, rd = rs + uu * kUnitD;
+        stage(std::integral_constant<int, 0>{}, k * C::U + uu, rq, rd);
+        stage(std::integral_constant<int, 1>{}, k * C::U + uu, rq, rd);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&rempty[rsl]);
     }
@@ -343,33 +377,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       umma::prefetch_tmap(&xmap);
       grid_dep_wait();
+      int issued = 0;
       for (int s = 0; s < nst; ++s) {
-        const int slot = s % C::NS;
-        if (s >= C::NS) wait_bounded(&empty[slot], (uint32_t)(((s / C::NS) - 1) & 1), abort_flag, a.status);
-        if (*abort_flag) {
-          mbar_arrive(&full[slot]);  // keep the phase count; nothing is loaded
-          continue;
-        }
-        mbar_arrive_expect_tx(&full[slot], (uint32_t)C::B);
-        umma::tma_load_2d(sbase + slot * C::STAGE + C::A, &xmap, (4 * ub + s) * kBK, n0, &full[slot]);
+        const int slot = s % C::NB;
+        if (s >= C::NB && !wait_bounded(&bempty[slot], (uint32_t)(((s / C::NB) - 1) & 1), abort_flag, a.status))
+          break;
+        if (*abort_flag) break;
+        mbar_arrive_expect_tx(&bfull[slot], (uint32_t)C::B);
+        uint8_t* dst = sbase + (bbase - base) + slot * C::B;
+        const int k0 = (2 * ub + s) * kBK;
+        umma::tma_load_2d(dst, &xmap, k0, n0, &bfull[slot]);
+        umma::tma_load_2d(dst + BN * 128, &xmap, k0 + 64, n0, &bfull[slot]);
+        ++issued;
       }
+      // every issued load lands before the CTA's shared memory is released
+      for (int s = (issued > C::NB ? issued - C::NB : 0); s < issued; ++s)
+        mbar_wait_timed(&bfull[s % C::NB], (uint32_t)((s / C::NB) & 1), kWaitNs);
     }
   } else if (warp == kWarpMMA) {
     // ------------------------------------------------------- MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc = umma::idesc_f16_f32(kBM, BN);
       for (int s = 0; s < nst; ++s) {
-        const int slot = s % C::NS;
-        const bool ok = wait_bounded(&full[slot], (uint32_t)((s / C::NS) & 1), abort_flag, a.status);
+        const int slot = s % C::NA, bslot = s % C::NB;
+        const bool ok = wait_bounded(&full[slot], (uint32_t)((s / C::NA) & 1), abort_flag, a.status) &&
+                        wait_bounded(&bfull[bslot], (uint32_t)((s / C::NB) & 1), abort_flag, a.status);
         umma::fence_after_sync();
-        const uint32_t A = base + slot * C::STAGE, B = A + C::A;
+        const uint32_t A = tmem + (uint32_t)(BN + 64 * slot), B = bbase + bslot * C::B;
         if (ok) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma::mma_f16(tmem, umma::desc_sw128(A + kk * 32), umma::desc_sw128(B + kk * 32), idesc,
-                          (s > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk)
+            umma::mma_f16_tmem_a(tmem, A + 8 * kk, umma::desc_sw128(B + (kk >> 2) * (BN * 128) + (kk & 3) * 32),
+                                 idesc, (s > 0 || kk > 0) ? 1u : 0u);
         }
-        umma::commit(&empty[slot]);  // the stage is free once these MMAs are done
+        umma::commit(&empty[slot]);  // both stages are free once these MMAs are done
+        umma::commit(&bempty[bslot]);
       }
       umma::commit(acc_bar);
     }
@@ -379,27 +421,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nt = 0;  // the CTA's tiles that exist
       for (int i = 0; i < kTiles; ++i)
         if (tile + i < m.T) ++nt;
+      const int nslots = (nu + C::U - 1) / C::U;
       int issued = 0;
-      for (int u = 0; u < nu; ++u) {
-        const int rsl = u % C::R;
-        if (u >= C::R && !wait_bounded(&rempty[rsl], (uint32_t)(((u / C::R) - 1) & 1), abort_flag, a.status))
+      for (int k = 0; k < nslots; ++k) {
+        const int rsl = k % C::R;
+        if (k >= C::R && !wait_bounded(&rempty[rsl], (uint32_t)(((k / C::R) - 1) & 1), abort_flag, a.status))
           break;
         if (*abort_flag) break;
-        const uint32_t dst = rbase + rsl * C::RAW;
-        mbar_arrive_expect_tx(&rfull[rsl], (uint32_t)(nt * (C::UQ + kUnitD)));
+        const int n = min(C::U, nu - k * C::U);  // units in this slot
+        uint8_t* dst = sbase + (rbase - base) + rsl * C::RAW;
+        mbar_arrive_expect_tx(&rfull[rsl], (uint32_t)(nt * n * (C::UQ + kUnitD)));
         for (int i = 0; i < nt; ++i) {
           const int t = tile + i, sg = seg_of(m, t);
           const GemvSeg& gs = a.seg[sg];
-          const int64_t unit = (int64_t)(t - m.tile0[sg]) * G + ub + u;
-          bulk_g2s(sbase + (dst - base) + i * C::UQ, gs.qs + unit * C::UQ, C::UQ, &rfull[rsl]);
-          bulk_g2s(sbase + (dst - base) + kTiles * C::UQ + i * kUnitD,
-                   reinterpret_cast<const uint8_t*>(gs.d) + unit * kUnitD, kUnitD, &rfull[rsl]);
+          const int64_t unit = (int64_t)(t - m.tile0[sg]) * G + ub + k * C::U;  // a tile's units are contiguous
+          bulk_g2s(dst + i * C::U * C::UQ, gs.qs + unit * C::UQ, (uint32_t)(n * C::UQ), &rfull[rsl]);
+          bulk_g2s(dst + kTiles * C::U * C::UQ + i * C::U * kUnitD,
+                   reinterpret_cast<const uint8_t*>(gs.d) + unit * kUnitD, (uint32_t)(n * kUnitD), &rfull[rsl]);
         }
         ++issued;
       }
       // every issued copy lands before the CTA's shared memory is released
-      for (int u = (issued > C::R ? issued - C::R : 0); u < issued; ++u)
-        mbar_wait_timed(&rfull[u % C::R], (uint32_t)((u / C::R) & 1), kWaitNs);
+      for (int k = (issued > C::R ? issued - C::R : 0); k < issued; ++k)
+        mbar_wait_timed(&rfull[k % C::R], (uint32_t)((k / C::R) & 1), kWaitNs);
     }
   }
 
@@ -427,24 +471,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (!*last_flag) return;
-  // element (row, token) -> thread; consecutive threads take consecutive rows
-  for (int e = tid; e < kBM * BN; e += kThreads) {
-    const int row = e % kBM, tok = n0 + e / kBM;
-    const int t = tile + row / kTileRows;
-    if (t >= m.T || tok >= a.T) continue;
-    const int sg = seg_of(m, t);
-    const int local = (t - m.tile0[sg]) * kTileRows + row % kTileRows;
-    if (local >= a.seg[sg].rows) continue;
-    const int col = (sg == 0 ? m.row0[0] : sg == 1 ? m.row0[1] : m.row0[2]) + local;
-    const int64_t o = (int64_t)tok * a.ldy + col;
-    float p[16];
+  // element (row, token) -> thread, consecutive threads on consecutive rows;
+  // a thread's elements are taken 8 at a time with every partial sum and
+  // residual of the 8 loaded before any add, so the reduction costs about one
+  // round trip per 8 elements rather than one per element
+  constexpr int EPT = 8;
+  for (int e0 = tid; e0 < kBM * BN; e0 += EPT * kThreads) {
+    int64_t off[EPT];
+    float v[EPT], r[EPT];
 #pragma unroll
-    for (int zz = 0; zz < 16; ++zz) p[zz] = zz < ks ? __ldcg(a.part + (int64_t)zz * a.T * a.ldy + o) : 0.f;
-    const float r = a.residual != nullptr ? __ldcg(a.residual + o) : 0.f;
-    float v = 0.f;
+    for (int k = 0; k < EPT; ++k) {
+      off[k] = -1;
+      const int e = e0 + k * kThreads;
+      if (e >= kBM * BN) continue;
+      const int row = e % kBM, tok = n0 + e / kBM;
+      const int t = tile + row / kTileRows;
+      if (t >= m.T || tok >= a.T) continue;
+      const int sg = seg_of(m, t);
+      const int local = (t - m.tile0[sg]) * kTileRows + row % kTileRows;
+      if (local >= a.seg[sg].rows) continue;
+      off[k] = (int64_t)tok * a.ldy + (sg == 0 ? m.row0[0] : sg == 1 ? m.row0[1] : m.row0[2]) + local;
+    }
 #pragma unroll
-    for (int zz = 0; zz < 16; ++zz) v += p[zz];  // split order
-    a.y[o] = r + v;
+    for (int k = 0; k < EPT; ++k) {
+      v[k] = 0.f;
+      r[k] = 0.f;
+      if (off[k] < 0) continue;
+      r[k] = a.residual != nullptr ? __ldcg(a.residual + off[k]) : 0.f;
+      for (int zz = 0; zz < ks; ++zz) v[k] += __ldcg(a.part + (int64_t)zz * a.T * a.ldy + off[k]);  // split order
+    }
+#pragma unroll
+    for (int k = 0; k < EPT; ++k)
+      if (off[k] >= 0) a.y[off[k]] = r[k] + v[k];
   }
 }
 
@@ -452,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Row t of the phase input (x, RMS-normalised with `gain`, or silu(x) * up)
 // -> fp16 row t of x16 after the power-of-two scale 2^e that puts its largest
-// magnitude in [2^14, 2^15); inv_s[t] = 2^-e.
+// magnitude in [2^14, 2^15), inputs in the word-major order of the GEMM's
+// weight operand; inv_s[t] = 2^-e.
 __global__ void __launch_bounds__(256) xprep16_kernel(const XPrep16Args a) {
   grid_dep_launch();
   grid_dep_wait();
@@ -468,11 +527,14 @@ __global__ void __launch_bounds__(256) xprep16_kernel(const XPrep16Args a) {
   for (int r = 0; r < CPT; ++r) {
     const int c = tid + r * 256;
     if (c < nch) {
-      float4 p0 = *reinterpret_cast<const float4*>(xr + 8 * c);
-      float4 p1 = *reinterpret_cast<const float4*>(xr + 8 * c + 4);
+      // output chunk c = positions 8c .. 8c + 7 of the word-major order: word
+      // i, block jb of its 128-input half unit
+      const int in0 = (c >> 4) * 128 + 32 * (c & 3) + 4 * ((c >> 2) & 3), in1 = in0 + 16;
+      float4 p0 = *reinterpret_cast<const float4*>(xr + in0);
+      float4 p1 = *reinterpret_cast<const float4*>(xr + in1);
       if (ur != nullptr) {  // silu(gate) * up
-        const float4 u0 = *reinterpret_cast<const float4*>(ur + 8 * c);
-        const float4 u1 = *reinterpret_cast<const float4*>(ur + 8 * c + 4);
+        const float4 u0 = *reinterpret_cast<const float4*>(ur + in0);
+        const float4 u1 = *reinterpret_cast<const float4*>(ur + in1);
         p0 = make_float4(p0.x / (1.f + __expf(-p0.x)) * u0.x, p0.y / (1.f + __expf(-p0.y)) * u0.y,
                          p0.z / (1.f + __expf(-p0.z)) * u0.z, p0.w / (1.f + __expf(-p0.w)) * u0.w);
         p1 = make_float4(p1.x / (1.f + __expf(-p1.x)) * u1.x, p1.y / (1.f + __expf(-p1.y)) * u1.y,
@@ -481,8 +543,8 @@ __global__ void __launch_bounds__(256) xprep16_kernel(const XPrep16Args a) {
       if (a.gain != nullptr) {
         ss = fmaf(p0.x, p0.x, fmaf(p0.y, p0.y, fmaf(p0.z, p0.z, fmaf(p0.w, p0.w, ss))));
         ss = fmaf(p1.x, p1.x, fmaf(p1.y, p1.y, fmaf(p1.z, p1.z, fmaf(p1.w, p1.w, ss))));
-        const float4 g0 = *reinterpret_cast<const float4*>(a.gain + 8 * c);
-        const float4 g1 = *reinterpret_cast<const float4*>(a.gain + 8 * c + 4);
+        const float4 g0 = *reinterpret_cast<const float4*>(a.gain + in0);
+        const float4 g1 = *reinterpret_cast<const float4*>(a.gain + in1);
         p0 = make_float4(p0.x * g0.x, p0.y * g0.y, p0.z * g0.z, p0.w * g0.w);
         p1 = make_float4(p1.x * g1.x, p1.y * g1.y, p1.z * g1.z, p1.w * g1.w);
       }
