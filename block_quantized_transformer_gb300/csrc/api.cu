@@ -153,6 +153,7 @@ struct tq_model {
   bool poisoned = false;
   std::string poison_reason;
   unsigned chain_wait_limit = 0;  // polls of a chain's grid-wide waits (0: the kernel's default)
+  std::vector<CUtensorMap> kmap, vmap;  // per layer, f16 caches: tensor maps of the prefill attention
   // decode-step graph
   cudaGraphExec_t gexec = nullptr;
   struct {
@@ -421,7 +422,15 @@ cudaError_t run_layers_gemm(tq_model* m, int T, const int32_t* pos, const int32_
       if ((e = tq::launch_rope_append(c.kvtype, hd, r, s)) != cudaSuccess) return e;
     }
     const tq::AttnArgs a = attn_args(m, l, T, pos, kv_len, pos_base, seq_fixed, block_table, prefill);
-    if ((e = tq::launch_attn_decode(c.kvtype, hd, G, a, s)) != cudaSuccess) return e;
+    if (prefill && c.kvtype == TQ_KV_F16) {
+      // prefill over an f16 cache: flash-attention tiles staged by tensor maps
+      // of this layer's caches (made at model creation; a paged cache's block
+      // table is read in the kernel)
+      e = tq::launch_attn_prefill(hd, G, m->kmap[l], m->vmap[l], a, s);
+    } else {
+      e = tq::launch_attn_decode(c.kvtype, hd, G, a, s);
+    }
+    if (e != cudaSuccess) return e;
     const tq::GemvSeg o = seg_of(ly.attn_output, c.hidden);
     if ((e = gemm_prep(m, T, m->att(), nullptr, nq * hd, nullptr, s)) != cudaSuccess) return e;
     if ((e = gemm_run(m, T, &o, 1, nq * hd, m->x(), c.hidden, m->x(), s)) != cudaSuccess) return e;
@@ -605,6 +614,15 @@ tq_status tq_model_create(const tq_config* cfg, const tq_weights* w, void* works
       sn[(size_t)p * half + i] = (float)std::sin(ang);
     }
   cudaError_t e = tq::attn_prepare(cfg->kvtype, cfg->head_dim, cfg->n_heads / cfg->n_kv_heads);
+  if (e == cudaSuccess && cfg->kvtype == TQ_KV_F16) {
+    m->kmap.resize(cfg->n_layers);
+    m->vmap.resize(cfg->n_layers);
+    const tq::CacheView cv = cache_view(m, nullptr);
+    for (int l = 0; l < cfg->n_layers && e == cudaSuccess; ++l) {
+      e = tq::encode_kv_map(&m->kmap[l], m->kc_layer(l), cfg->head_dim, cv, cfg->max_batch);
+      if (e == cudaSuccess) e = tq::encode_kv_map(&m->vmap[l], m->vc_layer(l), cfg->head_dim, cv, cfg->max_batch);
+    }
+  }
   if (e == cudaSuccess) e = cudaMemset(workspace, 0, m->L.total);
   if (e == cudaSuccess) e = cudaMemcpy(m->cos_t(), cs.data(), cs.size() * 4, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(m->sin_t(), sn.data(), sn.size() * 4, cudaMemcpyHostToDevice);

@@ -1,6 +1,8 @@
 // Internal launchers of the tq kernels (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace tq {
@@ -183,6 +185,12 @@ struct AttnArgs {
 };
 
 cudaError_t launch_rope_append(int kvtype, int hd, const RopeArgs& a, cudaStream_t s);
+// prefill attention over an f16 cache (attn_prefill.cu): T query rows of one
+// sequence (a.seq_fixed) at positions pos_base.., their K/V already appended;
+// kmap/vmap from encode_kv_map over this layer's caches
+cudaError_t encode_kv_map(CUtensorMap* map, const void* layer_base, int hd, const CacheView& c, int max_batch);
+cudaError_t launch_attn_prefill(int hd, int G, const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a,
+                                cudaStream_t s);
 cudaError_t launch_attn_decode(int kvtype, int hd, int G, const AttnArgs& a, cudaStream_t s);
 // one-time per-kernel attributes (dynamic shared memory); call outside stream capture
 cudaError_t attn_prepare(int kvtype, int hd, int G);

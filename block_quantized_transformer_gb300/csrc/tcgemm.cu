@@ -40,14 +40,12 @@
 // Every wait is bounded in time; a wait that gives up sets
 // TQ_DEV_WAIT_TIMEOUT and the CTA runs on without waiting, then waits
 // (bounded) for its MMAs and copies before it frees TMEM and exits.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <type_traits>
 
 #include "kernels.cuh"
 #include "launch.cuh"
 #include "ptx.cuh"
+#include "tmap.cuh"
 #include "umma.cuh"
 
 namespace tq {
@@ -590,32 +588,13 @@ __global__ void __launch_bounds__(256) xprep16_kernel(const XPrep16Args a) {
 
 // ------------------------------------------------------------ launch --
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }();
-  return fn;
-}
-
 // Tensor map of the fp16 activations [T][K]: boxes of 64 inputs x BN rows,
 // 128-byte swizzle; rows past T read as zeros.
 cudaError_t encode_x(CUtensorMap* map, const __half* x16, int K, int T, int BN) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (fn == nullptr) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)T};
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
   const cuuint32_t box[2] = {64u, (cuuint32_t)BN};
-  const cuuint32_t estr[2] = {1u, 1u};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(x16), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  return tmap_f16_sw128(map, x16, 2, dims, strides, box);
 }
 
 template <int WT, int BN>
