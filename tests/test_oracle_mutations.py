@@ -158,3 +158,43 @@ def test_planted_rounding_of_q_is_caught(monkeypatch):
     monkeypatch.setattr(om.OracleModel, "attn_block", _attn_block_variant(round_q=True))
     with pytest.raises(AssertionError):
         pins.test_f16_kv_store_point_matches_torch_recomposition()
+
+
+def test_planted_cutoff_without_plus_one_is_caught(monkeypatch):
+    from oracle import sample as osm
+
+    def nucleus(logits, temperature, top_p):
+        z = np.asarray(logits, dtype=np.float64) / float(temperature)
+        p = np.exp(z - z.max())
+        p /= p.sum()
+        order = np.argsort(-p, kind="stable")
+        sp = p[order]
+        cut = max(1, int(np.sum(np.cumsum(sp) < top_p)))   # planted: no "+ 1"
+        return order[:cut], sp[:cut] / sp[:cut].sum()
+    monkeypatch.setattr(osm, "nucleus", nucleus)
+    with pytest.raises(AssertionError):
+        pins.test_top_p_hand_worked()
+
+
+def test_planted_ascending_order_is_caught(monkeypatch):
+    from oracle import sample as osm
+
+    def nucleus(logits, temperature, top_p):
+        z = np.asarray(logits, dtype=np.float64) / float(temperature)
+        p = np.exp(z - z.max())
+        p /= p.sum()
+        order = np.argsort(p, kind="stable")               # planted: ascending
+        sp = p[order]
+        cut = int(np.sum(np.cumsum(sp) < top_p)) + 1
+        return order[:cut], sp[:cut] / sp[:cut].sum()
+    monkeypatch.setattr(osm, "nucleus", nucleus)
+    with pytest.raises(AssertionError):
+        pins.test_top_p_hand_worked()
+
+
+def test_planted_missing_temperature_is_caught(monkeypatch):
+    from oracle import sample as osm
+    real = osm.nucleus
+    monkeypatch.setattr(osm, "nucleus", lambda l, t, p: real(l, 1.0, p))  # planted: temperature ignored
+    with pytest.raises(AssertionError):
+        pins.test_sampling_special_cases()

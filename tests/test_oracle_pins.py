@@ -372,3 +372,50 @@ def test_f16_kv_store_point_matches_torch_recomposition():
                                        v16.repeat_interleave(w.group, 0), is_causal=True)
     ref = (o.transpose(0, 1).reshape(T, -1) @ W(f"{p}.attn_output").T).numpy()
     assert np.allclose(out, ref, rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------------------------------------- sampling
+
+def test_top_p_hand_worked():
+    from oracle import sample as osm
+    g = golden("sample_top_p.txt")
+    probs = np.array([float(v) for v in g["probs"][0]])
+    logits = np.log(probs)
+    top_p = float(g["top_p"][0][0])
+    order, q = osm.nucleus(logits, 1.0, top_p)
+    assert order.tolist() == [int(v) for v in g["kept"][0]]
+    assert np.allclose(q, np.array([0.5, 0.3, 0.15]) / 0.95, rtol=0, atol=1e-12)
+    for u, tok in g["draw"]:
+        assert osm.sample(logits, 1.0, top_p, float(u)) == int(tok), u
+    small = float(g["top_p_small"][0][0])
+    for u, tok in g["draw_small"]:
+        assert osm.sample(logits, 1.0, small, float(u)) == int(tok)
+
+
+def test_sampling_special_cases():
+    """Temperature 0 is the argmax; top_p = 1 keeps every token and the draw
+    follows the brute-force inverse CDF of the tempered softmax; a higher
+    temperature flattens the distribution; equal logits draw in index order."""
+    from oracle import sample as osm
+    rng = np.random.default_rng(3)
+    logits = rng.standard_normal(50) * 2.0
+    assert osm.sample(logits, 0.0, 0.95, 0.7) == int(np.argmax(logits))
+    T = 0.7
+    p = np.exp(logits / T - np.max(logits / T))
+    p /= p.sum()
+    order = sorted(range(50), key=lambda i: (-p[i], i))    # brute force, plain Python
+    for u in np.linspace(0.0, 0.999, 37):
+        acc, pick = 0.0, order[-1]
+        for i in order:
+            acc += p[i]
+            if acc > u:
+                pick = i
+                break
+        assert osm.sample(logits, T, 1.0, float(u)) == pick, u
+    o1, q1 = osm.nucleus(logits, 0.5, 1.0)
+    o2, q2 = osm.nucleus(logits, 2.0, 1.0)
+    assert q1[0] > q2[0]                                    # colder: a sharper top token
+    eq = np.zeros(6)
+    assert [osm.sample(eq, 1.0, 1.0, u) for u in (0.0, 0.2, 0.4, 0.6, 0.8, 0.95)] == [0, 1, 2, 3, 4, 5]
+    o, q = osm.nucleus(eq, 1.0, 0.5)                        # ties kept in index order
+    assert o.tolist() == [0, 1, 2] and np.allclose(q, 1 / 3)
