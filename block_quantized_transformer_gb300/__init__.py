@@ -40,7 +40,7 @@ EXPORTS = ("tq_workspace_bytes", "tq_kv_cache_bytes", "tq_model_create", "tq_pre
            "tq_model_poisoned",
            "tq_decode_launches", "tq_model_free", "tq_last_error", "tq_qmat_bytes", "tq_repack", "tq_quantize",
            "tq_dequantize", "tq_gemv", "tq_gemm_scratch_bytes", "tq_gemm", "tq_swiglu_gemv", "tq_lm_head",
-           "tq_lm_head_static")
+           "tq_sample", "tq_lm_head_static")
 LM_HEAD_STATIC_MAX_BATCH = 4096
 
 
@@ -122,6 +122,7 @@ def lib() -> ctypes.CDLL:
                 "tq_swiglu_gemv": (i32, [i32, TqQmat, TqQmat, i32, i32, vp, i32, vp, f32, vp, vp]),
                 "tq_lm_head": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, f32, vp, vp, vp, vp]),
                 "tq_lm_head_static": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, f32, vp, vp, vp]),
+                "tq_sample": (i32, [vp, i32, i32, vp, vp, vp, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -347,6 +348,23 @@ def tq_lm_head(m: QMat, x: torch.Tensor, gain: torch.Tensor, eps: float = 1e-6,
                           _dev(scratch, "scratch", torch.int64), _stream())
     _status(rc, "tq_lm_head")
     return logits, am
+
+
+def tq_sample(logits: torch.Tensor, temperature: torch.Tensor, top_p: torch.Tensor, u: torch.Tensor,
+              out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Temperature / top-p sampling of logits [batch][vocab] on the device:
+    per row a temperature (0: greedy), a top_p and a uniform number u in
+    [0, 1) (f32 device tensors of [batch]); returns int32 token ids."""
+    lg = logits.reshape(-1, logits.shape[-1])
+    B = _int("batch", lg.shape[0], 1, I32[1])
+    V = _int("vocab", lg.shape[1], 1, 1 << 24)
+    if out is None:
+        out = torch.empty(B, dtype=torch.int32, device=lg.device)
+    rc = lib().tq_sample(_dev(lg, "logits", torch.float32, B * V), B, V,
+                         _dev(temperature, "temperature", torch.float32, B), _dev(top_p, "top_p", torch.float32, B),
+                         _dev(u, "u", torch.float32, B), _dev(out, "out", torch.int32, B), _stream())
+    _status(rc, "tq_sample")
+    return out
 
 
 def tq_lm_head_static(m: QMat, x: torch.Tensor, gain: torch.Tensor, eps: float = 1e-6,

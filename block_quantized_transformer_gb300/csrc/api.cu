@@ -955,6 +955,16 @@ tq_status tq_swiglu_gemv(int32_t wtype, tq_qmat gate, tq_qmat up, int32_t ffn, i
   return TQ_OK;
 }
 
+tq_status tq_sample(const float* logits, int32_t batch, int32_t vocab, const float* temperature,
+                    const float* top_p, const float* u, int32_t* out, void* stream) {
+  if (batch < 1 || vocab < 1 || vocab > (1 << 24))
+    return set_error("batch must be >= 1 and vocab in [1, 2^24]"), TQ_REFUSED;
+  if (!logits || !temperature || !top_p || !u || !out) return set_error("pointers must not be NULL"), TQ_REFUSED;
+  cudaError_t e = tq::launch_sample(logits, batch, vocab, temperature, top_p, u, out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(nullptr, e, "tq_sample");
+  return TQ_OK;
+}
+
 tq_status tq_lm_head(int32_t wtype, tq_qmat w, int32_t vocab, int32_t hidden, const float* x,
                      int32_t batch, const float* gain, float eps, float* logits, int32_t* argmax,
                      void* scratch, void* stream) {

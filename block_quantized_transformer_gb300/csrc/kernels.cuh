@@ -198,6 +198,11 @@ cudaError_t attn_prepare(int kvtype, int hd, int G);
 // set the calling thread's tq_last_error() message (api.cu)
 void record_error(const char* msg);
 
+// temperature / top-p sampling of logits [n][V] (sample.cu): per row a
+// temperature (0: argmax), a top_p and a uniform number u in [0, 1)
+cudaError_t launch_sample(const float* logits, int n, int V, const float* temperature, const float* top_p,
+                          const float* u, int32_t* out, cudaStream_t s);
+
 // argmax keys -> int32 indices
 cudaError_t launch_argmax_finish(const unsigned long long* keys, int n, int32_t* out, cudaStream_t s);
 // logits [n][V] -> per-row argmax, ties to the lowest index

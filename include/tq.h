@@ -291,6 +291,26 @@ TQ_API tq_status tq_lm_head(int32_t wtype, tq_qmat w, int32_t vocab, int32_t hid
                      const float* x_dev, int32_t batch, const float* gain_dev, float eps,
                      float* logits_dev, int32_t* argmax_dev, void* scratch_dev, void* stream);
 
+/* Temperature / top-p sampling ("Всередині LLM ... Qwen3-0.6B на MLX", step
+ * 8, sample(logits, temperature, top_p)), on the device, one token per row:
+ *  logits_dev:      [batch][vocab] f32 (for instance tq_decode_step's logits);
+ *  temperature_dev: [batch] f32; 0 selects greedy decoding (the lowest index
+ *                   of the largest logit), > 0 divides the logits before the
+ *                   softmax;
+ *  top_p_dev:       [batch] f32: the tokens, ordered by descending probability
+ *                   (equal probabilities by ascending index), are kept up to
+ *                   and including the first whose cumulative probability
+ *                   reaches top_p, and renormalised;
+ *  u_dev:           [batch] f32 uniform numbers in [0, 1): the drawn token is
+ *                   the first kept token whose cumulative renormalised
+ *                   probability exceeds u (the caller owns the randomness);
+ *  out_dev:         [batch] int32 token ids.
+ * Probabilities are summed in f32; a draw whose u lies within f32 rounding
+ * of a cumulative sum may fall on the neighbouring token.  Refused when
+ * batch < 1, vocab < 1 or vocab > 2^24, or a pointer is NULL. */
+TQ_API tq_status tq_sample(const float* logits_dev, int32_t batch, int32_t vocab, const float* temperature_dev,
+                           const float* top_p_dev, const float* u_dev, int32_t* out_dev, void* stream);
+
 /* ------------------------------------------------- allocation-free head -- */
 
 /* Largest batch of one tq_lm_head_static() call. */
