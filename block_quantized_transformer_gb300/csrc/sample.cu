@@ -10,8 +10,9 @@
 // order, found by a radix select over the 32-bit order-preserving key of the
 // logit (four passes of 8 bits, each a histogram of the unnormalised mass
 // exp2((l - max) log2(e) / T) of the tokens that share the key's leading
-// bits), then, among tokens of exactly equal logit, a count-based select over
-// the index bits.  The row is read from L2 once per pass.
+// bits, summed in f64), then, among tokens of exactly equal logit, a
+// count-based select over the index bits.  The row is read from L2 once per
+// pass.
 #include "kernels.cuh"
 #include "launch.cuh"
 #include "ptx.cuh"
@@ -22,7 +23,7 @@ namespace smp {
 constexpr int kThreads = 1024;
 
 struct Hist {
-  float mass[256];
+  double mass[256];  // f64 sums: over 151936 tokens f32 sums would move a draw by tens of tokens
   unsigned cnt[256];
 };
 
@@ -41,17 +42,19 @@ __device__ __forceinline__ float block_max(float v, float* sh) {
   return r;
 }
 
-__device__ __forceinline__ float block_sum(float v, float* sh) {
-  v = warp_sum(v);
+__device__ __forceinline__ double block_sum(double v, double* sh) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
   __syncthreads();
   if (threadIdx.x < 32) {
-    float x = sh[threadIdx.x];
-    x = warp_sum(x);
+    double x = sh[threadIdx.x];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     if (threadIdx.x == 0) sh[32] = x;
   }
   __syncthreads();
-  const float r = sh[32];
+  const double r = sh[32];
   __syncthreads();
   return r;
 }
@@ -61,26 +64,27 @@ __device__ __forceinline__ float block_sum(float v, float* sh) {
 // larger key, and the number and mass of the tokens that share the key.
 struct Quantile {
   uint32_t key;
-  float above;
+  double above;
   unsigned n_tie;
-  float m_tie;
+  double m_tie;
 };
 
 // First token (descending key order) whose inclusive cumulative mass reaches
 // `target` (>= when !strict, > when strict); if rounding leaves the total
 // below the target, the last token.
-__device__ Quantile select_value(const float* row, int V, float lmax, float sc, float target, bool strict, Hist* h) {
+__device__ Quantile select_value(const float* row, int V, float lmax, float sc, double target, bool strict,
+                                 Hist* h) {
   __shared__ uint32_t s_prefix;
-  __shared__ float s_above;
+  __shared__ double s_above;
   __shared__ unsigned s_n;
-  __shared__ float s_m;
+  __shared__ double s_m;
   if (threadIdx.x == 0) {
     s_prefix = 0u;
     s_above = 0.f;
   }
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int b = threadIdx.x; b < 256; b += kThreads) {
-      h->mass[b] = 0.f;
+      h->mass[b] = 0.0;
       h->cnt[b] = 0u;
     }
     __syncthreads();
@@ -90,17 +94,17 @@ __device__ Quantile select_value(const float* row, int V, float lmax, float sc, 
       const uint32_t key = float_order_key(l);
       if (shift < 24 && (key >> (shift + 8)) != (prefix >> (shift + 8))) continue;
       const int b = (int)((key >> shift) & 255u);
-      atomicAdd(&h->mass[b], exp2f((l - lmax) * sc));
+      atomicAdd(&h->mass[b], (double)exp2f((l - lmax) * sc));
       atomicAdd(&h->cnt[b], 1u);
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      float cum = s_above;
+      double cum = s_above;
       int chosen = -1, lowest = -1;
-      float cum_low = cum;
+      double cum_low = cum;
       for (int b = 255; b >= 0; --b) {
         if (h->cnt[b] == 0u) continue;
-        const float nc = cum + h->mass[b];
+        const double nc = cum + h->mass[b];
         if (strict ? nc > target : nc >= target) {
           chosen = b;
           break;
@@ -170,12 +174,12 @@ __device__ int select_tie_index(const float* row, int V, uint32_t key, unsigned 
 
 // How many tokens of a tie group (n tokens of mass m each, `above` before
 // them) the cumulative mass needs to reach the target.
-__device__ __forceinline__ unsigned ties_needed(float above, unsigned n, float m, float target, bool strict) {
-  if (n <= 1u || m <= 0.f) return 1u;
-  const float w = m / (float)n;
-  float k = (target - above) / w;
-  unsigned r = strict ? (unsigned)floorf(k) + 1u : (unsigned)ceilf(k);
-  if (k < 0.f) r = 1u;
+__device__ __forceinline__ unsigned ties_needed(double above, unsigned n, double m, double target, bool strict) {
+  if (n <= 1u || m <= 0.0) return 1u;
+  const double k = (target - above) / (m / (double)n);
+  if (!(k >= 0.0)) return 1u;
+  if (k >= (double)n) return n;
+  const unsigned r = strict ? (unsigned)floor(k) + 1u : (unsigned)ceil(k);
   return r < 1u ? 1u : r > n ? n : r;
 }
 
@@ -185,6 +189,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const float* logits, i
   grid_dep_wait();
   __shared__ Hist hist;
   __shared__ float red[33];
+  __shared__ double red_d[33];
   __shared__ unsigned long long best_sh[32];
   const int b = blockIdx.x;
   const float* row = logits + (int64_t)b * V;
@@ -213,15 +218,16 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const float* logits, i
   float mx = -3.402823466e38f;
   for (int i = threadIdx.x; i < V; i += kThreads) mx = fmaxf(mx, row[i]);
   const float lmax = block_max(mx, red);
-  float z = 0.f;
-  for (int i = threadIdx.x; i < V; i += kThreads) z += exp2f((row[i] - lmax) * sc);
-  const float Z = block_sum(z, red);
+  double z = 0.0;
+  for (int i = threadIdx.x; i < V; i += kThreads) z += (double)exp2f((row[i] - lmax) * sc);
+  const double Z = block_sum(z, red_d);
   // top-p cutoff: the first token whose cumulative probability reaches top_p
-  const Quantile c = select_value(row, V, lmax, sc, top_p[b] * Z, false, &hist);
-  const unsigned rc = ties_needed(c.above, c.n_tie, c.m_tie, top_p[b] * Z, false);
-  const float z_kept = c.above + (c.n_tie > 0u ? c.m_tie / (float)c.n_tie : 0.f) * (float)rc;
+  const double tc = (double)top_p[b] * Z;
+  const Quantile c = select_value(row, V, lmax, sc, tc, false, &hist);
+  const unsigned rc = ties_needed(c.above, c.n_tie, c.m_tie, tc, false);
+  const double z_kept = c.above + (c.n_tie > 0u ? c.m_tie / (double)c.n_tie : 0.0) * (double)rc;
   // the draw: the first token whose cumulative mass exceeds u * (kept mass)
-  const float target = u[b] * z_kept;
+  const double target = (double)u[b] * z_kept;
   const Quantile d = select_value(row, V, lmax, sc, target, true, &hist);
   unsigned rd = ties_needed(d.above, d.n_tie, d.m_tie, target, true);
   if (d.key == c.key && rd > rc) rd = rc;  // stay inside the kept set

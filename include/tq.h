@@ -305,8 +305,9 @@ TQ_API tq_status tq_lm_head(int32_t wtype, tq_qmat w, int32_t vocab, int32_t hid
  *                   the first kept token whose cumulative renormalised
  *                   probability exceeds u (the caller owns the randomness);
  *  out_dev:         [batch] int32 token ids.
- * Probabilities are summed in f32; a draw whose u lies within f32 rounding
- * of a cumulative sum may fall on the neighbouring token.  Refused when
+ * Each probability is an f32 exp, the sums are f64; a draw whose u lies
+ * within that rounding of a cumulative sum may fall on the neighbouring
+ * token.  Refused when
  * batch < 1, vocab < 1 or vocab > 2^24, or a pointer is NULL. */
 TQ_API tq_status tq_sample(const float* logits_dev, int32_t batch, int32_t vocab, const float* temperature_dev,
                            const float* top_p_dev, const float* u_dev, int32_t* out_dev, void* stream);

@@ -2,8 +2,10 @@
 sampler on the same logits and uniform numbers.  The token is an integer
 decided by f32 sums on the GPU and f64 in the oracle, so a draw is compared
 exactly wherever u and top_p sit more than 1e-5 (in probability) from the
-cumulative sums that decide it, and otherwise must at least fall in the
-oracle's kept set."""
+cumulative sums that decide it; otherwise (over 151936 tokens of a flat
+distribution the sums are closer together than f32 resolves) the drawn token
+must lie in the oracle's kept set, with its interval of the oracle's
+cumulative distribution within 1e-4 of u."""
 import numpy as np
 import pytest
 import torch
@@ -38,8 +40,12 @@ def _check(logits, temps, top_ps, us, min_exact):
             assert got[r] == ref, (r, temps[r], top_ps[r], us[r], got[r], ref)
             exact += 1
         else:
-            kept, _ = osm.nucleus(row, temps[r], top_ps[r])
-            assert got[r] in set(kept.tolist()), (r, got[r])
+            kept, q = osm.nucleus(row, temps[r], top_ps[r])
+            pos = {int(t): k for k, t in enumerate(kept)}
+            assert int(got[r]) in pos, (r, got[r])
+            k = pos[int(got[r])]
+            lo, hi = float(np.sum(q[:k])), float(np.sum(q[:k + 1]))
+            assert lo - 1e-4 <= us[r] <= hi + 1e-4, (r, us[r], lo, hi)
     assert exact >= min_exact, exact
 
 
@@ -52,7 +58,7 @@ def test_sample_vocab_151936_matches_oracle():
     us = synth.uniform_below(11, 2, n, 1 << 24).astype(np.float64) / float(1 << 24)
     temps = [[0.0, 0.7, 1.0, 1.6][i % 4] for i in range(n)]
     top_ps = [[0.95, 0.5, 1.0, 0.9, 0.05, 0.99][i % 6] for i in range(n)]
-    _check(logits, temps, top_ps, list(us), min_exact=40)
+    _check(logits, temps, top_ps, list(us), min_exact=16)
 
 
 def test_sample_small_vocab_and_ties():
