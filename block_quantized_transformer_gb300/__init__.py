@@ -35,7 +35,7 @@ BLOCK_BYTES = {TQ_Q4_0: 18, TQ_Q8_0: 34}
 QS_BYTES = {TQ_Q4_0: 16, TQ_Q8_0: 32}
 
 EXPORTS = ("tq_workspace_bytes", "tq_kv_cache_bytes", "tq_model_create", "tq_prefill",
-           "tq_decode_step", "tq_decode_step_graph", "tq_decode_chain", "tq_model_status",
+           "tq_decode_step", "tq_step", "tq_decode_step_graph", "tq_decode_chain", "tq_model_status",
            "tq_model_set_wait_limit",
            "tq_model_poisoned",
            "tq_decode_launches", "tq_model_free", "tq_last_error", "tq_qmat_bytes", "tq_repack", "tq_quantize",
@@ -104,6 +104,7 @@ def lib() -> ctypes.CDLL:
                 "tq_prefill": (i32, [vp, i32, vp, i32, i32, vp, vp, vp, vp]),
                 "tq_decode_step": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
                 "tq_decode_step_graph": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
+                "tq_step": (i32, [vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp]),
                 "tq_model_status": (i32, [vp, vp, ctypes.POINTER(ctypes.c_uint32)]),
                 "tq_model_set_wait_limit": (i32, [vp, ctypes.c_uint32]),
                 "tq_decode_chain": (i32, [vp, i32, vp]),
@@ -549,6 +550,24 @@ class Model:
         default); a tiny limit exercises the timeout path (tq_model_set_wait_limit)."""
         _int("polls", polls, 0, 2**32 - 1)
         self._after(lib().tq_model_set_wait_limit(self._h(), polls), "tq_model_set_wait_limit")
+
+    def step(self, tokens: torch.Tensor, row_seq: torch.Tensor, row_pos: torch.Tensor, last_row: torch.Tensor,
+             block_table: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
+             argmax: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """One continuous-batching step (tq_step): token rows of several
+        sequences (prompt chunks and decode tokens mixed); returns the greedy
+        token of each sequence's `last_row`."""
+        n = _int("n_rows", tokens.numel(), 1, I32[1])
+        S = _int("n_seq", last_row.numel(), 1, I32[1])
+        if argmax is None:
+            argmax = torch.empty(S, dtype=torch.int32, device=self.device)
+        rc = lib().tq_step(self._h(), n, _dev(tokens, "tokens", torch.int32, n),
+                           _dev(row_seq, "row_seq", torch.int32, n), _dev(row_pos, "row_pos", torch.int32, n), S,
+                           _dev(last_row, "last_row", torch.int32, S), _dev(block_table, "block_table", torch.int32),
+                           _dev(logits, "logits", torch.float32, S * self.cfg.vocab),
+                           _dev(argmax, "argmax", torch.int32, S), _stream(self.device))
+        self._after(rc, "tq_step")
+        return argmax
 
     def status(self) -> int:
         bits = ctypes.c_uint32(0)

@@ -34,7 +34,7 @@ constexpr int64_t kGemmPartFloats = 4 << 20;  // 16 MB of split-K partial sums
 constexpr int kGemmCounters = 4096;
 
 struct Layout {
-  size_t x, qkv, att, act, act2, x16, inv_s, logits, cos_t, sin_t, part, counters, keys, status, chain_sync,
+  size_t x, qkv, att, act, act2, x16, inv_s, logits, xhead, cos_t, sin_t, part, counters, keys, status, chain_sync,
       gemm_part, gemm_ctr, total;
   int T;                 // rows of activation buffers
   int split_dec, splits_dec, split_pf, splits_pf;
@@ -105,6 +105,7 @@ Layout layout_of(const tq_config& c) {
   L.x16 = take((size_t)L.T * kmax * 2);
   L.inv_s = take((size_t)L.T * 4);
   L.logits = c.max_batch > 1 ? take((size_t)c.max_batch * c.vocab * 4) : 0;
+  L.xhead = take((size_t)c.max_batch * c.hidden * 4);  // tq_step: each sequence's last row
   L.cos_t = take((size_t)c.max_ctx * (c.head_dim / 2) * 4);
   L.sin_t = take((size_t)c.max_ctx * (c.head_dim / 2) * 4);
   L.part = take(part_rows * G * (c.head_dim + 2) * 4);
@@ -170,6 +171,7 @@ struct tq_model {
   __half* x16() const { return reinterpret_cast<__half*>(ws + L.x16); }
   float* inv_s() const { return reinterpret_cast<float*>(ws + L.inv_s); }
   float* logits_ws() const { return reinterpret_cast<float*>(ws + L.logits); }
+  float* xhead() const { return reinterpret_cast<float*>(ws + L.xhead); }
   float* cos_t() const { return reinterpret_cast<float*>(ws + L.cos_t); }
   float* sin_t() const { return reinterpret_cast<float*>(ws + L.sin_t); }
   float* part() const { return reinterpret_cast<float*>(ws + L.part); }
@@ -309,7 +311,7 @@ tq::GemvArgs head_args(const tq_model* m, const float* x, int B, float* logits) 
 }
 
 tq::RopeArgs rope_args(const tq_model* m, int l, int T, const int32_t* pos, const int32_t* kv_len, int pos_base,
-                       int seq_fixed, const int32_t* block_table) {
+                       int seq_fixed, const int32_t* block_table, const int32_t* seq_idx = nullptr) {
   const tq_config& c = m->cfg;
   tq::RopeArgs r{};
   r.qkv = m->qkv();
@@ -320,6 +322,7 @@ tq::RopeArgs rope_args(const tq_model* m, int l, int T, const int32_t* pos, cons
   r.kv_len = kv_len;
   r.pos_base = pos_base;
   r.seq_fixed = seq_fixed;
+  r.seq_idx = seq_idx;
   r.kc = m->kc_layer(l);
   r.vc = m->vc_layer(l);
   r.cache = cache_view(m, block_table);
@@ -333,7 +336,7 @@ tq::RopeArgs rope_args(const tq_model* m, int l, int T, const int32_t* pos, cons
 }
 
 tq::AttnArgs attn_args(const tq_model* m, int l, int T, const int32_t* pos, const int32_t* kv_len, int pos_base,
-                       int seq_fixed, const int32_t* block_table, bool prefill) {
+                       int seq_fixed, const int32_t* block_table, bool prefill, const int32_t* seq_idx = nullptr) {
   const tq_config& c = m->cfg;
   const int hd = c.head_dim;
   tq::AttnArgs a{};
@@ -346,6 +349,7 @@ tq::AttnArgs attn_args(const tq_model* m, int l, int T, const int32_t* pos, cons
   a.kv_len = kv_len;
   a.pos_base = pos_base;
   a.seq_fixed = seq_fixed;
+  a.seq_idx = seq_idx;
   a.kc = m->kc_layer(l);
   a.vc = m->vc_layer(l);
   a.cache = cache_view(m, block_table);
@@ -402,15 +406,21 @@ cudaError_t gemm_run(tq_model* m, int T, const tq::GemvSeg* seg, int nseg, int K
 
 // The layers for T >= 2 token rows with every projection as a tensor-core
 // GEMM over all rows (each weight tile decoded once per CTA of up to 256
-// rows), each phase's input turned into fp16 rows by one xprep16 launch.  Prefill (pos == nullptr): the
-// K/V of all rows are appended first, then each row attends over its causal
-// prefix.  Batched decode: row b is sequence b at positions[b]; QK-norm, RoPE
-// and the append happen inside the fused attention.
+// rows), each phase's input turned into fp16 rows by one xprep16 launch.
+//  - prefill (pos == nullptr): rows of one sequence at pos_base..; the K/V of
+//    all rows are appended first, then each row attends over its causal prefix;
+//  - mixed (seq_idx != nullptr): row t is a token of sequence seq_idx[t] at
+//    position pos[t] (its cache slot too), rows of a sequence in position
+//    order; appended first as well, then each row attends over its own prefix;
+//  - batched decode: row b is sequence b at positions[b]; QK-norm, RoPE and
+//    the append happen inside the fused attention.
 cudaError_t run_layers_gemm(tq_model* m, int T, const int32_t* pos, const int32_t* kv_len, int pos_base,
-                            int seq_fixed, const int32_t* block_table, cudaStream_t s) {
+                            int seq_fixed, const int32_t* block_table, cudaStream_t s,
+                            const int32_t* seq_idx = nullptr) {
   const tq_config& c = m->cfg;
   const int hd = c.head_dim, nq = c.n_heads, nkv = c.n_kv_heads, G = nq / nkv;
-  const bool prefill = pos == nullptr;
+  const bool mixed = seq_idx != nullptr;
+  const bool prefill = pos == nullptr || mixed;
   cudaError_t e;
   for (int l = 0; l < c.n_layers; ++l) {
     const tq_layer& ly = m->layers[l];
@@ -418,11 +428,11 @@ cudaError_t run_layers_gemm(tq_model* m, int T, const int32_t* pos, const int32_
     if ((e = gemm_prep(m, T, m->x(), nullptr, c.hidden, ly.attn_norm_dev, s)) != cudaSuccess) return e;
     if ((e = gemm_run(m, T, qkv, 3, c.hidden, m->qkv(), qkv_width(c), nullptr, s)) != cudaSuccess) return e;
     if (prefill) {
-      const tq::RopeArgs r = rope_args(m, l, T, pos, kv_len, pos_base, seq_fixed, block_table);
+      const tq::RopeArgs r = rope_args(m, l, T, pos, kv_len, pos_base, seq_fixed, block_table, seq_idx);
       if ((e = tq::launch_rope_append(c.kvtype, hd, r, s)) != cudaSuccess) return e;
     }
-    const tq::AttnArgs a = attn_args(m, l, T, pos, kv_len, pos_base, seq_fixed, block_table, prefill);
-    if (prefill && c.kvtype == TQ_KV_F16) {
+    const tq::AttnArgs a = attn_args(m, l, T, pos, kv_len, pos_base, seq_fixed, block_table, prefill, seq_idx);
+    if (prefill && !mixed && c.kvtype == TQ_KV_F16) {
       // prefill over an f16 cache: flash-attention tiles staged by tensor maps
       // of this layer's caches (made at model creation; a paged cache's block
       // table is read in the kernel)
@@ -457,13 +467,13 @@ cudaError_t run_head_one(tq_model* m, const float* x, float* logits, int32_t* ar
   return tq::launch_argmax_finish(m->keys(), 1, argmax, s);
 }
 
-// Greedy head on B >= 2 rows: final RMSNorm + LM head as a GEMM into the
-// logits (the caller's, or the workspace's), then a row argmax.
-cudaError_t run_head_gemm(tq_model* m, int B, float* logits, int32_t* argmax, cudaStream_t s) {
+// Greedy head on B >= 2 rows of x: final RMSNorm + LM head as a GEMM into
+// the logits (the caller's, or the workspace's), then a row argmax.
+cudaError_t run_head_gemm(tq_model* m, const float* x, int B, float* logits, int32_t* argmax, cudaStream_t s) {
   const tq_config& c = m->cfg;
   float* lg = logits != nullptr ? logits : m->logits_ws();
   const tq::GemvSeg h = seg_of(m->head, c.vocab);
-  cudaError_t e = gemm_prep(m, B, m->x(), nullptr, c.hidden, m->out_norm, s);
+  cudaError_t e = gemm_prep(m, B, x, nullptr, c.hidden, m->out_norm, s);
   if (e == cudaSuccess) e = gemm_run(m, B, &h, 1, c.hidden, lg, c.vocab, nullptr, s);
   if (e == cudaSuccess) e = tq::launch_argmax_rows(lg, B, c.vocab, argmax, s);
   return e;
@@ -539,7 +549,7 @@ cudaError_t enqueue_decode(tq_model* m, int batch, const int32_t* tokens, const 
   if (e != cudaSuccess) return e;
   if (batch >= 2) {  // batched: weights read once per 32 sequences
     e = run_layers_gemm(m, batch, positions, kv_lens, 0, -1, block_table, s);
-    return e == cudaSuccess ? run_head_gemm(m, batch, logits, argmax, s) : e;
+    return e == cudaSuccess ? run_head_gemm(m, m->x(), batch, logits, argmax, s) : e;
   }
   return run_layers(m, batch, positions, kv_lens, 0, -1, block_table, false, m->x(), batch, logits,
                     argmax, s);
@@ -690,6 +700,35 @@ tq_status tq_decode_step(tq_model* m, int32_t batch, const int32_t* tokens, cons
                                  m->cfg.page_size > 0 ? block_table : nullptr, logits, argmax,
                                  static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(m, e, "tq_decode_step");
+  return TQ_OK;
+}
+
+tq_status tq_step(tq_model* m, int32_t n_rows, const int32_t* tokens, const int32_t* row_seq,
+                  const int32_t* row_pos, int32_t n_seq, const int32_t* last_row, const int32_t* block_table,
+                  float* logits, int32_t* argmax, void* stream) {
+  if (refuse_if_poisoned(m)) return TQ_REFUSED;
+  const tq_config& c = m->cfg;
+  if (n_rows < 1 || n_rows > c.max_prefill)
+    return set_error("n_rows=%d outside [1, max_prefill=%d]", n_rows, c.max_prefill), TQ_REFUSED;
+  if (n_seq < 1 || n_seq > c.max_batch || n_seq > n_rows)
+    return set_error("n_seq=%d outside [1, min(max_batch=%d, n_rows)]", n_seq, c.max_batch), TQ_REFUSED;
+  if (!tokens || !row_seq || !row_pos || !last_row || !argmax)
+    return set_error("tokens, row_seq, row_pos, last_row and argmax must not be NULL"), TQ_REFUSED;
+  if (c.page_size > 0 && block_table == nullptr)
+    return set_error("paged cache: block_table must not be NULL"), TQ_REFUSED;
+  if (n_seq > 1 && logits == nullptr && m->L.logits == 0)
+    return set_error("n_seq > 1 needs logits or a model with max_batch > 1"), TQ_REFUSED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int32_t* bt = c.page_size > 0 ? block_table : nullptr;
+  cudaError_t e = tq::launch_embed(c.wtype, m->embd.qs_dev, m->embd.d_dev, c.vocab, c.hidden, tokens, n_rows, m->x(),
+                                   m->status(), m->keys(), n_seq, s);
+  if (e == cudaSuccess) e = run_layers_gemm(m, n_rows, row_pos, row_pos, 0, -1, bt, s, row_seq);
+  // the head reads each sequence's last row, gathered
+  float* xl = m->xhead();
+  if (e == cudaSuccess) e = tq::launch_gather_rows(m->x(), c.hidden, n_rows, last_row, n_seq, xl, m->status(), s);
+  if (e == cudaSuccess)
+    e = n_seq == 1 ? run_head_one(m, xl, logits, argmax, s) : run_head_gemm(m, xl, n_seq, logits, argmax, s);
+  if (e != cudaSuccess) return fail_cuda(m, e, "tq_step");
   return TQ_OK;
 }
 

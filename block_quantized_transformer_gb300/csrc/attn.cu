@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(128) rope_append_kernel(RopeArgs a) {
   if (hi >= a.nq + a.nkv) return;
   const int pos = a.pos != nullptr ? a.pos[t] : a.pos_base + t;
   const int slot = a.kv_len != nullptr ? a.kv_len[t] : a.pos_base + t;
-  const int seq = a.seq_fixed >= 0 ? a.seq_fixed : t;
+  const int seq = a.seq_idx != nullptr ? a.seq_idx[t] : a.seq_fixed >= 0 ? a.seq_fixed : t;
   const int row_stride = (a.nq + 2 * a.nkv) * HD;
   float* row = a.qkv + (int64_t)t * row_stride;
   const bool is_q = hi < a.nq;
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
   const int span = CL > 0 ? ((ctx + CL * TILE - 1) / (CL * TILE)) * TILE : a.split_keys;
   const int n_active = (ctx + span - 1) / span;
   if (CL == 0 && split >= n_active) return;
-  const int seq = a.seq_fixed >= 0 ? a.seq_fixed : t;
+  const int seq = a.seq_idx != nullptr ? a.seq_idx[t] : a.seq_fixed >= 0 ? a.seq_fixed : t;
   const int k0 = split * span;
   const int k1 = min(ctx, k0 + span);
   const int n_tiles = k1 > k0 ? (k1 - k0 + TILE - 1) / TILE : 0;
@@ -630,7 +630,7 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
   int ctx = new_slot + 1;
   if (ctx > a.cache.max_ctx) ctx = a.cache.max_ctx;
   const int span = ((ctx + CL * TILE - 1) / (CL * TILE)) * TILE;
-  const int seq = a.seq_fixed >= 0 ? a.seq_fixed : t;
+  const int seq = a.seq_idx != nullptr ? a.seq_idx[t] : a.seq_fixed >= 0 ? a.seq_fixed : t;
   const int k0 = split * span;
   const int k1 = min(ctx, k0 + span);
   const int n_tiles = k1 > k0 ? (k1 - k0 + TILE - 1) / TILE : 0;

@@ -44,6 +44,21 @@ __global__ void __launch_bounds__(256) argmax_rows_kernel(const float* logits, i
   }
 }
 
+// out[b] = x[rows[b]] for b < n, rows of H floats (H a multiple of 4); a row
+// index outside [0, n_rows) sets the KV-overflow status bit and yields zeros.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const float* x, int H, int n_rows, const int32_t* rows,
+                                                          float* out, uint32_t* status) {
+  grid_dep_launch();
+  grid_dep_wait();
+  const int b = blockIdx.x;
+  const int r = rows[b];
+  const bool ok = r >= 0 && r < n_rows;
+  if (!ok && threadIdx.x == 0) set_status(status, TQ_DEV_KV_OVERFLOW);
+  const float4* src = reinterpret_cast<const float4*>(x + (int64_t)(ok ? r : 0) * H);
+  float4* dst = reinterpret_cast<float4*>(out + (int64_t)b * H);
+  for (int i = threadIdx.x; i < H / 4; i += 256) dst[i] = ok ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 // Any K that is a multiple of 256 (whole 16-byte rows of fp16 scales) whose
 // activations and pipeline stages fit in shared memory.
 bool pick_mapping(int K) { return K > 0 && K % 256 == 0 && K <= 12288; }
@@ -73,6 +88,12 @@ cudaError_t launch_gemv(int wtype, int mode, const GemvArgs& a, cudaStream_t s) 
 cudaError_t launch_argmax_rows(const float* logits, int n, int V, int32_t* out, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   return launch_k(argmax_rows_kernel, dim3(n), dim3(256), 0, s, logits, V, out);
+}
+
+cudaError_t launch_gather_rows(const float* x, int H, int n_rows, const int32_t* rows, int n, float* out,
+                               uint32_t* status, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  return launch_k(gather_rows_kernel, dim3(n), dim3(256), 0, s, x, H, n_rows, rows, out, status);
 }
 
 cudaError_t launch_argmax_finish(const unsigned long long* keys, int n, int32_t* out, cudaStream_t s) {

@@ -135,9 +135,9 @@ struct CacheView {
   int bt_stride;
 };
 
-// Token t of a call belongs to sequence (seq_fixed >= 0 ? seq_fixed : t), is
-// rotated at position (pos ? pos[t] : pos_base + t) and stores / attends up to
-// cache index (kv_len ? kv_len[t] : pos_base + t).
+// Token t of a call belongs to sequence (seq_idx ? seq_idx[t] : seq_fixed >= 0
+// ? seq_fixed : t), is rotated at position (pos ? pos[t] : pos_base + t) and
+// stores / attends up to cache index (kv_len ? kv_len[t] : pos_base + t).
 struct RopeArgs {
   float* qkv;                // [T][(nq + 2 nkv) * hd]: q rotated in place
   int T, nq, nkv;
@@ -145,6 +145,7 @@ struct RopeArgs {
   const int32_t* kv_len;
   int pos_base;
   int seq_fixed;
+  const int32_t* seq_idx;    // per-token sequence, or null
   void* kc;
   void* vc;                  // this layer's caches
   CacheView cache;
@@ -164,6 +165,7 @@ struct AttnArgs {
   const int32_t* kv_len;
   int pos_base;
   int seq_fixed;
+  const int32_t* seq_idx;    // per-token sequence, or null
   const void* kc;
   const void* vc;
   CacheView cache;
@@ -202,6 +204,10 @@ void record_error(const char* msg);
 // temperature (0: argmax), a top_p and a uniform number u in [0, 1)
 cudaError_t launch_sample(const float* logits, int n, int V, const float* temperature, const float* top_p,
                           const float* u, int32_t* out, cudaStream_t s);
+
+// out[b] = x[rows[b]] (rows of H floats), b < n
+cudaError_t launch_gather_rows(const float* x, int H, int n_rows, const int32_t* rows, int n, float* out,
+                               uint32_t* status, cudaStream_t s);
 
 // argmax keys -> int32 indices
 cudaError_t launch_argmax_finish(const unsigned long long* keys, int n, int32_t* out, cudaStream_t s);

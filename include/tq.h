@@ -167,6 +167,31 @@ TQ_API tq_status tq_decode_step(tq_model* m, int32_t batch, const int32_t* token
                          const int32_t* block_table_dev, float* logits_dev, int32_t* argmax_dev,
                          void* stream);
 
+/* One step of continuous batching: n_rows token rows from n_seq sequences
+ * at once, any mix of prompt chunks (several rows of one sequence) and
+ * decode tokens (one row), through every layer with the projections as GEMMs
+ * over all rows ("Всередині LLM ... Qwen3-0.6B на MLX", step 9: a prompt pass
+ * and single-token steps are the same forward pass over different rows;
+ * "PyTensor Beyond PyMC", section "What the current speed tells us": paged
+ * cache and continuous batching).  Row t is token tokens_dev[t] of the
+ * sequence in block-table row (paged cache) or cache slot (contiguous)
+ * row_seq_dev[t], at position and cache index row_pos_dev[t]; it appends its
+ * K/V there and attends over indices 0 .. row_pos_dev[t] of its sequence.  A
+ * sequence's rows must come in ascending position order with no gaps after
+ * what its cache already holds.  For each sequence b < n_seq, last_row_dev[b]
+ * is the row whose logits / greedy token are produced:
+ *  logits_dev: [n_seq][vocab] f32, or NULL (then n_seq > 1 needs max_batch > 1);
+ *  argmax_dev: [n_seq] int32.
+ * Admission and eviction are the caller's: a sequence's pages are its
+ * block-table row; freeing them (and reusing them for a new sequence, which
+ * overwrites from position 0) is bookkeeping on the host.  Refused when
+ * n_rows < 1 or > max_prefill, n_seq < 1 or > max_batch or > n_rows.
+ * Device-side range errors (a bad token, position, page or last row) set
+ * status bits. */
+TQ_API tq_status tq_step(tq_model* m, int32_t n_rows, const int32_t* tokens_dev, const int32_t* row_seq_dev,
+                         const int32_t* row_pos_dev, int32_t n_seq, const int32_t* last_row_dev,
+                         const int32_t* block_table_dev, float* logits_dev, int32_t* argmax_dev, void* stream);
+
 /* Capture tq_decode_step(batch, ...) with these exact pointers into a CUDA
  * graph owned by the model and replay it on `stream`: same results, fewer
  * launch gaps.  The graph is rebuilt when any argument changes. */
