@@ -61,7 +61,9 @@ def parse():
     ap.add_argument("--prefill-reps", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--layers", type=int, default=0,
-                    help="profiling cases only: keep the first N layers of the workload")
+                    help="profiling cases only: keep the first N layers of the workloads")
+    ap.add_argument("--only", choices=["batched"], default=None,
+                    help="profiling cases only: run just the batched sub-benchmark")
     ap.add_argument("--workload", default="qwen3_8b_q4_0",
                     help="decode workload of the headline (profiling cases may pick another)")
     return ap.parse_args()
@@ -330,6 +332,11 @@ def run_gpu(args, rank, world):
     E = args.e2e_steps
     max_ctx = P + W + K + E + 16
     mats, gains = build_weights(w, dev)
+    if args.only == "batched":
+        b = run_batched(args, world, mats, gains, dev, torch.cuda.Stream(device=dev), pk)
+        if rank == 0:
+            print(json.dumps(b), flush=True)
+        return
     model = build_model(w, device=dev, max_ctx=max_ctx, max_prefill=P, weights=(mats, gains))
     torch.cuda.synchronize()
     weight_bytes = model.weight_bytes() + sum(g.numel() * 4 for g in gains.values())
@@ -461,7 +468,7 @@ def run_gpu(args, rank, world):
     del x, y, scr
 
     batched = None
-    if not args.no_batched and w.name == "qwen3_8b_q4_0":
+    if not args.no_batched and w.name.startswith("qwen3_8b_q4_0"):
         batched = run_batched(args, world, mats, gains, dev, stream, pk)
 
     line = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
@@ -534,6 +541,9 @@ def run_batched(args, world, mats, gains, dev, stream, pk):
     from block_quantized_transformer_gb300.synthetic import build_model
 
     w = synth.QWEN3_8B_Q4_BATCHED
+    if args.layers:
+        import dataclasses
+        w = dataclasses.replace(w, n_layers=args.layers)
     K, W = args.batched_steps, 3
     B, P = w.batch, w.page_size
     lens = w.context_lengths().astype(np.int64)
