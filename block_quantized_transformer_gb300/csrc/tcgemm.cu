@@ -16,27 +16,33 @@
 // CTA work item: 128 weight rows (8 tiles of 16) x BN token rows over a
 // range of K units (the whole K, or a 1/ks share when few CTAs would be busy:
 // the ks partial sums are then added by the last CTA of the group, in split
-// order).  K advances in stages of 64 inputs.  Roles:
+// order).  K advances in stages of 128 inputs.  Roles:
 //  - warp 18, lane 0: streams the CTA's weight units (codes and scales of
 //    its 8 tiles, runs of U units of 256 inputs) into a ring of R
 //    shared-memory slots with 1-D bulk copies (TMA engine); weights are
 //    read-only, so this starts before the preceding kernel is done;
 //  - 16 decode warps: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one weight
-//    row per thread) and a quarter of the stage's inputs (16 of one block);
-//    it decodes them from the raw slot to fp16 and writes them with
+//    row per thread) and one code word of each of the stage's 4 blocks; it
+//    decodes its 32 weights from the raw slot to fp16 and writes them with
 //    tcgen05.st into one of NA weight-operand stages held in tensor memory
-//    (32 columns each), so the decoded weights never pass through shared
+//    (64 columns each), so the decoded weights never pass through shared
 //    memory, whose bandwidth the tensor core's reads of the activations need;
-//  - warp 16: allocates the CTA's 512 TMEM columns (accumulator: columns
-//    0 .. BN-1; weight stages after it), and its lane 0 loads each stage's
-//    activations with one TMA tile load (64 inputs x BN rows, 128-byte
+//  - warp 16: allocates the CTA's 512 TMEM columns (NI accumulators of BN
+//    columns, then the weight stages), and its lane 0 loads each stage's
+//    activations with two TMA tile loads (64 inputs x BN rows, 128-byte
 //    swizzle) from the fp16 activation matrix into one of NB shared stages;
-//  - warp 17, lane 0: issues the stage's 4 tcgen05.mma (M 128, N BN, K 16;
-//    A from TMEM, B from shared memory) and commits them to the stages'
-//    "empty" barriers, and after the last stage to the accumulator barrier;
+//  - warp 17 (and warp 19 when NI = 2), lane 0: issues a stage's 8
+//    tcgen05.mma (M 128, N BN, K 16; A from TMEM, B from shared memory) into
+//    its own accumulator, the two taking alternate stages, and commits them
+//    to the stages' "empty" barriers, after its last stage to the
+//    accumulator barrier.  An MMA of few columns costs the issuing thread
+//    about as much as one of many (measured: ~60 cycles at N 32, plus
+//    ~500 cycles of barrier waits and commits per stage), so at N <= 128 one
+//    issuer would pace the whole CTA;
 //  - epilogue (decode warps 0-7, or 0-3 for 32 columns; 32 TMEM lanes
-//    each): TMEM -> registers, times the row scale, plus the residual (all
-//    loads of a chunk before its stores), to global memory.
+//    each): TMEM -> registers (the NI accumulators summed in order), times
+//    the row scale, plus the residual (all loads of a chunk before its
+//    stores), to global memory.
 // Every wait is bounded in time; a wait that gives up sets
 // TQ_DEV_WAIT_TIMEOUT and the CTA runs on without waiting, then waits
 // (bounded) for its MMAs and copies before it frees TMEM and exits.
@@ -55,8 +61,8 @@ constexpr int kBM = 128;          // weight rows per CTA
 constexpr int kBK = 128;          // inputs per operand stage (half a unit; two swizzle atoms of activations)
 constexpr int kTiles = kBM / kTileRows;
 constexpr int kDQ = 16;           // decode warps, warp w <-> rows 8 (w % 2) .. of tile w / 2
-constexpr int kWarpB = kDQ, kWarpMMA = kDQ + 1, kWarpRaw = kDQ + 2;
-constexpr int kThreads = (kDQ + 3) * 32;
+constexpr int kWarpB = kDQ, kWarpMMA = kDQ + 1, kWarpRaw = kDQ + 2, kWarpMMA2 = kDQ + 3;
+constexpr int kThreads = (kDQ + 4) * 32;
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait here
 constexpr int kSmemBudget = 212 * 1024;
 
@@ -68,7 +74,12 @@ struct Cfg {
   // inputs x 128 rows).  A stage returns to its producer only after the MMAs
   // that read it complete, so each ring covers its own round trip.
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr int NA0 = (int)(TMEM_COLS - BN) / 64;
+  // MMA issuers: one tcgen05.mma with few columns costs its issuing thread
+  // about as much as one with many, so up to 128 columns two threads issue
+  // alternate stages, each into its own accumulator (summed in the epilogue)
+  static constexpr int NI = BN <= 128 ? 2 : 1;
+  static constexpr int ACC = NI * BN;  // accumulator columns
+  static constexpr int NA0 = (int)(TMEM_COLS - ACC) / 64;
   static constexpr int NA = NA0 > 6 ? 6 : NA0;
   static constexpr int B = BN * kBK * 2;                       // BN * 256 bytes
   static constexpr int NB0 = (BN >= 256 ? 128 * 1024 : 64 * 1024) / B;
@@ -286,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&rfull[k], 1);
       mbar_init(&rempty[k], kDQ);
     }
-    mbar_init(acc_bar, 1);
+    mbar_init(acc_bar, C::NI);
     *abort_flag = 0;
     fence_proxy_async();
   }
@@ -307,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       decode_stage<WT, S>(rq, rd, L, w32);
       if (s >= C::NA) wait_bounded(&empty[slot], (uint32_t)(((s / C::NA) - 1) & 1), abort_flag, a.status);
       umma::fence_after_sync();
-      umma::tmem_st16(tmem + L.col + (uint32_t)(BN + 64 * slot), w32);
+      umma::tmem_st16(tmem + L.col + (uint32_t)(C::ACC + 64 * slot), w32);
       umma::fence_before_sync();  // the stores, before the MMA thread learns of them
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[slot]);
@@ -345,6 +356,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int cc = 0; cc < CW; cc += 16) {
         float v[16];
         umma::tmem_ld16(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(c0 + cc), v);
+        if (C::NI > 1) {  // the second issuer's accumulator (odd stages; every CTA has at least two stages)
+          float v2[16];
+          umma::tmem_ld16(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(BN + c0 + cc), v2);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] += v2[j];
+        }
         if (!valid) continue;
         const int tk0 = n0 + c0 + cc;
 #pragma unroll
@@ -392,21 +409,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = (issued > C::NB ? issued - C::NB : 0); s < issued; ++s)
         mbar_wait_timed(&bfull[s % C::NB], (uint32_t)((s / C::NB) & 1), kWaitNs);
     }
-  } else if (warp == kWarpMMA) {
+  } else if (warp == kWarpMMA || (C::NI > 1 && warp == kWarpMMA2)) {
     // ------------------------------------------------------- MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc = umma::idesc_f16_f32(kBM, BN);
-      for (int s = 0; s < nst; ++s) {
+      const int par = warp == kWarpMMA ? 0 : 1;  // stages par, par + NI, ...
+      const uint32_t D = tmem + (uint32_t)(par * BN);
+      for (int s = par; s < nst; s += C::NI) {
         const int slot = s % C::NA, bslot = s % C::NB;
         const bool ok = wait_bounded(&full[slot], (uint32_t)((s / C::NA) & 1), abort_flag, a.status) &&
                         wait_bounded(&bfull[bslot], (uint32_t)((s / C::NB) & 1), abort_flag, a.status);
         umma::fence_after_sync();
-        const uint32_t A = tmem + (uint32_t)(BN + 64 * slot), B = bbase + bslot * C::B;
+        const uint32_t A = tmem + (uint32_t)(C::ACC + 64 * slot), B = bbase + bslot * C::B;
         if (ok) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma::mma_f16_tmem_a(tmem, A + 8 * kk, umma::desc_sw128(B + (kk >> 2) * (BN * 128) + (kk & 3) * 32),
-                                 idesc, (s > 0 || kk > 0) ? 1u : 0u);
+            umma::mma_f16_tmem_a(D, A + 8 * kk, umma::desc_sw128(B + (kk >> 2) * (BN * 128) + (kk & 3) * 32),
+                                 idesc, (s > par || kk > 0) ? 1u : 0u);
         }
         umma::commit(&empty[slot]);  // both stages are free once these MMAs are done
         umma::commit(&bempty[bslot]);
@@ -469,38 +488,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (!*last_flag) return;
-  // element (row, token) -> thread, consecutive threads on consecutive rows;
-  // a thread's elements are taken 8 at a time with every partial sum and
-  // residual of the 8 loaded before any add, so the reduction costs about one
-  // round trip per 8 elements rather than one per element
-  constexpr int EPT = 8;
-  for (int e0 = tid; e0 < kBM * BN; e0 += EPT * kThreads) {
-    int64_t off[EPT];
-    float v[EPT], r[EPT];
+  // Groups of 4 consecutive rows of one token -> threads.  Every partial sum
+  // of a group (8 splits at a time) and its residual are loaded before any
+  // add, as float4 where the group is whole and 16-byte aligned; the adds
+  // run in split order.
+  const bool vec = (a.ldy & 3) == 0 && (m.row0[1] & 3) == 0 && (m.row0[2] & 3) == 0 &&
+                   ((reinterpret_cast<uintptr_t>(a.y) | reinterpret_cast<uintptr_t>(a.part) |
+                     reinterpret_cast<uintptr_t>(a.residual)) & 15u) == 0;
+  const int64_t pstride = (int64_t)a.T * a.ldy;
+  for (int gi = tid; gi < (kBM / 4) * BN; gi += kThreads) {
+    const int row = 4 * (gi % (kBM / 4)), tok = n0 + gi / (kBM / 4);
+    const int t = tile + row / kTileRows;
+    if (t >= m.T || tok >= a.T) continue;
+    const int sg = seg_of(m, t);
+    const int local = (t - m.tile0[sg]) * kTileRows + row % kTileRows;
+    const int rows = a.seg[sg].rows;
+    if (local >= rows) continue;
+    const int64_t off = (int64_t)tok * a.ldy + (sg == 0 ? m.row0[0] : sg == 1 ? m.row0[1] : m.row0[2]) + local;
+    if (vec && local + 4 <= rows) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 r = a.residual != nullptr ? __ldcg(reinterpret_cast<const float4*>(a.residual + off)) : v;
+      for (int z0 = 0; z0 < ks; z0 += 8) {
+        float4 p[8];
 #pragma unroll
-    for (int k = 0; k < EPT; ++k) {
-      off[k] = -1;
-      const int e = e0 + k * kThreads;
-      if (e >= kBM * BN) continue;
-      const int row = e % kBM, tok = n0 + e / kBM;
-      const int t = tile + row / kTileRows;
-      if (t >= m.T || tok >= a.T) continue;
-      const int sg = seg_of(m, t);
-      const int local = (t - m.tile0[sg]) * kTileRows + row % kTileRows;
-      if (local >= a.seg[sg].rows) continue;
-      off[k] = (int64_t)tok * a.ldy + (sg == 0 ? m.row0[0] : sg == 1 ? m.row0[1] : m.row0[2]) + local;
+        for (int j = 0; j < 8; ++j)
+          if (z0 + j < ks) p[j] = __ldcg(reinterpret_cast<const float4*>(a.part + (int64_t)(z0 + j) * pstride + off));
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (z0 + j < ks) {  // split order
+            v.x += p[j].x;
+            v.y += p[j].y;
+            v.z += p[j].z;
+            v.w += p[j].w;
+          }
+      }
+      *reinterpret_cast<float4*>(a.y + off) = make_float4(r.x + v.x, r.y + v.y, r.z + v.z, r.w + v.w);
+    } else {
+      const int n = min(4, rows - local);
+      for (int k = 0; k < n; ++k) {
+        float v = 0.f;
+        const float r = a.residual != nullptr ? __ldcg(a.residual + off + k) : 0.f;
+        for (int zz = 0; zz < ks; ++zz) v += __ldcg(a.part + (int64_t)zz * pstride + off + k);  // split order
+        a.y[off + k] = r + v;
+      }
     }
-#pragma unroll
-    for (int k = 0; k < EPT; ++k) {
-      v[k] = 0.f;
-      r[k] = 0.f;
-      if (off[k] < 0) continue;
-      r[k] = a.residual != nullptr ? __ldcg(a.residual + off[k]) : 0.f;
-      for (int zz = 0; zz < ks; ++zz) v[k] += __ldcg(a.part + (int64_t)zz * a.T * a.ldy + off[k]);  // split order
-    }
-#pragma unroll
-    for (int k = 0; k < EPT; ++k)
-      if (off[k] >= 0) a.y[off[k]] = r[k] + v[k];
   }
 }
 
