@@ -223,6 +223,12 @@ tq::CacheView cache_view(const tq_model* m, const int32_t* block_table) {
   return v;
 }
 
+// Layer l's tensor map of the K (V) cache; null for an f32 cache.
+const CUtensorMap* kv_map(const tq_model* m, int l, bool v) {
+  if (m->kmap.empty()) return nullptr;
+  return v ? &m->vmap[l] : &m->kmap[l];
+}
+
 // The layer loop shared by decode (T = batch, one token per sequence) and
 // prefill (T tokens of sequence `seq` at positions pos_base..).
 // GEMV arguments of the projections of layer l over T token rows.
@@ -438,7 +444,7 @@ cudaError_t run_layers_gemm(tq_model* m, int T, const int32_t* pos, const int32_
       // table is read in the kernel)
       e = tq::launch_attn_prefill(hd, G, m->kmap[l], m->vmap[l], a, s);
     } else {
-      e = tq::launch_attn_decode(c.kvtype, hd, G, a, s);
+      e = tq::launch_attn_decode(c.kvtype, hd, G, kv_map(m, l, false), kv_map(m, l, true), a, s);
     }
     if (e != cudaSuccess) return e;
     const tq::GemvSeg o = seg_of(ly.attn_output, c.hidden);
@@ -532,7 +538,8 @@ cudaError_t run_layers(tq_model* m, int T, const int32_t* pos, const int32_t* kv
       if ((e = tq::launch_rope_append(c.kvtype, hd, r, s)) != cudaSuccess) return e;
     }
     const tq::AttnArgs a = attn_args(m, l, T, pos, kv_len, pos_base, seq_fixed, block_table, prefill);
-    if ((e = tq::launch_attn_decode(c.kvtype, hd, G, a, s)) != cudaSuccess) return e;
+    e = tq::launch_attn_decode(c.kvtype, hd, G, kv_map(m, l, false), kv_map(m, l, true), a, s);
+    if (e != cudaSuccess) return e;
     // output projection, FFN, and the next layer's Q/K/V (or the head)
     const tq::GemvChain ch = layer_chain(m, l, T, head_x, head_B, logits);
     if ((e = tq::launch_gemv_chain(c.wtype, ch, s)) != cudaSuccess) return e;

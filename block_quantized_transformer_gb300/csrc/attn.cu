@@ -22,6 +22,7 @@
 #include "kernels.cuh"
 #include "launch.cuh"
 #include "ptx.cuh"
+#include "umma.cuh"
 
 namespace tq {
 namespace {
@@ -545,9 +546,12 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
 // Fused decode over an f16 cache with the products on the tensor cores.  Same
 // split of work, prologue (QK-norm, RoPE, append) and cluster merge as
 // attn_decode_kernel<__half, .., FUSED, kCluster>; per 32-key tile:
-//  * the warp stages K and V with 16-byte cp.async copies into shared memory
-//    whose 16-byte chunks are XOR-swizzled by the key's low three bits, so
-//    ldmatrix reads of eight keys hit eight different banks;
+//  * the warp's lane 0 stages K and V through the layer's tensor maps (TMA:
+//    boxes of 32 keys x 64 dimensions, 128-byte swizzle, one mbarrier per
+//    buffer), so a key's 16-byte chunks are XOR-swizzled by its low three
+//    bits and ldmatrix reads of eight keys hit eight different banks; V rows
+//    past the context are zeroed once the tile has landed (p = 0 must meet
+//    finite values);
 //  * scores S^T = K Q^T with mma.m16n8k16: A = K rows (exact f16), B = the
 //    query group, every head as an unevaluated sum hi + lo of two fp16 values
 //    after a per-head power-of-two scale (columns 2h, 2h+1), f32 sums;
@@ -561,7 +565,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
 template <int HD, int G, int CL>
 struct TcSmem {
   static constexpr int TILE = 32;
-  static constexpr int TILE_BYTES = TILE * HD * 2;       // one K or V tile
+  static constexpr int BOX = TILE * 128;                 // 32 keys x 64 dimensions
+  static constexpr int TILE_BYTES = TILE * HD * 2;       // one K or V tile: HD / 64 boxes
   static constexpr int WARP_BYTES = 2 * TILE_BYTES;
   static constexpr int OFF_P = 4 * WARP_BYTES;           // [warp][G][32] probabilities
   static constexpr int OFF_Q = OFF_P + 4 * G * 32 * 4;   // [G][HD] scaled q
@@ -572,15 +577,10 @@ struct TcSmem {
   static constexpr int OFF_RES = OFF_O + 4 * G * HD * 4;
   static constexpr int SHARE = G * HD / CL;              // outputs each cluster rank finishes
   static constexpr int OFF_IN = OFF_RES + (2 * G + G * HD) * 4;  // [rank][SHARE + 2G] pushed to this rank
-  static constexpr int BYTES = OFF_IN + CL * (SHARE + 2 * G) * 4;
+  static constexpr int OFF_BAR = (OFF_IN + CL * (SHARE + 2 * G) * 4 + 15) / 16 * 16;  // [warp][K, V] mbarriers
+  static constexpr int BYTES = OFF_BAR + 8 * 8 + 1024;   // + slack to align the tiles to 1024 bytes (swizzle atom)
 };
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// all but the most recent group of this thread's copies have landed
-__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
@@ -610,15 +610,23 @@ __device__ __forceinline__ uint32_t split_pair(float a, float b, bool lo_part) {
 // (prefill): the append kernel already normalised and rotated q and stored
 // every row's K/V, so nothing is staged before the wait; rows are taken
 // longest prefix first.
+// Shared-memory address of 16-byte chunk c (dimensions 8c .. 8c + 7) of key
+// row `key` in a tile staged as 128-byte-swizzled boxes of 64 dimensions.
+__device__ __forceinline__ uint32_t tile_chunk(uint32_t tile, int key, int c) {
+  return tile + (uint32_t)((c >> 3) * (32 * 128) + key * 128 + (((c & 7) ^ (key & 7)) << 4));
+}
+
 template <int HD, int G, int CL, bool FUSED>
-__global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(128) attn_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                      const __grid_constant__ CUtensorMap vmap, AttnArgs a) {
   using S = TcSmem<HD, G, CL>;
   constexpr int DPL = HD / 32;
   constexpr int TILE = S::TILE;
   constexpr int NT = G > 4 ? 2 : 1;        // n-tiles of 4 heads (8 columns: hi, lo)
   constexpr int KS = HD / 16;              // k-steps of the score MMA
-  constexpr int CH = HD / 8;               // 16-byte chunks per key row
-  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr uint64_t kTileWaitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
 
   grid_dep_launch();
   const int split = blockIdx.x, h = blockIdx.y, t = FUSED ? blockIdx.z : gridDim.z - 1 - blockIdx.z;
@@ -647,31 +655,80 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
   float* o_s = reinterpret_cast<float*>(smem + S::OFF_O);
 
   auto tile_key0 = [&](int k) { return k0 + (warp + 4 * k) * TILE; };
-  // stage tile k: cp.async of the valid keys' rows into swizzled chunks, zeros
-  // for the keys past the end (so that p = 0 meets finite V)
-  // stage the K (V) rows of tile k: cp.async of the valid keys' rows into
-  // swizzled chunks, zeros for the keys past the end (so that p = 0 meets
-  // finite V), then one commit group.  A tile's 32 keys are consecutive rows
-  // of one page (pages hold a multiple of 32 keys, tiles start at multiples of 32).
-  auto stage_one = [&](int k, bool is_v) {
-    const int key0 = tile_key0(k);
-    const int nv = min(TILE, k1 - key0);
-    const __half* base = cache_row<__half, HD>(const_cast<void*>(is_v ? a.vc : a.kc), seq, h, key0, a.cache);
-    uint8_t* dst = is_v ? vt : kt;
-    const uint32_t dst_s = is_v ? vt_s : kt_s;
-    for (int i = lane; i < TILE * CH; i += 32) {
-      const int key = i / CH, ch = i % CH;
-      const uint32_t off = (uint32_t)(key * HD * 2 + ((ch ^ (key & 7)) * 16));
-      if (key < nv && base != nullptr)
-        cp_async16(dst_s + off, base + key * HD + ch * 8);
-      else
-        *reinterpret_cast<uint4*>(dst + off) = make_uint4(0u, 0u, 0u, 0u);
+  uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR) + 2 * warp;
+  uint64_t* vbar = kbar + 1;
+  if (lane == 0) {
+    if (warp == 0) {
+      umma::prefetch_tmap(&kmap);
+      umma::prefetch_tmap(&vmap);
     }
-    cp_async_commit();
+    mbar_init(kbar, 1);
+    mbar_init(vbar, 1);
+    fence_proxy_async();
+  }
+  __syncwarp();
+  // Stage the K (V) rows of tile k: lane 0 issues the tile's boxes through
+  // the tensor map (a tile's 32 keys are consecutive rows of one page: pages
+  // hold a multiple of 32 keys, tiles start at multiples of 32); a page
+  // outside the pool stages nothing (its rows are zeroed after the wait).
+  // Keys past max_ctx read as zeros; keys past the context are masked.
+  bool stage_ok = true;  // false once a wait gave up: no copy is issued after that
+  int pend_k = -1, pend_v = -1;  // parity of a K (V) wait that gave up: that copy may still land
+  auto page_of = [&](int key0) {
+    return a.cache.page_size > 0 ? a.cache.block_table[(int64_t)seq * a.cache.bt_stride + key0 / a.cache.page_size]
+                                 : 0;
+  };
+  auto stage_one = [&](int k, bool is_v) {
+    if (lane == 0 && stage_ok) {
+      const int key0 = tile_key0(k);
+      uint64_t* bar = is_v ? vbar : kbar;
+      uint8_t* dst = is_v ? vt : kt;
+      const CUtensorMap* map = is_v ? &vmap : &kmap;
+      const int page = page_of(key0);
+      fence_proxy_async();  // this warp's reads (and zeroing) of the buffer come before the copy's writes
+      if (page >= 0 && page < (a.cache.page_size > 0 ? a.cache.n_pages : 1)) {
+        mbar_arrive_expect_tx(bar, (uint32_t)S::TILE_BYTES);
+#pragma unroll
+        for (int dh = 0; dh < HD / 64; ++dh) {
+          if (a.cache.page_size > 0)
+            umma::tma_load_4d(dst + dh * S::BOX, map, dh * 64, key0 % a.cache.page_size, h, page, bar);
+          else
+            umma::tma_load_3d(dst + dh * S::BOX, map, dh * 64, key0, seq * a.nkv + h, bar);
+        }
+      } else {
+        mbar_arrive(bar);
+      }
+    }
   };
   auto stage = [&](int k) {
     stage_one(k, false);
     stage_one(k, true);
+  };
+  // wait for tile k of K (V); on a time-out the status is set and no further
+  // copy is issued (the values are then garbage, the status says so)
+  auto wait_tile = [&](int k, bool is_v) {
+    if (!mbar_wait_timed(is_v ? vbar : kbar, (uint32_t)(k & 1), kTileWaitNs)) {
+      if (lane == 0) set_status(a.status, TQ_DEV_WAIT_TIMEOUT);
+      int& pend = is_v ? pend_v : pend_k;
+      if (pend < 0) pend = k & 1;  // the buffer's one copy in flight
+      stage_ok = false;
+    }
+    __syncwarp();
+  };
+  // rows [nvalid, 32) of a landed tile are zeroed (all of it for a page
+  // outside the pool, so its keys score 0 against finite values)
+  auto zero_rows = [&](uint8_t* buf, int k) {
+    const int key0 = tile_key0(k);
+    const int page = page_of(key0);
+    const bool in_pool = page >= 0 && page < (a.cache.page_size > 0 ? a.cache.n_pages : 1);
+    const int nvalid = in_pool ? min(TILE, k1 - key0) : 0;
+    if (nvalid >= TILE) return;
+    for (int i = lane; i < (TILE - nvalid) * (HD / 8); i += 32) {
+      const int key = nvalid + i / (HD / 8), c = i % (HD / 8);
+      *reinterpret_cast<uint4*>(buf + tile_chunk(0u, key, c)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async();  // these writes, before a later tensor copy into the buffer
+    __syncwarp();
   };
   const bool owns_new =
       FUSED && my_n > 0 && new_slot >= k0 && new_slot < k1 && ((new_slot - k0) / TILE) % 4 == warp;
@@ -735,7 +792,8 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
     } else if (lane == 0) {
       set_status(a.status, TQ_DEV_KV_OVERFLOW);
     }
-    __threadfence();  // the new row is read back by this warp's copies
+    __threadfence();
+    fence_proxy_async_global();  // the new row is read back by this warp's tensor copies
     __syncwarp();
     if (my_n == 1) stage(0);
   }
@@ -769,10 +827,10 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
 #pragma unroll
     for (int md = 0; md < KS; ++md) o[nt][md][0] = o[nt][md][1] = o[nt][md][2] = o[nt][md][3] = 0.f;
   }
-  // copy groups in flight at the top of iteration k: K(k), V(k)
+  // copies in flight at the top of iteration k: K(k), V(k)
   for (int k = 0; k < my_n; ++k) {
-    cp_async_wait_prev();  // K(k)
-    __syncwarp();
+    wait_tile(k, false);  // K(k): rows past the context only meet masked scores
+    zero_rows(kt, k);     // (a page outside the pool: zeros, as for V)
     const int nv = min(TILE, k1 - tile_key0(k));
     // scores of the tile: two m-tiles of 16 keys
     float sc[NT][2][4];
@@ -784,14 +842,13 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
       for (int ks = 0; ks < KS; ++ks) {
         const int key = mt * 16 + (lane & 15), ch = 2 * ks + (lane >> 4);
         uint32_t af[4];
-        ldsm_x4(kt_s + key * HD * 2 + ((ch ^ (key & 7)) * 16), af[0], af[1], af[2], af[3]);
+        ldsm_x4(tile_chunk(kt_s, key, ch), af[0], af[1], af[2], af[3]);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_f16(sc[nt][mt], af, qb[nt][ks][0], qb[nt][ks][1]);
       }
     }
     __syncwarp();  // every lane is done with K(k): load K(k+1) behind the rest of this tile
     if (k + 1 < my_n) stage_one(k + 1, false);
-    else cp_async_commit();
     // online softmax per head (this thread: head 4 nt + c, keys g, g+8, 16+g, 24+g)
     float alpha[NT];
 #pragma unroll
@@ -826,8 +883,8 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) o[nt][md][r] *= alpha[nt];
     }
-    cp_async_wait_prev();  // V(k)
-    __syncwarp();
+    wait_tile(k, true);  // V(k)
+    zero_rows(vt, k);
     // O^T += V^T P^T: two k-steps of 16 keys
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
@@ -849,15 +906,18 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
         const int mi = lane >> 3;
         const int key = kk * 16 + (lane & 7) + ((mi >> 1) & 1) * 8, ch = 2 * md + (mi & 1);
         uint32_t af[4];
-        ldsm_x4_t(vt_s + key * HD * 2 + ((ch ^ (key & 7)) * 16), af[0], af[1], af[2], af[3]);
+        ldsm_x4_t(tile_chunk(vt_s, key, ch), af[0], af[1], af[2], af[3]);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_f16(o[nt][md], af, pb[nt][0], pb[nt][1]);
       }
     }
     __syncwarp();  // p_s and the V buffer are rewritten next
     if (k + 1 < my_n) stage_one(k + 1, true);
-    else cp_async_commit();
   }
+  // after a wait gave up (no copy was issued after it), the copy it waited
+  // for lands before the CTA exits
+  if (pend_k >= 0) mbar_wait_timed(kbar, (uint32_t)pend_k, kTileWaitNs);
+  if (pend_v >= 0) mbar_wait_timed(vbar, (uint32_t)pend_v, kTileWaitNs);
 
   // ---- this warp's (m, l, o) per head into shared memory, then merge as the
   // scalar path does
@@ -929,7 +989,7 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(AttnArgs a) {
 }
 
 template <int HD, int G, int CL, bool FUSED>
-cudaError_t attn_tc_cl(const AttnArgs& a, cudaStream_t s) {
+cudaError_t attn_tc_cl(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a, cudaStream_t s) {
   using S = TcSmem<HD, G, CL>;
   static PerDevice setup;
   cudaError_t e = per_device(setup, nullptr, [](int, int&) {
@@ -940,7 +1000,8 @@ cudaError_t attn_tc_cl(const AttnArgs& a, cudaStream_t s) {
     return r;
   });
   if (e != cudaSuccess) return e;
-  return launch_cluster(attn_tc_kernel<HD, G, CL, FUSED>, dim3(CL, a.nkv, a.T), dim3(128), S::BYTES, CL, s, a);
+  return launch_cluster(attn_tc_kernel<HD, G, CL, FUSED>, dim3(CL, a.nkv, a.T), dim3(128), S::BYTES, CL, s, kmap, vmap,
+                        a);
 }
 
 // One token: 16 CTAs per KV head share its context (parallelism for one
@@ -948,8 +1009,8 @@ cudaError_t attn_tc_cl(const AttnArgs& a, cudaStream_t s) {
 // so every warp has several tiles to pipeline and the launch still has
 // thousands of CTAs.
 template <int HD, int G>
-cudaError_t attn_tc_t(const AttnArgs& a, cudaStream_t s) {
-  return a.T == 1 ? attn_tc_cl<HD, G, kCluster, true>(a, s) : attn_tc_cl<HD, G, 4, true>(a, s);
+cudaError_t attn_tc_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a, cudaStream_t s) {
+  return a.T == 1 ? attn_tc_cl<HD, G, kCluster, true>(kmap, vmap, a, s) : attn_tc_cl<HD, G, 4, true>(kmap, vmap, a, s);
 }
 
 template <typename KT, int HD>
@@ -996,22 +1057,25 @@ cudaError_t attn_t(const AttnArgs& a, cudaStream_t s) {
 // several tiles, except for f32 rows of 128 dimensions (the second stage
 // would not fit in shared memory).
 template <typename KT, int HD, int G>
-cudaError_t attn_g(const AttnArgs& a, cudaStream_t s) {
-  if (sizeof(KT) == 2 && a.fused) return attn_tc_t<HD, G>(a, s);
-  // prefill over an f16 cache: one CTA per (query row, KV head), its whole
-  // causal prefix (rows are many; the K/V of the prompt stay in L2)
-  if (sizeof(KT) == 2) return attn_tc_cl<HD, G, 1, false>(a, s);
+cudaError_t attn_g(const CUtensorMap* kmap, const CUtensorMap* vmap, const AttnArgs& a, cudaStream_t s) {
+  if (sizeof(KT) == 2) {
+    if (kmap == nullptr || vmap == nullptr) return cudaErrorInvalidValue;  // f16 caches are staged by TMA
+    if (a.fused) return attn_tc_t<HD, G>(*kmap, *vmap, a, s);
+    // rows of a prompt or mixed step: one CTA per (query row, KV head), its
+    // whole causal prefix (the K/V of the step's rows stay in L2)
+    return attn_tc_cl<HD, G, 1, false>(*kmap, *vmap, a, s);
+  }
   if (a.fused || a.split_keys <= 4 * 32 || (sizeof(KT) == 4 && HD == 128)) return attn_t<KT, HD, G, 1>(a, s);
   return attn_t<KT, HD, G, 2>(a, s);
 }
 
 template <typename KT, int HD>
-cudaError_t attn_h(int G, const AttnArgs& a, cudaStream_t s) {
+cudaError_t attn_h(int G, const CUtensorMap* kmap, const CUtensorMap* vmap, const AttnArgs& a, cudaStream_t s) {
   switch (G) {
-    case 1: return attn_g<KT, HD, 1>(a, s);
-    case 2: return attn_g<KT, HD, 2>(a, s);
-    case 4: return attn_g<KT, HD, 4>(a, s);
-    case 8: return attn_g<KT, HD, 8>(a, s);
+    case 1: return attn_g<KT, HD, 1>(kmap, vmap, a, s);
+    case 2: return attn_g<KT, HD, 2>(kmap, vmap, a, s);
+    case 4: return attn_g<KT, HD, 4>(kmap, vmap, a, s);
+    case 8: return attn_g<KT, HD, 8>(kmap, vmap, a, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -1047,10 +1111,12 @@ cudaError_t launch_rope_append(int kvtype, int hd, const RopeArgs& a, cudaStream
   return hd == 128 ? rope_t<float, 128>(a, s) : rope_t<float, 64>(a, s);
 }
 
-cudaError_t launch_attn_decode(int kvtype, int hd, int G, const AttnArgs& a, cudaStream_t s) {
+cudaError_t launch_attn_decode(int kvtype, int hd, int G, const CUtensorMap* kmap, const CUtensorMap* vmap,
+                               const AttnArgs& a, cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
-  if (kvtype == TQ_KV_F16) return hd == 128 ? attn_h<__half, 128>(G, a, s) : attn_h<__half, 64>(G, a, s);
-  return hd == 128 ? attn_h<float, 128>(G, a, s) : attn_h<float, 64>(G, a, s);
+  if (kvtype == TQ_KV_F16)
+    return hd == 128 ? attn_h<__half, 128>(G, kmap, vmap, a, s) : attn_h<__half, 64>(G, kmap, vmap, a, s);
+  return hd == 128 ? attn_h<float, 128>(G, kmap, vmap, a, s) : attn_h<float, 64>(G, kmap, vmap, a, s);
 }
 
 }  // namespace tq

@@ -193,7 +193,9 @@ cudaError_t launch_rope_append(int kvtype, int hd, const RopeArgs& a, cudaStream
 cudaError_t encode_kv_map(CUtensorMap* map, const void* layer_base, int hd, const CacheView& c, int max_batch);
 cudaError_t launch_attn_prefill(int hd, int G, const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a,
                                 cudaStream_t s);
-cudaError_t launch_attn_decode(int kvtype, int hd, int G, const AttnArgs& a, cudaStream_t s);
+// f16 caches: kmap / vmap are the layer's tensor maps (encode_kv_map); f32: unused.
+cudaError_t launch_attn_decode(int kvtype, int hd, int G, const CUtensorMap* kmap, const CUtensorMap* vmap,
+                               const AttnArgs& a, cudaStream_t s);
 // one-time per-kernel attributes (dynamic shared memory); call outside stream capture
 cudaError_t attn_prepare(int kvtype, int hd, int G);
 
