@@ -19,6 +19,24 @@ reordering beyond the definitions:
   ("last(x)") feeds the head
 * greedy sampling and the prefill-then-decode loop ... same page, steps 8-9
 
+Sibling architectures ("Inferencia local y arquitecturas", section "El
+formato": an architecture is its layer recipe, the same operations in
+another order; section "Las operaciones" lists them):
+
+* llama: qwen3 without the per-head Q/K RMSNorm (the qwen3.archdef header
+  names that norm as qwen3's only difference from llama);
+* qwen2: llama plus three bias additions, read as a bias vector added to the
+  q, k and v projections right after their matmuls;
+* gemma3-style: the qwen3 recipe with ``gelu_tanh`` (the tanh approximation
+  of GELU, which the page distinguishes from exact ``gelu``) as the gate's
+  activation, sliding-window attention on a pattern of layers (the one
+  ``param`` gemma3 takes), and a final logit softcap (the Gemma 3n
+  configuration table of "Alchemize PyTensor ... Gemma 3n": sliding window
+  512, final logit softcap 30).  The window counts the query's own position:
+  key j is visible to a query at position p iff p - window < j <= p; with
+  pattern P, layer i attends the whole context when i % P == P - 1.
+  softcap(x) = c * tanh(x / c).
+
 Readings where the pages leave a step open: the mask is
 "key position <= query position" (adding -1e9 above the diagonal gives
 exactly the same softmax in f64); an f16 KV cache rounds K (after QK-norm and
@@ -64,19 +82,24 @@ def softmax(s: np.ndarray) -> np.ndarray:
     return e / np.sum(e, axis=-1, keepdims=True)
 
 
-def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos: np.ndarray) -> np.ndarray:
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos: np.ndarray, window: int = 0) -> np.ndarray:
     """Grouped-query attention.
 
     q [nq, T, hd]; k, v [nkv, S, hd] holding key positions 0..S-1;
     q_pos [T] absolute positions of the queries.  Query head h reads KV head
-    h // (nq/nkv).  Key j is visible to query t iff j <= q_pos[t].
+    h // (nq/nkv).  Key j is visible to query t iff j <= q_pos[t] and, with a
+    sliding window, j > q_pos[t] - window.
     Returns [nq, T, hd].
     """
     nq, T, hd = q.shape
     nkv, S, _ = k.shape
     G = nq // nkv
     out = np.empty_like(q)
-    visible = np.arange(S)[None, :] <= np.asarray(q_pos)[:, None]      # [T, S]
+    keys = np.arange(S)[None, :]
+    qp = np.asarray(q_pos)[:, None]
+    visible = keys <= qp                                                # [T, S]
+    if window > 0:
+        visible = visible & (keys > qp - window)
     for h in range(nq):
         kv = h // G
         s = (q[h] @ k[kv].T) * (hd ** -0.5)
@@ -89,6 +112,16 @@ def silu(z: np.ndarray) -> np.ndarray:
     return z / (1.0 + np.exp(-z))
 
 
+def gelu_tanh(z: np.ndarray) -> np.ndarray:
+    """The tanh approximation of GELU: z/2 * (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))."""
+    return 0.5 * z * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (z + 0.044715 * z ** 3)))
+
+
+def softcap(x: np.ndarray, c: float) -> np.ndarray:
+    """c * tanh(x / c)."""
+    return c * np.tanh(x / c)
+
+
 class OracleModel:
     """Decoder over quantized block bytes.
 
@@ -96,7 +129,8 @@ class OracleModel:
     [out, in/32, 34|18] for the matrices ``token_embd`` and
     ``blk.{i}.{attn_q,attn_k,attn_v,attn_output,ffn_gate,ffn_up,ffn_down}``
     (optionally ``output``), f32 gains for ``blk.{i}.{attn_norm,ffn_norm,
-    attn_q_norm,attn_k_norm}`` and ``output_norm``.
+    attn_q_norm,attn_k_norm}`` (no Q/K norms for llama and qwen2) and
+    ``output_norm``, and for qwen2 the f32 biases ``blk.{i}.attn_{q,k,v}_bias``.
     """
 
     def __init__(self, w, weights: dict, dtype=np.float64, cache_dequant: bool = True):
@@ -125,6 +159,14 @@ class OracleModel:
     def head_name(self) -> str:
         return "output" if "output" in self.weights else "token_embd"
 
+    def window_of(self, i: int) -> int:
+        """Sliding window of layer i (0: the whole context)."""
+        w = self.w
+        if w.arch != "gemma3" or w.sliding_window <= 0:
+            return 0
+        P = w.sliding_pattern
+        return 0 if P > 0 and i % P == P - 1 else w.sliding_window
+
     # -- steps ----------------------------------------------------------------
     def embed(self, tokens) -> np.ndarray:
         blocks = self.weights["token_embd"][np.asarray(tokens, dtype=np.int64)]
@@ -142,8 +184,13 @@ class OracleModel:
         q = self.linear(h, f"{p}.attn_q").reshape(T, w.n_heads, w.head_dim).transpose(1, 0, 2)
         k = self.linear(h, f"{p}.attn_k").reshape(T, w.n_kv_heads, w.head_dim).transpose(1, 0, 2)
         v = self.linear(h, f"{p}.attn_v").reshape(T, w.n_kv_heads, w.head_dim).transpose(1, 0, 2)
-        q = rms_norm(q, self.gain(f"{p}.attn_q_norm"), w.rms_eps)
-        k = rms_norm(k, self.gain(f"{p}.attn_k_norm"), w.rms_eps)
+        if w.arch == "qwen2":
+            q = q + self.gain(f"{p}.attn_q_bias").reshape(w.n_heads, 1, w.head_dim)
+            k = k + self.gain(f"{p}.attn_k_bias").reshape(w.n_kv_heads, 1, w.head_dim)
+            v = v + self.gain(f"{p}.attn_v_bias").reshape(w.n_kv_heads, 1, w.head_dim)
+        if w.arch in ("qwen3", "gemma3"):
+            q = rms_norm(q, self.gain(f"{p}.attn_q_norm"), w.rms_eps)
+            k = rms_norm(k, self.gain(f"{p}.attn_k_norm"), w.rms_eps)
         q = rope(q, positions, w.rope_theta)
         k = rope(k, positions, w.rope_theta)
         k = self.store_kv(k)
@@ -153,7 +200,7 @@ class OracleModel:
             k = np.concatenate([ck, k], axis=1)
             v = np.concatenate([cv, v], axis=1)
         cache[i] = (k, v)
-        o = attention(q, k, v, positions)
+        o = attention(q, k, v, positions, self.window_of(i))
         o = o.transpose(1, 0, 2).reshape(T, w.n_heads * w.head_dim)
         return self.linear(o, f"{p}.attn_output")
 
@@ -161,7 +208,8 @@ class OracleModel:
         p = f"blk.{i}"
         gate = self.linear(h, f"{p}.ffn_gate")
         up = self.linear(h, f"{p}.ffn_up")
-        return self.linear(silu(gate) * up, f"{p}.ffn_down")
+        act = gelu_tanh(gate) if self.w.arch == "gemma3" else silu(gate)
+        return self.linear(act * up, f"{p}.ffn_down")
 
     def block(self, i: int, x: np.ndarray, cache: list, positions: np.ndarray) -> np.ndarray:
         p = f"blk.{i}"
@@ -172,7 +220,10 @@ class OracleModel:
 
     def head(self, x_last: np.ndarray) -> np.ndarray:
         x = rms_norm(x_last, self.gain("output_norm"), self.w.rms_eps)
-        return self.linear(x, self.head_name())
+        logits = self.linear(x, self.head_name())
+        if self.w.arch == "gemma3" and self.w.logit_softcap > 0:
+            logits = softcap(logits, self.w.logit_softcap)
+        return logits
 
     def new_cache(self) -> list:
         return [None] * self.w.n_layers
@@ -223,6 +274,6 @@ def synth_weights(w) -> dict:
     out = {}
     for name in w.matrices():
         out[name] = quant.quantize(synth.host_tensor(w, name), w.wtype)
-    for name in w.gains():
+    for name in w.gains() + w.biases():
         out[name] = synth.host_tensor(w, name)
     return out

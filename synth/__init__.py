@@ -43,10 +43,14 @@ IH8_SD = math.sqrt(8.0 * (65536.0 * 65536.0 - 1.0) / 12.0)
 # prompt of sequence b uses PROMPT_STREAM + b, ragged lengths LENGTH_STREAM.
 LAYER_TENSORS = ("attn_q", "attn_k", "attn_v", "attn_output", "ffn_gate", "ffn_up",
                  "ffn_down", "attn_norm", "ffn_norm", "attn_q_norm", "attn_k_norm")
+BIAS_TENSORS = ("attn_q_bias", "attn_k_bias", "attn_v_bias")  # qwen2 only
 PROMPT_STREAM = 1_000_000
 LENGTH_STREAM = 2_000_000
 KV_STREAM = 3_000_000
+BIAS_STREAM = 4_000_000   # + 3 * layer + index in BIAS_TENSORS
 WEIGHT_SIGMA = 0.02
+BIAS_SIGMA = 0.1
+ARCHS = ("qwen3", "llama", "qwen2", "gemma3")
 
 
 def normal_scale(sigma: float) -> np.float32:
@@ -240,6 +244,14 @@ class Workload:
     ctx_lo: int = 0       # ragged batched mix: context lengths uniform in [ctx_lo, ctx_hi]
     ctx_hi: int = 0
     length_seed: int = 0
+    # architecture of the decoder (which tensors exist; the oracle and the
+    # library each read what it means): qwen3, llama (no per-head Q/K norm),
+    # qwen2 (llama + Q/K/V biases), gemma3 (sliding window on a layer
+    # pattern, tanh-approximated GELU in the gated FFN, final logit softcap)
+    arch: str = "qwen3"
+    sliding_window: int = 0
+    sliding_pattern: int = 0
+    logit_softcap: float = 0.0
 
     @property
     def group(self) -> int:
@@ -253,6 +265,8 @@ class Workload:
             return 1 + len(LAYER_TENSORS) * self.n_layers
         parts = name.split(".")
         assert parts[0] == "blk" and len(parts) == 3, name
+        if parts[2] in BIAS_TENSORS:
+            return BIAS_STREAM + 3 * int(parts[1]) + BIAS_TENSORS.index(parts[2])
         return 1 + len(LAYER_TENSORS) * int(parts[1]) + LAYER_TENSORS.index(parts[2])
 
     def matrix_shape(self, name: str) -> tuple:
@@ -270,6 +284,10 @@ class Workload:
         kind = name.split(".")[-1]
         return self.head_dim if kind in ("attn_q_norm", "attn_k_norm") else self.hidden
 
+    def bias_len(self, name: str) -> int:
+        kind = name.split(".")[-1]
+        return (self.n_heads if kind == "attn_q_bias" else self.n_kv_heads) * self.head_dim
+
     def matrices(self) -> list:
         out = ["token_embd"]
         for i in range(self.n_layers):
@@ -277,10 +295,16 @@ class Workload:
         return out
 
     def gains(self) -> list:
+        kinds = LAYER_TENSORS[7:] if self.arch in ("qwen3", "gemma3") else LAYER_TENSORS[7:9]
         out = []
         for i in range(self.n_layers):
-            out += [f"blk.{i}.{t}" for t in LAYER_TENSORS[7:]]
+            out += [f"blk.{i}.{t}" for t in kinds]
         return out + ["output_norm"]
+
+    def biases(self) -> list:
+        if self.arch != "qwen2":
+            return []
+        return [f"blk.{i}.{t}" for i in range(self.n_layers) for t in BIAS_TENSORS]
 
     def weight_count(self) -> int:
         return sum(int(np.prod(self.matrix_shape(m))) for m in self.matrices())
@@ -316,14 +340,31 @@ QWEN3_8B_Q4_BATCHED = Workload("qwen3_8b_q4_0_batched32_paged", vocab=151936, hi
                                ctx_hi=8192, length_seed=3)
 WORKLOADS = [TINY, QWEN3_0P6B_Q8, QWEN3_0P6B_Q4_LONG, QWEN3_8B_Q4, QWEN3_8B_Q4_BATCHED]
 
+# Sibling architectures on the tiny shape (parity cases): the same sizes and
+# seed as TINY, another layer recipe.
+TINY_LLAMA = Workload("tiny_llama", vocab=4096, hidden=256, n_layers=2, n_heads=4, n_kv_heads=2,
+                      head_dim=64, ffn=768, wtype="q8_0", kv="f32", seed=0, prompt_len=8,
+                      decode_steps=16, arch="llama")
+TINY_QWEN2 = Workload("tiny_qwen2", vocab=4096, hidden=256, n_layers=2, n_heads=4, n_kv_heads=2,
+                      head_dim=64, ffn=768, wtype="q8_0", kv="f32", seed=0, prompt_len=8,
+                      decode_steps=16, arch="qwen2")
+TINY_GEMMA3 = Workload("tiny_gemma3", vocab=4096, hidden=256, n_layers=4, n_heads=4, n_kv_heads=2,
+                       head_dim=64, ffn=768, wtype="q8_0", kv="f32", seed=0, prompt_len=8,
+                       decode_steps=16, arch="gemma3", sliding_window=6, sliding_pattern=2,
+                       logit_softcap=0.5)
+ARCH_WORKLOADS = [TINY_LLAMA, TINY_QWEN2, TINY_GEMMA3]
+
 
 def host_tensor(w: Workload, name: str, rows: Optional[slice] = None) -> np.ndarray:
     """A synthetic weight (f32, [out, in] row-major) or gain (f32), on the host.
 
-    Matrices are N(0, 0.02); gains are 1 + N(0, 0.02).  ``rows`` selects a
-    contiguous row range of a matrix without generating the rest.
+    Matrices are N(0, 0.02); gains are 1 + N(0, 0.02); biases N(0, 0.1).
+    ``rows`` selects a contiguous row range of a matrix without generating
+    the rest.
     """
     stream = w.stream_of(name)
+    if name.split(".")[-1] in BIAS_TENSORS:
+        return host_normal(w.seed, stream, w.bias_len(name), sigma=BIAS_SIGMA)
     if name == "output_norm" or name.split(".")[-1] in LAYER_TENSORS[7:]:
         return host_normal(w.seed, stream, w.gain_len(name), mean=1.0)
     n_out, n_in = w.matrix_shape(name)

@@ -198,3 +198,70 @@ def test_planted_missing_temperature_is_caught(monkeypatch):
     monkeypatch.setattr(osm, "nucleus", lambda l, t, p: real(l, 1.0, p))  # planted: temperature ignored
     with pytest.raises(AssertionError):
         pins.test_sampling_special_cases()
+
+
+# --------------------------------------------------------------------------- sibling architectures
+
+def test_planted_exact_gelu_is_caught(monkeypatch):
+    import scipy.special
+    monkeypatch.setattr(om, "gelu_tanh", lambda z: 0.5 * z * (1.0 + scipy.special.erf(z / math.sqrt(2.0))))
+    with pytest.raises(AssertionError):
+        pins.test_gelu_tanh_matches_torch_and_is_not_exact_gelu()
+    with pytest.raises(AssertionError):
+        pins.test_arch_models_match_torch_library_composition("gemma3")
+
+
+def test_planted_window_off_by_one_is_caught(monkeypatch):
+    real = om.attention
+
+    def wide(q, k, v, q_pos, window=0):
+        return real(q, k, v, q_pos, window + 1 if window > 0 else 0)   # planted: j >= p - window
+    monkeypatch.setattr(om, "attention", wide)
+    with pytest.raises(AssertionError):
+        pins.test_sliding_window_attention_matches_sdpa_band_mask(3)
+    with pytest.raises(AssertionError):
+        pins.test_arch_models_match_torch_library_composition("gemma3")
+
+
+def test_planted_inverted_layer_pattern_is_caught(monkeypatch):
+    real = om.OracleModel.window_of
+    monkeypatch.setattr(om.OracleModel, "window_of",
+                        lambda self, i: real(self, i + 1))               # planted: global layers swapped
+    with pytest.raises(AssertionError):
+        pins.test_arch_models_match_torch_library_composition("gemma3")
+
+
+def test_planted_missing_softcap_is_caught(monkeypatch):
+    monkeypatch.setattr(om, "softcap", lambda x, c: x)
+    with pytest.raises(AssertionError):
+        pins.test_softcap_closed_form()
+    with pytest.raises(AssertionError):
+        pins.test_arch_models_match_torch_library_composition("gemma3")
+
+
+def test_planted_dropped_bias_is_caught(monkeypatch):
+    real = om.OracleModel.gain
+
+    def no_bias(self, name):                                           # planted: biases dropped
+        g = real(self, name)
+        return g * 0.0 if name.endswith("_bias") else g
+    monkeypatch.setattr(om.OracleModel, "gain", no_bias)
+    with pytest.raises(AssertionError):
+        pins.test_arch_models_match_torch_library_composition("qwen2")
+
+
+def test_planted_qk_norm_in_llama_is_caught(monkeypatch):
+    real = om.OracleModel.attn_block
+
+    def with_norm(self, i, h, cache, positions):
+        w = self.w
+        object.__setattr__(w, "arch", "qwen3")                         # planted: llama with qwen3's norm
+        try:
+            self.weights.setdefault(f"blk.{i}.attn_q_norm", np.ones(w.head_dim, np.float32) * 1.5)
+            self.weights.setdefault(f"blk.{i}.attn_k_norm", np.ones(w.head_dim, np.float32) * 1.5)
+            return real(self, i, h, cache, positions)
+        finally:
+            object.__setattr__(w, "arch", "llama")
+    monkeypatch.setattr(om.OracleModel, "attn_block", with_norm)
+    with pytest.raises(AssertionError):
+        pins.test_arch_models_match_torch_library_composition("llama")

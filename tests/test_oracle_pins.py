@@ -419,3 +419,122 @@ def test_sampling_special_cases():
     assert [osm.sample(eq, 1.0, 1.0, u) for u in (0.0, 0.2, 0.4, 0.6, 0.8, 0.95)] == [0, 1, 2, 3, 4, 5]
     o, q = osm.nucleus(eq, 1.0, 0.5)                        # ties kept in index order
     assert o.tolist() == [0, 1, 2] and np.allclose(q, 1 / 3)
+
+
+# --------------------------------------------------------------------------- sibling architectures
+
+def test_gelu_tanh_matches_torch_and_is_not_exact_gelu():
+    z = np.linspace(-12, 12, 4001)
+    ref = F.gelu(torch.from_numpy(z), approximate="tanh").numpy()
+    assert np.allclose(om.gelu_tanh(z), ref, rtol=1e-14, atol=1e-15)
+    exact = F.gelu(torch.from_numpy(z)).numpy()
+    gap = np.max(np.abs(om.gelu_tanh(z) - exact))
+    assert 1e-5 < gap < 2e-3           # two different functions, ~1e-3 apart at most
+    assert om.gelu_tanh(np.array([0.0]))[0] == 0.0
+    assert np.isclose(om.gelu_tanh(np.array([30.0]))[0], 30.0, rtol=0, atol=1e-12)
+
+
+def test_softcap_closed_form():
+    c = 30.0
+    x = np.array([-1e4, -30.0, -1e-3, 0.0, 1e-3, 30.0, 1e4])
+    y = om.softcap(x, c)
+    assert np.allclose(y, c * torch.tanh(torch.from_numpy(x) / c).numpy(), rtol=1e-15)
+    assert np.isclose(y[0], -c) and np.isclose(y[-1], c)                  # saturates at +-c
+    assert np.isclose(y[4], 1e-3, rtol=1e-9) and y[3] == 0.0             # identity near 0
+    assert np.isclose(y[5], c * math.tanh(1.0), rtol=1e-15)
+    r = np.random.default_rng(1).standard_normal(1000) * 50
+    assert np.all(np.diff(om.softcap(np.sort(r), c)) >= 0)               # order kept: argmax unchanged
+
+
+@pytest.mark.parametrize("window", [1, 3, 5, 13, 40])
+def test_sliding_window_attention_matches_sdpa_band_mask(window):
+    rng = np.random.default_rng(window)
+    nq, nkv, T, hd = 4, 2, 13, 16
+    q, k, v = (rng.standard_normal((n, T, hd)) for n in (nq, nkv, nkv))
+    pos = np.arange(T)
+    out = om.attention(q, k, v, pos, window)
+    j, p = np.arange(T)[None, :], pos[:, None]
+    band = torch.from_numpy((j <= p) & (j > p - window))
+    G = nq // nkv
+    ref = F.scaled_dot_product_attention(torch.from_numpy(q), torch.from_numpy(k).repeat_interleave(G, 0),
+                                         torch.from_numpy(v).repeat_interleave(G, 0), attn_mask=band).numpy()
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-13)
+    if window >= T:
+        assert np.allclose(out, om.attention(q, k, v, pos), rtol=0, atol=0)
+    if window == 1:  # each query sees only its own key: the output is that key's value row
+        assert np.allclose(out, np.repeat(v, G, axis=0), rtol=1e-13)
+
+
+def _tiny_arch(arch, kv="f32"):
+    w = synth.Workload("pin_" + arch, vocab=512, hidden=128, n_layers=4, n_heads=4, n_kv_heads=2,
+                       head_dim=32, ffn=256, wtype="q8_0", kv=kv, seed=0, arch=arch,
+                       sliding_window=3 if arch == "gemma3" else 0, sliding_pattern=2,
+                       logit_softcap=0.5 if arch == "gemma3" else 0.0)
+    return w, om.OracleModel(w, om.synth_weights(w))
+
+
+@pytest.mark.parametrize("arch", ["llama", "qwen2", "gemma3", "qwen3"])
+def test_arch_models_match_torch_library_composition(arch):
+    """Each layer recipe recomposed from torch library routines: F.rms_norm,
+    bias adds, SDPA with a band mask for sliding layers, F.gelu(approximate=
+    "tanh") or F.silu, torch.tanh for the softcap."""
+    w, m = _tiny_arch(arch)
+    prompt = list(w.prompt(n=9))
+    T, hd = len(prompt), w.head_dim
+
+    def W(n):
+        return torch.from_numpy(m.matrix(n))
+
+    def g(n):
+        return torch.from_numpy(np.asarray(m.weights[n], dtype=np.float32).astype(np.float64))
+
+    x = torch.from_numpy(m.embed(prompt))
+    pos = np.arange(T)
+    ang = torch.from_numpy(om.rope_angles(pos, hd, w.rope_theta))
+    cos, sin = torch.cos(ang), torch.sin(ang)
+
+    def rot(t):
+        a, b = t[..., : hd // 2], t[..., hd // 2:]
+        return torch.cat([a * cos - b * sin, a * sin + b * cos], -1)
+
+    for i in range(w.n_layers):
+        p = f"blk.{i}"
+        h = F.rms_norm(x, (w.hidden,), weight=g(f"{p}.attn_norm"), eps=w.rms_eps)
+        q, k, v = h @ W(f"{p}.attn_q").T, h @ W(f"{p}.attn_k").T, h @ W(f"{p}.attn_v").T
+        if arch == "qwen2":
+            q, k, v = q + g(f"{p}.attn_q_bias"), k + g(f"{p}.attn_k_bias"), v + g(f"{p}.attn_v_bias")
+        q = q.view(T, w.n_heads, hd).transpose(0, 1)
+        k = k.view(T, w.n_kv_heads, hd).transpose(0, 1)
+        v = v.view(T, w.n_kv_heads, hd).transpose(0, 1)
+        if arch in ("qwen3", "gemma3"):
+            q = F.rms_norm(q, (hd,), weight=g(f"{p}.attn_q_norm"), eps=w.rms_eps)
+            k = F.rms_norm(k, (hd,), weight=g(f"{p}.attn_k_norm"), eps=w.rms_eps)
+        q, k = rot(q), rot(k)
+        sliding = arch == "gemma3" and i % 2 == 0      # pattern 2: odd layers are global
+        j, pp = torch.arange(T)[None, :], torch.arange(T)[:, None]
+        mask = (j <= pp) & ((j > pp - 3) if sliding else True)
+        o = F.scaled_dot_product_attention(q, k.repeat_interleave(w.group, 0), v.repeat_interleave(w.group, 0),
+                                           attn_mask=mask)
+        x = x + o.transpose(0, 1).reshape(T, -1) @ W(f"{p}.attn_output").T
+        h = F.rms_norm(x, (w.hidden,), weight=g(f"{p}.ffn_norm"), eps=w.rms_eps)
+        gate = h @ W(f"{p}.ffn_gate").T
+        act = F.gelu(gate, approximate="tanh") if arch == "gemma3" else F.silu(gate)
+        x = x + (act * (h @ W(f"{p}.ffn_up").T)) @ W(f"{p}.ffn_down").T
+    xl = F.rms_norm(x[-1], (w.hidden,), weight=g("output_norm"), eps=w.rms_eps)
+    ref = xl @ W("token_embd").T
+    if arch == "gemma3":
+        ref = 0.5 * torch.tanh(ref / 0.5)
+    assert np.allclose(m.forward_nocache(prompt), ref.numpy(), rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("arch", ["llama", "qwen2", "gemma3"])
+def test_arch_cached_decode_equals_full_recompute(arch):
+    """The KV cache (and the sliding window on it) gives the same logits as
+    rebuilding the prefix with no state, every step."""
+    w, m = _tiny_arch(arch)
+    prompt = list(w.prompt(n=5))
+    toks, logits = om.run_greedy(m, prompt, 6)
+    seq = prompt + toks[:-1]
+    for s in range(7):
+        ref = m.forward_nocache(seq[: len(prompt) + s])
+        assert np.allclose(logits[s], ref, rtol=1e-12, atol=1e-12), s
