@@ -62,7 +62,9 @@ class TqConfig(ctypes.Structure):
                 ("rope_theta", ctypes.c_float), ("wtype", ctypes.c_int32),
                 ("kvtype", ctypes.c_int32), ("max_batch", ctypes.c_int32),
                 ("max_ctx", ctypes.c_int32), ("max_prefill", ctypes.c_int32),
-                ("page_size", ctypes.c_int32), ("n_pages", ctypes.c_int32)]
+                ("page_size", ctypes.c_int32), ("n_pages", ctypes.c_int32),
+                ("arch", ctypes.c_int32), ("sliding_window", ctypes.c_int32),
+                ("sliding_pattern", ctypes.c_int32), ("logit_softcap", ctypes.c_float)]
 
 
 class TqQmat(ctypes.Structure):
@@ -73,7 +75,9 @@ class TqLayer(ctypes.Structure):
     _fields_ = [(n, TqQmat) for n in ("attn_q", "attn_k", "attn_v", "attn_output", "ffn_gate",
                                       "ffn_up", "ffn_down")] + \
                [(n, ctypes.c_void_p) for n in ("attn_norm_dev", "ffn_norm_dev",
-                                               "attn_q_norm_dev", "attn_k_norm_dev")]
+                                               "attn_q_norm_dev", "attn_k_norm_dev",
+                                               "attn_q_bias_dev", "attn_k_bias_dev",
+                                               "attn_v_bias_dev")]
 
 
 class TqWeights(ctypes.Structure):
@@ -394,30 +398,38 @@ def tq_lm_head_static(m: QMat, x: torch.Tensor, gain: torch.Tensor, eps: float =
 
 LAYER_MATS = ("attn_q", "attn_k", "attn_v", "attn_output", "ffn_gate", "ffn_up", "ffn_down")
 LAYER_GAINS = ("attn_norm", "ffn_norm", "attn_q_norm", "attn_k_norm")
+LAYER_BIASES = ("attn_q_bias", "attn_k_bias", "attn_v_bias")
+ARCHS = {"qwen3": 0, "llama": 1, "qwen2": 2, "gemma3": 3}
 
 
 class Model:
     """A decoder over tiled quantized weights, a torch-allocated workspace and
     KV cache.  ``mats`` maps GGUF-style names (``token_embd``,
     ``blk.{i}.attn_q`` ...; optionally ``output``) to QMat; ``gains`` maps
-    ``blk.{i}.attn_norm`` ... and ``output_norm`` to f32 device tensors."""
+    ``blk.{i}.attn_norm`` ... and ``output_norm`` (and for qwen2 the biases
+    ``blk.{i}.attn_{q,k,v}_bias``) to f32 device tensors.  ``arch`` names the
+    layer recipe: qwen3, llama, qwen2 or gemma3 (with ``sliding_window``,
+    ``sliding_pattern`` and ``logit_softcap``)."""
 
     def __init__(self, *, vocab, hidden, n_layers, n_heads, n_kv_heads, head_dim, ffn,
                  wtype, kv, mats: dict, gains: dict, max_batch=1, max_ctx=4096,
                  max_prefill=512, page_size=0, n_pages=0, rms_eps=1e-6, rope_theta=1e6,
-                 device="cuda"):
+                 device="cuda", arch="qwen3", sliding_window=0, sliding_pattern=0, logit_softcap=0.0):
         self._handle = None
         self._thread = threading.get_ident()
         wt = WTYPES[wtype] if isinstance(wtype, str) else wtype
         kvt = {"f32": TQ_KV_F32, "f16": TQ_KV_F16}[kv] if isinstance(kv, str) else kv
+        if arch not in ARCHS:
+            raise TqError(f"arch must be one of {sorted(ARCHS)} (got {arch!r})")
+        self.arch = arch
         vals = dict(vocab=vocab, hidden=hidden, n_layers=n_layers, n_heads=n_heads,
                     n_kv_heads=n_kv_heads, head_dim=head_dim, ffn=ffn, max_batch=max_batch,
                     max_ctx=max_ctx, max_prefill=max_prefill, page_size=page_size,
-                    n_pages=n_pages)
+                    n_pages=n_pages, sliding_window=sliding_window, sliding_pattern=sliding_pattern)
         for k, v in vals.items():
             _int(k, v, 0, I32[1])
         self.cfg = TqConfig(rms_eps=float(rms_eps), rope_theta=float(rope_theta), wtype=wt,
-                            kvtype=kvt, **vals)
+                            kvtype=kvt, arch=ARCHS[arch], logit_softcap=float(logit_softcap), **vals)
         self.device = torch.device(device)
         if self.device.type != "cuda" or (self.device.index is not None and
                                           self.device.index != torch.cuda.current_device()):
@@ -440,8 +452,10 @@ class Model:
             L = layers[i]
             for n in LAYER_MATS:
                 setattr(L, n, mats[f"blk.{i}.{n}"].abi)
-            for n in LAYER_GAINS:
-                setattr(L, n + "_dev", gains[f"blk.{i}.{n}"].data_ptr())
+            for n in LAYER_GAINS + LAYER_BIASES:
+                g = gains.get(f"blk.{i}.{n}")
+                if g is not None:
+                    setattr(L, n + "_dev", g.data_ptr())
         self._layers = layers
         out = mats.get("output")
         self._weights = TqWeights(mats["token_embd"].abi, out.abi if out is not None else TqQmat(0, 0),

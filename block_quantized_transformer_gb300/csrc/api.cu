@@ -35,7 +35,7 @@ constexpr int kGemmCounters = 4096;
 
 struct Layout {
   size_t x, qkv, att, act, act2, x16, inv_s, logits, xhead, cos_t, sin_t, part, counters, keys, status, chain_sync,
-      gemm_part, gemm_ctr, total;
+      gemm_part, gemm_ctr, bias, total;
   int T;                 // rows of activation buffers
   int split_dec, splits_dec, split_pf, splits_pf;
 };
@@ -67,6 +67,14 @@ bool validate(const tq_config* c) {
     return set_error("config: max_batch, max_ctx and max_prefill must be >= 1"), false;
   if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f))
     return set_error("config: rms_eps and rope_theta must be positive"), false;
+  if (c->arch < TQ_ARCH_QWEN3 || c->arch > TQ_ARCH_GEMMA3)
+    return set_error("config: arch must be a tq_arch (0..3, got %d)", c->arch), false;
+  if (c->sliding_window < 0 || c->sliding_pattern < 0 || !(c->logit_softcap >= 0.f) ||
+      !(c->logit_softcap < 3.0e38f))
+    return set_error("config: sliding_window, sliding_pattern and logit_softcap must be >= 0"), false;
+  if (c->arch != TQ_ARCH_GEMMA3 && (c->sliding_window != 0 || c->sliding_pattern != 0 || c->logit_softcap != 0.f))
+    return set_error("config: sliding_window, sliding_pattern and logit_softcap are gemma3's (set them to 0)"),
+           false;
   if (c->page_size < 0) return set_error("config: page_size must be >= 0"), false;
   if (c->page_size > 0) {
     if (c->page_size % 32 != 0) return set_error("config: page_size must be a multiple of 32"), false;
@@ -116,6 +124,8 @@ Layout layout_of(const tq_config& c) {
   // split-K partial sums of the GEMMs over few rows (batched decode)
   L.gemm_part = L.T > 1 ? take((size_t)kGemmPartFloats * 4) : 0;
   L.gemm_ctr = L.T > 1 ? take((size_t)kGemmCounters * 4) : 0;
+  // qwen2: each layer's q, k and v biases side by side, as the Q/K/V output rows
+  L.bias = c.arch == TQ_ARCH_QWEN2 ? take((size_t)c.n_layers * qkv_width(c) * 4) : 0;
   L.total = off;
   return L;
 }
@@ -182,6 +192,18 @@ struct tq_model {
   float* gemm_part() const { return L.T > 1 ? reinterpret_cast<float*>(ws + L.gemm_part) : nullptr; }
   unsigned* gemm_ctr() const { return L.T > 1 ? reinterpret_cast<unsigned*>(ws + L.gemm_ctr) : nullptr; }
   void* kc_layer(int l) const { return static_cast<uint8_t*>(kc) + (size_t)l * layer_kv_bytes; }
+  const float* qkv_bias(int l) const {
+    return cfg.arch == TQ_ARCH_QWEN2 ? reinterpret_cast<const float*>(ws + L.bias) + (size_t)l * qkv_width(cfg)
+                                     : nullptr;
+  }
+  bool qk_norm() const { return cfg.arch == TQ_ARCH_QWEN3 || cfg.arch == TQ_ARCH_GEMMA3; }
+  int gate_act() const { return cfg.arch == TQ_ARCH_GEMMA3 ? tq::ACT_GELU_TANH : tq::ACT_SILU; }
+  // sliding window of layer l (0: the whole context)
+  int window(int l) const {
+    if (cfg.arch != TQ_ARCH_GEMMA3 || cfg.sliding_window <= 0) return 0;
+    const int p = cfg.sliding_pattern;
+    return p > 0 && l % p == p - 1 ? 0 : cfg.sliding_window;
+  }
   void* vc_layer(int l) const { return static_cast<uint8_t*>(vc) + (size_t)l * layer_kv_bytes; }
 };
 
@@ -248,6 +270,7 @@ tq::GemvArgs qkv_args(const tq_model* m, int l, int T) {
   g.eps = c.rms_eps;
   g.y = m->qkv();
   g.status = m->status();
+  g.bias = m->qkv_bias(l);
   return g;
 }
 
@@ -281,6 +304,7 @@ tq::GemvArgs ffn_args(const tq_model* m, int l, int T) {
   f.eps = c.rms_eps;
   f.y = m->act();
   f.status = m->status();
+  f.act = m->gate_act();
   return f;
 }
 
@@ -313,6 +337,7 @@ tq::GemvArgs head_args(const tq_model* m, const float* x, int B, float* logits) 
   h.y = logits;
   h.argmax_keys = m->keys();
   h.status = m->status();
+  h.softcap = c.logit_softcap;
   return h;
 }
 
@@ -334,8 +359,8 @@ tq::RopeArgs rope_args(const tq_model* m, int l, int T, const int32_t* pos, cons
   r.cache = cache_view(m, block_table);
   r.cos_t = m->cos_t();
   r.sin_t = m->sin_t();
-  r.gq = m->layers[l].attn_q_norm_dev;
-  r.gk = m->layers[l].attn_k_norm_dev;
+  r.gq = m->qk_norm() ? m->layers[l].attn_q_norm_dev : nullptr;
+  r.gk = m->qk_norm() ? m->layers[l].attn_k_norm_dev : nullptr;
   r.eps = c.rms_eps;
   r.status = m->status();
   return r;
@@ -369,9 +394,10 @@ tq::AttnArgs attn_args(const tq_model* m, int l, int T, const int32_t* pos, cons
   a.pos = pos;
   a.cos_t = m->cos_t();
   a.sin_t = m->sin_t();
-  a.gq = m->layers[l].attn_q_norm_dev;
-  a.gk = m->layers[l].attn_k_norm_dev;
+  a.gq = m->qk_norm() ? m->layers[l].attn_q_norm_dev : nullptr;
+  a.gk = m->qk_norm() ? m->layers[l].attn_k_norm_dev : nullptr;
   a.eps = c.rms_eps;
+  a.window = m->window(l);
   return a;
 }
 
@@ -380,6 +406,7 @@ cudaError_t gemm_prep(tq_model* m, int T, const float* x, const float* up, int K
   tq::XPrep16Args p{};
   p.x = x;
   p.up = up;
+  p.act = m->gate_act();
   p.ldx = ldx > 0 ? ldx : K;
   p.gain = gain;
   p.eps = m->cfg.rms_eps;
@@ -391,7 +418,7 @@ cudaError_t gemm_prep(tq_model* m, int T, const float* x, const float* up, int K
 }
 
 cudaError_t gemm_run(tq_model* m, int T, const tq::GemvSeg* seg, int nseg, int K, float* y, int ldy,
-                     const float* residual, cudaStream_t s) {
+                     const float* residual, cudaStream_t s, const float* bias = nullptr) {
   tq::TcGemmArgs g{};
   for (int i = 0; i < nseg; ++i) g.seg[i] = seg[i];
   g.nseg = nseg;
@@ -402,6 +429,7 @@ cudaError_t gemm_run(tq_model* m, int T, const tq::GemvSeg* seg, int nseg, int K
   g.y = y;
   g.ldy = ldy;
   g.residual = residual;
+  g.bias = bias;
   g.status = m->status();
   g.part = m->gemm_part();
   g.part_cap = kGemmPartFloats;
@@ -432,7 +460,8 @@ cudaError_t run_layers_gemm(tq_model* m, int T, const int32_t* pos, const int32_
     const tq_layer& ly = m->layers[l];
     const tq::GemvSeg qkv[3] = {seg_of(ly.attn_q, nq * hd), seg_of(ly.attn_k, nkv * hd), seg_of(ly.attn_v, nkv * hd)};
     if ((e = gemm_prep(m, T, m->x(), nullptr, c.hidden, ly.attn_norm_dev, s)) != cudaSuccess) return e;
-    if ((e = gemm_run(m, T, qkv, 3, c.hidden, m->qkv(), qkv_width(c), nullptr, s)) != cudaSuccess) return e;
+    e = gemm_run(m, T, qkv, 3, c.hidden, m->qkv(), qkv_width(c), nullptr, s, m->qkv_bias(l));
+    if (e != cudaSuccess) return e;
     if (prefill) {
       const tq::RopeArgs r = rope_args(m, l, T, pos, kv_len, pos_base, seq_fixed, block_table, seq_idx);
       if ((e = tq::launch_rope_append(c.kvtype, hd, r, s)) != cudaSuccess) return e;
@@ -481,7 +510,7 @@ cudaError_t run_head_gemm(tq_model* m, const float* x, int B, float* logits, int
   const tq::GemvSeg h = seg_of(m->head, c.vocab);
   cudaError_t e = gemm_prep(m, B, x, nullptr, c.hidden, m->out_norm, s);
   if (e == cudaSuccess) e = gemm_run(m, B, &h, 1, c.hidden, lg, c.vocab, nullptr, s);
-  if (e == cudaSuccess) e = tq::launch_argmax_rows(lg, B, c.vocab, argmax, s);
+  if (e == cudaSuccess) e = tq::launch_argmax_rows(lg, B, c.vocab, c.logit_softcap, argmax, s);
   return e;
 }
 
@@ -600,11 +629,15 @@ tq_status tq_model_create(const tq_config* cfg, const tq_weights* w, void* works
       snprintf(name, sizeof(name), "blk.%d matrix %d", l, i);
       if (!check_qmat(*mats[i], name)) return TQ_REFUSED;
     }
-    if (!ly.attn_norm_dev || !ly.ffn_norm_dev || !ly.attn_q_norm_dev || !ly.attn_k_norm_dev)
+    const bool qk_norm = cfg->arch == TQ_ARCH_QWEN3 || cfg->arch == TQ_ARCH_GEMMA3;
+    if (!ly.attn_norm_dev || !ly.ffn_norm_dev || (qk_norm && (!ly.attn_q_norm_dev || !ly.attn_k_norm_dev)))
       return set_error("weights: a gain of blk.%d is NULL", l), TQ_REFUSED;
-    const float* gs[4] = {ly.attn_norm_dev, ly.ffn_norm_dev, ly.attn_q_norm_dev, ly.attn_k_norm_dev};
+    const float* gs[4] = {ly.attn_norm_dev, ly.ffn_norm_dev, qk_norm ? ly.attn_q_norm_dev : nullptr,
+                          qk_norm ? ly.attn_k_norm_dev : nullptr};
     for (const float* gp : gs)
       if (!aligned16(gp)) return set_error("weights: gains of blk.%d must be 16-byte aligned", l), TQ_REFUSED;
+    if (cfg->arch == TQ_ARCH_QWEN2 && (!ly.attn_q_bias_dev || !ly.attn_k_bias_dev || !ly.attn_v_bias_dev))
+      return set_error("weights: qwen2 needs the q, k and v biases of blk.%d", l), TQ_REFUSED;
   }
   if (!aligned16(w->output_norm_dev)) return set_error("weights: output_norm must be 16-byte aligned"), TQ_REFUSED;
 
@@ -641,6 +674,15 @@ tq_status tq_model_create(const tq_config* cfg, const tq_weights* w, void* works
     }
   }
   if (e == cudaSuccess) e = cudaMemset(workspace, 0, m->L.total);
+  if (cfg->arch == TQ_ARCH_QWEN2)  // [bq | bk | bv] of each layer, in the order of the Q/K/V rows
+    for (int l = 0; l < cfg->n_layers && e == cudaSuccess; ++l) {
+      float* b = const_cast<float*>(m->qkv_bias(l));
+      const size_t nq = (size_t)cfg->n_heads * cfg->head_dim, nk = (size_t)cfg->n_kv_heads * cfg->head_dim;
+      e = cudaMemcpy(b, w->layers[l].attn_q_bias_dev, nq * 4, cudaMemcpyDeviceToDevice);
+      if (e == cudaSuccess) e = cudaMemcpy(b + nq, w->layers[l].attn_k_bias_dev, nk * 4, cudaMemcpyDeviceToDevice);
+      if (e == cudaSuccess)
+        e = cudaMemcpy(b + nq + nk, w->layers[l].attn_v_bias_dev, nk * 4, cudaMemcpyDeviceToDevice);
+    }
   if (e == cudaSuccess) e = cudaMemcpy(m->cos_t(), cs.data(), cs.size() * 4, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(m->sin_t(), sn.data(), sn.size() * 4, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();

@@ -76,11 +76,13 @@ __global__ void __launch_bounds__(128) rope_append_kernel(RopeArgs a) {
     x[j] = src[lane + 32 * j];
     ss = fmaf(x[j], x[j], ss);
   }
-  ss = warp_sum(ss);
-  const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
   const float* g = is_q ? a.gq : a.gk;
+  if (g != nullptr) {  // per-head RMSNorm (absent from some layer recipes)
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
 #pragma unroll
-  for (int j = 0; j < DPL; ++j) x[j] = x[j] * inv * g[lane + 32 * j];
+    for (int j = 0; j < DPL; ++j) x[j] = x[j] * inv * g[lane + 32 * j];
+  }
 
   if (pos >= 0 && pos < a.cache.max_ctx) {
     constexpr int HALF = HD / 2;
@@ -144,20 +146,22 @@ __device__ __forceinline__ void load_row<float, 2>(const float* p, float (&v)[2]
   v[0] = a.x; v[1] = a.y;
 }
 
-// RMSNorm over the head (gain g) and half-split RoPE at `pos` of one head held
+// RMSNorm over the head (gain g; skipped when !norm) and half-split RoPE at `pos` of one head held
 // as DPL consecutive dimensions per lane (lane l: dims l*DPL ..): the partner
 // of dimension i < hd/2 is i + hd/2, which lives in lane l ^ 16.
 template <int HD, int DPL>
 __device__ __forceinline__ void norm_rope_head(float (&x)[DPL], const float (&g)[DPL], float eps,
                                                const float (&c)[DPL], const float (&sn)[DPL],
-                                               int lane, bool rope_ok) {
-  float ss = 0.f;
+                                               int lane, bool rope_ok, bool norm) {
+  if (norm) {
+    float ss = 0.f;
 #pragma unroll
-  for (int d = 0; d < DPL; ++d) ss = fmaf(x[d], x[d], ss);
-  ss = warp_sum(ss);
-  const float inv = 1.0f / sqrtf(ss / (float)HD + eps);
+    for (int d = 0; d < DPL; ++d) ss = fmaf(x[d], x[d], ss);
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / (float)HD + eps);
 #pragma unroll
-  for (int d = 0; d < DPL; ++d) x[d] = x[d] * inv * g[d];
+    for (int d = 0; d < DPL; ++d) x[d] = x[d] * inv * g[d];
+  }
   if (!rope_ok) return;
   const bool first = lane < 16;
 #pragma unroll
@@ -228,12 +232,15 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
   const int new_slot = a.kv_len != nullptr ? a.kv_len[t] : a.pos_base + t;
   int ctx = new_slot + 1;
   if (ctx > a.cache.max_ctx) ctx = a.cache.max_ctx;
+  // sliding window: keys lo .. ctx - 1, split from lo rounded down to a tile
+  const int lo = a.window > 0 ? max(0, new_slot + 1 - a.window) : 0;
+  const int lo_t = (min(lo, ctx - 1) / TILE) * TILE;
   // cluster: keys per CTA rounded up to whole tiles
-  const int span = CL > 0 ? ((ctx + CL * TILE - 1) / (CL * TILE)) * TILE : a.split_keys;
-  const int n_active = (ctx + span - 1) / span;
+  const int span = CL > 0 ? ((ctx - lo_t + CL * TILE - 1) / (CL * TILE)) * TILE : a.split_keys;
+  const int n_active = (ctx - lo_t + span - 1) / span;
   if (CL == 0 && split >= n_active) return;
   const int seq = a.seq_idx != nullptr ? a.seq_idx[t] : a.seq_fixed >= 0 ? a.seq_fixed : t;
-  const int k0 = split * span;
+  const int k0 = lo_t + split * span;
   const int k1 = min(ctx, k0 + span);
   const int n_tiles = k1 > k0 ? (k1 - k0 + TILE - 1) / TILE : 0;
   const int my_n = warp < n_tiles ? (n_tiles - warp + 3) / 4 : 0;
@@ -293,8 +300,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
 #pragma unroll
     for (int d = 0; d < DPL; ++d) {
       const int i = (lane * DPL + d) % (HD / 2);
-      gq[d] = a.gq[lane * DPL + d];
-      gk[d] = a.gk[lane * DPL + d];
+      gq[d] = a.gq != nullptr ? a.gq[lane * DPL + d] : 1.f;
+      gk[d] = a.gk != nullptr ? a.gk[lane * DPL + d] : 1.f;
       cs[d] = rope_ok ? a.cos_t[(int64_t)pos * (HD / 2) + i] : 1.f;
       sn[d] = rope_ok ? a.sin_t[(int64_t)pos * (HD / 2) + i] : 0.f;
     }
@@ -325,12 +332,12 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
   }
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    if (FUSED) norm_rope_head<HD, DPL>(qr[g], gq, a.eps, cs, sn, lane, rope_ok);
+    if (FUSED) norm_rope_head<HD, DPL>(qr[g], gq, a.eps, cs, sn, lane, rope_ok, a.gq != nullptr);
 #pragma unroll
     for (int d = 0; d < DPL; ++d) qr[g][d] *= a.scale_log2;
   }
   if (owns_new) {
-    norm_rope_head<HD, DPL>(kx, gk, a.eps, cs, sn, lane, rope_ok);
+    norm_rope_head<HD, DPL>(kx, gk, a.eps, cs, sn, lane, rope_ok, a.gk != nullptr);
     KT* kd = cache_row<KT, HD>(const_cast<void*>(a.kc), seq, h, new_slot, a.cache);
     KT* vd = cache_row<KT, HD>(const_cast<void*>(a.vc), seq, h, new_slot, a.cache);
     if (kd != nullptr && vd != nullptr) {
@@ -362,6 +369,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
     const KT* Ks = reinterpret_cast<const KT*>(smem + (warp * NS + stage) * S::STAGE_BYTES);
     const KT* Vs = reinterpret_cast<const KT*>(smem + (warp * NS + stage) * S::STAGE_BYTES + S::TILE_BYTES);
     const int nv = min(TILE, k1 - tile_key0(k));
+    const int nlo = lo - tile_key0(k);  // keys of the tile before the window
 
     // scores of the whole query group against the tile's keys
     float sc[NCH];
@@ -381,7 +389,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
         }
       }
       const float s = reduce_scatter32(v, lane);
-      sc[c] = (c * CK + lane % CK) < nv ? s : kNegInf;
+      sc[c] = (c * CK + lane % CK) < nv && (c * CK + lane % CK) >= nlo ? s : kNegInf;
     }
     // online softmax for head gl
     float mt = sc[0];
@@ -637,9 +645,12 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(const __grid_constant__ CU
   const int pos = FUSED ? a.pos[t] : 0;
   int ctx = new_slot + 1;
   if (ctx > a.cache.max_ctx) ctx = a.cache.max_ctx;
-  const int span = ((ctx + CL * TILE - 1) / (CL * TILE)) * TILE;
+  // sliding window: keys lo .. ctx - 1, split from lo rounded down to a tile
+  const int lo = a.window > 0 ? max(0, new_slot + 1 - a.window) : 0;
+  const int lo_t = (min(lo, ctx - 1) / TILE) * TILE;
+  const int span = ((ctx - lo_t + CL * TILE - 1) / (CL * TILE)) * TILE;
   const int seq = a.seq_idx != nullptr ? a.seq_idx[t] : a.seq_fixed >= 0 ? a.seq_fixed : t;
-  const int k0 = split * span;
+  const int k0 = lo_t + split * span;
   const int k1 = min(ctx, k0 + span);
   const int n_tiles = k1 > k0 ? (k1 - k0 + TILE - 1) / TILE : 0;
   const int my_n = warp < n_tiles ? (n_tiles - warp + 3) / 4 : 0;
@@ -739,8 +750,8 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(const __grid_constant__ CU
 #pragma unroll
   for (int d = 0; d < DPL; ++d) {
     const int i = (lane * DPL + d) % (HD / 2);
-    gq[d] = FUSED ? a.gq[lane * DPL + d] : 1.f;
-    gk[d] = FUSED ? a.gk[lane * DPL + d] : 1.f;
+    gq[d] = FUSED && a.gq != nullptr ? a.gq[lane * DPL + d] : 1.f;
+    gk[d] = FUSED && a.gk != nullptr ? a.gk[lane * DPL + d] : 1.f;
     cs[d] = FUSED && rope_ok ? a.cos_t[(int64_t)pos * (HD / 2) + i] : 1.f;
     sn[d] = FUSED && rope_ok ? a.sin_t[(int64_t)pos * (HD / 2) + i] : 0.f;
   }
@@ -755,7 +766,7 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(const __grid_constant__ CU
     const float* qp = qrow + (h * G + gg) * HD + lane * DPL;
 #pragma unroll
     for (int d = 0; d < DPL; ++d) qr[d] = qp[d];
-    if (FUSED) norm_rope_head<HD, DPL>(qr, gq, a.eps, cs, sn, lane, rope_ok);
+    if (FUSED) norm_rope_head<HD, DPL>(qr, gq, a.eps, cs, sn, lane, rope_ok, a.gq != nullptr);
     float mx = 0.f;
 #pragma unroll
     for (int d = 0; d < DPL; ++d) {
@@ -780,7 +791,7 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(const __grid_constant__ CU
       kx[d] = kp[d];
       vx[d] = vp[d];
     }
-    norm_rope_head<HD, DPL>(kx, gk, a.eps, cs, sn, lane, rope_ok);
+    norm_rope_head<HD, DPL>(kx, gk, a.eps, cs, sn, lane, rope_ok, a.gk != nullptr);
     __half* kd = cache_row<__half, HD>(const_cast<void*>(a.kc), seq, h, new_slot, a.cache);
     __half* vd = cache_row<__half, HD>(const_cast<void*>(a.vc), seq, h, new_slot, a.cache);
     if (kd != nullptr && vd != nullptr) {
@@ -832,6 +843,7 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(const __grid_constant__ CU
     wait_tile(k, false);  // K(k): rows past the context only meet masked scores
     zero_rows(kt, k);     // (a page outside the pool: zeros, as for V)
     const int nv = min(TILE, k1 - tile_key0(k));
+    const int nlo = lo - tile_key0(k);  // keys of the tile before the window
     // scores of the tile: two m-tiles of 16 keys
     float sc[NT][2][4];
 #pragma unroll
@@ -856,8 +868,9 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(const __grid_constant__ CU
       float s4[4];
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
-        s4[2 * mt] = (mt * 16 + g) < nv ? (sc[nt][mt][0] + sc[nt][mt][1]) * inv_q[nt] : kNegInf;
-        s4[2 * mt + 1] = (mt * 16 + g + 8) < nv ? (sc[nt][mt][2] + sc[nt][mt][3]) * inv_q[nt] : kNegInf;
+        const int ka = mt * 16 + g, kb = ka + 8;
+        s4[2 * mt] = ka < nv && ka >= nlo ? (sc[nt][mt][0] + sc[nt][mt][1]) * inv_q[nt] : kNegInf;
+        s4[2 * mt + 1] = kb < nv && kb >= nlo ? (sc[nt][mt][2] + sc[nt][mt][3]) * inv_q[nt] : kNegInf;
       }
       float mt_ = fmaxf(fmaxf(s4[0], s4[1]), fmaxf(s4[2], s4[3]));
       mt_ = fmaxf(mt_, __shfl_xor_sync(0xffffffffu, mt_, 4));

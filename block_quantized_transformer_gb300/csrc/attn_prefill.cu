@@ -106,6 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int seq = a.seq_fixed;
   const int n_keys = min(a.pos_base + t_last + 1, a.cache.max_ctx);
   const int n_tiles = (n_keys + kTile - 1) / kTile;
+  // sliding window: tiles before the first key any query row of the CTA sees
+  // are skipped (the rows' own lower bounds are masked below)
+  const int i0 = a.window > 0 ? min(max(0, a.pos_base + t0 + 1 - a.window), n_keys) / kTile : 0;
 
   // zero the stages once: a box that is not loaded (past the prefix) then
   // holds finite values, which the mask turns into p = 0
@@ -130,9 +133,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::prefetch_tmap(&vmap);
       grid_dep_wait();  // the append kernel wrote this prompt's K/V rows
       int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int slot = i % kNS;
-        if (i >= kNS && !mbar_wait_timed(&empty[slot], (uint32_t)(((i / kNS) - 1) & 1), kWaitNs)) {
+      for (int i = i0; i < n_tiles; ++i) {
+        const int ii = i - i0, slot = ii % kNS;  // stage ring position
+        if (ii >= kNS && !mbar_wait_timed(&empty[slot], (uint32_t)(((ii / kNS) - 1) & 1), kWaitNs)) {
           set_status(a.status, TQ_DEV_WAIT_TIMEOUT);
           *abort_flag = 1;
           break;
@@ -190,6 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // rows past the prompt compute on zeros and are not written
   const int pos_a = a.pos_base + min(tok_a, t_last), pos_b = a.pos_base + min(tok_b, t_last);
   const int pmax = a.pos_base + min(t0 + (warp * 16 + 15) / G, t_last);
+  // key j is visible to a row at position p iff lo < j <= p (lo = p - window, or -1)
+  const int lo_a = a.window > 0 ? pos_a - a.window : -1, lo_b = a.window > 0 ? pos_b - a.window : -1;
 
   grid_dep_wait();  // q was normalised and rotated by the append kernel
   // ---- Q: both rows as fp16 hi/lo A fragments after a power-of-two scale
@@ -260,9 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int nd = 0; nd < ND; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
   float m_a = kNegInf, m_b = kNegInf, l_a = 0.f, l_b = 0.f;
 
-  for (int i = 0; i < n_tiles; ++i) {
-    const int slot = i % kNS;
-    bool ok = *abort_flag == 0 && mbar_wait_timed(&full[slot], (uint32_t)((i / kNS) & 1), kWaitNs);
+  for (int i = i0; i < n_tiles; ++i) {
+    const int ii = i - i0, slot = ii % kNS;
+    bool ok = *abort_flag == 0 && mbar_wait_timed(&full[slot], (uint32_t)((ii / kNS) & 1), kWaitNs);
     if (!__all_sync(0xffffffffu, ok) && lane == 0 && *abort_flag == 0) {
       set_status(a.status, TQ_DEV_WAIT_TIMEOUT);
       *abort_flag = 1;
@@ -294,10 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int j = key0 + 8 * nt + 2 * c;
-        s[nt][0] = j <= pos_a ? s[nt][0] * mult_a : kNegInf;
-        s[nt][1] = j + 1 <= pos_a ? s[nt][1] * mult_a : kNegInf;
-        s[nt][2] = j <= pos_b ? s[nt][2] * mult_b : kNegInf;
-        s[nt][3] = j + 1 <= pos_b ? s[nt][3] * mult_b : kNegInf;
+        s[nt][0] = j <= pos_a && j > lo_a ? s[nt][0] * mult_a : kNegInf;
+        s[nt][1] = j + 1 <= pos_a && j + 1 > lo_a ? s[nt][1] * mult_a : kNegInf;
+        s[nt][2] = j <= pos_b && j > lo_b ? s[nt][2] * mult_b : kNegInf;
+        s[nt][3] = j + 1 <= pos_b && j + 1 > lo_b ? s[nt][3] * mult_b : kNegInf;
         mx_a = fmaxf(mx_a, fmaxf(s[nt][0], s[nt][1]));
         mx_b = fmaxf(mx_b, fmaxf(s[nt][2], s[nt][3]));
       }

@@ -20,13 +20,18 @@ __global__ void argmax_finish_kernel(const unsigned long long* keys, int n, int3
 
 // out[b] = index of the largest of logits[b][0..V), the lowest index on ties
 // (the same 64-bit keys as the GEMV's argmax epilogue).  One CTA per row.
-__global__ void __launch_bounds__(256) argmax_rows_kernel(const float* logits, int V, int32_t* out) {
+__global__ void __launch_bounds__(256) argmax_rows_kernel(float* logits, int V, float softcap, int32_t* out) {
   grid_dep_launch();
   grid_dep_wait();
-  const float* row = logits + (int64_t)blockIdx.x * V;
+  float* row = logits + (int64_t)blockIdx.x * V;
   unsigned long long best = 0ull;
   for (int i = threadIdx.x; i < V; i += 256) {
-    const unsigned long long k = argmax_key(row[i], (uint32_t)i);
+    float v = row[i];
+    if (softcap > 0.f) {
+      v = softcap * tanhf(v / softcap);
+      row[i] = v;
+    }
+    const unsigned long long k = argmax_key(v, (uint32_t)i);
     best = k > best ? k : best;
   }
 #pragma unroll
@@ -85,9 +90,9 @@ cudaError_t launch_gemv(int wtype, int mode, const GemvArgs& a, cudaStream_t s) 
   return launch_gemv_chain(wtype, c, s);
 }
 
-cudaError_t launch_argmax_rows(const float* logits, int n, int V, int32_t* out, cudaStream_t s) {
+cudaError_t launch_argmax_rows(float* logits, int n, int V, float softcap, int32_t* out, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  return launch_k(argmax_rows_kernel, dim3(n), dim3(256), 0, s, logits, V, out);
+  return launch_k(argmax_rows_kernel, dim3(n), dim3(256), 0, s, logits, V, softcap, out);
 }
 
 cudaError_t launch_gather_rows(const float* x, int H, int n_rows, const int32_t* rows, int n, float* out,

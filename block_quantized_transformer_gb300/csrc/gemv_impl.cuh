@@ -262,7 +262,6 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory"); }
 
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
 
 // Final value(s) of row rr of tile t: scale, epilogue, store.  resid: this
 // CTA's residual rows from tile t0 on, prefetched to shared memory, or null.
@@ -277,8 +276,9 @@ __device__ __forceinline__ void finish_row(const GemvArgs& a, int mode, const Ge
   const int64_t o = (int64_t)b * a.N + row;
   v *= inv_s;
   if (mode == GEMV_SWIGLU) {
-    a.y[o] = silu(v) * (up * inv_s);
+    a.y[o] = gate_act(v, a.act) * (up * inv_s);
   } else if (mode == GEMV_ARGMAX) {
+    if (a.softcap > 0.f) v = a.softcap * tanhf(v / a.softcap);
     if (a.y != nullptr) a.y[o] = v;
     const unsigned long long key = argmax_key(v, (uint32_t)row);
     best = key > best ? key : best;
@@ -286,7 +286,7 @@ __device__ __forceinline__ void finish_row(const GemvArgs& a, int mode, const Ge
     const float r = a.residual == nullptr ? 0.f
                     : resid != nullptr ? resid[(t - t0) * kTileRows + rr]
                                        : __ldcg(a.residual + o);
-    a.y[o] = r + v;
+    a.y[o] = a.bias != nullptr ? (r + v) + a.bias[row] : r + v;
   }
 }
 

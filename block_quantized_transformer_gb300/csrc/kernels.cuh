@@ -52,6 +52,14 @@ cudaError_t launch_embed(int wtype, const void* qs, const uint16_t* d, int vocab
 
 // ---- decode GEMV (gemv.cu)
 enum GemvMode { GEMV_STORE = 0, GEMV_SWIGLU = 1, GEMV_ARGMAX = 2 };
+// activation of a gated FFN's gate: silu(z) = z / (1 + e^-z), or the tanh
+// approximation of GELU, z/2 (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))
+enum GateAct { ACT_SILU = 0, ACT_GELU_TANH = 1 };
+
+__device__ __forceinline__ float gate_act(float z, int act) {
+  if (act == ACT_GELU_TANH) return 0.5f * z * (1.0f + tanhf(0.7978845608028654f * (z + 0.044715f * z * z * z)));
+  return z / (1.0f + __expf(-z));
+}
 
 struct GemvSeg {
   const uint8_t* qs;
@@ -72,6 +80,9 @@ struct GemvArgs {
   const float* residual; // [B][N] or null (STORE only); may alias y
   unsigned long long* argmax_keys;  // [B] (ARGMAX)
   uint32_t* status;      // device status word (bounded waits), or null
+  const float* bias;     // STORE: [N] added to every output row, or null
+  int act;               // SWIGLU: the gate's activation (ACT_SILU or ACT_GELU_TANH)
+  float softcap;         // ARGMAX: logits = c tanh(logits / c) when c > 0
 };
 
 // Up to kMaxPhases GEMVs run by one persistent kernel; phase p+1 starts
@@ -96,7 +107,8 @@ bool gemv_supported(int K);
 // Phase input rows -> fp16 rows after a power-of-two scale per row.
 struct XPrep16Args {
   const float* x;
-  const float* up;       // optional: the input is silu(x) * up
+  const float* up;       // optional: the input is act(x) * up
+  int act;               // GateAct of act()
   int ldx;
   const float* gain;     // optional RMSNorm gain
   float eps;
@@ -114,6 +126,7 @@ struct TcGemmArgs {
   float* y;                // [T][ldy]
   int ldy;
   const float* residual;   // [T][ldy] or null; may alias y
+  const float* bias;       // [ldy] added to every row, or null
   uint32_t* status;
   // split over K (few token rows): part_cap floats of partial sums, n_counters
   // zero counters between launches; null part keeps one split
@@ -151,7 +164,7 @@ struct RopeArgs {
   CacheView cache;
   const float* cos_t;        // [max_ctx][hd/2]
   const float* sin_t;
-  const float* gq;
+  const float* gq;           // per-head RMSNorm gains of q and k, or null: no norm
   const float* gk;
   float eps;
   uint32_t* status;
@@ -181,9 +194,10 @@ struct AttnArgs {
   const int32_t* pos;        // rope position per token
   const float* cos_t;
   const float* sin_t;
-  const float* gq;
+  const float* gq;           // null: no per-head norm
   const float* gk;
   float eps;
+  int window;                // > 0: keys j with slot - window < j <= slot only (sliding window)
 };
 
 cudaError_t launch_rope_append(int kvtype, int hd, const RopeArgs& a, cudaStream_t s);
@@ -214,6 +228,8 @@ cudaError_t launch_gather_rows(const float* x, int H, int n_rows, const int32_t*
 // argmax keys -> int32 indices
 cudaError_t launch_argmax_finish(const unsigned long long* keys, int n, int32_t* out, cudaStream_t s);
 // logits [n][V] -> per-row argmax, ties to the lowest index
-cudaError_t launch_argmax_rows(const float* logits, int n, int V, int32_t* out, cudaStream_t s);
+// row argmax of [n][V] logits; softcap > 0 first replaces each logit by
+// softcap * tanh(logit / softcap) in place
+cudaError_t launch_argmax_rows(float* logits, int n, int V, float softcap, int32_t* out, cudaStream_t s);
 
 }  // namespace tq

@@ -352,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int local = row_ok ? (t - m.tile0[sg]) * kTileRows + row % kTileRows : 0;
       const bool valid = row_ok && local < a.seg[sg].rows;
       const int col = (sg == 0 ? m.row0[0] : sg == 1 ? m.row0[1] : m.row0[2]) + local;
+      const float bcol = valid && a.bias != nullptr && ks == 1 ? __ldg(a.bias + col) : 0.f;
       const int c0 = (warp >> 2) * CW;
       for (int cc = 0; cc < CW; cc += 16) {
         float v[16];
@@ -379,11 +380,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             r[j] = tk0 + j < a.T ? __ldcg(a.residual + (int64_t)(tk0 + j) * a.ldy + col) : 0.f;
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (tk0 + j < a.T) a.y[(int64_t)(tk0 + j) * a.ldy + col] = r[j] + v[j];
+            if (tk0 + j < a.T) a.y[(int64_t)(tk0 + j) * a.ldy + col] = (r[j] + v[j]) + bcol;
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (tk0 + j < a.T) a.y[(int64_t)(tk0 + j) * a.ldy + col] = v[j];
+            if (tk0 + j < a.T) a.y[(int64_t)(tk0 + j) * a.ldy + col] = v[j] + bcol;
         }
       }
     }
@@ -494,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // run in split order.
   const bool vec = (a.ldy & 3) == 0 && (m.row0[1] & 3) == 0 && (m.row0[2] & 3) == 0 &&
                    ((reinterpret_cast<uintptr_t>(a.y) | reinterpret_cast<uintptr_t>(a.part) |
-                     reinterpret_cast<uintptr_t>(a.residual)) & 15u) == 0;
+                     reinterpret_cast<uintptr_t>(a.residual) | reinterpret_cast<uintptr_t>(a.bias)) & 15u) == 0;
   const int64_t pstride = (int64_t)a.T * a.ldy;
   for (int gi = tid; gi < (kBM / 4) * BN; gi += kThreads) {
     const int row = 4 * (gi % (kBM / 4)), tok = n0 + gi / (kBM / 4);
@@ -504,7 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int local = (t - m.tile0[sg]) * kTileRows + row % kTileRows;
     const int rows = a.seg[sg].rows;
     if (local >= rows) continue;
-    const int64_t off = (int64_t)tok * a.ldy + (sg == 0 ? m.row0[0] : sg == 1 ? m.row0[1] : m.row0[2]) + local;
+    const int col = (sg == 0 ? m.row0[0] : sg == 1 ? m.row0[1] : m.row0[2]) + local;
+    const int64_t off = (int64_t)tok * a.ldy + col;
     if (vec && local + 4 <= rows) {
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       const float4 r = a.residual != nullptr ? __ldcg(reinterpret_cast<const float4*>(a.residual + off)) : v;
@@ -522,14 +524,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             v.w += p[j].w;
           }
       }
-      *reinterpret_cast<float4*>(a.y + off) = make_float4(r.x + v.x, r.y + v.y, r.z + v.z, r.w + v.w);
+      const float4 b = a.bias != nullptr ? __ldg(reinterpret_cast<const float4*>(a.bias + col))
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(a.y + off) =
+          make_float4((r.x + v.x) + b.x, (r.y + v.y) + b.y, (r.z + v.z) + b.z, (r.w + v.w) + b.w);
     } else {
       const int n = min(4, rows - local);
       for (int k = 0; k < n; ++k) {
         float v = 0.f;
         const float r = a.residual != nullptr ? __ldcg(a.residual + off + k) : 0.f;
         for (int zz = 0; zz < ks; ++zz) v += __ldcg(a.part + (int64_t)zz * pstride + off + k);  // split order
-        a.y[off + k] = r + v;
+        a.y[off + k] = (r + v) + (a.bias != nullptr ? __ldg(a.bias + col + k) : 0.f);
       }
     }
   }
@@ -537,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------ xprep16 --
 
-// Row t of the phase input (x, RMS-normalised with `gain`, or silu(x) * up)
+// Row t of the phase input (x, RMS-normalised with `gain`, or act(x) * up)
 // -> fp16 row t of x16 after the power-of-two scale 2^e that puts its largest
 // magnitude in [2^14, 2^15), inputs in the word-major order of the GEMM's
 // weight operand; inv_s[t] = 2^-e.
@@ -561,13 +566,13 @@ __global__ void __launch_bounds__(256) xprep16_kernel(const XPrep16Args a) {
       const int in0 = (c >> 4) * 128 + 32 * (c & 3) + 4 * ((c >> 2) & 3), in1 = in0 + 16;
       float4 p0 = *reinterpret_cast<const float4*>(xr + in0);
       float4 p1 = *reinterpret_cast<const float4*>(xr + in1);
-      if (ur != nullptr) {  // silu(gate) * up
+      if (ur != nullptr) {  // act(gate) * up
         const float4 u0 = *reinterpret_cast<const float4*>(ur + in0);
         const float4 u1 = *reinterpret_cast<const float4*>(ur + in1);
-        p0 = make_float4(p0.x / (1.f + __expf(-p0.x)) * u0.x, p0.y / (1.f + __expf(-p0.y)) * u0.y,
-                         p0.z / (1.f + __expf(-p0.z)) * u0.z, p0.w / (1.f + __expf(-p0.w)) * u0.w);
-        p1 = make_float4(p1.x / (1.f + __expf(-p1.x)) * u1.x, p1.y / (1.f + __expf(-p1.y)) * u1.y,
-                         p1.z / (1.f + __expf(-p1.z)) * u1.z, p1.w / (1.f + __expf(-p1.w)) * u1.w);
+        p0 = make_float4(gate_act(p0.x, a.act) * u0.x, gate_act(p0.y, a.act) * u0.y, gate_act(p0.z, a.act) * u0.z,
+                         gate_act(p0.w, a.act) * u0.w);
+        p1 = make_float4(gate_act(p1.x, a.act) * u1.x, gate_act(p1.y, a.act) * u1.y, gate_act(p1.z, a.act) * u1.z,
+                         gate_act(p1.w, a.act) * u1.w);
       }
       if (a.gain != nullptr) {
         ss = fmaf(p0.x, p0.x, fmaf(p0.y, p0.y, fmaf(p0.z, p0.z, fmaf(p0.w, p0.w, ss))));

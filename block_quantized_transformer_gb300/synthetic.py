@@ -41,9 +41,16 @@ def build_gain(w: "synth.Workload", name: str, device="cuda") -> torch.Tensor:
     return g
 
 
+def build_bias(w: "synth.Workload", name: str, device="cuda") -> torch.Tensor:
+    b = torch.empty(w.bias_len(name), dtype=torch.float32, device=device)
+    synth.dev_normal(b, w.seed, w.stream_of(name), sigma=synth.BIAS_SIGMA)
+    return b
+
+
 def build_weights(w: "synth.Workload", device="cuda"):
     mats = {n: build_matrix(w, n, device) for n in w.matrices()}
     gains = {n: build_gain(w, n, device) for n in w.gains()}
+    gains.update({n: build_bias(w, n, device) for n in w.biases()})
     return mats, gains
 
 
@@ -57,4 +64,6 @@ def build_model(w: "synth.Workload", device="cuda", max_batch=None, max_ctx=None
                  max_ctx=max_ctx or (w.prompt_len + w.decode_steps + 1),
                  max_prefill=max_prefill or w.prompt_len,
                  page_size=(w.page_size if w.paged else 0) if page_size is None else page_size,
-                 n_pages=n_pages or 0, rms_eps=w.rms_eps, rope_theta=w.rope_theta, device=device)
+                 n_pages=n_pages or 0, rms_eps=w.rms_eps, rope_theta=w.rope_theta, device=device,
+                 arch=w.arch, sliding_window=w.sliding_window, sliding_pattern=w.sliding_pattern,
+                 logit_softcap=w.logit_softcap)

@@ -79,7 +79,23 @@ typedef struct {
   int32_t max_prefill;  /* tokens one tq_prefill call may process */
   int32_t page_size;    /* 0 = contiguous cache */
   int32_t n_pages;      /* pages in the pool (paged cache only) */
+  /* Layer recipe ("Inferencia local y arquitecturas", sections "El formato"
+   * and "Las operaciones": an architecture is the same operations in another
+   * order).  All zero = qwen3. */
+  int32_t arch;            /* tq_arch */
+  int32_t sliding_window;  /* gemma3: a sliding layer's query at cache index p sees keys j with
+                              p - sliding_window < j <= p (0 = every layer sees the whole context) */
+  int32_t sliding_pattern; /* gemma3: layer l sees the whole context when l % p == p - 1
+                              (0 = every layer slides) */
+  float logit_softcap;     /* gemma3: logits = c * tanh(logits / c) (0 = none) */
 } tq_config;
+
+/* qwen3: per-head RMSNorm of q and k before RoPE, SiLU-gated FFN;
+ * llama: qwen3 without the per-head norm (attn_q_norm / attn_k_norm unused);
+ * qwen2: llama plus bias vectors added to q, k and v after their matmuls;
+ * gemma3: qwen3 with a tanh-approximated-GELU gate, sliding-window attention
+ *         on a layer pattern and a final logit softcap (the config fields above). */
+typedef enum { TQ_ARCH_QWEN3 = 0, TQ_ARCH_LLAMA = 1, TQ_ARCH_QWEN2 = 2, TQ_ARCH_GEMMA3 = 3 } tq_arch;
 
 /* One quantized matrix [rows][cols] (cols a multiple of 256) in the tiled
  * layout.  Rows are padded with zero rows to a multiple of 16 (R rows) and
@@ -105,8 +121,11 @@ typedef struct {
   tq_qmat attn_q, attn_k, attn_v, attn_output, ffn_gate, ffn_up, ffn_down;
   const float* attn_norm_dev;     /* [hidden] */
   const float* ffn_norm_dev;      /* [hidden] */
-  const float* attn_q_norm_dev;   /* [head_dim] */
-  const float* attn_k_norm_dev;   /* [head_dim] */
+  const float* attn_q_norm_dev;   /* [head_dim] (qwen3, gemma3; else unused) */
+  const float* attn_k_norm_dev;   /* [head_dim] (qwen3, gemma3; else unused) */
+  const float* attn_q_bias_dev;   /* qwen2: [n_heads * head_dim]; else unused */
+  const float* attn_k_bias_dev;   /* qwen2: [n_kv_heads * head_dim] */
+  const float* attn_v_bias_dev;   /* qwen2: [n_kv_heads * head_dim] */
 } tq_layer;
 
 typedef struct {

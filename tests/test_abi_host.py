@@ -66,6 +66,12 @@ def test_workspace_and_cache_sizes():
     (dict(page_size=48, n_pages=4), "page_size"),
     (dict(page_size=32, n_pages=4, max_ctx=40), "multiple of page_size"),
     (dict(page_size=32, n_pages=0), "n_pages"),
+    (dict(arch=4), "arch"),
+    (dict(arch=-1), "arch"),
+    (dict(arch=1, sliding_window=8), "gemma3"),
+    (dict(arch=0, logit_softcap=30.0), "gemma3"),
+    (dict(arch=3, sliding_window=-2), ">= 0"),
+    (dict(arch=3, logit_softcap=-1.0), ">= 0"),
 ])
 def test_invalid_configs_refused_with_reason(bad, msg):
     assert tq.tq_workspace_bytes(_cfg(**bad)) == 0
@@ -139,3 +145,12 @@ def test_gemm_scratch_bytes():
         assert L.tq_gemm_scratch_bytes(rows, n_rows, cols) == want
     for rows, n_rows, cols in [(16, 0, 256), (16, 4, 0), (16, 4, 288), (16, 4, 12544), (0, 4, 256)]:
         assert L.tq_gemm_scratch_bytes(rows, n_rows, cols) == 0
+
+
+def test_layer_recipes_accepted_and_qwen2_holds_its_biases():
+    base = tq.tq_workspace_bytes(_cfg())
+    assert tq.tq_workspace_bytes(_cfg(arch=1)) == base
+    assert tq.tq_workspace_bytes(_cfg(arch=3, sliding_window=512, sliding_pattern=6, logit_softcap=30.0)) == base
+    q2 = tq.tq_workspace_bytes(_cfg(arch=2))
+    # the q, k and v biases of both layers side by side: 2 * (4 + 2 * 2) * 64 floats
+    assert q2 - base == (2 * (4 + 2 * 2) * 64 * 4 + 255) // 256 * 256
