@@ -1,4 +1,4 @@
-"""Q8_0 and Q4_0 block encodings, written out plainly (oracle; test infrastructure).
+"""Q8_0, Q4_0 and affine 4-bit encodings, written out plainly (oracle; test infrastructure).
 
 The pages name GGUF weights and say that large weights stay quantized and are
 multiplied in f32 after decoding ("Inferencia local y arquitecturas", section
@@ -24,6 +24,22 @@ Readings where the definition is open:
 
 Decoding is exact in f32 and f64: an fp16 significand (11 bits) times an
 integer of at most 8 bits.
+
+Affine 4-bit ("Alchemize PyTensor ... Gemma 3n", section on streaming the
+affine-4 checkpoint): W[r, c] = q[r, c] * s[r, g(c)] + b[r, g(c)] with 4-bit q,
+eight of them per uint32 word, and a bf16 scale and bias per group.  The page
+gives the decoding; the readings taken for the rest:
+
+* groups of 64 consecutive inputs of a row; element 8w + i of a group sits in
+  bits 4i .. 4i + 3 of its word w (low nibble first);
+* encoding in f32: s = (max - min) / 15 and b = min over the group, q =
+  clamp(round((w - b) / s), 0, 15) with round-half-away and the f32 s and b;
+  a group of equal values has s = 0 and q = 0; the stored s and b are bf16,
+  rounded to nearest even;
+* this module's record of a group is 36 bytes: the 8 words (little-endian),
+  then the bf16 scale, then the bf16 bias.
+
+Decoding q * s + b is exact in f64; in f32 the sum rounds once.
 """
 from __future__ import annotations
 
@@ -32,6 +48,8 @@ import numpy as np
 QK = 32
 Q8_0_BYTES = 34
 Q4_0_BYTES = 18
+AFFINE_GROUP = 64
+AFFINE4_BYTES = 36
 
 
 def round_half_away(x: np.ndarray) -> np.ndarray:
@@ -80,7 +98,58 @@ def quantize_q4_0(w: np.ndarray) -> np.ndarray:
     return out.reshape(*lead, w.shape[-1] // QK, Q4_0_BYTES)
 
 
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns (uint16), rounded to nearest even."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return r.astype(np.uint16)
+
+
+def bf16_value(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns -> float32 (exact)."""
+    return (np.asarray(bits, dtype=np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def quantize_affine4(w: np.ndarray) -> np.ndarray:
+    """f32 rows [..., K] -> affine 4-bit group records [..., K/64, 36] (uint8)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    assert w.shape[-1] % AFFINE_GROUP == 0, "row length must be a multiple of 64"
+    lead = w.shape[:-1]
+    g = w.reshape(-1, AFFINE_GROUP)
+    lo = np.min(g, axis=1)
+    hi = np.max(g, axis=1)
+    s = ((hi - lo) / np.float32(15.0)).astype(np.float32)        # f32 division
+    b = lo
+    safe = np.where(s == 0, np.float32(1.0), s)
+    q = round_half_away(((g - b[:, None]) / safe[:, None]).astype(np.float32))
+    q = np.where(s[:, None] == 0, np.float32(0.0), q)
+    q = np.clip(q, 0, 15).astype(np.uint32)
+    words = np.zeros((g.shape[0], 8), dtype=np.uint32)
+    for i in range(8):                                            # element 8w + i at bits 4i
+        words |= q[:, i::8] << np.uint32(4 * i)
+    out = np.empty((g.shape[0], AFFINE4_BYTES), dtype=np.uint8)
+    out[:, 0:32] = words.astype("<u4").view(np.uint8)
+    out[:, 32:34] = bf16_bits(s).astype("<u2").view(np.uint8).reshape(-1, 2)
+    out[:, 34:36] = bf16_bits(b).astype("<u2").view(np.uint8).reshape(-1, 2)
+    return out.reshape(*lead, w.shape[-1] // AFFINE_GROUP, AFFINE4_BYTES)
+
+
+def affine4_parts(groups: np.ndarray):
+    """Group records [..., G, 36] -> (codes [..., G, 64] uint8, scale bf16 bits
+    [..., G], bias bf16 bits [..., G])."""
+    g = np.ascontiguousarray(groups)
+    words = g[..., 0:32].copy().view("<u4")                      # [..., G, 8]
+    q = np.empty(g.shape[:-1] + (AFFINE_GROUP,), dtype=np.uint8)
+    for i in range(8):
+        q[..., i::8] = (words >> np.uint32(4 * i)) & np.uint32(15)
+    s = g[..., 32:34].copy().view("<u2")[..., 0]
+    b = g[..., 34:36].copy().view("<u2")[..., 0]
+    return q, s, b
+
+
 def quantize(w: np.ndarray, wtype: str) -> np.ndarray:
+    if wtype == "affine4":
+        return quantize_affine4(w)
     return quantize_q8_0(w) if wtype == "q8_0" else quantize_q4_0(w)
 
 
@@ -98,7 +167,12 @@ def codes(blocks: np.ndarray, wtype: str) -> np.ndarray:
 
 
 def dequantize(blocks: np.ndarray, wtype: str, dtype=np.float64) -> np.ndarray:
-    """Block bytes [..., nb, 34|18] -> weights [..., nb*32] in ``dtype``."""
+    """Block bytes [..., nb, 34|18] (group records [..., G, 36] for affine4)
+    -> weights [..., nb*32] in ``dtype``."""
+    if wtype == "affine4":
+        q, s, b = affine4_parts(blocks)
+        v = q.astype(dtype) * bf16_value(s).astype(dtype)[..., None] + bf16_value(b).astype(dtype)[..., None]
+        return v.reshape(*blocks.shape[:-2], blocks.shape[-2] * AFFINE_GROUP)
     d = scales(blocks).astype(dtype)[..., None]
     q = codes(blocks, wtype).astype(dtype)
     if wtype == "q4_0":

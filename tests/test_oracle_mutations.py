@@ -265,3 +265,40 @@ def test_planted_qk_norm_in_llama_is_caught(monkeypatch):
     monkeypatch.setattr(om.OracleModel, "attn_block", with_norm)
     with pytest.raises(AssertionError):
         pins.test_arch_models_match_torch_library_composition("llama")
+
+
+# --------------------------------------------------------------------------- affine 4-bit format
+
+def test_planted_reversed_nibble_order_is_caught(monkeypatch):
+    real = quant.affine4_parts
+
+    def reversed_parts(groups):
+        q, s, b = real(groups)
+        q = q.reshape(*q.shape[:-1], 8, 8)[..., ::-1].reshape(q.shape)   # planted: high nibble first
+        return q, s, b
+    monkeypatch.setattr(quant, "affine4_parts", reversed_parts)
+    with pytest.raises(AssertionError):
+        pins.test_affine4_hand_worked_group()
+
+
+def test_planted_half_even_codes_are_caught(monkeypatch):
+    monkeypatch.setattr(quant, "round_half_away", lambda x: np.round(x))   # numpy: halves to even
+    with pytest.raises(AssertionError):
+        pins.test_affine4_hand_worked_group()
+
+
+def test_planted_bias_dropped_is_caught(monkeypatch):
+    real = quant.bf16_value
+
+    def deq_without_bias(blocks, wtype, dtype=np.float64):
+        q, s, b = quant.affine4_parts(blocks)
+        v = q.astype(dtype) * real(s).astype(dtype)[..., None]                # planted: + b missing
+        return v.reshape(*blocks.shape[:-2], blocks.shape[-2] * 64)
+    orig = quant.dequantize
+    monkeypatch.setattr(quant, "dequantize",
+                        lambda blocks, wtype, dtype=np.float64: deq_without_bias(blocks, wtype, dtype)
+                        if wtype == "affine4" else orig(blocks, wtype, dtype))
+    with pytest.raises(AssertionError):
+        pins.test_affine4_hand_worked_group()
+    with pytest.raises(AssertionError):
+        pins.test_affine4_brute_force_error_bound_and_equal_groups()

@@ -538,3 +538,47 @@ def test_arch_cached_decode_equals_full_recompute(arch):
     for s in range(7):
         ref = m.forward_nocache(seq[: len(prompt) + s])
         assert np.allclose(logits[s], ref, rtol=1e-12, atol=1e-12), s
+
+
+# --------------------------------------------------------------------------- affine 4-bit format
+
+def _golden_affine():
+    return {k: v[0] for k, v in golden("affine4_group.txt").items()}
+
+
+def test_affine4_hand_worked_group():
+    rec = _golden_affine()
+    w = np.zeros(64, dtype=np.float32)
+    w[:5] = [float(v) for v in rec["values"]]
+    g = quant.quantize_affine4(w[None, :])[0, 0]
+    words = g[0:32].copy().view("<u4")
+    assert int(words[0]) == int(rec["word0"][0], 16)
+    assert all(int(x) == int(rec["word_rest"][0], 16) for x in words[1:])
+    assert int(g[32:34].copy().view("<u2")[0]) == int(rec["scale_bf16"][0], 16)
+    assert int(g[34:36].copy().view("<u2")[0]) == int(rec["bias_bf16"][0], 16)
+    q, _, _ = quant.affine4_parts(g[None, :])
+    assert q[0, :5].tolist() == [int(v) for v in rec["codes"]]
+    deq = quant.dequantize(g[None, None, :], "affine4")[0]
+    assert deq[:5].tolist() == [float(v) for v in rec["decoded"]]
+    assert np.all(deq[5:] == 0.0)
+
+
+def test_affine4_brute_force_error_bound_and_equal_groups():
+    rng = np.random.default_rng(5)
+    w = (rng.standard_normal((7, 256)) * 0.02).astype(np.float32)
+    w[3, 64:128] = 0.0375                                  # a group of equal values
+    g = quant.quantize_affine4(w)
+    q, sb, bb = quant.affine4_parts(g)
+    deq = quant.dequantize(g, "affine4").reshape(7, 4, 64)
+    grp = w.astype(np.float64).reshape(7, 4, 64)
+    lo, hi = grp.min(-1), grp.max(-1)
+    s = (hi - lo) / 15
+    s_bf, b_bf = quant.bf16_value(sb).astype(np.float64), quant.bf16_value(bb).astype(np.float64)
+    bound = s / 2 + 15 * np.abs(s - s_bf) + np.abs(lo - b_bf) + 1e-9
+    assert np.all(np.abs(deq - grp) <= bound[..., None])
+    assert q[3, 1].max() == 0 and s_bf[3, 1] == 0.0 and np.all(deq[3, 1] == b_bf[3, 1])
+    # codes in range, extremes hit
+    assert q.max() == 15 and q.min() == 0
+    # decoding in f32 rounds once: within half an ulp of the f64 value
+    d32 = quant.dequantize(g, "affine4", np.float32).astype(np.float64).reshape(7, 4, 64)
+    assert np.all(np.abs(d32 - deq) <= np.abs(deq) * 2.0 ** -24 + 1e-30)
