@@ -27,12 +27,12 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.environ.get("TQ_LIB", os.path.join(_PKG, "_build", "libtq.so"))
 
 TQ_OK, TQ_REFUSED, TQ_INTERNAL = 0, 1, 2
-TQ_Q4_0, TQ_Q8_0 = 2, 8
+TQ_Q4_0, TQ_AFFINE4, TQ_Q8_0 = 2, 4, 8
 TQ_KV_F32, TQ_KV_F16 = 0, 1
 TQ_DEV_BAD_TOKEN, TQ_DEV_KV_OVERFLOW, TQ_DEV_WAIT_TIMEOUT = 1, 2, 4
-WTYPES = {"q4_0": TQ_Q4_0, "q8_0": TQ_Q8_0}
+WTYPES = {"q4_0": TQ_Q4_0, "q8_0": TQ_Q8_0, "affine4": TQ_AFFINE4}
 BLOCK_BYTES = {TQ_Q4_0: 18, TQ_Q8_0: 34}
-QS_BYTES = {TQ_Q4_0: 16, TQ_Q8_0: 32}
+QS_BYTES = {TQ_Q4_0: 16, TQ_Q8_0: 32, TQ_AFFINE4: 16}  # code bytes per 32 inputs in the tiled layout
 
 EXPORTS = ("tq_workspace_bytes", "tq_kv_cache_bytes", "tq_model_create", "tq_prefill",
            "tq_decode_step", "tq_step", "tq_decode_step_graph", "tq_decode_chain", "tq_model_status",
@@ -40,7 +40,7 @@ EXPORTS = ("tq_workspace_bytes", "tq_kv_cache_bytes", "tq_model_create", "tq_pre
            "tq_model_poisoned",
            "tq_decode_launches", "tq_model_free", "tq_last_error", "tq_qmat_bytes", "tq_repack", "tq_quantize",
            "tq_dequantize", "tq_gemv", "tq_gemm_scratch_bytes", "tq_gemm", "tq_swiglu_gemv", "tq_lm_head",
-           "tq_sample", "tq_lm_head_static")
+           "tq_sample", "tq_lm_head_static", "tq_quantize_affine4", "tq_repack_affine4")
 LM_HEAD_STATIC_MAX_BATCH = 4096
 
 
@@ -128,6 +128,8 @@ def lib() -> ctypes.CDLL:
                 "tq_lm_head": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, f32, vp, vp, vp, vp]),
                 "tq_lm_head_static": (i32, [i32, TqQmat, i32, i32, vp, i32, vp, f32, vp, vp, vp]),
                 "tq_sample": (i32, [vp, i32, i32, vp, vp, vp, vp, vp]),
+                "tq_quantize_affine4": (i32, [vp, i64, i64, vp, vp, vp, vp]),
+                "tq_repack_affine4": (i32, [vp, vp, vp, i64, i64, vp, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -230,6 +232,42 @@ def tq_quantize(wtype: int, w: torch.Tensor, rows: int, cols: int, blocks: torch
                            _dev(blocks, "blocks", torch.uint8, rows * (cols // 32) * BLOCK_BYTES[wtype]),
                            _stream())
     _status(rc, "tq_quantize")
+
+
+def tq_quantize_affine4(w: torch.Tensor, rows: int, cols: int, words: torch.Tensor, scales: torch.Tensor,
+                        biases: torch.Tensor) -> None:
+    """f32 [rows][cols] -> MLX-layout affine 4-bit groups: words int32 [rows][cols/8],
+    scales and biases int16 (bf16 bit patterns) [rows][cols/64]."""
+    _int("rows", rows, 0, I64[1])
+    _int("cols", cols, 0, I64[1])
+    rc = lib().tq_quantize_affine4(_dev(w, "w", torch.float32, rows * cols), rows, cols,
+                                   _dev(words, "words", torch.int32, rows * (cols // 8)),
+                                   _dev(scales, "scales", torch.int16, rows * (cols // 64)),
+                                   _dev(biases, "biases", torch.int16, rows * (cols // 64)), _stream())
+    _status(rc, "tq_quantize_affine4")
+
+
+def tq_repack_affine4(words: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor, rows: int, cols: int,
+                      qs: torch.Tensor, d: torch.Tensor) -> None:
+    """MLX-layout affine 4-bit groups -> tiled layout (TQ_AFFINE4)."""
+    _int("rows", rows, 0, I64[1])
+    _int("cols", cols, 0, I64[1])
+    qb, db = tq_qmat_bytes(TQ_AFFINE4, rows, cols)
+    rc = lib().tq_repack_affine4(_dev(words, "words", torch.int32, rows * (cols // 8)),
+                                 _dev(scales, "scales", torch.int16, rows * (cols // 64)),
+                                 _dev(biases, "biases", torch.int16, rows * (cols // 64)), rows, cols,
+                                 _dev(qs, "qs", torch.uint8, qb), _dev(d, "d", torch.int16, db // 2), _stream())
+    _status(rc, "tq_repack_affine4")
+
+
+def quantize_affine4(w: torch.Tensor):
+    """f32 [rows][cols] (device) -> (words, scales, biases) in MLX's layout."""
+    rows, cols = w.shape
+    words = torch.empty(rows, cols // 8, dtype=torch.int32, device=w.device)
+    scales = torch.empty(rows, cols // 64, dtype=torch.int16, device=w.device)
+    biases = torch.empty(rows, cols // 64, dtype=torch.int16, device=w.device)
+    tq_quantize_affine4(w.contiguous(), rows, cols, words, scales, biases)
+    return words, scales, biases
 
 
 # ----------------------------------------------------------------------------- matrices

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libtq.so")
-SOURCES = ["api.cu", "quant.cu", "gemv.cu", "gemv_q4.cu", "gemv_q8.cu", "tcgemm.cu", "attn.cu", "attn_prefill.cu", "sample.cu", "lm_head_static.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemv.cu", "gemv_q4.cu", "gemv_q8.cu", "gemv_a4.cu", "tcgemm.cu", "attn.cu", "attn_prefill.cu", "sample.cu", "lm_head_static.cu"]
 
 
 def nvcc() -> str:

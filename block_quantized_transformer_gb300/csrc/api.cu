@@ -30,6 +30,9 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// formats of the tiled layout: Q4_0, AFFINE4, Q8_0
+bool tiled_wtype(int32_t w) { return w == TQ_Q4_0 || w == TQ_AFFINE4 || w == TQ_Q8_0; }
+
 constexpr int64_t kGemmPartFloats = 4 << 20;  // 16 MB of split-K partial sums
 constexpr int kGemmCounters = 4096;
 
@@ -54,8 +57,8 @@ bool validate(const tq_config* c) {
   const int G = c->n_heads / c->n_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8)
     return set_error("config: n_heads / n_kv_heads must be 1, 2, 4 or 8 (got %d)", G), false;
-  if (c->wtype != TQ_Q4_0 && c->wtype != TQ_Q8_0)
-    return set_error("config: wtype must be TQ_Q4_0 (2) or TQ_Q8_0 (8)"), false;
+  if (!tiled_wtype(c->wtype))
+    return set_error("config: wtype must be TQ_Q4_0 (2), TQ_AFFINE4 (4) or TQ_Q8_0 (8)"), false;
   if (c->kvtype != TQ_KV_F32 && c->kvtype != TQ_KV_F16)
     return set_error("config: kvtype must be TQ_KV_F32 (0) or TQ_KV_F16 (1)"), false;
   const int ks[3] = {c->hidden, c->n_heads * c->head_dim, c->ffn};
@@ -876,17 +879,18 @@ void tq_model_free(tq_model* m) {
 // ------------------------------------------------------------- formats --
 
 tq_status tq_qmat_bytes(int32_t wtype, int64_t rows, int64_t cols, int64_t* qs_bytes, int64_t* d_bytes) {
-  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (!tiled_wtype(wtype)) return set_error("wtype must be 2, 4 or 8"), TQ_REFUSED;
   if (rows < 0 || cols < 0 || cols % 256 != 0) return set_error("cols must be a multiple of 256"), TQ_REFUSED;
   const int64_t blocks = tq::tiled_rows(rows) * (cols / 32);
-  if (qs_bytes != nullptr) *qs_bytes = blocks * (wtype == TQ_Q4_0 ? 16 : 32);
+  if (qs_bytes != nullptr) *qs_bytes = blocks * (wtype == TQ_Q8_0 ? 32 : 16);
   if (d_bytes != nullptr) *d_bytes = blocks * 2;
   return TQ_OK;
 }
 
 tq_status tq_repack(int32_t wtype, const void* blocks, int64_t rows, int64_t cols, void* qs,
                     uint16_t* d, void* stream) {
-  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0)
+    return set_error("wtype must be 2 or 8 (affine 4-bit groups: tq_repack_affine4)"), TQ_REFUSED;
   if (rows < 0 || cols < 0 || cols % 256 != 0) return set_error("cols must be a multiple of 256"), TQ_REFUSED;
   if (rows * cols == 0) return TQ_OK;
   if (!blocks || !qs || !d) return set_error("pointers must not be NULL"), TQ_REFUSED;
@@ -898,7 +902,8 @@ tq_status tq_repack(int32_t wtype, const void* blocks, int64_t rows, int64_t col
 }
 
 tq_status tq_quantize(int32_t wtype, const float* w, int64_t rows, int64_t cols, void* blocks, void* stream) {
-  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0)
+    return set_error("wtype must be 2 or 8 (affine 4-bit: tq_quantize_affine4)"), TQ_REFUSED;
   if (rows < 0 || cols < 0 || cols % 32 != 0) return set_error("cols must be a multiple of 32"), TQ_REFUSED;
   if (rows * cols == 0) return TQ_OK;
   if (!w || !blocks) return set_error("pointers must not be NULL"), TQ_REFUSED;
@@ -907,9 +912,35 @@ tq_status tq_quantize(int32_t wtype, const float* w, int64_t rows, int64_t cols,
   return TQ_OK;
 }
 
+tq_status tq_quantize_affine4(const float* w, int64_t rows, int64_t cols, uint32_t* words, uint16_t* scales,
+                              uint16_t* biases, void* stream) {
+  if (rows < 0 || cols < 0 || cols % 64 != 0) return set_error("cols must be a multiple of 64"), TQ_REFUSED;
+  if (rows * cols == 0) return TQ_OK;
+  if (!w || !words || !scales || !biases) return set_error("pointers must not be NULL"), TQ_REFUSED;
+  if ((reinterpret_cast<uintptr_t>(w) & 3u) || (reinterpret_cast<uintptr_t>(words) & 3u) ||
+      (reinterpret_cast<uintptr_t>(scales) & 1u) || (reinterpret_cast<uintptr_t>(biases) & 1u))
+    return set_error("w and words must be 4-byte, scales and biases 2-byte aligned"), TQ_REFUSED;
+  cudaError_t e = tq::launch_quantize_affine4(w, rows, cols, words, scales, biases, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(nullptr, e, "tq_quantize_affine4");
+  return TQ_OK;
+}
+
+tq_status tq_repack_affine4(const uint32_t* words, const uint16_t* scales, const uint16_t* biases, int64_t rows,
+                            int64_t cols, void* qs, uint16_t* d, void* stream) {
+  if (rows < 0 || cols < 0 || cols % 256 != 0) return set_error("cols must be a multiple of 256"), TQ_REFUSED;
+  if (rows * cols == 0) return TQ_OK;
+  if (!words || !scales || !biases || !qs || !d) return set_error("pointers must not be NULL"), TQ_REFUSED;
+  if ((reinterpret_cast<uintptr_t>(words) & 3u) || (reinterpret_cast<uintptr_t>(scales) & 1u) ||
+      (reinterpret_cast<uintptr_t>(biases) & 1u) || !aligned16(qs) || !aligned16(d))
+    return set_error("words must be 4-byte, scales and biases 2-byte, qs and d 16-byte aligned"), TQ_REFUSED;
+  cudaError_t e = tq::launch_repack_affine4(words, scales, biases, rows, cols, qs, d, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(nullptr, e, "tq_repack_affine4");
+  return TQ_OK;
+}
+
 tq_status tq_dequantize(int32_t wtype, tq_qmat w, int64_t cols, int64_t row0, int64_t n_rows,
                         float* out, void* stream) {
-  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (!tiled_wtype(wtype)) return set_error("wtype must be 2, 4 or 8"), TQ_REFUSED;
   if (cols <= 0 || cols % 256 != 0 || row0 < 0 || n_rows < 0)
     return set_error("cols must be a positive multiple of 256; rows non-negative"), TQ_REFUSED;
   if (n_rows == 0) return TQ_OK;
@@ -925,7 +956,7 @@ tq_status tq_dequantize(int32_t wtype, tq_qmat w, int64_t cols, int64_t row0, in
 
 tq_status tq_gemv(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const float* x, int32_t batch,
                   const float* residual, float* y, void* stream) {
-  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (!tiled_wtype(wtype)) return set_error("wtype must be 2, 4 or 8"), TQ_REFUSED;
   if (rows < 1 || batch < 1 || !tq::gemv_supported(cols))
     return set_error("rows and batch must be >= 1 and cols have a GEMV mapping (got %d)", cols), TQ_REFUSED;
   if (!w.qs_dev || !w.d_dev || !x || !y) return set_error("pointers must not be NULL"), TQ_REFUSED;
@@ -976,7 +1007,7 @@ size_t tq_gemm_scratch_bytes(int32_t rows, int32_t n_rows, int32_t cols) {
 
 tq_status tq_gemm(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const float* x, int32_t n_rows,
                   const float* residual, float* y, void* scratch, void* stream) {
-  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (!tiled_wtype(wtype)) return set_error("wtype must be 2, 4 or 8"), TQ_REFUSED;
   if (rows < 1 || n_rows < 1 || cols < 256 || cols % 256 != 0 || cols > 12288)
     return set_error("rows, n_rows must be >= 1 and cols a multiple of 256 up to 12288"), TQ_REFUSED;
   if (!w.qs_dev || !w.d_dev || !x || !y || !scratch) return set_error("pointers must not be NULL"), TQ_REFUSED;
@@ -1019,7 +1050,7 @@ tq_status tq_gemm(int32_t wtype, tq_qmat w, int32_t rows, int32_t cols, const fl
 tq_status tq_swiglu_gemv(int32_t wtype, tq_qmat gate, tq_qmat up, int32_t ffn, int32_t hidden,
                          const float* x, int32_t batch, const float* gain, float eps, float* out,
                          void* stream) {
-  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (!tiled_wtype(wtype)) return set_error("wtype must be 2, 4 or 8"), TQ_REFUSED;
   if (ffn < 1 || batch < 1 || !tq::gemv_supported(hidden))
     return set_error("ffn and batch must be >= 1 and hidden have a GEMV mapping"), TQ_REFUSED;
   if (!gate.qs_dev || !gate.d_dev || !up.qs_dev || !up.d_dev || !x || !out)
@@ -1056,7 +1087,7 @@ tq_status tq_sample(const float* logits, int32_t batch, int32_t vocab, const flo
 tq_status tq_lm_head(int32_t wtype, tq_qmat w, int32_t vocab, int32_t hidden, const float* x,
                      int32_t batch, const float* gain, float eps, float* logits, int32_t* argmax,
                      void* scratch, void* stream) {
-  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) return set_error("wtype must be 2 or 8"), TQ_REFUSED;
+  if (!tiled_wtype(wtype)) return set_error("wtype must be 2, 4 or 8"), TQ_REFUSED;
   if (vocab < 1 || batch < 1 || !tq::gemv_supported(hidden))
     return set_error("vocab and batch must be >= 1 and hidden have a GEMV mapping"), TQ_REFUSED;
   if (!w.qs_dev || !w.d_dev || !x || !gain || !argmax || !scratch)

@@ -8,6 +8,7 @@ namespace tq {
 
 cudaError_t launch_gemv_chain_q4(const GemvChain& c, cudaStream_t s);
 cudaError_t launch_gemv_chain_q8(const GemvChain& c, cudaStream_t s);
+cudaError_t launch_gemv_chain_a4(const GemvChain& c, cudaStream_t s);
 
 namespace {
 
@@ -77,6 +78,7 @@ cudaError_t launch_gemv_chain(int wtype, const GemvChain& c, cudaStream_t s) {
   if (c.n > 1 && c.sync == nullptr) return cudaErrorInvalidValue;
   for (int p = 0; p < c.n; ++p)
     if (!pick_mapping(c.ph[p].K) || c.ph[p].N <= 0 || c.ph[p].B <= 0) return cudaErrorInvalidValue;
+  if (wtype == TQ_AFFINE4) return launch_gemv_chain_a4(c, s);
   return wtype == TQ_Q4_0 ? launch_gemv_chain_q4(c, s) : launch_gemv_chain_q8(c, s);
 }
 

@@ -80,7 +80,7 @@ template <int WT>
 struct Fmt {
   static constexpr int QU = unit_qs_bytes(WT);       // code bytes of a unit
   static constexpr int UB = QU + kUnitD;             // unit bytes
-  static constexpr int SU = WT == TQ_Q4_0 ? TQ_GEMV_SLOT_UNITS_Q4 : 2;  // units per slot (even)
+  static constexpr int SU = nib4(WT) ? TQ_GEMV_SLOT_UNITS_Q4 : 2;  // units per slot (even)
   static constexpr int SLOT = SU * UB;
 };
 
@@ -138,11 +138,13 @@ __device__ __forceinline__ void q8_operands(uint32_t w, uint32_t& p01, uint32_t&
 // xt / xn: shared addresses of the x fragments and of the negated bias sums
 // of the unit's first block (the operands carry the biased codes, so a
 // block's tensor-core sum exceeds the wanted sum by bias * sum(x) * 2^-24,
-// which the prologue computed once for all rows).
+// which the prologue computed once for all rows).  AFFINE4: the operands are
+// the plain codes q, the prologue's table holds -sum(x) * 2^-24 per block,
+// and a block adds s * (its sum) + b * sum(x) with its group's bf16 s and b.
 template <int WT, int MATS>
 __device__ __forceinline__ void unit_dot(uint32_t qs, uint32_t mstride_q, uint32_t dq, uint32_t mstride_d,
                                          uint32_t xt, uint32_t xn, int lane, float (&acc)[MATS][2]) {
-  constexpr int NS = WT == TQ_Q4_0 ? 2 : 4;  // 16-byte code loads per row half
+  constexpr int NS = nib4(WT) ? 2 : 4;  // 16-byte code loads per row half
   const int g = lane >> 2;
   uint4 wv[MATS][2][NS];
   uint4 dv[MATS][2];
@@ -165,7 +167,7 @@ __device__ __forceinline__ void unit_dot(uint32_t qs, uint32_t mstride_q, uint32
 #pragma unroll
     for (int m = 0; m < MATS; ++m) {
       float c[4];
-      if (WT == TQ_Q4_0) {
+      if (nib4(WT)) {
         uint32_t g02, g13, gh02, gh13, e02, e13, eh02, eh13;
         q4_operands(word_of(wv[m][0][j >> 2], j & 3), g02, g13, gh02, gh13);
         q4_operands(word_of(wv[m][1][j >> 2], j & 3), e02, e13, eh02, eh13);
@@ -183,8 +185,16 @@ __device__ __forceinline__ void unit_dot(uint32_t qs, uint32_t mstride_q, uint32
         q8_operands(word_of(r1, o + 1), e01, e23);
         mma16816(c, g01, e01, g23, e23, xf.z, xf.w, c);
       }
-      acc[m][0] = fmaf(half_bits_to_float(half_of(dv[m][0], j)), (c[0] + c[1]) + nb, acc[m][0]);
-      acc[m][1] = fmaf(half_bits_to_float(half_of(dv[m][1], j)), (c[2] + c[3]) + nb, acc[m][1]);
+      if (WT == TQ_AFFINE4) {  // group j / 2: (s, b) at elements 2 (j / 2), + 1
+        const int e = j & ~1;
+        acc[m][0] = fmaf(bf16_bits_to_float(half_of(dv[m][0], e)), c[0] + c[1],
+                         fmaf(-bf16_bits_to_float(half_of(dv[m][0], e + 1)), nb, acc[m][0]));
+        acc[m][1] = fmaf(bf16_bits_to_float(half_of(dv[m][1], e)), c[2] + c[3],
+                         fmaf(-bf16_bits_to_float(half_of(dv[m][1], e + 1)), nb, acc[m][1]));
+      } else {
+        acc[m][0] = fmaf(half_bits_to_float(half_of(dv[m][0], j)), (c[0] + c[1]) + nb, acc[m][0]);
+        acc[m][1] = fmaf(half_bits_to_float(half_of(dv[m][1], j)), (c[2] + c[3]) + nb, acc[m][1]);
+      }
     }
   }
 }
@@ -582,10 +592,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
           const int blk = pr >> 2, c = pr & 3;
           float e[8] = {v0[r].x * f, v0[r].y * f, v0[r].z * f, v0[r].w * f,
                         v1[r].x * f, v1[r].y * f, v1[r].z * f, v1[r].w * f};
-          // code bias x sum of the pair's activations (8 for Q4_0, 128 for Q8_0)
+          // code bias x sum of the pair's activations (8 for Q4_0, 128 for Q8_0;
+          // AFFINE4: the sum itself, which the group's bias multiplies)
           float bias = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-          bias *= WT == TQ_Q4_0 ? 8.0f : 128.0f;
-          if (WT == TQ_Q4_0) {  // pairs (0,2) (1,3) (4,6)/16 (5,7)/16
+          bias *= WT == TQ_Q4_0 ? 8.0f : WT == TQ_Q8_0 ? 128.0f : 1.0f;
+          if (nib4(WT)) {  // pairs (0,2) (1,3) (4,6)/16 (5,7)/16
             const float t1 = e[1], t5 = e[5];
             e[1] = e[2];
             e[2] = t1;

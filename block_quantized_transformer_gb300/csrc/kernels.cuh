@@ -24,14 +24,17 @@ constexpr int kTileRows = 16;
 constexpr int kUnitBlocks = 8;
 constexpr int kUnitD = 256;  // bytes of scales per unit
 
-__host__ __device__ constexpr int unit_qs_bytes(int wt) { return wt == TQ_Q4_0 ? 2048 : 4096; }
+// 4-bit formats (Q4_0, AFFINE4) share the code arrangement; AFFINE4's
+// scale elements hold (bf16 scale, bf16 bias) of each 64-input group.
+__host__ __device__ constexpr bool nib4(int wt) { return wt != TQ_Q8_0; }
+__host__ __device__ constexpr int unit_qs_bytes(int wt) { return nib4(wt) ? 2048 : 4096; }
 
 __host__ __device__ inline int64_t tiled_rows(int64_t rows) { return (rows + 15) / 16 * 16; }
 
 __host__ __device__ inline int64_t tiled_qs_offset(int wt, int64_t r, int64_t blk, int64_t nb, int i) {
   const int64_t unit = (r >> 4) * (nb / kUnitBlocks) + (blk >> 3);
   const int h = (int)((r >> 3) & 1), g = (int)(r & 7), j = (int)(blk & 7);
-  if (wt == TQ_Q4_0) return unit * 2048 + (int64_t)(((h * 2 + (j >> 2)) * 32 + g * 4 + i) * 16 + (j & 3) * 4);
+  if (nib4(wt)) return unit * 2048 + (int64_t)(((h * 2 + (j >> 2)) * 32 + g * 4 + i) * 16 + (j & 3) * 4);
   return unit * 4096 + (int64_t)(((h * 4 + (j >> 1)) * 32 + g * 4 + (i & 3)) * 16 + (j & 1) * 8 + (i >> 2) * 4);
 }
 
@@ -44,6 +47,10 @@ __host__ __device__ inline int64_t tiled_d_index(int64_t r, int64_t blk, int64_t
 cudaError_t launch_quantize(int wtype, const float* w, int64_t n_blocks, void* out, cudaStream_t s);
 cudaError_t launch_repack(int wtype, const void* src, int64_t rows, int64_t nb, void* qs,
                           uint16_t* d, cudaStream_t s);
+cudaError_t launch_quantize_affine4(const float* w, int64_t rows, int64_t cols, uint32_t* words, uint16_t* scales,
+                                    uint16_t* biases, cudaStream_t s);
+cudaError_t launch_repack_affine4(const uint32_t* words, const uint16_t* scales, const uint16_t* biases,
+                                  int64_t rows, int64_t cols, void* qs, uint16_t* d, cudaStream_t s);
 cudaError_t launch_dequant(int wtype, const void* qs, const uint16_t* d, int64_t nb, int64_t row0,
                            int64_t n_rows, float* out, cudaStream_t s);
 cudaError_t launch_embed(int wtype, const void* qs, const uint16_t* d, int vocab, int hidden,

@@ -53,8 +53,8 @@ cudaError_t keys_on_current_device(unsigned long long** out) {
 extern "C" tq_status tq_lm_head_static(int32_t wtype, tq_qmat w, int32_t vocab, int32_t hidden,
                                        const float* x, int32_t batch, const float* gain, float eps,
                                        float* logits, int32_t* argmax, void* stream) {
-  if (wtype != TQ_Q4_0 && wtype != TQ_Q8_0) {
-    tq::record_error("tq_lm_head_static: wtype must be 2 or 8");
+  if (wtype != TQ_Q4_0 && wtype != TQ_AFFINE4 && wtype != TQ_Q8_0) {
+    tq::record_error("tq_lm_head_static: wtype must be 2, 4 or 8");
     return TQ_REFUSED;
   }
   if (batch < 1 || batch > TQ_LM_HEAD_STATIC_MAX_BATCH) {

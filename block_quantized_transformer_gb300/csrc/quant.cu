@@ -1,11 +1,18 @@
-// Block formats on the GPU: encode f32 -> GGUF-order Q8_0/Q4_0 blocks,
-// repack GGUF-order blocks into the tiled layout the GEMV streams (see
-// kernels.cuh), decode rows of it to f32, and gather embedding rows.
+// Block formats on the GPU: encode f32 -> GGUF-order Q8_0/Q4_0 blocks or
+// MLX-layout affine 4-bit groups, repack either into the tiled layout the
+// GEMV streams (see kernels.cuh), decode rows of it to f32, and gather
+// embedding rows.
 //
 // The formats are the workload descriptions' Q8_0 (fp16 d = max|w|/127,
 // int8 q = round(w/d), value d*q) and Q4_0 (fp16 d = m/-8 at the signed
 // extreme, q = clamp(round(w/d)+8, 0, 15), value d*(q-8)).  Encoding decisions
 // are taken in f32 exactly as the header tq.h states; decoding is exact.
+// Affine 4-bit ("Alchemize PyTensor ... Gemma 3n": W = q s + b per group of
+// inputs, eight 4-bit values per uint32 word, bf16 scale and bias): groups of
+// 64, s = (max - min) / 15, b = min, q = round((w - b) / s) decided in f32,
+// s and b stored as bf16; decoding q s + b rounds once in f32.
+#include <cuda_bf16.h>
+
 #include "kernels.cuh"
 #include "launch.cuh"
 #include "ptx.cuh"
@@ -69,6 +76,46 @@ __global__ void quantize_kernel(const float* __restrict__ w, int64_t n_blocks,
   }
 }
 
+// One warp per group of 64 inputs: lane l holds inputs l and l + 32.
+__global__ void quantize_affine4_kernel(const float* __restrict__ w, int64_t n_groups, uint32_t* __restrict__ words,
+                                        uint16_t* __restrict__ scales, uint16_t* __restrict__ biases) {
+  const int lane = threadIdx.x & 31;
+  int64_t grp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t stride = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (; grp < n_groups; grp += stride) {
+    const float x0 = w[grp * 64 + lane], x1 = w[grp * 64 + 32 + lane];
+    float lo = fminf(x0, x1), hi = fmaxf(x0, x1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    const float s = (hi - lo) / 15.0f;
+    const float b = lo;
+    int q0 = 0, q1 = 0;
+    if (s != 0.0f) {
+      q0 = max(0, min(15, (int)round_half_away((x0 - b) / s)));
+      q1 = max(0, min(15, (int)round_half_away((x1 - b) / s)));
+    }
+    // element 8w + i of the group in bits 4i of word w: lanes 8w .. 8w+7 (w < 4)
+    // hold the first half's words, the same lanes' second values words 4 .. 7
+    uint32_t p0 = (uint32_t)q0 << (4 * (lane & 7)), p1 = (uint32_t)q1 << (4 * (lane & 7));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      p0 |= __shfl_xor_sync(0xffffffffu, p0, o);
+      p1 |= __shfl_xor_sync(0xffffffffu, p1, o);
+    }
+    if ((lane & 7) == 0) {
+      words[grp * 8 + (lane >> 3)] = p0;
+      words[grp * 8 + 4 + (lane >> 3)] = p1;
+    }
+    if (lane == 0) {
+      scales[grp] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+      biases[grp] = __bfloat16_as_ushort(__float2bfloat16_rn(b));
+    }
+  }
+}
+
 // ----------------------------------------------------------------- repack --
 
 // One thread per (row, block) of the padded matrix.  GGUF blocks start at even
@@ -100,14 +147,63 @@ __global__ void repack_kernel(const uint16_t* __restrict__ src, int64_t rows, in
   }
 }
 
+// One thread per (row, 32-input block) of the padded matrix: the block's 32
+// codes from the MLX words rearranged as a Q4_0 block's bytes (q[j] |
+// q[j+16] << 4), and the group's scale (even block) or bias (odd block).
+__global__ void repack_affine4_kernel(const uint32_t* __restrict__ words, const uint16_t* __restrict__ scales,
+                                      const uint16_t* __restrict__ biases, int64_t rows, int64_t nb,
+                                      uint8_t* __restrict__ qs, uint16_t* __restrict__ d) {
+  const int64_t n = tiled_rows(rows) * nb;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / nb, blk = i % nb;
+    uint32_t v[4] = {0u, 0u, 0u, 0u};
+    uint16_t dv = 0;
+    if (r < rows) {
+      const uint32_t* wr = words + r * (nb * 4) + blk * 4;  // inputs 32 blk .. 32 blk + 31
+      uint32_t q[32];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t x = wr[w];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[8 * w + k] = (x >> (4 * k)) & 15u;
+      }
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[w] |= (q[4 * w + k] | (q[4 * w + k + 16] << 4)) << (8 * k);
+      const int64_t grp = r * (nb / 2) + blk / 2;
+      dv = (blk & 1) ? biases[grp] : scales[grp];
+    }
+    d[tiled_d_index(r, blk, nb)] = dv;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      *reinterpret_cast<uint32_t*>(qs + tiled_qs_offset(TQ_AFFINE4, r, blk, nb, k)) = v[k];
+  }
+}
+
 // --------------------------------------------------------------- decoding --
 
-// Decode block `blk` of row `row` into 32 exact f32 values d * code.
+// Decode block `blk` of row `row` into 32 f32 values: d * code (exact), or
+// for AFFINE4 q * s + b with one rounding.
 template <int WT>
 __device__ __forceinline__ void decode_block(const uint8_t* qs, const uint16_t* dptr, int64_t row,
                                              int64_t nb, int64_t blk, float* out32) {
   const float d = half_bits_to_float(dptr[tiled_d_index(row, blk, nb)]);
-  if (WT == TQ_Q4_0) {
+  if (WT == TQ_AFFINE4) {
+    const float s = bf16_bits_to_float(dptr[tiled_d_index(row, blk & ~1ll, nb)]);
+    const float b = bf16_bits_to_float(dptr[tiled_d_index(row, blk | 1ll, nb)]);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t word = *reinterpret_cast<const uint32_t*>(qs + tiled_qs_offset(WT, row, blk, nb, w));
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t byte = (word >> (8 * k)) & 0xffu;
+        out32[4 * w + k] = fmaf((float)(byte & 0xf), s, b);
+        out32[4 * w + k + 16] = fmaf((float)(byte >> 4), s, b);
+      }
+    }
+  } else if (WT == TQ_Q4_0) {
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       const uint32_t word = *reinterpret_cast<const uint32_t*>(qs + tiled_qs_offset(WT, row, blk, nb, w));
@@ -199,11 +295,28 @@ cudaError_t launch_repack(int wtype, const void* src, int64_t rows, int64_t nb, 
   return cudaGetLastError();
 }
 
+cudaError_t launch_quantize_affine4(const float* w, int64_t rows, int64_t cols, uint32_t* words, uint16_t* scales,
+                                    uint16_t* biases, cudaStream_t s) {
+  const int64_t n_groups = rows * (cols / 64);
+  quantize_affine4_kernel<<<grid_1d(n_groups * 32, 256), 256, 0, s>>>(w, n_groups, words, scales, biases);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack_affine4(const uint32_t* words, const uint16_t* scales, const uint16_t* biases,
+                                  int64_t rows, int64_t cols, void* qs, uint16_t* d, cudaStream_t s) {
+  const int64_t nb = cols / 32;
+  repack_affine4_kernel<<<grid_1d(tiled_rows(rows) * nb, 256), 256, 0, s>>>(words, scales, biases, rows, nb,
+                                                                            (uint8_t*)qs, d);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dequant(int wtype, const void* qs, const uint16_t* d, int64_t nb, int64_t row0,
                            int64_t n_rows, float* out, cudaStream_t s) {
   const unsigned g = grid_1d(n_rows * nb, 256);
   if (wtype == TQ_Q8_0)
     dequant_kernel<TQ_Q8_0><<<g, 256, 0, s>>>((const uint8_t*)qs, d, nb, row0, n_rows, out);
+  else if (wtype == TQ_AFFINE4)
+    dequant_kernel<TQ_AFFINE4><<<g, 256, 0, s>>>((const uint8_t*)qs, d, nb, row0, n_rows, out);
   else
     dequant_kernel<TQ_Q4_0><<<g, 256, 0, s>>>((const uint8_t*)qs, d, nb, row0, n_rows, out);
   return cudaGetLastError();
@@ -215,6 +328,9 @@ cudaError_t launch_embed(int wtype, const void* qs, const uint16_t* d, int vocab
   const int threads = hidden / 32 < 128 ? 32 * ((hidden / 32 + 31) / 32) : 128;
   if (wtype == TQ_Q8_0)
     return launch_k(embed_kernel<TQ_Q8_0>, dim3(n_tokens), dim3(threads), 0, s, (const uint8_t*)qs, d,
+                    vocab, hidden, tokens, x, status, argmax_keys, n_keys);
+  if (wtype == TQ_AFFINE4)
+    return launch_k(embed_kernel<TQ_AFFINE4>, dim3(n_tokens), dim3(threads), 0, s, (const uint8_t*)qs, d,
                     vocab, hidden, tokens, x, status, argmax_keys, n_keys);
   return launch_k(embed_kernel<TQ_Q4_0>, dim3(n_tokens), dim3(threads), 0, s, (const uint8_t*)qs, d,
                   vocab, hidden, tokens, x, status, argmax_keys, n_keys);

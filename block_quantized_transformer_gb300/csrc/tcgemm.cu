@@ -173,6 +173,16 @@ __device__ __forceinline__ void decode4(uint32_t w, __half2 bias2, __half2 d2, u
   p23 = h2bits(__hmul2(__hsub2(*reinterpret_cast<const __half2*>(&b), bias2), d2));
 }
 
+// AFFINE4: four codes -> fp16 q s + b (q = (1024 + q) - 1024 exactly, then
+// one fused multiply-add).
+__device__ __forceinline__ void decode4_affine(uint32_t w, __half2 off2, __half2 s2, __half2 b2, uint32_t& p01,
+                                               uint32_t& p23) {
+  const uint32_t a = __byte_perm(w, 0x64646464u, 0x5150);
+  const uint32_t b = __byte_perm(w, 0x64646464u, 0x5352);
+  p01 = h2bits(__hfma2(__hsub2(*reinterpret_cast<const __half2*>(&a), off2), s2, b2));
+  p23 = h2bits(__hfma2(__hsub2(*reinterpret_cast<const __half2*>(&b), off2), s2, b2));
+}
+
 __device__ __forceinline__ __half2 scale2(uint32_t bits) {
   const __half h = __ushort_as_half((uint16_t)(bits & 0xffffu));
   return __halves2half2(h, h);
@@ -205,7 +215,7 @@ __device__ __forceinline__ DecodeLane decode_lane(int lane, int w, bool tile_ok)
   DecodeLane d;
   // Q4_0: the 16-byte piece (h*2 + j/4)*32 + 4g + i holds word i of blocks 4(j/4) .. +3;
   // Q8_0: the piece (h*4 + j/2)*32 + 4g + i holds code words i, i + 4 of blocks 2(j/2), +1
-  d.qs = (uint32_t)(tw * U * UQ + ((WT == TQ_Q4_0 ? h * 2 : h * 4) * 32 + 4 * g + i) * 16);
+  d.qs = (uint32_t)(tw * U * UQ + ((nib4(WT) ? h * 2 : h * 4) * 32 + 4 * g + i) * 16);
   d.dd = (uint32_t)(kTiles * U * UQ + tw * U * kUnitD + (h * 8 + g) * 16);
   d.col = ((uint32_t)(32 * q) << 16) | (uint32_t)(16 * i);
   d.ok = tile_ok;
@@ -223,11 +233,11 @@ __device__ __forceinline__ void decode_stage(uint32_t rq, uint32_t rd, const Dec
     for (int k = 0; k < 16; ++k) out[k] = 0u;
     return;
   }
-  const uint2 dv = lds64(rd + L.dd + 8 * S);  // scales of blocks 4S .. 4S + 3
+  const uint2 dv = lds64(rd + L.dd + 8 * S);  // scales of blocks 4S .. 4S + 3 (AFFINE4: s, b of 2 groups)
   const uint32_t ds[2] = {dv.x, dv.y};
-  const __half2 bias2 = __float2half2_rn(WT == TQ_Q4_0 ? 1032.f : 1152.f);
+  const __half2 bias2 = __float2half2_rn(WT == TQ_Q4_0 ? 1032.f : WT == TQ_Q8_0 ? 1152.f : 1024.f);
   uint32_t lo[4], hi[4];  // per block: first and second four inputs of word i
-  if (WT == TQ_Q4_0) {
+  if (nib4(WT)) {
     const uint4 v = lds128(rq + L.qs + S * 512);
     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -244,6 +254,21 @@ __device__ __forceinline__ void decode_stage(uint32_t rq, uint32_t rd, const Dec
       lo[2 * jp + 1] = v.z ^ 0x80808080u;
       hi[2 * jp + 1] = v.w ^ 0x80808080u;
     }
+  }
+  if (WT == TQ_AFFINE4) {
+    // group of blocks (2k, 2k+1): bf16 scale and bias in element pair k,
+    // converted to fp16 (exact within fp16's range); one fused rounding of q s + b
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const __half2 s2 = __float2half2_rn(__uint_as_float(ds[k] << 16));
+      const __half2 b2 = __float2half2_rn(__uint_as_float(ds[k] & 0xffff0000u));
+#pragma unroll
+      for (int jb = 2 * k; jb < 2 * k + 2; ++jb) {
+        decode4_affine(lo[jb], bias2, s2, b2, out[4 * jb], out[4 * jb + 1]);
+        decode4_affine(hi[jb], bias2, s2, b2, out[4 * jb + 2], out[4 * jb + 3]);
+      }
+    }
+    return;
   }
 #pragma unroll
   for (int jb = 0; jb < 4; ++jb) {
@@ -688,6 +713,7 @@ cudaError_t launch_tcgemm(int wtype, const TcGemmArgs& a, cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
   if (a.K % 256 != 0 || a.K > 12288 || a.nseg < 1 || a.nseg > 3) return cudaErrorInvalidValue;
   if ((reinterpret_cast<uintptr_t>(a.x16) & 15u) != 0) return cudaErrorInvalidValue;
+  if (wtype == TQ_AFFINE4) return tc::launch_wt<TQ_AFFINE4>(a, s);
   return wtype == TQ_Q4_0 ? tc::launch_wt<TQ_Q4_0>(a, s) : tc::launch_wt<TQ_Q8_0>(a, s);
 }
 

@@ -2,8 +2,9 @@
 
 Weights come from the shared counter-based generator (``synth``: N(0, 0.02)
 matrices, 1 + N(0, 0.02) gains) written on the GPU, are encoded to GGUF-order
-Q8_0/Q4_0 blocks by the library's own encoder (tq_quantize) and repacked to
-the tiled layout (tq_repack), in row chunks of at most 2^28 weights (a
+Q8_0/Q4_0 blocks (or MLX-layout affine 4-bit groups) by the library's own
+encoder (tq_quantize, tq_quantize_affine4) and repacked to the tiled layout
+(tq_repack, tq_repack_affine4), in row chunks of at most 2^28 weights (a
 multiple of 16 rows) so the f32 staging buffer stays at 1 GB.
 """
 from __future__ import annotations
@@ -12,7 +13,7 @@ import torch
 
 import synth
 
-from . import QMat, Model, WTYPES, QS_BYTES, quantize, tq_repack
+from . import QMat, Model, WTYPES, QS_BYTES, TQ_AFFINE4, quantize, quantize_affine4, tq_repack, tq_repack_affine4
 
 CHUNK = 1 << 28
 
@@ -27,11 +28,17 @@ def build_matrix(w: "synth.Workload", name: str, device="cuda") -> QMat:
         r1 = min(rows, r0 + step)
         f = torch.empty((r1 - r0) * cols, dtype=torch.float32, device=device)
         synth.dev_normal(f, w.seed, w.stream_of(name), first=r0 * cols)
-        blocks = quantize(f.view(r1 - r0, cols), wt)
         p1 = min(r0 + step, (rows + 15) // 16 * 16)  # padded rows of this chunk
-        tq_repack(wt, blocks, r1 - r0, cols, m.qs[r0 * nb * QS_BYTES[wt]: p1 * nb * QS_BYTES[wt]],
-                  m.d[r0 * nb: p1 * nb])
-        del f, blocks
+        qs, d = m.qs[r0 * nb * QS_BYTES[wt]: p1 * nb * QS_BYTES[wt]], m.d[r0 * nb: p1 * nb]
+        if wt == TQ_AFFINE4:
+            words, scales, biases = quantize_affine4(f.view(r1 - r0, cols))
+            tq_repack_affine4(words, scales, biases, r1 - r0, cols, qs, d)
+            del words, scales, biases
+        else:
+            blocks = quantize(f.view(r1 - r0, cols), wt)
+            tq_repack(wt, blocks, r1 - r0, cols, qs, d)
+            del blocks
+        del f
     return m
 
 

@@ -50,8 +50,13 @@ typedef enum { TQ_OK = 0, TQ_REFUSED = 1, TQ_INTERNAL = 2 } tq_status;
 /* Block formats (GGUF type ids).  Q8_0: 32 weights, fp16 d, int8 q; value
  * d*q.  Q4_0: 32 weights, fp16 d, 4-bit q; value d*(q-8).  GGUF byte order of
  * one block: Q8_0 = fp16 d, int8 q[32] (34 B); Q4_0 = fp16 d, uint8 qs[16],
- * qs[j] = q[j] | q[j+16] << 4 (18 B). */
-typedef enum { TQ_Q4_0 = 2, TQ_Q8_0 = 8 } tq_wtype;
+ * qs[j] = q[j] | q[j+16] << 4 (18 B).
+ * AFFINE4 ("Alchemize PyTensor ... Gemma 3n", the affine-4 checkpoint):
+ * groups of 64 inputs, 4-bit q, bf16 scale s and bias b per group; value
+ * q*s + b.  Its source layout is MLX's planar one: words [rows][cols/8]
+ * uint32 (input c in bits 4(c%8) .. 4(c%8)+3 of word c/8), scales and biases
+ * [rows][cols/64] bf16 (tq_quantize_affine4, tq_repack_affine4). */
+typedef enum { TQ_Q4_0 = 2, TQ_AFFINE4 = 4, TQ_Q8_0 = 8 } tq_wtype;
 typedef enum { TQ_KV_F32 = 0, TQ_KV_F16 = 1 } tq_kvtype;
 
 /* Bits of the device status word (tq_model_status()). */
@@ -101,8 +106,8 @@ typedef enum { TQ_ARCH_QWEN3 = 0, TQ_ARCH_LLAMA = 1, TQ_ARCH_QWEN2 = 2, TQ_ARCH_
  * layout.  Rows are padded with zero rows to a multiple of 16 (R rows) and
  * grouped in tiles of 16; the 8-block runs of a tile row ("units", 16 rows x
  * 256 inputs) are stored tile after tile:
- *  qs_dev: R/16 * cols/256 units of 2048 (Q4_0) or 4096 (Q8_0) bytes, i.e.
- *          R * cols/32 * 16 (Q4_0) or * 32 (Q8_0) bytes in all;
+ *  qs_dev: R/16 * cols/256 units of 2048 (Q4_0, AFFINE4) or 4096 (Q8_0) bytes,
+ *          i.e. R * cols/32 * 16 (Q4_0, AFFINE4) or * 32 (Q8_0) bytes in all;
  *  d_dev:  R/16 * cols/256 units of 128 fp16 scales (R * cols/32 scales).
  * Inside a unit, 32-bit code word i (Q4_0: bytes 4i..4i+3 of the block's 16
  * nibble bytes, i < 4; Q8_0: codes 4i..4i+3, i < 8) of block j (0-7) of tile
@@ -111,6 +116,9 @@ typedef enum { TQ_ARCH_QWEN3 = 0, TQ_ARCH_LLAMA = 1, TQ_ARCH_QWEN2 = 2, TQ_ARCH_
  *   Q8_0: ((h*4 + j/2)*32 + 4g + i%4)*16 + (j%2)*8 + (i/4)*4
  * and its scale at element (h*8 + g)*8 + j; so each lane of a warp loads the
  * words of its tensor-core operand fragment with one 16-byte load.
+ * AFFINE4 takes the Q4_0 arrangement (each 32-input block's codes as a Q4_0
+ * block's bytes q[j] | q[j+16] << 4); its 16-bit elements hold the bf16
+ * scale of group k (blocks 2k, 2k+1) at block 2k and its bias at block 2k+1.
  * tq_qmat_bytes() gives the sizes.  Both pointers 16-byte aligned. */
 typedef struct {
   const void* qs_dev;
@@ -282,7 +290,25 @@ TQ_API tq_status tq_repack(int32_t wtype, const void* blocks_dev, int64_t rows, 
 TQ_API tq_status tq_quantize(int32_t wtype, const float* w_dev, int64_t rows, int64_t cols,
                       void* blocks_dev, void* stream);
 
-/* Decode rows [row0, row0+n_rows) of a tiled matrix to f32 (exact). */
+/* Encode f32 weights [rows][cols] (cols a multiple of 64) into MLX-layout
+ * affine 4-bit groups: per group of 64 inputs of a row, s = (max - min) / 15
+ * and b = min in f32, q = round-half-away((w - b) / s) in f32 clamped to
+ * [0, 15] (q = 0 when s = 0); the stored s and b are bf16, rounded to
+ * nearest even.  words_dev [rows][cols/8] uint32, scales_dev and
+ * biases_dev [rows][cols/64] bf16 bit patterns. */
+TQ_API tq_status tq_quantize_affine4(const float* w_dev, int64_t rows, int64_t cols, uint32_t* words_dev,
+                                     uint16_t* scales_dev, uint16_t* biases_dev, void* stream);
+
+/* MLX-layout affine 4-bit groups (as written by tq_quantize_affine4) ->
+ * tiled layout (tq_qmat of wtype TQ_AFFINE4), padding rows included; row
+ * chunks as for tq_repack.  Refused when cols % 256 != 0 or a pointer is
+ * NULL or misaligned. */
+TQ_API tq_status tq_repack_affine4(const uint32_t* words_dev, const uint16_t* scales_dev,
+                                   const uint16_t* biases_dev, int64_t rows, int64_t cols, void* qs_dev,
+                                   uint16_t* d_dev, void* stream);
+
+/* Decode rows [row0, row0+n_rows) of a tiled matrix to f32 (exact for Q8_0
+ * and Q4_0; AFFINE4: q*s + b rounded once to f32). */
 TQ_API tq_status tq_dequantize(int32_t wtype, tq_qmat w, int64_t cols, int64_t row0, int64_t n_rows,
                         float* out_dev, void* stream);
 
