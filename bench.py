@@ -66,6 +66,11 @@ def parse():
                     help="profiling cases only: run just the batched sub-benchmark")
     ap.add_argument("--workload", default="qwen3_8b_q4_0",
                     help="decode workload of the headline (profiling cases may pick another)")
+    ap.add_argument("--arch", default="qwen3", choices=["qwen3", "llama", "qwen2", "gemma3"],
+                    help="layer recipe of the same shape (gemma3: window 512 on 5 of every 6 layers, "
+                         "final logit softcap 30)")
+    ap.add_argument("--wtype", default=None, choices=["q4_0", "q8_0", "affine4"],
+                    help="weight format of the same shape")
     return ap.parse_args()
 
 
@@ -308,6 +313,19 @@ def time_graph(fn, n, stream, reps=3):
 
 # ----------------------------------------------------------------------------- GPU bench
 
+def apply_variant(w, args):
+    """The workload with the layer recipe and weight format the options name."""
+    import dataclasses
+    if args.arch == "qwen3" and (args.wtype is None or args.wtype == w.wtype):
+        return w
+    kw = {"arch": args.arch}
+    if args.arch == "gemma3":
+        kw.update(sliding_window=512, sliding_pattern=6, logit_softcap=30.0)
+    if args.wtype is not None:
+        kw["wtype"] = args.wtype
+    return dataclasses.replace(w, name=f"{w.name}[{args.arch}, {kw.get('wtype', w.wtype)}]", **kw)
+
+
 def q4_bytes(rows, cols):
     return rows * cols // 32 * 18
 
@@ -323,9 +341,11 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = {x.name: x for x in synth.WORKLOADS}[args.workload]
+    import dataclasses
     if args.layers:
-        import dataclasses
         w = dataclasses.replace(w, n_layers=args.layers)
+    variant = args.arch != "qwen3" or (args.wtype is not None and args.wtype != w.wtype)
+    w = apply_variant(w, args)
     pk = peaks()
     K, W = args.steps, args.warmup
     P = w.prompt_len
@@ -403,9 +423,9 @@ def run_gpu(args, rank, world):
     chain_alg = chain_bytes + chain_act
     roofline = {"bound": "hbm", "achieved": round(chain_alg / (chain_ms / 1e3) / 1e9, 1), "peak": pk["hbm"],
                 "unit": "GB/s", "frac": round(chain_alg / (chain_ms / 1e3) / 1e9 / pk["hbm"], 4),
-                "traffic": traffic_of("gemv_chain_layer_qwen3_8b_q4_0", "gemv_impl.cuh", "gemv.cu",
-                                      "gemv_q4.cu"),
-                "kernel": "gemv_chain_kernel<Q4_0>: output projection + residual, RMSNorm + gate/up "
+                "traffic": None if variant else traffic_of("gemv_chain_layer_qwen3_8b_q4_0", "gemv_impl.cuh",
+                                                           "gemv.cu", "gemv_q4.cu"),
+                "kernel": f"gemv_chain_kernel<{w.wtype.upper()}>: output projection + residual, RMSNorm + gate/up "
                           "+ SwiGLU, down projection + residual, next layer's RMSNorm + Q/K/V",
                 "timing": f"tq_decode_chain for layers 0..{n_chain - 1} in one CUDA graph, CUDA events",
                 "peak_kind": pk["kind"] + " copy bandwidth",
@@ -460,7 +480,7 @@ def run_gpu(args, rank, world):
                             "peak": pk["tc"], "unit": "TFLOP/s",
                             "frac": round(gemm_flop / (gemm_ms / 1e3) / 1e12 / pk["tc"], 4),
                             "traffic": traffic_of("tcgemm_prefill_gate_qwen3_8b_q4_0", "tcgemm.cu"),
-                            "kernel": "tcgemm_kernel<Q4_0, 256> (tcgen05, fp16 operands, f32 TMEM) + "
+                            "kernel": f"tcgemm_kernel<{w.wtype.upper()}, 256> (tcgen05, fp16 operands, f32 TMEM) + "
                                       "xprep16: gate projection 12288x4096 at 2048 rows",
                             "timing": f"tq_gemm over the {L} layers' gate matrices in one CUDA graph",
                             "peak_kind": pk["kind"] + " bf16 dense burst (fp16 has the same rate)",
@@ -479,7 +499,7 @@ def run_gpu(args, rank, world):
             "data": "synthetic",
             "config": {"workload": f"{w.name} batch-1 greedy decode after a {P}-token prompt "
                                    f"(context {ctx0}..{ctx0 + K - 1})",
-                       "weights": "Q4_0, 4.26 GB, seeded N(0,0.02)", "kv_cache": "f16",
+                       "weights": f"{w.wtype.upper()}, {weight_bytes / 1e9:.2f} GB, seeded N(0,0.02)", "kv_cache": "f16",
                        "l2": "inputs exceed L2 (4.3 GB of weights read every step)",
                        "parallelism": f"replicas x{world}"},
             "hbm": {"step_bytes": int(step_bytes), "achieved_gbs": round(step_bytes / (ms_step / 1e3) / 1e9, 1),
@@ -544,6 +564,7 @@ def run_batched(args, world, mats, gains, dev, stream, pk):
     if args.layers:
         import dataclasses
         w = dataclasses.replace(w, n_layers=args.layers)
+    w = apply_variant(w, args)
     K, W = args.batched_steps, 3
     B, P = w.batch, w.page_size
     lens = w.context_lengths().astype(np.int64)
@@ -609,7 +630,7 @@ def run_batched(args, world, mats, gains, dev, stream, pk):
     scr = torch.empty(tq.lib().tq_gemm_scratch_bytes(H, B, F) + 256, dtype=torch.uint8, device=dev)
     gemm_ms = time_graph(lambda i: tq.tq_gemm(mats[f"blk.{i}.ffn_down"], x, out=y, scratch=scr), L, stream)
     gemm_bytes = q4_bytes(H, F) + 4 * B * (F + H)
-    return {"metric": f"decode tokens/s (B={B}, Q4_0 Qwen3-8B shape, paged f16 KV)",
+    return {"metric": f"decode tokens/s (B={B}, {w.wtype.upper()} Qwen3-8B shape, paged f16 KV)",
             "value": round(world * B * K / (ms_max / 1e3), 2), "unit": "tokens/s", "steps": K, "warmup": W,
             "ms_per_step": round(ms_step, 4),
             "config": {"workload": f"{w.name}: {B} sequences, cached lengths {int(lens.min())}..{int(lens.max())} "
@@ -622,7 +643,7 @@ def run_batched(args, world, mats, gains, dev, stream, pk):
                          "peak": pk["hbm"], "unit": "GB/s",
                          "frac": round(gemm_bytes / (gemm_ms / 1e3) / 1e9 / pk["hbm"], 4),
                          "traffic": traffic_of("tcgemm_batched_down_qwen3_8b_q4_0", "tcgemm.cu"),
-                         "kernel": "tcgemm_kernel<Q4_0, 32> (tcgen05) + xprep16: down projection "
+                         "kernel": f"tcgemm_kernel<{w.wtype.upper()}, 32> (tcgen05) + xprep16: down projection "
                                    "4096x12288 at 32 rows, K split across CTAs as in the step",
                          "timing": f"tq_gemm over the {L} layers' down matrices in one CUDA graph",
                          "peak_kind": pk["kind"] + " copy bandwidth",
