@@ -268,13 +268,13 @@ __device__ __forceinline__ void decode_stage(uint32_t rq, uint32_t rd, const Dec
         decode4_affine(hi[jb], bias2, s2, b2, out[4 * jb + 2], out[4 * jb + 3]);
       }
     }
-    return;
-  }
+  } else {
 #pragma unroll
-  for (int jb = 0; jb < 4; ++jb) {
-    const __half2 d2 = scale2(ds[jb >> 1] >> (16 * (jb & 1)));
-    decode4(lo[jb], bias2, d2, out[4 * jb], out[4 * jb + 1]);
-    decode4(hi[jb], bias2, d2, out[4 * jb + 2], out[4 * jb + 3]);
+    for (int jb = 0; jb < 4; ++jb) {
+      const __half2 d2 = scale2(ds[jb >> 1] >> (16 * (jb & 1)));
+      decode4(lo[jb], bias2, d2, out[4 * jb], out[4 * jb + 1]);
+      decode4(hi[jb], bias2, d2, out[4 * jb + 2], out[4 * jb + 3]);
+    }
   }
 }
 
