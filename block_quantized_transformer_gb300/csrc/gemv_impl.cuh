@@ -274,9 +274,11 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
 
 
 // Final value(s) of row rr of tile t: scale, epilogue, store.  resid: this
-// CTA's residual rows from tile t0 on, prefetched to shared memory, or null.
+// CTA's residual rows from tile t0 on, prefetched to shared memory, or null;
+// keep: the stored value also replaces the residual row in shared memory (a
+// later phase of the chain adds to the same rows).
 __device__ __forceinline__ void finish_row(const GemvArgs& a, int mode, const Geo& q, int b, int t, int rr,
-                                           float v, float up, const float* resid, int t0, float inv_s,
+                                           float v, float up, float* resid, bool keep, int t0, float inv_s,
                                            unsigned long long& best) {
   const int s = seg_of_tile(q, t);
   const int local = (t - seg_tile0(q, s)) * kTileRows + rr;
@@ -296,7 +298,9 @@ __device__ __forceinline__ void finish_row(const GemvArgs& a, int mode, const Ge
     const float r = a.residual == nullptr ? 0.f
                     : resid != nullptr ? resid[(t - t0) * kTileRows + rr]
                                        : __ldcg(a.residual + o);
-    a.y[o] = a.bias != nullptr ? (r + v) + a.bias[row] : r + v;
+    const float yv = a.bias != nullptr ? (r + v) + a.bias[row] : r + v;
+    a.y[o] = yv;
+    if (keep) resid[(t - t0) * kTileRows + rr] = yv;
   }
 }
 
@@ -304,12 +308,13 @@ __device__ __forceinline__ void finish_row(const GemvArgs& a, int mode, const Ge
 // else kept as a partial (slot 0: the warp's first tile, 1: its last).
 __device__ __forceinline__ void flush_tile(const GemvArgs& a, int mode, const Geo& q, int b, int t, int wa,
                                            int wb, int warp, int lane, const float (&acc)[2][2], float* red,
-                                           const float* resid, int t0, float inv_s, unsigned long long& best) {
+                                           float* resid, bool keep, int t0, float inv_s,
+                                           unsigned long long& best) {
   const int g = lane >> 2;
   if ((lane & 3) != 0) return;
   if (t * q.G >= wa && t * q.G + q.G <= wb) {
-    finish_row(a, mode, q, b, t, g, acc[0][0], acc[1][0], resid, t0, inv_s, best);
-    finish_row(a, mode, q, b, t, g + 8, acc[0][1], acc[1][1], resid, t0, inv_s, best);
+    finish_row(a, mode, q, b, t, g, acc[0][0], acc[1][0], resid, keep, t0, inv_s, best);
+    finish_row(a, mode, q, b, t, g + 8, acc[0][1], acc[1][1], resid, keep, t0, inv_s, best);
   } else {
     float* r = red + (warp * 2 + (t == wa / q.G ? 0 : 1)) * 32;
     r[g] = acc[0][0];
@@ -323,7 +328,7 @@ __device__ __forceinline__ void flush_tile(const GemvArgs& a, int mode, const Ge
 // warp from the partials in warp order.  Lane r < 16 ends with row r (lanes
 // 16-31: the up rows of SWIGLU).
 __device__ __forceinline__ void reduce_tile(const GemvArgs& a, int mode, const Geo& q, int b, int t, int u0, int u1,
-                                            int warp, int lane, const float* red, const float* resid, int t0,
+                                            int warp, int lane, const float* red, float* resid, bool keep, int t0,
                                             float inv_s, unsigned long long& best) {
   const int te = min(t * q.G + q.G, u1);
   float v = 0.f;
@@ -335,12 +340,13 @@ __device__ __forceinline__ void reduce_tile(const GemvArgs& a, int mode, const G
     v += red[(w * 2 + (t == xa / q.G ? 0 : 1)) * 32 + lane];
   }
   const float up = __shfl_down_sync(0xffffffffu, v, 16);
-  if (lane < 16) finish_row(a, mode, q, b, t, lane, v, up, resid, t0, inv_s, best);
+  if (lane < 16) finish_row(a, mode, q, b, t, lane, v, up, resid, keep, t0, inv_s, best);
 }
 
 // ---------------------------------------------------------------- layout --
 
 constexpr int kResidTiles = 64;  // residual rows prefetched to shared memory (tiles per CTA)
+constexpr int kResidPerThread = (kResidTiles * kTileRows + kCT - 1) / kCT;
 
 struct Smem {
   int ring, xtab, xneg, red, resid, misc, bars, bytes;
@@ -501,6 +507,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
   const uint32_t ring_s = sbase + L.ring + warp * depth * F::SLOT;
   const uint32_t xtab = sbase + L.xtab, xneg = sbase + L.xneg;
   int i = 0;  // slots consumed
+  // Phase 0 (output projection) and phase 2 (down projection) both add to the
+  // residual stream: with one token, the same output rows and hence the same
+  // tiles per CTA, phase 0's results are phase 2's residual rows.
+  const bool carry = ch.n > 2 && ch.mode[0] == GEMV_STORE && ch.mode[2] == GEMV_STORE && ch.ph[0].B == 1 &&
+                     ch.ph[2].B == 1 && ch.ph[0].nseg == 1 && ch.ph[2].nseg == 1 &&
+                     ch.ph[0].residual != nullptr && ch.ph[2].residual == ch.ph[0].y && ch.ph[2].N == ch.ph[0].N &&
+                     ch.ph[0].y != nullptr;
   for (int p = 0; p < ch.n; ++p) {
     const GemvArgs& a = ch.ph[p];
     const int mode = ch.mode[p];
@@ -528,14 +541,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
       consumer_sync();
     }
     for (int b = 0; b < a.B; ++b) {
-      // -- this CTA's residual rows, fetched now and read by the epilogues
+      // -- this CTA's residual rows, read by the epilogues: loaded into
+      // registers here and stored to shared memory after the activation loads
+      // are issued (one memory round trip for both); the down projection's
+      // residual rows are the output projection's outputs of the same CTA
+      // (same rows, same tiles), kept in shared memory since phase 0
       const int t0c = u0 / q.G, ntiles = (u1 - u0) / q.G;
       float* rsd = nullptr;
+      const bool carried = carry && p == 2;
+      const bool keep = carry && p == 0;
+      float rv[kResidPerThread];
       if (mode == GEMV_STORE && a.residual != nullptr && a.nseg == 1 && ntiles <= kResidTiles) {
         rsd = reinterpret_cast<float*>(smem + L.resid);
-        for (int r = tid; r < ntiles * kTileRows; r += kCT) {
-          const int row = t0c * kTileRows + r;
-          if (row < a.N) rsd[r] = __ldcg(a.residual + (int64_t)b * a.N + row);
+        if (!carried) {
+#pragma unroll
+          for (int k = 0; k < kResidPerThread; ++k) {
+            const int r = tid + k * kCT, row = t0c * kTileRows + r;
+            rv[k] = r < ntiles * kTileRows && row < a.N ? __ldcg(a.residual + (int64_t)b * a.N + row) : 0.f;
+          }
         }
       }
       // -- activations -> fp16 hi/lo fragments in shared memory.  Pair index
@@ -563,6 +586,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
           }
           mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v0[r].x), fabsf(v0[r].y)), fmaxf(fabsf(v0[r].z), fabsf(v0[r].w))));
           mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v1[r].x), fabsf(v1[r].y)), fmaxf(fabsf(v1[r].z), fabsf(v1[r].w))));
+        }
+      }
+      if (rsd != nullptr && !carried) {
+#pragma unroll
+        for (int k = 0; k < kResidPerThread; ++k) {
+          const int r = tid + k * kCT;
+          if (r < ntiles * kTileRows) rsd[r] = rv[k];
         }
       }
       ss = warp_sum(ss);
@@ -633,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
         const int t = u / q.G;
         const int n = min(q.k, min((t + 1) * q.G, wb) - u);
         if (t != cur) {
-          if (cur >= 0) flush_tile(a, mode, q, b, cur, wa, wb, warp, lane, acc, red, rsd, t0c, inv_s, best);
+          if (cur >= 0) flush_tile(a, mode, q, b, cur, wa, wb, warp, lane, acc, red, rsd, keep, t0c, inv_s, best);
           cur = t;
           acc[0][0] = acc[0][1] = acc[1][0] = acc[1][1] = 0.f;
         }
@@ -664,16 +694,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
         u += n;
         ++i;
       }
-      if (cur >= 0) flush_tile(a, mode, q, b, cur, wa, wb, warp, lane, acc, red, rsd, t0c, inv_s, best);
+      if (cur >= 0) flush_tile(a, mode, q, b, cur, wa, wb, warp, lane, acc, red, rsd, keep, t0c, inv_s, best);
       consumer_sync();
 
       // -- tiles shared between warps (and CTAs): the first contributing warp sums
       if (wa < wb) {
         const int tf = wa / q.G, tl = (wb - 1) / q.G;
         if ((tf * q.G < wa || tf * q.G + q.G > wb) && wa == max(u0, tf * q.G))
-          reduce_tile(a, mode, q, b, tf, u0, u1, warp, lane, red, rsd, t0c, inv_s, best);
+          reduce_tile(a, mode, q, b, tf, u0, u1, warp, lane, red, rsd, keep, t0c, inv_s, best);
         if (tl != tf && tl * q.G + q.G > wb)
-          reduce_tile(a, mode, q, b, tl, u0, u1, warp, lane, red, rsd, t0c, inv_s, best);
+          reduce_tile(a, mode, q, b, tl, u0, u1, warp, lane, red, rsd, keep, t0c, inv_s, best);
       }
 
       if (mode == GEMV_ARGMAX) {
