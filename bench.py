@@ -344,7 +344,6 @@ def run_gpu(args, rank, world):
     import dataclasses
     if args.layers:
         w = dataclasses.replace(w, n_layers=args.layers)
-    variant = args.arch != "qwen3" or (args.wtype is not None and args.wtype != w.wtype)
     w = apply_variant(w, args)
     pk = peaks()
     K, W = args.steps, args.warmup
@@ -423,8 +422,8 @@ def run_gpu(args, rank, world):
     chain_alg = chain_bytes + chain_act
     roofline = {"bound": "hbm", "achieved": round(chain_alg / (chain_ms / 1e3) / 1e9, 1), "peak": pk["hbm"],
                 "unit": "GB/s", "frac": round(chain_alg / (chain_ms / 1e3) / 1e9 / pk["hbm"], 4),
-                "traffic": None if variant else traffic_of("gemv_chain_layer_qwen3_8b_q4_0", "gemv_impl.cuh",
-                                                           "gemv.cu", "gemv_q4.cu"),
+                "traffic": traffic_of("gemv_chain_layer_qwen3_8b_q4_0", "gemv_impl.cuh", "gemv.cu", "gemv_q4.cu")
+                if w.name == "qwen3_8b_q4_0" else None,
                 "kernel": f"gemv_chain_kernel<{w.wtype.upper()}>: output projection + residual, RMSNorm + gate/up "
                           "+ SwiGLU, down projection + residual, next layer's RMSNorm + Q/K/V",
                 "timing": f"tq_decode_chain for layers 0..{n_chain - 1} in one CUDA graph, CUDA events",
@@ -479,9 +478,10 @@ def run_gpu(args, rank, world):
                "roofline": {"bound": "tensor", "achieved": round(gemm_flop / (gemm_ms / 1e3) / 1e12, 1),
                             "peak": pk["tc"], "unit": "TFLOP/s",
                             "frac": round(gemm_flop / (gemm_ms / 1e3) / 1e12 / pk["tc"], 4),
-                            "traffic": traffic_of("tcgemm_prefill_gate_qwen3_8b_q4_0", "tcgemm.cu"),
+                            "traffic": traffic_of("tcgemm_prefill_gate_qwen3_8b_q4_0", "tcgemm.cu")
+                            if w.name == "qwen3_8b_q4_0" else None,
                             "kernel": f"tcgemm_kernel<{w.wtype.upper()}, 256> (tcgen05, fp16 operands, f32 TMEM) + "
-                                      "xprep16: gate projection 12288x4096 at 2048 rows",
+                                      f"xprep16: gate projection {F}x{H} at {P} rows",
                             "timing": f"tq_gemm over the {L} layers' gate matrices in one CUDA graph",
                             "peak_kind": pk["kind"] + " bf16 dense burst (fp16 has the same rate)",
                             "launch_ms": round(gemm_ms, 5), "flop_per_launch": gemm_flop}}
@@ -642,9 +642,10 @@ def run_batched(args, world, mats, gains, dev, stream, pk):
             "roofline": {"bound": "hbm", "achieved": round(gemm_bytes / (gemm_ms / 1e3) / 1e9, 1),
                          "peak": pk["hbm"], "unit": "GB/s",
                          "frac": round(gemm_bytes / (gemm_ms / 1e3) / 1e9 / pk["hbm"], 4),
-                         "traffic": traffic_of("tcgemm_batched_down_qwen3_8b_q4_0", "tcgemm.cu"),
+                         "traffic": traffic_of("tcgemm_batched_down_qwen3_8b_q4_0", "tcgemm.cu")
+                         if w.name == "qwen3_8b_q4_0_batched32_paged" else None,
                          "kernel": f"tcgemm_kernel<{w.wtype.upper()}, 32> (tcgen05) + xprep16: down projection "
-                                   "4096x12288 at 32 rows, K split across CTAs as in the step",
+                                   f"{H}x{F} at {B} rows, K split across CTAs as in the step",
                          "timing": f"tq_gemm over the {L} layers' down matrices in one CUDA graph",
                          "peak_kind": pk["kind"] + " copy bandwidth",
                          "launch_ms": round(gemm_ms, 5), "bytes_per_launch": int(gemm_bytes)},
