@@ -6,13 +6,38 @@
 // top_p kept and renormalised, and the draw is the first kept token whose
 // cumulative probability exceeds u (a uniform number the caller supplies).
 //
-// One CTA per row, no sort: both decisions are weighted quantiles of the
-// order, found by a radix select over the 32-bit order-preserving key of the
-// logit (four passes of 8 bits, each a histogram of the unnormalised mass
-// exp2((l - max) log2(e) / T) of the tokens that share the key's leading
-// bits, summed in f64), then, among tokens of exactly equal logit, a
-// count-based select over the index bits.  The row is read from L2 once per
-// pass.
+// Masses.  Token i's unnormalised mass is the f32 exp2(-d_i), d_i = (max -
+// l_i) log2(e) / T, held as an integer multiple of 2^-F with F = 62 -
+// ceil(log2 V), so that V masses of at most 1 sum below 2^62.  Integer sums
+// are exact in any order, so the draw does not depend on timing, and the
+// rounding (at most 2^-F-1 per token, V 2^-F-1 <= 2^-25 of the total mass)
+// lies far below the f32 exp's own.  Both targets become integers: the cutoff
+// is the first token whose inclusive cumulative mass reaches ceil(top_p Z),
+// the draw the first whose cumulative mass reaches floor(u kept) + 1.  A
+// token whose mass rounds to 0 is never the first to reach a target >= 1 and
+// is skipped everywhere.
+//
+// One CTA per row, no sort of the row:
+//  1. the row's largest logit;
+//  2. a histogram of masses and counts over 2048 bins of d (32 per halving of
+//     the mass): each bin is a contiguous run of the descending order, and
+//     the tokens spread over many bins, so the shared-memory atomics seldom
+//     meet (a radix histogram over the logits' leading bits puts nearly every
+//     token in two or three bins);
+//  3. a prefix sum over the bins finds the bin in which the cumulative mass
+//     reaches the cutoff; that bin's tokens are gathered into shared memory,
+//     sorted by (logit descending, index ascending) and summed in that order,
+//     which gives the cutoff token and the kept mass exactly;
+//  4. the same for the draw (the sorted bin is reused when the draw falls in
+//     it).
+// A bin of more than kCap tokens is resolved by a radix select over the
+// bin's logit keys, then over the indices of the tie group that holds the
+// target, with warp-aggregated counts.  The row is read once per pass (three
+// or four passes in the common case), each thread with four 16-byte loads in
+// flight.
+#include <cooperative_groups.h>
+#include <cooperative_groups/reduce.h>
+
 #include "kernels.cuh"
 #include "launch.cuh"
 #include "ptx.cuh"
@@ -20,229 +45,437 @@
 namespace tq {
 namespace smp {
 
+namespace cg = cooperative_groups;
+
 constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+constexpr int kBins = 2048;      // bins of d, 32 per halving of the mass
+constexpr int kCap = 4096;       // tokens of one bin sorted in shared memory
+constexpr int kNone = 256;       // "no digit" label of the radix fallback
+typedef unsigned long long u64;
 
-struct Hist {
-  double mass[256];  // f64 sums: over 151936 tokens f32 sums would move a draw by tens of tokens
-  unsigned cnt[256];
+struct Smem {
+  u64 cum[kBins];        // bin masses, then their inclusive prefix sums
+  unsigned cnt[kBins];   // tokens of nonzero mass per bin
+  u64 list[kCap];        // gathered tokens: (~key << 32) | index, sorted ascending
+  u64 lcum[kCap];        // inclusive prefix sums of the sorted tokens' masses
+  u64 dmass[256];        // radix fallback: mass and count per digit
+  unsigned dcnt[256];
+  u64 wsum[kWarps];
+  unsigned long long best[kWarps];
+  float fred[kWarps];
+  int n_list, list_bin, found;
+  u64 found_cum;
+  unsigned prefix;
+  u64 above;
 };
 
-__device__ __forceinline__ float block_max(float v, float* sh) {
-  v = warp_max(v);
-  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
+// d -> bin: d * 32 rounded to an integer through the f32 mantissa (monotone
+// in d, the same in every pass), at most kBins - 1.
+__device__ __forceinline__ int bin_of(float d) {
+  const float x = fminf(d * 32.f, (float)(kBins - 1));
+  return (int)(__float_as_uint(x + 8388608.f) - 0x4B000000u);
+}
+
+// exp2(-d) as an integer multiple of 2^-F, rounded to nearest (half up), from
+// the f32 bits: m = (2^23 + mantissa) 2^(e - 150).
+__device__ __forceinline__ u64 mass_fix(float d, int F) {
+  if (!(d < 126.f)) return 0ull;  // also NaN
+  const uint32_t b = __float_as_uint(exp2f(-d));
+  const int e = (int)(b >> 23);
+  if (e == 0) return 0ull;
+  const u64 m = (u64)((b & 0x7FFFFFu) | 0x800000u);
+  const int sh = e - 150 + F;
+  if (sh >= 0) return m << sh;
+  if (sh < -24) return 0ull;
+  return (m + (1ull << (-sh - 1))) >> (-sh);
+}
+
+// Calls fn(i, l, ok) for every token of the row, warp-uniformly (every
+// thread makes the same number of calls; ok is false for padding), with
+// kU float4 loads of each thread in flight before any is used (a pass is
+// bound by load latency otherwise); rows that are not 16-byte aligned are
+// read as scalars, kU * 4 at a time.
+constexpr int kU = 4;
+template <typename Fn>
+__device__ __forceinline__ void walk_row(const float* row, int V, Fn&& fn) {
+  const int tid = threadIdx.x;
+  if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0u) {
+    const int V4 = V >> 2;
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    for (int j0 = 0; j0 < V4; j0 += kThreads * kU) {
+      float4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int j = j0 + u * kThreads + tid;
+        v[u] = j < V4 ? __ldg(r4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int j = j0 + u * kThreads + tid;
+        const bool ok = j < V4;
+        fn(4 * j, v[u].x, ok);
+        fn(4 * j + 1, v[u].y, ok);
+        fn(4 * j + 2, v[u].z, ok);
+        fn(4 * j + 3, v[u].w, ok);
+      }
+    }
+    const int i = 4 * V4 + tid;  // the last V % 4 tokens
+    fn(i, i < V ? __ldg(row + i) : 0.f, i < V);
+  } else {
+    for (int i0 = 0; i0 < V; i0 += kThreads * 4 * kU) {
+      float v[4 * kU];
+#pragma unroll
+      for (int u = 0; u < 4 * kU; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        v[u] = i < V ? __ldg(row + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4 * kU; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        fn(i, v[u], i < V);
+      }
+    }
+  }
+}
+
+// Inclusive prefix sum in place of a[0 .. PER * kThreads) (entries >= n read
+// as 0 and left alone); every thread of the CTA calls it.
+template <int PER>
+__device__ void block_scan(u64* a, int n, u64* wsum) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  u64 v[PER];
+  u64 s = 0ull;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int i = t * PER + k;
+    s += i < n ? a[i] : 0ull;
+    v[k] = s;
+  }
+  u64 x = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const u64 y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[w] = x;
   __syncthreads();
-  if (threadIdx.x < 32) {
-    float x = sh[threadIdx.x];
-    x = warp_max(x);
-    if (threadIdx.x == 0) sh[32] = x;
+  if (w == 0) {
+    u64 z = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const u64 y = __shfl_up_sync(0xffffffffu, z, o);
+      if (lane >= o) z += y;
+    }
+    wsum[lane] = z;
   }
   __syncthreads();
-  const float r = sh[32];
+  const u64 off = (w > 0 ? wsum[w - 1] : 0ull) + (x - s);
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int i = t * PER + k;
+    if (i < n) a[i] = v[k] + off;
+  }
+  __syncthreads();
+}
+
+// The bin in which the inclusive cumulative mass first reaches T (1 <= T <= Z).
+__device__ int find_bin(Smem& sm, u64 T) {
+  if (threadIdx.x == 0) sm.found = kBins - 1;
+  __syncthreads();
+  for (int b = threadIdx.x; b < kBins; b += kThreads) {
+    const u64 lo = b > 0 ? sm.cum[b - 1] : 0ull;
+    if (lo < T && T <= sm.cum[b]) sm.found = b;  // at most one bin qualifies
+  }
+  __syncthreads();
+  const int r = sm.found;
   __syncthreads();
   return r;
 }
 
-__device__ __forceinline__ double block_sum(double v, double* sh) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    double x = sh[threadIdx.x];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    if (threadIdx.x == 0) sh[32] = x;
-  }
-  __syncthreads();
-  const double r = sh[32];
-  __syncthreads();
-  return r;
-}
-
-// Result of a weighted quantile: the key of the token where the cumulative
-// mass (descending order) reaches the target, the mass of all tokens with a
-// larger key, and the number and mass of the tokens that share the key.
-struct Quantile {
-  uint32_t key;
-  double above;
-  unsigned n_tie;
-  double m_tie;
+struct Pick {
+  int index;
+  u64 cum;  // inclusive cumulative mass at the picked token
 };
 
-// First token (descending key order) whose inclusive cumulative mass reaches
-// `target` (>= when !strict, > when strict); if rounding leaves the total
-// below the target, the last token.
-__device__ Quantile select_value(const float* row, int V, float lmax, float sc, double target, bool strict,
-                                 Hist* h) {
-  __shared__ uint32_t s_prefix;
-  __shared__ double s_above;
-  __shared__ unsigned s_n;
-  __shared__ double s_m;
-  if (threadIdx.x == 0) {
-    s_prefix = 0u;
-    s_above = 0.f;
+// Gather the tokens of bin `bin` into shared memory, sort them by (logit
+// descending, index ascending) and prefix-sum their masses.
+__device__ void gather_sort(Smem& sm, const float* row, int V, float lmax, float sc, int F, int bin, int n) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid == 0) sm.n_list = 0;
+  __syncthreads();
+  walk_row(row, V, [&](int i, float l, bool ok) {
+    bool hit = false;
+    if (ok) {
+      const float d = (lmax - l) * sc;
+      hit = bin_of(d) == bin && mass_fix(d, F) != 0ull;
+    }
+    const unsigned ball = __ballot_sync(0xffffffffu, hit);
+    if (ball != 0u) {
+      const int leader = __ffs(ball) - 1;
+      int base = 0;
+      if (lane == leader) base = atomicAdd(&sm.n_list, __popc(ball));
+      base = __shfl_sync(0xffffffffu, base, leader);
+      const int at = base + __popc(ball & ((1u << lane) - 1u));
+      if (hit && at < kCap) sm.list[at] = ((u64)(~float_order_key(l)) << 32) | (u64)(uint32_t)i;
+    }
+  });
+  __syncthreads();
+  int m = 2;
+  while (m < n) m <<= 1;
+  for (int i = n + tid; i < m; i += kThreads) sm.list[i] = ~0ull;
+  __syncthreads();
+  for (int k = 2; k <= m; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int t = tid; t < m / 2; t += kThreads) {
+        const int i = (t / j) * 2 * j + (t % j), p = i + j;
+        const u64 a = sm.list[i], b = sm.list[p];
+        if ((a > b) == ((i & k) == 0)) {
+          sm.list[i] = b;
+          sm.list[p] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = tid; i < n; i += kThreads) {
+    const int idx = (int)(uint32_t)(sm.list[i] & 0xFFFFFFFFull);
+    sm.lcum[i] = mass_fix((lmax - __ldg(row + idx)) * sc, F);
+  }
+  __syncthreads();
+  block_scan<kCap / kThreads>(sm.lcum, n, sm.wsum);
+  if (tid == 0) sm.list_bin = bin;
+  __syncthreads();
+}
+
+// Radix fallback for a bin too large to sort: the key (8 bits a level, top
+// down; larger digits come first in the order), then the r-th lowest index
+// among the tokens of that key.  Counts and masses per digit are summed over
+// each warp's lanes of equal digit before one shared-memory atomic.
+__device__ Pick radix_pick(Smem& sm, const float* row, int V, float lmax, float sc, int F, int bin, u64 base,
+                           u64 T) {
+  const int tid = threadIdx.x;
+  auto warp = cg::tiled_partition<32>(cg::this_thread_block());
+  if (tid == 0) {
+    sm.prefix = 0u;
+    sm.above = base;
   }
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int b = threadIdx.x; b < 256; b += kThreads) {
-      h->mass[b] = 0.0;
-      h->cnt[b] = 0u;
+    for (int k = tid; k < 256; k += kThreads) {
+      sm.dmass[k] = 0ull;
+      sm.dcnt[k] = 0u;
     }
     __syncthreads();
-    const uint32_t prefix = s_prefix;
-    for (int i = threadIdx.x; i < V; i += kThreads) {
-      const float l = row[i];
-      const uint32_t key = float_order_key(l);
-      if (shift < 24 && (key >> (shift + 8)) != (prefix >> (shift + 8))) continue;
-      const int b = (int)((key >> shift) & 255u);
-      atomicAdd(&h->mass[b], (double)exp2f((l - lmax) * sc));
-      atomicAdd(&h->cnt[b], 1u);
-    }
+    const uint32_t prefix = sm.prefix;
+    walk_row(row, V, [&](int i, float l, bool ok) {
+      int dg = kNone;
+      u64 mf = 0ull;
+      if (ok) {
+        const float d = (lmax - l) * sc;
+        const uint32_t key = float_order_key(l);
+        if (bin_of(d) == bin && (shift == 24 || (key >> (shift + 8)) == (prefix >> (shift + 8)))) {
+          mf = mass_fix(d, F);
+          if (mf != 0ull) dg = (int)((key >> shift) & 255u);
+        }
+      }
+      if (__any_sync(0xffffffffu, dg != kNone)) {
+        auto g = cg::labeled_partition(warp, dg);
+        const u64 s = cg::reduce(g, mf, cg::plus<u64>());
+        if (g.thread_rank() == 0 && dg != kNone) {
+          atomicAdd(&sm.dmass[dg], s);
+          atomicAdd(&sm.dcnt[dg], (unsigned)g.size());
+        }
+      }
+    });
     __syncthreads();
-    if (threadIdx.x == 0) {
-      double cum = s_above;
-      int chosen = -1, lowest = -1;
-      double cum_low = cum;
-      for (int b = 255; b >= 0; --b) {
-        if (h->cnt[b] == 0u) continue;
-        const double nc = cum + h->mass[b];
-        if (strict ? nc > target : nc >= target) {
-          chosen = b;
+    if (tid == 0) {
+      u64 cum = sm.above;
+      int chosen = -1, last = -1;
+      u64 cum_last = cum;
+      for (int k = 255; k >= 0; --k) {
+        if (sm.dcnt[k] == 0u) continue;
+        if (cum + sm.dmass[k] >= T) {
+          chosen = k;
           break;
         }
-        lowest = b;
-        cum_low = cum;
-        cum = nc;
+        last = k;
+        cum_last = cum;
+        cum += sm.dmass[k];
       }
-      if (chosen < 0) {  // the total stays below the target: the last token
-        chosen = lowest;
-        cum = cum_low;
+      if (chosen < 0) {  // not reached inside the bin (cannot happen for a T inside it): its last group
+        chosen = last < 0 ? 0 : last;
+        cum = cum_last;
       }
-      s_above = cum;
-      s_prefix = prefix | ((uint32_t)chosen << shift);
-      s_n = h->cnt[chosen];
-      s_m = h->mass[chosen];
+      sm.above = cum;
+      sm.prefix = prefix | ((uint32_t)chosen << shift);
     }
     __syncthreads();
   }
-  Quantile q;
-  q.key = s_prefix;
-  q.above = s_above;
-  q.n_tie = s_n;
-  q.m_tie = s_m;
+  // the tie group of key K: n tokens of one mass m1 each, `above` before them
+  const uint32_t K = sm.prefix;
+  const u64 above = sm.above;
+  const unsigned n_tie = sm.dcnt[K & 255u];
+  const u64 m_tie = sm.dmass[K & 255u];
   __syncthreads();
-  return q;
-}
-
-// The r-th (1-based) lowest index among the tokens whose key equals `key`.
-__device__ int select_tie_index(const float* row, int V, uint32_t key, unsigned r, Hist* h) {
-  __shared__ uint32_t s_prefix;
-  __shared__ unsigned s_before;
-  if (threadIdx.x == 0) {
-    s_prefix = 0u;
-    s_before = 0u;
+  const u64 m1 = n_tie > 0u ? m_tie / n_tie : 1ull;
+  u64 r = T > above ? (T - above + m1 - 1ull) / m1 : 1ull;  // tokens of the group needed
+  if (r < 1ull) r = 1ull;
+  if (r > n_tie) r = n_tie > 0u ? n_tie : 1u;
+  // the r-th lowest index among the tokens of key K
+  if (tid == 0) {
+    sm.prefix = 0u;
+    sm.found_cum = 0ull;  // tokens before the chosen index digits
   }
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int b = threadIdx.x; b < 256; b += kThreads) h->cnt[b] = 0u;
+  for (int shift = 16; shift >= 0; shift -= 8) {
+    for (int k = tid; k < 256; k += kThreads) sm.dcnt[k] = 0u;
     __syncthreads();
-    const uint32_t prefix = s_prefix;
-    for (int i = threadIdx.x; i < V; i += kThreads) {
-      if (float_order_key(row[i]) != key) continue;
-      const uint32_t ui = (uint32_t)i;
-      if (shift < 24 && (ui >> (shift + 8)) != (prefix >> (shift + 8))) continue;
-      atomicAdd(&h->cnt[(ui >> shift) & 255u], 1u);
-    }
+    const uint32_t prefix = sm.prefix;
+    walk_row(row, V, [&](int i, float l, bool ok) {
+      int dg = kNone;
+      if (ok && float_order_key(l) == K &&
+          (shift == 16 || ((uint32_t)i >> (shift + 8)) == (prefix >> (shift + 8))))
+        dg = (int)(((uint32_t)i >> shift) & 255u);
+      if (__any_sync(0xffffffffu, dg != kNone)) {
+        auto g = cg::labeled_partition(warp, dg);
+        if (g.thread_rank() == 0 && dg != kNone) atomicAdd(&sm.dcnt[dg], (unsigned)g.size());
+      }
+    });
     __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned before = s_before;
+    if (tid == 0) {
+      u64 before = sm.found_cum;
       int chosen = 255;
-      for (int b = 0; b < 256; ++b) {  // ascending index
-        if (before + h->cnt[b] >= r) {
-          chosen = b;
+      for (int k = 0; k < 256; ++k) {  // ascending index
+        if (before + sm.dcnt[k] >= r) {
+          chosen = k;
           break;
         }
-        before += h->cnt[b];
+        before += sm.dcnt[k];
       }
-      s_before = before;
-      s_prefix = prefix | ((uint32_t)chosen << shift);
+      sm.found_cum = before;
+      sm.prefix = prefix | ((uint32_t)chosen << shift);
     }
     __syncthreads();
   }
-  const int idx = (int)s_prefix;
+  Pick p;
+  p.index = (int)sm.prefix;
+  p.cum = above + r * m1;
   __syncthreads();
-  return idx;
+  return p;
 }
 
-// How many tokens of a tie group (n tokens of mass m each, `above` before
-// them) the cumulative mass needs to reach the target.
-__device__ __forceinline__ unsigned ties_needed(double above, unsigned n, double m, double target, bool strict) {
-  if (n <= 1u || m <= 0.0) return 1u;
-  const double k = (target - above) / (m / (double)n);
-  if (!(k >= 0.0)) return 1u;
-  if (k >= (double)n) return n;
-  const unsigned r = strict ? (unsigned)floor(k) + 1u : (unsigned)ceil(k);
-  return r < 1u ? 1u : r > n ? n : r;
+// The first token (in the order) whose inclusive cumulative mass reaches T.
+__device__ Pick pick(Smem& sm, const float* row, int V, float lmax, float sc, int F, u64 T) {
+  const int bin = find_bin(sm, T);
+  const u64 base = bin > 0 ? sm.cum[bin - 1] : 0ull;
+  const int n = (int)sm.cnt[bin];
+  if (n == 0) {  // no bin holds the target (not reachable for 1 <= T <= Z)
+    Pick p;
+    p.index = -1;
+    p.cum = base;
+    return p;
+  }
+  if (n > kCap) return radix_pick(sm, row, V, lmax, sc, F, bin, base, T);
+  if (sm.list_bin != bin) gather_sort(sm, row, V, lmax, sc, F, bin, n);
+  if (threadIdx.x == 0) {
+    sm.found = n - 1;
+    sm.found_cum = base + (n > 0 ? sm.lcum[n - 1] : 0ull);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const u64 lo = base + (i > 0 ? sm.lcum[i - 1] : 0ull);
+    const u64 hi = base + sm.lcum[i];
+    if (lo < T && T <= hi) {  // exactly one position
+      sm.found = i;
+      sm.found_cum = hi;
+    }
+  }
+  __syncthreads();
+  Pick p;
+  p.index = (int)(uint32_t)(sm.list[sm.found] & 0xFFFFFFFFull);
+  p.cum = sm.found_cum;
+  __syncthreads();
+  return p;
 }
 
 __global__ void __launch_bounds__(kThreads) sample_kernel(const float* logits, int V, const float* temperature,
                                                            const float* top_p, const float* u, int32_t* out) {
   grid_dep_launch();
   grid_dep_wait();
-  __shared__ Hist hist;
-  __shared__ float red[33];
-  __shared__ double red_d[33];
-  __shared__ unsigned long long best_sh[32];
-  const int b = blockIdx.x;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  const int b = blockIdx.x, tid = threadIdx.x;
   const float* row = logits + (int64_t)b * V;
   const float T = temperature[b];
-  if (!(T > 0.f)) {  // greedy: lowest index of the largest logit
+
+  float mx = -3.402823466e38f;
+  walk_row(row, V, [&](int, float l, bool ok) {
+    if (ok) mx = fmaxf(mx, l);
+  });
+  mx = warp_max(mx);
+  if ((tid & 31) == 0) sm.fred[tid >> 5] = mx;
+  __syncthreads();
+  float lmax = sm.fred[0];
+  for (int w = 1; w < kWarps; ++w) lmax = fmaxf(lmax, sm.fred[w]);
+
+  if (!(T > 0.f) || !(lmax <= 3.402823466e38f)) {
+    // greedy (also for a row whose largest logit is +inf): lowest index of the largest logit
     unsigned long long best = 0ull;
-    for (int i = threadIdx.x; i < V; i += kThreads) {
-      const unsigned long long k = argmax_key(row[i], (uint32_t)i);
+    walk_row(row, V, [&](int i, float l, bool ok) {
+      const unsigned long long k = ok ? argmax_key(l, (uint32_t)i) : 0ull;
       best = k > best ? k : best;
-    }
+    });
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
       const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
       best = other > best ? other : best;
     }
-    if ((threadIdx.x & 31) == 0) best_sh[threadIdx.x >> 5] = best;
+    if ((tid & 31) == 0) sm.best[tid >> 5] = best;
     __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned long long m = best_sh[0];
-      for (int w = 1; w < kThreads / 32; ++w) m = best_sh[w] > m ? best_sh[w] : m;
+    if (tid == 0) {
+      unsigned long long m = sm.best[0];
+      for (int w = 1; w < kWarps; ++w) m = sm.best[w] > m ? sm.best[w] : m;
       out[b] = (int32_t)argmax_key_index(m);
     }
     return;
   }
   const float sc = 1.4426950408889634f / T;  // log2(e) / T
-  float mx = -3.402823466e38f;
-  for (int i = threadIdx.x; i < V; i += kThreads) mx = fmaxf(mx, row[i]);
-  const float lmax = block_max(mx, red);
-  double z = 0.0;
-  for (int i = threadIdx.x; i < V; i += kThreads) z += (double)exp2f((row[i] - lmax) * sc);
-  const double Z = block_sum(z, red_d);
-  // top-p cutoff: the first token whose cumulative probability reaches top_p
-  const double tc = (double)top_p[b] * Z;
-  const Quantile c = select_value(row, V, lmax, sc, tc, false, &hist);
-  const unsigned rc = ties_needed(c.above, c.n_tie, c.m_tie, tc, false);
-  const double z_kept = c.above + (c.n_tie > 0u ? c.m_tie / (double)c.n_tie : 0.0) * (double)rc;
-  // the draw: the first token whose cumulative mass exceeds u * (kept mass)
-  const double target = (double)u[b] * z_kept;
-  const Quantile d = select_value(row, V, lmax, sc, target, true, &hist);
-  unsigned rd = ties_needed(d.above, d.n_tie, d.m_tie, target, true);
-  if (d.key == c.key && rd > rc) rd = rc;  // stay inside the kept set
-  const int idx = d.n_tie <= 1u ? -1 : select_tie_index(row, V, d.key, rd, &hist);
-  if (d.n_tie <= 1u) {  // the one token with this key
-    __shared__ int s_idx;
-    if (threadIdx.x == 0) s_idx = V;
-    __syncthreads();
-    for (int i = threadIdx.x; i < V; i += kThreads)
-      if (float_order_key(row[i]) == d.key) atomicMin(&s_idx, i);
-    __syncthreads();
-    if (threadIdx.x == 0) out[b] = s_idx < V ? s_idx : 0;
-    return;
+  const int F = 62 - (V > 1 ? 32 - __clz(V - 1) : 0);
+
+  // histogram of masses and counts over the bins of d
+  for (int k = tid; k < kBins; k += kThreads) {
+    sm.cum[k] = 0ull;
+    sm.cnt[k] = 0u;
   }
-  if (threadIdx.x == 0) out[b] = idx;
+  if (tid == 0) sm.list_bin = -1;
+  __syncthreads();
+  walk_row(row, V, [&](int, float l, bool ok) {
+    const float d = (lmax - l) * sc;
+    const u64 mf = ok ? mass_fix(d, F) : 0ull;
+    if (mf != 0ull) {
+      const int k = bin_of(d);
+      atomicAdd(&sm.cum[k], mf);
+      atomicAdd(&sm.cnt[k], 1u);
+    }
+  });
+  __syncthreads();
+  block_scan<kBins / kThreads>(sm.cum, kBins, sm.wsum);
+  const u64 Z = sm.cum[kBins - 1];  // >= 2^F: the largest logit's mass is 1
+
+  // cutoff: the first token whose cumulative mass reaches ceil(top_p Z)
+  float tp = top_p[b];
+  if (!(tp < 1.f)) tp = 1.f;  // also NaN
+  if (!(tp > 0.f)) tp = 0.f;
+  u64 Tc = (u64)ceil((double)tp * (double)Z);
+  Tc = Tc < 1ull ? 1ull : Tc > Z ? Z : Tc;
+  const Pick c = pick(sm, row, V, lmax, sc, F, Tc);
+
+  // the draw: the first kept token whose cumulative mass exceeds u * kept
+  float uu = u[b];
+  if (!(uu > 0.f)) uu = 0.f;  // also NaN
+  u64 Td = (u64)floor((double)uu * (double)c.cum) + 1ull;
+  Td = Td > c.cum ? c.cum : Td;
+  const Pick d = pick(sm, row, V, lmax, sc, F, Td);
+  if (tid == 0) out[b] = d.index >= 0 && d.index < V ? d.index : c.index >= 0 && c.index < V ? c.index : 0;
 }
 
 }  // namespace smp
@@ -250,8 +483,14 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const float* logits, i
 cudaError_t launch_sample(const float* logits, int batch, int V, const float* temperature, const float* top_p,
                           const float* u, int32_t* out, cudaStream_t s) {
   if (batch <= 0) return cudaSuccess;
-  return launch_k(smp::sample_kernel, dim3(batch), dim3(smp::kThreads), 0, s, logits, V, temperature, top_p, u,
-                  out);
+  static PerDevice setup;
+  cudaError_t e = per_device(setup, nullptr, [](int, int&) {
+    return cudaFuncSetAttribute(smp::sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sizeof(smp::Smem));
+  });
+  if (e != cudaSuccess) return e;
+  return launch_k(smp::sample_kernel, dim3(batch), dim3(smp::kThreads), sizeof(smp::Smem), s, logits, V,
+                  temperature, top_p, u, out);
 }
 
 }  // namespace tq
