@@ -22,8 +22,13 @@ HBM.  The same JSON line carries:
 * `batched`: 32 sequences with seeded ragged contexts over a paged f16 cache,
   one decode step of the whole batch per graph replay, with the batched
   GEMM's roofline (tq_gemm at 32 rows over the 36 layers' down projections);
-* `cpu_baseline` (also inside `prefill` and `batched`): the oracle timed on
-  this host's cores on a bounded sample of each workload.
+* `mixed`: one continuous-batching step (tq_step) of the same 32-sequence
+  mix in which one sequence is still prefilling: 31 decode rows and a
+  512-row prompt chunk, every projection a tensor-core GEMM over 543 rows;
+* `sampling`: temperature / top-p sampling (tq_sample) of 151936-entry
+  logit rows, 1 and 32 rows per call, L2 flushed between calls;
+* `cpu_baseline` (also inside each sub-benchmark): the oracle timed on this
+  host's cores on a bounded sample of each workload.
 
 Under torchrun every rank runs an independent replica (the step does not
 shard); `value` is the sum of tokens over all ranks divided by the slowest
@@ -58,12 +63,15 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-batched", action="store_true", help="skip the batched sub-benchmark")
     ap.add_argument("--batched-steps", type=int, default=30)
+    ap.add_argument("--no-mixed", action="store_true", help="skip the continuous-batching sub-benchmark")
+    ap.add_argument("--mixed-steps", type=int, default=10)
+    ap.add_argument("--no-sampling", action="store_true", help="skip the sampling sub-benchmark")
     ap.add_argument("--prefill-reps", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling cases only: keep the first N layers of the workloads")
-    ap.add_argument("--only", choices=["batched"], default=None,
-                    help="profiling cases only: run just the batched sub-benchmark")
+    ap.add_argument("--only", choices=["batched", "mixed", "sampling"], default=None,
+                    help="profiling cases only: run just one sub-benchmark")
     ap.add_argument("--workload", default="qwen3_8b_q4_0",
                     help="decode workload of the headline (profiling cases may pick another)")
     ap.add_argument("--arch", default="qwen3", choices=["qwen3", "llama", "qwen2", "gemma3"],
@@ -227,6 +235,42 @@ class OracleSample:
         t_head = time.perf_counter() - t0
         return t_layers / n_seq * len(lens) / N_SAMPLE_LAYERS * self.w.n_layers + t_head
 
+    def mixed_step(self, lens, cached, chunk, n_seq=4):
+        """Seconds of one continuous-batching step: decode rows of len(lens)
+        sequences (`n_seq` of them timed, scaled to all) and a `chunk`-row
+        prompt chunk after `cached` positions, through 2 layers scaled to 36,
+        plus the head for every sequence's last row."""
+        import numpy as np
+        import synth
+        t_dec = self.batched_step(lens[:n_seq], n_seq) - self._head_time(n_seq)
+        t_dec *= len(lens) / n_seq
+        kv = self._kv(synth.KV_STREAM + 1, cached)
+        cache = [(kv[0].copy(), kv[1].copy()) for _ in range(N_SAMPLE_LAYERS)]
+        x = self.m.embed(self.w.prompt(n=chunk))
+        t0 = time.perf_counter()
+        for i in range(N_SAMPLE_LAYERS):
+            x = self.m.block(i, x, cache, np.arange(cached, cached + chunk))
+        t_chunk = (time.perf_counter() - t0) / N_SAMPLE_LAYERS * self.w.n_layers
+        return t_dec + t_chunk + self._head_time(len(lens) + 1)
+
+    def sampling(self, V, n=4):
+        """Seconds of the oracle sampler on n seeded rows of V logits."""
+        import numpy as np
+        import synth
+        from oracle import sample as osm
+        rows = synth.host_normal(5, 7, n * V, sigma=2.0).astype(np.float64).reshape(n, V)
+        us = synth.uniform_below(5, 8, n, 1 << 24).astype(np.float64) / float(1 << 24)
+        t0 = time.perf_counter()
+        for r in range(n):
+            osm.sample(rows[r], 0.7, 0.9, float(us[r]))
+        return time.perf_counter() - t0, n
+
+    def _head_time(self, rows):
+        x = self.m.embed(list(range(1, rows + 1)))
+        t0 = time.perf_counter()
+        self.m.head(x)
+        return time.perf_counter() - t0
+
     def prefill(self, n=PROMPT):
         """Seconds of a full n-token prefill (36 layers scaled from 2, last-row head)."""
         import numpy as np
@@ -351,8 +395,11 @@ def run_gpu(args, rank, world):
     E = args.e2e_steps
     max_ctx = P + W + K + E + 16
     mats, gains = build_weights(w, dev)
-    if args.only == "batched":
-        b = run_batched(args, world, mats, gains, dev, torch.cuda.Stream(device=dev), pk)
+    if args.only is not None:
+        st = torch.cuda.Stream(device=dev)
+        b = (run_batched(args, world, mats, gains, dev, st, pk) if args.only == "batched" else
+             run_mixed(args, world, mats, gains, dev, st, pk) if args.only == "mixed" else
+             run_sampling(dev, st, pk, w.vocab))
         if rank == 0:
             print(json.dumps(b), flush=True)
         return
@@ -487,9 +534,13 @@ def run_gpu(args, rank, world):
                             "launch_ms": round(gemm_ms, 5), "flop_per_launch": gemm_flop}}
     del x, y, scr
 
-    batched = None
+    batched = mixed = sampling = None
     if not args.no_batched and w.name.startswith("qwen3_8b_q4_0"):
         batched = run_batched(args, world, mats, gains, dev, stream, pk)
+    if not args.no_mixed and w.name.startswith("qwen3_8b_q4_0"):
+        mixed = run_mixed(args, world, mats, gains, dev, stream, pk)
+    if not args.no_sampling:
+        sampling = run_sampling(dev, stream, pk, w.vocab)
 
     line = {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
@@ -510,6 +561,10 @@ def run_gpu(args, rank, world):
             "prefill": prefill}
     if batched is not None:
         line["batched"] = batched
+    if mixed is not None:
+        line["mixed"] = mixed
+    if sampling is not None:
+        line["sampling"] = sampling
     if rank == 0 and not args.no_cpu_baseline and w.name == "qwen3_8b_q4_0" and not args.layers:
         o = OracleSample()
         o.decode_step()
@@ -529,6 +584,21 @@ def run_gpu(args, rank, world):
                 "sample": f"oracle float32 batched step: 4 of {len(lens)} sequences (their seeded "
                           f"contexts) through {N_SAMPLE_LAYERS} of {w.n_layers} full-size layers, scaled "
                           f"to all sequences and layers, plus the LM head for all {len(lens)}"}
+        if mixed is not None:
+            ml = synth.QWEN3_8B_Q4_BATCHED.context_lengths()[:-1]
+            ts = o.mixed_step(ml, 1024, 512)
+            line["mixed"]["cpu_baseline"] = {
+                "value": round((len(ml) + 512) / ts, 4), "unit": "tokens/s", "cores": o.cores, "kind": "oracle",
+                "sample": f"oracle float32 mixed step: decode rows of 4 of the {len(ml)} sequences and the "
+                          f"512-row chunk after 1024 cached positions through {N_SAMPLE_LAYERS} of "
+                          f"{w.n_layers} full-size layers, scaled to all rows and layers, plus the LM head "
+                          f"for {len(ml) + 1} rows"}
+        if sampling is not None:
+            ts, n = o.sampling(w.vocab)
+            line["sampling"]["cpu_baseline"] = {
+                "value": round(n / ts, 3), "unit": "rows/s", "cores": o.cores, "kind": "oracle",
+                "sample": f"oracle sampler (f64, sort-based) on {n} seeded {w.vocab}-entry rows, "
+                          "temperature 0.7, top-p 0.9"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -650,6 +720,156 @@ def run_batched(args, world, mats, gains, dev, stream, pk):
                          "peak_kind": pk["kind"] + " copy bandwidth",
                          "launch_ms": round(gemm_ms, 5), "bytes_per_launch": int(gemm_bytes)},
             "gpu_launches": launches}
+
+
+def run_mixed(args, world, mats, gains, dev, stream, pk):
+    """Continuous batching: the 32-sequence serving mix with its last sequence
+    still prefilling.  One tq_step carries a decode row of each of the first
+    31 sequences (seeded ragged contexts) and a 512-row prompt chunk of the
+    32nd after 1024 cached positions; the paged f16 cache holds seeded N(0, 1)
+    values.  Every timed step repeats the same rows (same positions, so the
+    same work), eager launches, CUDA events around the whole run."""
+    import numpy as np
+    import torch
+    import synth
+    from block_quantized_transformer_gb300.synthetic import build_model
+
+    w = synth.QWEN3_8B_Q4_BATCHED
+    if args.layers:
+        import dataclasses
+        w = dataclasses.replace(w, n_layers=args.layers)
+    w = apply_variant(w, args)
+    K, W = args.mixed_steps, 3
+    B, P, H, V = w.batch, w.page_size, w.hidden, w.vocab
+    CACHED, CHUNK = 1024, 512
+    lens = w.context_lengths().astype(np.int64)
+    lens[B - 1] = CACHED
+    need = lens + 1
+    need[B - 1] = CACHED + CHUNK
+    per_seq = int((need.max() + P - 1) // P)
+    n_pages_seq = (need + P - 1) // P
+    n_pages = int(n_pages_seq.sum())
+    keys = synth.host_normal(w.length_seed, synth.LENGTH_STREAM + 1, n_pages, sigma=1.0)
+    order = np.argsort(keys, kind="stable").astype(np.int32)
+    table = np.zeros((B, per_seq), dtype=np.int32)
+    at = 0
+    for b in range(B):
+        table[b, :n_pages_seq[b]] = order[at:at + n_pages_seq[b]]
+        at += n_pages_seq[b]
+    n_rows = (B - 1) + CHUNK
+    model = build_model(w, device=dev, max_batch=B, max_ctx=per_seq * P, max_prefill=n_rows,
+                        page_size=P, n_pages=n_pages, weights=(mats, gains))
+    chunk = 1 << 26
+    for cache, stream_id in ((model.k_cache, synth.KV_STREAM), (model.v_cache, synth.KV_STREAM + 1)):
+        for i0 in range(0, cache.numel(), chunk):
+            n = min(chunk, cache.numel() - i0)
+            f = torch.empty(n, dtype=torch.float32, device=dev)
+            synth.dev_normal(f, w.seed, stream_id, first=i0, sigma=1.0)
+            cache[i0:i0 + n].copy_(f)
+            del f
+    torch.cuda.synchronize()
+    toks = synth.uniform_below(w.seed, synth.PROMPT_STREAM + 200, n_rows, w.vocab).astype(np.int32)
+    seq = np.concatenate([np.arange(B - 1), np.full(CHUNK, B - 1)]).astype(np.int32)
+    pos = np.concatenate([lens[:B - 1], CACHED + np.arange(CHUNK)]).astype(np.int32)
+    last = np.concatenate([np.arange(B - 1), [n_rows - 1]]).astype(np.int32)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    d_tok, d_seq, d_pos, d_last, bt = d(toks), d(seq), d(pos), d(last), d(table)
+    am = torch.empty(B, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            model.step(d_tok, d_seq, d_pos, d_last, block_table=bt, argmax=am)
+        stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            model.step(d_tok, d_seq, d_pos, d_last, block_table=bt, argmax=am)
+        e1.record(stream)
+        stream.synchronize()
+        ms = e0.elapsed_time(e1)
+        barrier(world)
+        assert model.status() == 0
+    weight_bytes = model.weight_bytes() + sum(g.numel() * 4 for g in gains.values())
+    model.close()
+    del model
+    torch.cuda.empty_cache()
+    ms_max = reduce_max(ms, world)
+    ms_step = ms_max / K
+    L, nq, hd = w.n_layers, w.n_heads, w.head_dim
+    kv_row = 2 * w.n_kv_heads * hd * 2 * L
+    keys_read = float((lens[:B - 1] + 1).sum()) + (CACHED + CHUNK)       # each decode row's context, the chunk's keys once
+    step_bytes = weight_bytes + kv_row * keys_read + kv_row * n_rows
+    pairs = float((lens[:B - 1] + 1).sum()) + CHUNK * CACHED + CHUNK * (CHUNK + 1) / 2.0
+    flop = 2.0 * n_rows * weight_count_layers(w) + 2.0 * B * V * H + 4.0 * pairs * nq * hd * L
+    s_step = ms_step / 1e3
+    return {"metric": f"continuous-batching step rows/s ({B - 1} decode rows + a {CHUNK}-row prompt chunk, "
+                      f"{w.wtype.upper()} Qwen3-8B shape, paged f16 KV)",
+            "value": round(world * n_rows * K / (ms_max / 1e3), 1), "unit": "tokens/s", "steps": K, "warmup": W,
+            "ms_per_step": round(ms_step, 4),
+            "config": {"workload": f"{w.name}: decode rows of sequences 0..{B - 2} (cached lengths "
+                                   f"{int(lens[:B - 1].min())}..{int(lens[:B - 1].max())}) and sequence {B - 1}'s "
+                                   f"prompt rows {CACHED}..{CACHED + CHUNK - 1} in one tq_step ({n_rows} rows), "
+                                   f"pages of {P} tokens in a seeded shuffled order",
+                       "kv_cache": "f16, seeded N(0,1)", "l2": "inputs exceed L2",
+                       "timing": f"{K} eager tq_step calls between CUDA events (the same rows each time)"},
+            "tensor": {"flop": flop, "achieved_tflops": round(flop / s_step / 1e12, 1),
+                       "frac_of_peak": round(flop / s_step / 1e12 / pk["tc_sust"], 4), "peak_tflops": pk["tc_sust"],
+                       "peak_kind": pk["kind"] + " bf16 dense sustained"},
+            "hbm": {"step_bytes": int(step_bytes), "achieved_gbs": round(step_bytes / s_step / 1e9, 1),
+                    "frac_of_peak": round(step_bytes / s_step / 1e9 / pk["hbm"], 4), "peak_gbs": pk["hbm"]}}
+
+
+def run_sampling(dev, stream, pk, V, reps=20):
+    """tq_sample over seeded N(0, 2^2) logit rows of the vocabulary (temperature
+    0.7, top-p 0.9, seeded u), 1 and 32 rows per call; a 256 MB write between
+    calls flushes L2, and each call is timed alone with CUDA events."""
+    import numpy as np
+    import torch
+    import synth
+    import block_quantized_transformer_gb300 as tq
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    for B in (1, 32):
+        lg = torch.empty(B * V, dtype=torch.float32, device=dev)
+        synth.dev_normal(lg, 5, 7, sigma=2.0)
+        lg = lg.view(B, V)
+        t = torch.full((B,), 0.7, dtype=torch.float32, device=dev)
+        p = torch.full((B,), 0.9, dtype=torch.float32, device=dev)
+        u = torch.from_numpy(synth.uniform_below(5, 8, B, 1 << 24).astype(np.float32) / float(1 << 24)).to(dev)
+        tok = torch.empty(B, dtype=torch.int32, device=dev)
+        times = []
+        with torch.cuda.stream(stream):
+            for i in range(reps + 3):
+                flush.fill_(i & 255)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                tq.tq_sample(lg, t, p, u, out=tok)
+                e1.record(stream)
+                stream.synchronize()
+                if i >= 3:
+                    times.append(e0.elapsed_time(e1))
+        ms = statistics.mean(times)
+        nbytes = B * V * 4
+        out[f"rows_{B}"] = {"us_per_call": round(ms * 1e3, 2), "rows_per_s": round(B / (ms / 1e3), 1),
+                            "bytes_per_call": nbytes, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
+                            "frac_of_hbm_peak": round(nbytes / (ms / 1e3) / 1e9 / pk["hbm"], 4)}
+    del flush
+    r32 = out["rows_32"]
+    return {"metric": f"temperature/top-p sampling of {V}-entry logit rows, rows/s", "value": r32["rows_per_s"],
+            "unit": "rows/s",
+            "config": {"workload": f"{V}-entry f32 logit rows, seeded N(0, 2^2); temperature 0.7, top-p 0.9, "
+                                   "seeded u", "l2": "flushed before every call (256 MB write)",
+                       "timing": f"{reps} calls after 3, each between CUDA events"},
+            **out,
+            "roofline": {"bound": "hbm", "achieved": r32["achieved_gbs"], "peak": pk["hbm"], "unit": "GB/s",
+                         "frac": r32["frac_of_hbm_peak"], "traffic": None,
+                         "kernel": "sample_kernel, 32 rows (one CTA per row; the row is read once per pass)",
+                         "bytes_per_launch": r32["bytes_per_call"], "launch_ms": round(r32["us_per_call"] / 1e3, 5),
+                         "peak_kind": pk["kind"] + " copy bandwidth"}}
 
 
 def main():

@@ -240,6 +240,7 @@ tq::CacheView cache_view(const tq_model* m, const int32_t* block_table) {
   const tq_config& c = m->cfg;
   tq::CacheView v{};
   v.max_ctx = c.max_ctx;
+  v.max_seq = c.max_batch;
   v.n_kv = c.n_kv_heads;
   v.page_size = c.page_size;
   v.n_pages = c.n_pages;
@@ -475,6 +476,14 @@ cudaError_t run_layers_gemm(tq_model* m, int T, const int32_t* pos, const int32_
       // of this layer's caches (made at model creation; a paged cache's block
       // table is read in the kernel)
       e = tq::launch_attn_prefill(hd, G, m->kmap[l], m->vmap[l], a, s);
+    } else if (mixed && c.kvtype == TQ_KV_F16) {
+      // mixed rows over an f16 cache: blocks of rows that are one sequence's
+      // consecutive positions (prompt chunks) take the flash kernel, the
+      // other rows (decode tokens, a chunk's ragged ends) the row-wise kernel
+      tq::AttnArgs af = a;
+      af.flash_rows = 1;
+      e = tq::launch_attn_prefill(hd, G, m->kmap[l], m->vmap[l], af, s);
+      if (e == cudaSuccess) e = tq::launch_attn_decode(c.kvtype, hd, G, kv_map(m, l, false), kv_map(m, l, true), af, s);
     } else {
       e = tq::launch_attn_decode(c.kvtype, hd, G, kv_map(m, l, false), kv_map(m, l, true), a, s);
     }

@@ -39,9 +39,10 @@ template <>
 __device__ __forceinline__ __half to_kv<__half>(float v) { return __float2half_rn(v); }
 
 // Pointer to element 0 of cache row `slot` of (seq, kv head h), or null when
-// the slot or page is out of range.
+// the sequence, the slot or the page is out of range.
 template <typename KT, int HD>
 __device__ __forceinline__ KT* cache_row(void* base, int seq, int h, int slot, const CacheView& c) {
+  if (seq < 0 || seq >= c.max_seq) return nullptr;
   if (slot < 0 || slot >= c.max_ctx) return nullptr;
   if (c.page_size == 0) {
     return reinterpret_cast<KT*>(base) + (((int64_t)seq * c.n_kv + h) * c.max_ctx + slot) * HD;
@@ -640,6 +641,14 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(const __grid_constant__ CU
   const int split = blockIdx.x, h = blockIdx.y, t = FUSED ? blockIdx.z : gridDim.z - 1 - blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int g = lane >> 2, c = lane & 3;
+  // mixed rows: a block that attn_prefill takes (one sequence's consecutive
+  // positions) is not computed here (every warp, and every CTA of a cluster,
+  // reaches the same answer)
+  if (!FUSED && a.flash_rows && a.seq_idx != nullptr && a.kv_len != nullptr) {
+    constexpr int BQ = kFlashRows / G;
+    const int tb = (t / BQ) * BQ;
+    if (rows_uniform(a.seq_idx, a.kv_len, tb, min(a.T, tb + BQ) - tb, a.cache)) return;
+  }
   // step inputs, never written by a kernel of the step: load both at once
   const int new_slot = a.kv_len != nullptr ? a.kv_len[t] : a.pos_base + t;
   const int pos = FUSED ? a.pos[t] : 0;
@@ -649,7 +658,12 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(const __grid_constant__ CU
   const int lo = a.window > 0 ? max(0, new_slot + 1 - a.window) : 0;
   const int lo_t = (min(lo, ctx - 1) / TILE) * TILE;
   const int span = ((ctx - lo_t + CL * TILE - 1) / (CL * TILE)) * TILE;
-  const int seq = a.seq_idx != nullptr ? a.seq_idx[t] : a.seq_fixed >= 0 ? a.seq_fixed : t;
+  // a sequence index outside the cache: reads stay in bounds (sequence 0),
+  // the new row is not written, the status says so
+  const int seq_in = a.seq_idx != nullptr ? a.seq_idx[t] : a.seq_fixed >= 0 ? a.seq_fixed : t;
+  const bool seq_ok = seq_in >= 0 && seq_in < a.cache.max_seq;
+  const int seq = seq_ok ? seq_in : 0;
+  if (!seq_ok && tid == 0) set_status(a.status, TQ_DEV_KV_OVERFLOW);
   const int k0 = lo_t + split * span;
   const int k1 = min(ctx, k0 + span);
   const int n_tiles = k1 > k0 ? (k1 - k0 + TILE - 1) / TILE : 0;
@@ -792,8 +806,8 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(const __grid_constant__ CU
       vx[d] = vp[d];
     }
     norm_rope_head<HD, DPL>(kx, gk, a.eps, cs, sn, lane, rope_ok, a.gk != nullptr);
-    __half* kd = cache_row<__half, HD>(const_cast<void*>(a.kc), seq, h, new_slot, a.cache);
-    __half* vd = cache_row<__half, HD>(const_cast<void*>(a.vc), seq, h, new_slot, a.cache);
+    __half* kd = cache_row<__half, HD>(const_cast<void*>(a.kc), seq_ok ? seq : -1, h, new_slot, a.cache);
+    __half* vd = cache_row<__half, HD>(const_cast<void*>(a.vc), seq_ok ? seq : -1, h, new_slot, a.cache);
     if (kd != nullptr && vd != nullptr) {
 #pragma unroll
       for (int d = 0; d < DPL; ++d) {
@@ -1074,9 +1088,10 @@ cudaError_t attn_g(const CUtensorMap* kmap, const CUtensorMap* vmap, const AttnA
   if (sizeof(KT) == 2) {
     if (kmap == nullptr || vmap == nullptr) return cudaErrorInvalidValue;  // f16 caches are staged by TMA
     if (a.fused) return attn_tc_t<HD, G>(*kmap, *vmap, a, s);
-    // rows of a prompt or mixed step: one CTA per (query row, KV head), its
-    // whole causal prefix (the K/V of the step's rows stay in L2)
-    return attn_tc_cl<HD, G, 1, false>(*kmap, *vmap, a, s);
+    // rows of a mixed step (those not in a flash block: decode tokens, the
+    // ragged ends of prompt chunks): 4 CTAs per (row, KV head) share the row's
+    // causal prefix, as in batched decode
+    return attn_tc_cl<HD, G, 4, false>(*kmap, *vmap, a, s);
   }
   if (a.fused || a.split_keys <= 4 * 32 || (sizeof(KT) == 4 && HD == 128)) return attn_t<KT, HD, G, 1>(a, s);
   return attn_t<KT, HD, G, 2>(a, s);

@@ -1,5 +1,5 @@
 // Prefill attention over an f16 cache: every prompt row attends to its causal
-// prefix ("Всередині LLM: чисте виконання на Python для Qwen3-0.6B на MLX",
+// prefix (also the prompt chunks inside a continuous-batching step) ("Всередині LLM: чисте виконання на Python для Qwen3-0.6B на MLX",
 // step 5, "Вся функція уваги": softmax(q k^T / sqrt(hd)) v with the causal
 // mask over the whole prompt; query head h reads KV head h / G).  The rows
 // were normalised, rotated and appended to the cache by rope_append.
@@ -36,6 +36,7 @@ constexpr int kTile = 64;                  // keys per stage
 constexpr int kSub = 32;                   // keys per TMA box
 constexpr int kNS = 3;                     // stages
 constexpr int kThreads = (kWarps + 1) * 32;
+static_assert(kRows == kFlashRows, "the row-wise kernel skips blocks of kFlashRows / G rows");
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 template <int HD>
@@ -103,12 +104,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = blockIdx.y;
   const int t0 = qb * BQ;
   const int t_last = min(a.T, t0 + BQ) - 1;
-  const int seq = a.seq_fixed;
-  const int n_keys = min(a.pos_base + t_last + 1, a.cache.max_ctx);
+  // rows of a mixed step (seq_idx set): this block only when it is one
+  // sequence's consecutive positions (every warp reaches the same answer);
+  // the row-wise decode kernel takes the other rows
+  int seq = a.seq_fixed, pos_base = a.pos_base;
+  if (a.seq_idx != nullptr) {
+    if (a.kv_len == nullptr || !rows_uniform(a.seq_idx, a.kv_len, t0, t_last + 1 - t0, a.cache)) return;
+    seq = a.seq_idx[t0];
+    pos_base = a.kv_len[t0] - t0;
+  }
+  const int n_keys = min(pos_base + t_last + 1, a.cache.max_ctx);
   const int n_tiles = (n_keys + kTile - 1) / kTile;
   // sliding window: tiles before the first key any query row of the CTA sees
   // are skipped (the rows' own lower bounds are masked below)
-  const int i0 = a.window > 0 ? min(max(0, a.pos_base + t0 + 1 - a.window), n_keys) / kTile : 0;
+  const int i0 = a.window > 0 ? min(max(0, pos_base + t0 + 1 - a.window), n_keys) / kTile : 0;
 
   // zero the stages once: a box that is not loaded (past the prefix) then
   // holds finite values, which the mask turns into p = 0
@@ -191,8 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tok_a = t0 + ra / G, tok_b = t0 + rb / G;
   const int ha = h * G + ra % G, hb = h * G + rb % G;
   // rows past the prompt compute on zeros and are not written
-  const int pos_a = a.pos_base + min(tok_a, t_last), pos_b = a.pos_base + min(tok_b, t_last);
-  const int pmax = a.pos_base + min(t0 + (warp * 16 + 15) / G, t_last);
+  const int pos_a = pos_base + min(tok_a, t_last), pos_b = pos_base + min(tok_b, t_last);
+  const int pmax = pos_base + min(t0 + (warp * 16 + 15) / G, t_last);
   // key j is visible to a row at position p iff lo < j <= p (lo = p - window, or -1)
   const int lo_a = a.window > 0 ? pos_a - a.window : -1, lo_b = a.window > 0 ? pos_b - a.window : -1;
 
@@ -422,7 +431,7 @@ cudaError_t launch_fa_h(int G, const CUtensorMap& km, const CUtensorMap& vm, con
 cudaError_t launch_attn_prefill(int hd, int G, const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a,
                                 cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
-  if (a.seq_fixed < 0) return cudaErrorInvalidValue;
+  if (a.seq_fixed < 0 && a.seq_idx == nullptr) return cudaErrorInvalidValue;
   return hd == 128 ? launch_fa_h<128>(G, kmap, vmap, a, s) : launch_fa_h<64>(G, kmap, vmap, a, s);
 }
 

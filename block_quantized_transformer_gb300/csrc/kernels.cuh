@@ -148,6 +148,7 @@ cudaError_t launch_tcgemm(int wtype, const TcGemmArgs& a, cudaStream_t s);
 // ---- attention side (attn.cu)
 struct CacheView {
   int max_ctx;               // slots per sequence (contiguous) or tokens per sequence (paged)
+  int max_seq;               // sequences: cache slots (contiguous) or block-table rows (paged)
   int n_kv;
   int page_size;             // 0: contiguous [seq][n_kv][max_ctx][hd]; else pages [page][n_kv][page_size][hd]
   int n_pages;
@@ -205,7 +206,24 @@ struct AttnArgs {
   const float* gk;
   float eps;
   int window;                // > 0: keys j with slot - window < j <= slot only (sliding window)
+  // rows of a mixed step (seq_idx set): the blocks of kFlashRows / G rows that
+  // rows_uniform accepts are attn_prefill's; the row-wise kernel skips them
+  int flash_rows;
 };
+
+// Query rows per attn_prefill CTA (query tokens x the G heads of a KV head).
+constexpr int kFlashRows = 128;
+
+// Rows t0 .. t0 + n - 1 of a mixed step are consecutive positions of one
+// sequence, all inside the cache.  Every lane of the calling warp gets the same
+// answer.
+__device__ __forceinline__ bool rows_uniform(const int32_t* seq, const int32_t* pos, int t0, int n,
+                                             const CacheView& c) {
+  const int s0 = seq[t0], p0 = pos[t0];
+  bool ok = s0 >= 0 && s0 < c.max_seq && p0 >= 0 && p0 + n <= c.max_ctx;
+  for (int i = (int)(threadIdx.x & 31u); i < n; i += 32) ok = ok && seq[t0 + i] == s0 && pos[t0 + i] == p0 + i;
+  return __all_sync(0xffffffffu, ok);
+}
 
 cudaError_t launch_rope_append(int kvtype, int hd, const RopeArgs& a, cudaStream_t s);
 // prefill attention over an f16 cache (attn_prefill.cu): T query rows of one

@@ -201,9 +201,14 @@ TQ_API tq_status tq_decode_step(tq_model* m, int32_t batch, const int32_t* token
  * and single-token steps are the same forward pass over different rows;
  * "PyTensor Beyond PyMC", section "What the current speed tells us": paged
  * cache and continuous batching).  Row t is token tokens_dev[t] of the
- * sequence in block-table row (paged cache) or cache slot (contiguous)
- * row_seq_dev[t], at position and cache index row_pos_dev[t]; it appends its
- * K/V there and attends over indices 0 .. row_pos_dev[t] of its sequence.  A
+ * sequence in block-table row (paged cache: block_table_dev is
+ * [max_batch][max_ctx / page_size]) or cache slot (contiguous)
+ * row_seq_dev[t] in [0, max_batch), at position and cache index
+ * row_pos_dev[t]; it appends its K/V there and attends over indices
+ * 0 .. row_pos_dev[t] of its sequence.  Where rows t0 .. t0 + 128/G - 1 (t0 a
+ * multiple of 128/G, G query heads per KV head) are consecutive positions of
+ * one sequence, an f16 cache's attention runs them as one flash-attention
+ * block, as in tq_prefill; other rows attend one by one.  A
  * sequence's rows must come in ascending position order with no gaps after
  * what its cache already holds.  For each sequence b < n_seq, last_row_dev[b]
  * is the row whose logits / greedy token are produced:
@@ -213,8 +218,8 @@ TQ_API tq_status tq_decode_step(tq_model* m, int32_t batch, const int32_t* token
  * block-table row; freeing them (and reusing them for a new sequence, which
  * overwrites from position 0) is bookkeeping on the host.  Refused when
  * n_rows < 1 or > max_prefill, n_seq < 1 or > max_batch or > n_rows.
- * Device-side range errors (a bad token, position, page or last row) set
- * status bits. */
+ * Device-side range errors (a bad token, sequence index, position, page or
+ * last row) set status bits and skip the access. */
 TQ_API tq_status tq_step(tq_model* m, int32_t n_rows, const int32_t* tokens_dev, const int32_t* row_seq_dev,
                          const int32_t* row_pos_dev, int32_t n_seq, const int32_t* last_row_dev,
                          const int32_t* block_table_dev, float* logits_dev, int32_t* argmax_dev, void* stream);
@@ -375,9 +380,13 @@ TQ_API tq_status tq_lm_head(int32_t wtype, tq_qmat w, int32_t vocab, int32_t hid
  *                   the first kept token whose cumulative renormalised
  *                   probability exceeds u (the caller owns the randomness);
  *  out_dev:         [batch] int32 token ids.
- * Each probability is an f32 exp, the sums are f64; a draw whose u lies
- * within that rounding of a cumulative sum may fall on the neighbouring
- * token.  Refused when
+ * Each unnormalised probability is an f32 exp2 of (l - max) log2(e) / T,
+ * held as an integer multiple of 2^-(62 - ceil(log2 vocab)) of the largest,
+ * and the cumulative sums are exact integer sums (the same token for the
+ * same inputs, whatever the timing); a draw whose u lies within the f32
+ * exp's rounding of a cumulative sum may fall on the neighbouring token.  A
+ * row whose largest logit is +inf is decoded greedily; a NaN top_p keeps
+ * every token, a NaN u reads as 0.  Refused when
  * batch < 1, vocab < 1 or vocab > 2^24, or a pointer is NULL. */
 TQ_API tq_status tq_sample(const float* logits_dev, int32_t batch, int32_t vocab, const float* temperature_dev,
                            const float* top_p_dev, const float* u_dev, int32_t* out_dev, void* stream);

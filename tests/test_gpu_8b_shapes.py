@@ -78,20 +78,16 @@ def _page_table(lens, extra, P):
     return table, n_pages, per_seq
 
 
-def test_qwen3_8b_shape_batched32_paged_ragged(weights):
-    host, dev = weights
-    steps = 4
+def _seeded_contexts(lens, table, n_pages):
+    """Seeded f16 K/V of every cached position, written identically to the
+    paged device layout [layer][page][kv head][slot][hd] (host tensors) and to
+    the oracle's per-sequence caches ([layer] -> (K, V) of [nkv][len][hd])."""
     w = WB
     B, P, L, nkv, hd = w.batch, w.page_size, w.n_layers, w.n_kv_heads, w.head_dim
-    lens = w.context_lengths().astype(np.int64)
-    assert len(lens) == 32 and lens.min() >= 512 and lens.max() <= 8192
-    table, n_pages, per_seq = _page_table(lens, steps + 1, P)
-
-    # seeded f16 contexts: K and V of layer l, sequence b, [nkv][len][hd]
     caches = []
     kc = torch.zeros(L, n_pages, nkv, P, hd, dtype=torch.float16)
     vc = torch.zeros(L, n_pages, nkv, P, hd, dtype=torch.float16)
-    for b in range(B):
+    for b in range(len(lens)):
         n = int(lens[b])
         npg = (n + P - 1) // P
         per_layer = []
@@ -102,12 +98,27 @@ def test_qwen3_8b_shape_batched32_paged_ragged(weights):
                 x = synth.host_normal(w.seed, stream, nkv * n * hd, sigma=1.0).astype(np.float16)
                 x = x.reshape(nkv, n, hd)
                 kv.append(x.astype(np.float32))
+                if n == 0:
+                    continue
                 pad = np.zeros((nkv, npg * P, hd), dtype=np.float16)
                 pad[:, :n] = x
                 pages = torch.from_numpy(pad.reshape(nkv, npg, P, hd).transpose(1, 0, 2, 3).copy())
                 dst[l, torch.from_numpy(table[b, :npg]).long()] = pages
             per_layer.append((kv[0], kv[1]))
         caches.append(per_layer)
+    return kc, vc, caches
+
+
+def test_qwen3_8b_shape_batched32_paged_ragged(weights):
+    host, dev = weights
+    steps = 4
+    w = WB
+    B, P, L, nkv, hd = w.batch, w.page_size, w.n_layers, w.n_kv_heads, w.head_dim
+    lens = w.context_lengths().astype(np.int64)
+    assert len(lens) == 32 and lens.min() >= 512 and lens.max() <= 8192
+    table, n_pages, per_seq = _page_table(lens, steps + 1, P)
+
+    kc, vc, caches = _seeded_contexts(lens, table, n_pages)
 
     # oracle: each sequence on its own cache, greedy from a seeded first token
     ref = om.OracleModel(w, host, dtype=np.float32)
@@ -146,3 +157,70 @@ def test_qwen3_8b_shape_batched32_paged_ragged(weights):
         assert max(errs) <= TOL, (b, int(lens[b]), max(errs), int(np.argmax(errs)))
         check_tokens(got_t[b], ref_logits[b], TOL)
     print(f"8B-shape batched 32 paged: max rel logit err {worst:.3e}")
+
+
+def test_qwen3_8b_shape_mixed_step_paged(weights):
+    """Continuous batching at the 8B shape: one tq_step over 8 decode rows of
+    the batched mix's first 8 sequences, a 249-row prompt chunk of a sequence
+    with 320 cached positions and a 40-row prompt from position 0 (297 rows:
+    the GEMMs take two 256-row token tiles, the second ragged), then one step
+    in which all 10 sequences decode; each sequence's rows are compared with
+    the oracle running that sequence alone on the same cache."""
+    host, dev = weights
+    w = WB
+    P = w.page_size
+    dec = w.context_lengths().astype(np.int64)[:8]
+    chunk_a, cached_a, chunk_b = 249, 320, 40
+    lens = np.concatenate([dec, [cached_a, 0]]).astype(np.int64)
+    S = len(lens)
+    table, n_pages, per_seq = _page_table(lens, chunk_a + 2, P)
+    kc, vc, caches = _seeded_contexts(lens, table, n_pages)
+    first = synth.uniform_below(w.seed, synth.PROMPT_STREAM + 100, S, w.vocab)
+    feeds = [[int(first[b])] for b in range(8)]
+    feeds.append(list(synth.uniform_below(w.seed, synth.PROMPT_STREAM + 101, chunk_a, w.vocab)))
+    feeds.append(list(synth.uniform_below(w.seed, synth.PROMPT_STREAM + 102, chunk_b, w.vocab)))
+
+    ref = om.OracleModel(w, host, dtype=np.float32)
+    ref_l = [[] for _ in range(S)]
+    nxt = []
+    for b in range(S):
+        lg = ref.forward(feeds[b], caches[b], int(lens[b]))
+        ref_l[b].append(lg)
+        nxt.append(om.argmax(lg))
+    for b in range(S):                                 # step 2: every sequence decodes its greedy token
+        ref_l[b].append(ref.forward([nxt[b]], caches[b], int(lens[b]) + len(feeds[b])))
+
+    n_rows = sum(len(f) for f in feeds)
+    model = build_model(w, device=DEV, max_batch=S, max_ctx=per_seq * P, max_prefill=n_rows,
+                        page_size=P, n_pages=n_pages, weights=dev)
+    model.k_cache.copy_(kc.reshape(-1))
+    model.v_cache.copy_(vc.reshape(-1))
+    del kc, vc
+    bt = torch.from_numpy(table).to(DEV)
+    got_l = [[] for _ in range(S)]
+    got_t = [[] for _ in range(S)]
+    steps = [[(b, feeds[b], int(lens[b])) for b in range(S)],
+             [(b, [nxt[b]], int(lens[b]) + len(feeds[b])) for b in range(S)]]
+    for rows in steps:
+        tok, seq, pos, last = [], [], [], []
+        for b, toks, p0 in rows:
+            tok += [int(t) for t in toks]
+            seq += [b] * len(toks)
+            pos += list(range(p0, p0 + len(toks)))
+            last.append(len(tok) - 1)
+        i32 = lambda v: torch.tensor(v, dtype=torch.int32, device=DEV)
+        lg = torch.empty(S, w.vocab, dtype=torch.float32, device=DEV)
+        am = model.step(i32(tok), i32(seq), i32(pos), i32(last), block_table=bt, logits=lg)
+        lg_h, am_h = lg.double().cpu().numpy(), am.cpu().numpy()
+        for b in range(S):
+            got_l[b].append(lg_h[b])
+            got_t[b].append(int(am_h[b]))
+    assert model.status() == 0
+    model.close()
+    worst = 0.0
+    for b in range(S):
+        errs = [rel_logit_err(g, r) for g, r in zip(got_l[b], ref_l[b])]
+        worst = max(worst, max(errs))
+        assert max(errs) <= TOL, (b, int(lens[b]), max(errs), int(np.argmax(errs)))
+        check_tokens(got_t[b], ref_l[b], TOL)
+    print(f"8B-shape mixed step ({n_rows} rows, {S} sequences): max rel logit err {worst:.3e}")

@@ -80,3 +80,25 @@ def test_continuous_batching_f32_cache():
     w = dataclasses.replace(synth.TINY, name="tiny_batching_f32")
     worst = _scenario(w, 2e-3)
     print(f"continuous batching f32: max rel logit err {worst:.3e}")
+
+
+@pytest.mark.parametrize("kv", ["f16", "f32"])
+def test_bad_sequence_index_sets_status_and_poisons(kv):
+    """A row whose sequence index lies outside [0, max_batch) touches no
+    cache row of another sequence and nothing out of bounds: its K/V are not
+    appended, its attention reads stay inside the cache, and the step sets the
+    out-of-range status bit, which poisons the model."""
+    import block_quantized_transformer_gb300 as tq
+    w = dataclasses.replace(synth.TINY, kv=kv)
+    model = build_model(w, device=DEV, max_batch=2, max_ctx=64, max_prefill=48, page_size=32, n_pages=4)
+    n = 34
+    tok = torch.ones(n, dtype=torch.int32, device=DEV)
+    seq = torch.zeros(n, dtype=torch.int32, device=DEV)
+    seq[-1] = 7
+    pos = torch.arange(n, dtype=torch.int32, device=DEV)
+    pos[-1] = 0
+    last = torch.tensor([n - 2, n - 1], dtype=torch.int32, device=DEV)
+    bt = torch.tensor([[0, 1], [2, 3]], dtype=torch.int32, device=DEV)
+    model.step(tok, seq, pos, last, block_table=bt)
+    with pytest.raises(tq.TqPoisoned, match="out of range"):
+        model.status()
