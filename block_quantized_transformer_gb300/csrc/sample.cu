@@ -17,22 +17,29 @@
 // token whose mass rounds to 0 is never the first to reach a target >= 1 and
 // is skipped everywhere.
 //
-// One CTA per row, no sort of the row:
-//  1. the row's largest logit;
+// One thread-block cluster per row (up to 16 CTAs at batch 1, fewer as the
+// batch fills the GPU), each CTA over its own slice of the row; no sort of
+// the row:
+//  1. the row's largest logit (each rank's maximum pushed to every rank);
 //  2. a histogram of masses and counts over 2048 bins of d (32 per halving of
 //     the mass): each bin is a contiguous run of the descending order, and
 //     the tokens spread over many bins, so the shared-memory atomics seldom
 //     meet (a radix histogram over the logits' leading bits puts nearly every
 //     token in two or three bins);
-//  3. a prefix sum over the bins finds the bin in which the cumulative mass
-//     reaches the cutoff; that bin's tokens are gathered into shared memory,
-//     sorted by (logit descending, index ascending) and summed in that order,
-//     which gives the cutoff token and the kept mass exactly;
+//     each rank bins its slice, then sums one share of the bins over all
+//     ranks (distributed shared memory) into rank 0;
+//  3. on rank 0, a prefix sum over the bins finds the bin in which the
+//     cumulative mass reaches the cutoff; every rank appends that bin's tokens
+//     of its slice to rank 0's list, which rank 0 sorts by (logit descending,
+//     index ascending) and sums in that order: the cutoff token and the kept
+//     mass, exactly;
 //  4. the same for the draw (the sorted bin is reused when the draw falls in
 //     it).
-// A bin of more than kCap tokens is resolved by a radix select over the
-// bin's logit keys, then over the indices of the tie group that holds the
-// target, with warp-aggregated counts.  The row is read once per pass (three
+// Every rank passes the same seven cluster barriers; what the ranks do
+// between them is decided on rank 0 and pushed to every rank first.
+// A bin of more than kCap tokens is resolved on rank 0 alone by a radix select
+// over the bin's logit keys, then over the indices of the tie group that holds
+// the target, with warp-aggregated counts.  The row is read once per pass (three
 // or four passes in the common case), each thread with four 16-byte loads in
 // flight.
 #include <cooperative_groups.h>
@@ -52,6 +59,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;      // bins of d, 32 per halving of the mass
 constexpr int kCap = 4096;       // tokens of one bin sorted in shared memory
 constexpr int kNone = 256;       // "no digit" label of the radix fallback
+constexpr int kMaxCluster = 16;  // CTAs per row at most
 typedef unsigned long long u64;
 
 struct Smem {
@@ -68,6 +76,13 @@ struct Smem {
   u64 found_cum;
   unsigned prefix;
   u64 above;
+  // cluster: rank 0's merged histogram, and what each rank receives
+  u64 mcum[kBins];       // merged bin masses, then their inclusive prefix sums
+  unsigned mcnt[kBins];
+  float fin[kMaxCluster];             // every rank's largest logit
+  unsigned long long kin[kMaxCluster];  // every rank's argmax key (greedy)
+  int ctl_bin, ctl_mode;              // the cutoff bin; 0: gather it, 1: rank 0 alone
+  int ctl2_bin, ctl2_need;            // the draw bin; 1: gather it
 };
 
 // d -> bin: d * 32 rounded to an integer through the f32 mantissa (monotone
@@ -91,49 +106,49 @@ __device__ __forceinline__ u64 mass_fix(float d, int F) {
   return (m + (1ull << (-sh - 1))) >> (-sh);
 }
 
-// Calls fn(i, l, ok) for every token of the row, warp-uniformly (every
-// thread makes the same number of calls; ok is false for padding), with
-// kU float4 loads of each thread in flight before any is used (a pass is
-// bound by load latency otherwise); rows that are not 16-byte aligned are
-// read as scalars, kU * 4 at a time.
+// Calls fn(i, l, ok) for every token i in [lo, hi) of the row, warp-uniformly
+// (every thread makes the same number of calls; ok is false for padding),
+// with kU float4 loads of each thread in flight before any is used (a pass is
+// bound by load latency otherwise).  lo is a multiple of 4; rows that are not
+// 16-byte aligned are read as scalars, kU * 4 at a time.
 constexpr int kU = 4;
 template <typename Fn>
-__device__ __forceinline__ void walk_row(const float* row, int V, Fn&& fn) {
+__device__ __forceinline__ void walk_row(const float* row, int lo, int hi, Fn&& fn) {
   const int tid = threadIdx.x;
   if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0u) {
-    const int V4 = V >> 2;
+    const int j_lo = lo >> 2, j_hi = hi >> 2;
     const float4* r4 = reinterpret_cast<const float4*>(row);
-    for (int j0 = 0; j0 < V4; j0 += kThreads * kU) {
+    for (int j0 = j_lo; j0 < j_hi; j0 += kThreads * kU) {
       float4 v[kU];
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int j = j0 + u * kThreads + tid;
-        v[u] = j < V4 ? __ldg(r4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u] = j < j_hi ? __ldg(r4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int j = j0 + u * kThreads + tid;
-        const bool ok = j < V4;
+        const bool ok = j < j_hi;
         fn(4 * j, v[u].x, ok);
         fn(4 * j + 1, v[u].y, ok);
         fn(4 * j + 2, v[u].z, ok);
         fn(4 * j + 3, v[u].w, ok);
       }
     }
-    const int i = 4 * V4 + tid;  // the last V % 4 tokens
-    fn(i, i < V ? __ldg(row + i) : 0.f, i < V);
+    const int i = 4 * j_hi + tid;  // hi % 4 tokens past the last whole float4
+    fn(i, i < hi ? __ldg(row + i) : 0.f, i < hi);
   } else {
-    for (int i0 = 0; i0 < V; i0 += kThreads * 4 * kU) {
+    for (int i0 = lo; i0 < hi; i0 += kThreads * 4 * kU) {
       float v[4 * kU];
 #pragma unroll
       for (int u = 0; u < 4 * kU; ++u) {
         const int i = i0 + u * kThreads + tid;
-        v[u] = i < V ? __ldg(row + i) : 0.f;
+        v[u] = i < hi ? __ldg(row + i) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < 4 * kU; ++u) {
         const int i = i0 + u * kThreads + tid;
-        fn(i, v[u], i < V);
+        fn(i, v[u], i < hi);
       }
     }
   }
@@ -179,13 +194,14 @@ __device__ void block_scan(u64* a, int n, u64* wsum) {
   __syncthreads();
 }
 
-// The bin in which the inclusive cumulative mass first reaches T (1 <= T <= Z).
-__device__ int find_bin(Smem& sm, u64 T) {
+// The bin in which the inclusive cumulative mass (prefix sums `cum`) first
+// reaches T (1 <= T <= Z).
+__device__ int find_bin(Smem& sm, const u64* cum, u64 T) {
   if (threadIdx.x == 0) sm.found = kBins - 1;
   __syncthreads();
   for (int b = threadIdx.x; b < kBins; b += kThreads) {
-    const u64 lo = b > 0 ? sm.cum[b - 1] : 0ull;
-    if (lo < T && T <= sm.cum[b]) sm.found = b;  // at most one bin qualifies
+    const u64 lo = b > 0 ? cum[b - 1] : 0ull;
+    if (lo < T && T <= cum[b]) sm.found = b;  // at most one bin qualifies
   }
   __syncthreads();
   const int r = sm.found;
@@ -198,13 +214,12 @@ struct Pick {
   u64 cum;  // inclusive cumulative mass at the picked token
 };
 
-// Gather the tokens of bin `bin` into shared memory, sort them by (logit
-// descending, index ascending) and prefix-sum their masses.
-__device__ void gather_sort(Smem& sm, const float* row, int V, float lmax, float sc, int F, int bin, int n) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  if (tid == 0) sm.n_list = 0;
-  __syncthreads();
-  walk_row(row, V, [&](int i, float l, bool ok) {
+// Append the tokens of bin `bin` in [lo, hi) of the row to dst's list (this
+// CTA's shared memory or rank 0's, through the cluster window): one atomic
+// per warp reserves the warp's slots.
+__device__ void gather(Smem* dst, const float* row, int lo, int hi, float lmax, float sc, int F, int bin) {
+  const int lane = threadIdx.x & 31;
+  walk_row(row, lo, hi, [&](int i, float l, bool ok) {
     bool hit = false;
     if (ok) {
       const float d = (lmax - l) * sc;
@@ -214,28 +229,57 @@ __device__ void gather_sort(Smem& sm, const float* row, int V, float lmax, float
     if (ball != 0u) {
       const int leader = __ffs(ball) - 1;
       int base = 0;
-      if (lane == leader) base = atomicAdd(&sm.n_list, __popc(ball));
+      if (lane == leader) base = atomicAdd(&dst->n_list, __popc(ball));
       base = __shfl_sync(0xffffffffu, base, leader);
       const int at = base + __popc(ball & ((1u << lane) - 1u));
-      if (hit && at < kCap) sm.list[at] = ((u64)(~float_order_key(l)) << 32) | (u64)(uint32_t)i;
+      if (hit && at < kCap) dst->list[at] = ((u64)(~float_order_key(l)) << 32) | (u64)(uint32_t)i;
     }
   });
-  __syncthreads();
+}
+
+// Sort this CTA's list of n <= kCap gathered tokens by (logit descending,
+// index ascending) and prefix-sum their masses.
+__device__ void sort_scan(Smem& sm, const float* row, float lmax, float sc, int F, int n) {
+  const int tid = threadIdx.x;
   int m = 2;
   while (m < n) m <<= 1;
   for (int i = n + tid; i < m; i += kThreads) sm.list[i] = ~0ull;
   __syncthreads();
-  for (int k = 2; k <= m; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int t = tid; t < m / 2; t += kThreads) {
-        const int i = (t / j) * 2 * j + (t % j), p = i + j;
-        const u64 a = sm.list[i], b = sm.list[p];
-        if ((a > b) == ((i & k) == 0)) {
-          sm.list[i] = b;
-          sm.list[p] = a;
+  if (m <= kThreads) {
+    // one element per thread: exchanges at distance < 32 by warp shuffles,
+    // the others through shared memory (a pair (i, i ^ j) keeps its smaller
+    // key at i in an ascending run, at i ^ j in a descending one)
+    u64 v = tid < m ? sm.list[tid] : ~0ull;
+    for (int k = 2; k <= m; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        u64 o;
+        if (j >= 32) {
+          if (tid < m) sm.list[tid] = v;
+          __syncthreads();
+          o = tid < m ? sm.list[tid ^ j] : v;
+          __syncthreads();
+        } else {
+          o = __shfl_xor_sync(0xffffffffu, v, j);
         }
+        const bool keep_min = ((tid & j) == 0) == ((tid & k) == 0);
+        v = keep_min ? (o < v ? o : v) : (o > v ? o : v);
       }
-      __syncthreads();
+    }
+    if (tid < m) sm.list[tid] = v;
+    __syncthreads();
+  } else {
+    for (int k = 2; k <= m; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int t = tid; t < m / 2; t += kThreads) {
+          const int i = (t / j) * 2 * j + (t % j), p = i + j;
+          const u64 a = sm.list[i], b = sm.list[p];
+          if ((a > b) == ((i & k) == 0)) {
+            sm.list[i] = b;
+            sm.list[p] = a;
+          }
+        }
+        __syncthreads();
+      }
     }
   }
   for (int i = tid; i < n; i += kThreads) {
@@ -244,8 +288,6 @@ __device__ void gather_sort(Smem& sm, const float* row, int V, float lmax, float
   }
   __syncthreads();
   block_scan<kCap / kThreads>(sm.lcum, n, sm.wsum);
-  if (tid == 0) sm.list_bin = bin;
-  __syncthreads();
 }
 
 // Radix fallback for a bin too large to sort: the key (8 bits a level, top
@@ -267,7 +309,7 @@ __device__ Pick radix_pick(Smem& sm, const float* row, int V, float lmax, float 
     }
     __syncthreads();
     const uint32_t prefix = sm.prefix;
-    walk_row(row, V, [&](int i, float l, bool ok) {
+    walk_row(row, 0, V, [&](int i, float l, bool ok) {
       int dg = kNone;
       u64 mf = 0ull;
       if (ok) {
@@ -330,7 +372,7 @@ __device__ Pick radix_pick(Smem& sm, const float* row, int V, float lmax, float 
     for (int k = tid; k < 256; k += kThreads) sm.dcnt[k] = 0u;
     __syncthreads();
     const uint32_t prefix = sm.prefix;
-    walk_row(row, V, [&](int i, float l, bool ok) {
+    walk_row(row, 0, V, [&](int i, float l, bool ok) {
       int dg = kNone;
       if (ok && float_order_key(l) == K &&
           (shift == 16 || ((uint32_t)i >> (shift + 8)) == (prefix >> (shift + 8))))
@@ -363,19 +405,9 @@ __device__ Pick radix_pick(Smem& sm, const float* row, int V, float lmax, float 
   return p;
 }
 
-// The first token (in the order) whose inclusive cumulative mass reaches T.
-__device__ Pick pick(Smem& sm, const float* row, int V, float lmax, float sc, int F, u64 T) {
-  const int bin = find_bin(sm, T);
-  const u64 base = bin > 0 ? sm.cum[bin - 1] : 0ull;
-  const int n = (int)sm.cnt[bin];
-  if (n == 0) {  // no bin holds the target (not reachable for 1 <= T <= Z)
-    Pick p;
-    p.index = -1;
-    p.cum = base;
-    return p;
-  }
-  if (n > kCap) return radix_pick(sm, row, V, lmax, sc, F, bin, base, T);
-  if (sm.list_bin != bin) gather_sort(sm, row, V, lmax, sc, F, bin, n);
+// The first token of the sorted list (n tokens of one bin, `base` the mass
+// before the bin) whose inclusive cumulative mass reaches T.
+__device__ Pick pick_list(Smem& sm, int n, u64 base, u64 T) {
   if (threadIdx.x == 0) {
     sm.found = n - 1;
     sm.found_cum = base + (n > 0 ? sm.lcum[n - 1] : 0ull);
@@ -391,36 +423,55 @@ __device__ Pick pick(Smem& sm, const float* row, int V, float lmax, float sc, in
   }
   __syncthreads();
   Pick p;
-  p.index = (int)(uint32_t)(sm.list[sm.found] & 0xFFFFFFFFull);
+  p.index = n > 0 ? (int)(uint32_t)(sm.list[sm.found] & 0xFFFFFFFFull) : -1;
   p.cum = sm.found_cum;
   __syncthreads();
   return p;
 }
 
-__global__ void __launch_bounds__(kThreads) sample_kernel(const float* logits, int V, const float* temperature,
-                                                           const float* top_p, const float* u, int32_t* out) {
+template <int CL>
+__global__ void __launch_bounds__(kThreads, 1) sample_kernel(const float* logits, int V, const float* temperature,
+                                                              const float* top_p, const float* u, int32_t* out) {
+  // every CTA of the cluster has started before any of them touches another's
+  // shared memory: arrive here, wait before the first remote store
+  cluster_arrive_relaxed();
   grid_dep_launch();
   grid_dep_wait();
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
-  const int b = blockIdx.x, tid = threadIdx.x;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  Smem* s0 = cluster.map_shared_rank(&sm, 0u);  // rank 0's shared memory
+  const int b = blockIdx.y, tid = threadIdx.x;
   const float* row = logits + (int64_t)b * V;
+  // this rank's slice: whole float4 groups, the last rank also takes the tail
+  const int G4 = V >> 2;
+  const int i_lo = 4 * (int)((int64_t)G4 * rank / CL);
+  const int i_hi = rank == CL - 1 ? V : 4 * (int)((int64_t)G4 * (rank + 1) / CL);
   const float T = temperature[b];
 
+  // 1. the largest logit, pushed to every rank
   float mx = -3.402823466e38f;
-  walk_row(row, V, [&](int, float l, bool ok) {
+  walk_row(row, i_lo, i_hi, [&](int, float l, bool ok) {
     if (ok) mx = fmaxf(mx, l);
   });
   mx = warp_max(mx);
   if ((tid & 31) == 0) sm.fred[tid >> 5] = mx;
   __syncthreads();
-  float lmax = sm.fred[0];
-  for (int w = 1; w < kWarps; ++w) lmax = fmaxf(lmax, sm.fred[w]);
+  cluster_wait();
+  if (tid < CL) {
+    float m = sm.fred[0];
+    for (int w = 1; w < kWarps; ++w) m = fmaxf(m, sm.fred[w]);
+    cluster.map_shared_rank(&sm, (unsigned)tid)->fin[rank] = m;
+  }
+  cluster.sync();  // barrier 1
+  float lmax = sm.fin[0];
+  for (int r = 1; r < CL; ++r) lmax = fmaxf(lmax, sm.fin[r]);
 
   if (!(T > 0.f) || !(lmax <= 3.402823466e38f)) {
     // greedy (also for a row whose largest logit is +inf): lowest index of the largest logit
     unsigned long long best = 0ull;
-    walk_row(row, V, [&](int i, float l, bool ok) {
+    walk_row(row, i_lo, i_hi, [&](int i, float l, bool ok) {
       const unsigned long long k = ok ? argmax_key(l, (uint32_t)i) : 0ull;
       best = k > best ? k : best;
     });
@@ -434,6 +485,12 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const float* logits, i
     if (tid == 0) {
       unsigned long long m = sm.best[0];
       for (int w = 1; w < kWarps; ++w) m = sm.best[w] > m ? sm.best[w] : m;
+      s0->kin[rank] = m;
+    }
+    cluster.sync();  // the greedy path's only other barrier
+    if (rank == 0 && tid == 0) {
+      unsigned long long m = sm.kin[0];
+      for (int r = 1; r < CL; ++r) m = sm.kin[r] > m ? sm.kin[r] : m;
       out[b] = (int32_t)argmax_key_index(m);
     }
     return;
@@ -441,14 +498,17 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const float* logits, i
   const float sc = 1.4426950408889634f / T;  // log2(e) / T
   const int F = 62 - (V > 1 ? 32 - __clz(V - 1) : 0);
 
-  // histogram of masses and counts over the bins of d
+  // 2. this slice's histogram of masses and counts over the bins of d
   for (int k = tid; k < kBins; k += kThreads) {
     sm.cum[k] = 0ull;
     sm.cnt[k] = 0u;
   }
-  if (tid == 0) sm.list_bin = -1;
+  if (tid == 0) {
+    sm.list_bin = -1;
+    sm.n_list = 0;
+  }
   __syncthreads();
-  walk_row(row, V, [&](int, float l, bool ok) {
+  walk_row(row, i_lo, i_hi, [&](int, float l, bool ok) {
     const float d = (lmax - l) * sc;
     const u64 mf = ok ? mass_fix(d, F) : 0ull;
     if (mf != 0ull) {
@@ -457,40 +517,174 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const float* logits, i
       atomicAdd(&sm.cnt[k], 1u);
     }
   });
-  __syncthreads();
-  block_scan<kBins / kThreads>(sm.cum, kBins, sm.wsum);
-  const u64 Z = sm.cum[kBins - 1];  // >= 2^F: the largest logit's mass is 1
+  cluster.sync();  // barrier 2: every slice's histogram is complete
+  // this rank's share of the bins, summed over the ranks, into rank 0
+  for (int k = kBins * rank / CL + tid; k < kBins * (rank + 1) / CL; k += kThreads) {
+    u64 m = 0ull;
+    unsigned c = 0u;
+    for (int r = 0; r < CL; ++r) {
+      const Smem* sr = cluster.map_shared_rank(&sm, (unsigned)r);
+      m += sr->cum[k];
+      c += sr->cnt[k];
+    }
+    s0->mcum[k] = m;
+    s0->mcnt[k] = c;
+  }
+  cluster.sync();  // barrier 3: rank 0 holds the whole histogram
 
-  // cutoff: the first token whose cumulative mass reaches ceil(top_p Z)
-  float tp = top_p[b];
-  if (!(tp < 1.f)) tp = 1.f;  // also NaN
-  if (!(tp > 0.f)) tp = 0.f;
-  u64 Tc = (u64)ceil((double)tp * (double)Z);
-  Tc = Tc < 1ull ? 1ull : Tc > Z ? Z : Tc;
-  const Pick c = pick(sm, row, V, lmax, sc, F, Tc);
-
-  // the draw: the first kept token whose cumulative mass exceeds u * kept
-  float uu = u[b];
-  if (!(uu > 0.f)) uu = 0.f;  // also NaN
-  u64 Td = (u64)floor((double)uu * (double)c.cum) + 1ull;
-  Td = Td > c.cum ? c.cum : Td;
-  const Pick d = pick(sm, row, V, lmax, sc, F, Td);
-  if (tid == 0) out[b] = d.index >= 0 && d.index < V ? d.index : c.index >= 0 && c.index < V ? c.index : 0;
+  // 3. the cutoff: the first token whose cumulative mass reaches ceil(top_p Z)
+  Pick cut, draw;
+  cut.index = draw.index = -1;
+  cut.cum = draw.cum = 0ull;
+  int c_bin = 0;
+  u64 c_base = 0ull;
+  if (rank == 0) {
+    block_scan<kBins / kThreads>(sm.mcum, kBins, sm.wsum);
+    const u64 Z = sm.mcum[kBins - 1];  // >= 2^F: the largest logit's mass is 1
+    float tp = top_p[b];
+    if (!(tp < 1.f)) tp = 1.f;  // also NaN
+    if (!(tp > 0.f)) tp = 0.f;
+    u64 Tc = (u64)ceil((double)tp * (double)Z);
+    Tc = Tc < 1ull ? 1ull : Tc > Z ? Z : Tc;
+    c_bin = find_bin(sm, sm.mcum, Tc);
+    c_base = c_bin > 0 ? sm.mcum[c_bin - 1] : 0ull;
+    if (tid == 0) {
+      sm.found_cum = Tc;  // kept for rank 0's own use after the gather
+      const int mode = sm.mcnt[c_bin] > (unsigned)kCap ? 1 : 0;
+      for (int r = 0; r < CL; ++r) {
+        Smem* sr = cluster.map_shared_rank(&sm, (unsigned)r);
+        sr->ctl_bin = c_bin;
+        sr->ctl_mode = mode;
+      }
+    }
+  }
+  cluster.sync();  // barrier 4: every rank knows the cutoff bin
+  const int mode = sm.ctl_mode;
+  if (mode == 0) gather(s0, row, i_lo, i_hi, lmax, sc, F, sm.ctl_bin);
+  cluster.sync();  // barrier 5: rank 0's list holds the cutoff bin
+  int need2 = 0;
+  if (rank == 0) {
+    const u64 Tc = sm.found_cum;
+    if (mode == 0) {
+      const int n = min(sm.n_list, kCap);
+      sort_scan(sm, row, lmax, sc, F, n);
+      cut = pick_list(sm, n, c_base, Tc);
+    } else {
+      cut = radix_pick(sm, row, V, lmax, sc, F, c_bin, c_base, Tc);
+    }
+    // 4. the draw: the first kept token whose cumulative mass exceeds u * kept
+    float uu = u[b];
+    if (!(uu > 0.f)) uu = 0.f;  // also NaN
+    u64 Td = (u64)floor((double)uu * (double)cut.cum) + 1ull;
+    Td = Td > cut.cum ? cut.cum : Td;
+    const int d_bin = find_bin(sm, sm.mcum, Td);
+    const u64 d_base = d_bin > 0 ? sm.mcum[d_bin - 1] : 0ull;
+    if (d_bin == c_bin && mode == 0) {
+      draw = pick_list(sm, min(sm.n_list, kCap), d_base, Td);
+    } else if (sm.mcnt[d_bin] <= (unsigned)kCap) {
+      need2 = 1;  // gathered by every rank
+    } else {
+      draw = radix_pick(sm, row, V, lmax, sc, F, d_bin, d_base, Td);
+    }
+    if (tid == 0) {
+      sm.found_cum = Td;
+      sm.n_list = 0;
+      for (int r = 0; r < CL; ++r) {
+        Smem* sr = cluster.map_shared_rank(&sm, (unsigned)r);
+        sr->ctl2_bin = d_bin;
+        sr->ctl2_need = need2;
+      }
+    }
+  }
+  cluster.sync();  // barrier 6: every rank knows whether to gather the draw bin
+  if (sm.ctl2_need) gather(s0, row, i_lo, i_hi, lmax, sc, F, sm.ctl2_bin);
+  cluster.sync();  // barrier 7: rank 0's list holds the draw bin; no remote access after this
+  if (rank == 0) {
+    if (sm.ctl2_need) {
+      const int d_bin = sm.ctl2_bin;
+      const int n = min(sm.n_list, kCap);
+      sort_scan(sm, row, lmax, sc, F, n);
+      draw = pick_list(sm, n, d_bin > 0 ? sm.mcum[d_bin - 1] : 0ull, sm.found_cum);
+    }
+    if (tid == 0) out[b] = draw.index >= 0 && draw.index < V ? draw.index
+                           : cut.index >= 0 && cut.index < V ? cut.index : 0;
+  }
 }
 
 }  // namespace smp
 
+namespace {
+template <int CL>
+cudaError_t sample_setup() {
+  cudaError_t e = cudaFuncSetAttribute(smp::sample_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sizeof(smp::Smem));
+  if (e == cudaSuccess && CL > 8)
+    e = cudaFuncSetAttribute(smp::sample_kernel<CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+// Clusters of CL CTAs (one per SM) can be resident at once on this device.
+template <int CL>
+int sample_clusters() {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CL, 1, 1);
+  cfg.blockDim = dim3(smp::kThreads);
+  cfg.dynamicSmemBytes = sizeof(smp::Smem);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = CL;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, smp::sample_kernel<CL>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int CL>
+cudaError_t sample_launch(const float* logits, int batch, int V, const float* temperature, const float* top_p,
+                          const float* u, int32_t* out, cudaStream_t s) {
+  return launch_cluster(smp::sample_kernel<CL>, dim3(CL, batch, 1), dim3(smp::kThreads), sizeof(smp::Smem), CL, s,
+                        logits, V, temperature, top_p, u, out);
+}
+}  // namespace
+
 cudaError_t launch_sample(const float* logits, int batch, int V, const float* temperature, const float* top_p,
                           const float* u, int32_t* out, cudaStream_t s) {
   if (batch <= 0) return cudaSuccess;
+  // the largest cluster the device runs, and the SM count
   static PerDevice setup;
-  cudaError_t e = per_device(setup, nullptr, [](int, int&) {
-    return cudaFuncSetAttribute(smp::sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)sizeof(smp::Smem));
+  int caps = 0;
+  cudaError_t e = per_device(setup, &caps, [](int dev, int& v) {
+    cudaError_t r = sample_setup<1>();
+    if (r == cudaSuccess) r = sample_setup<2>();
+    if (r == cudaSuccess) r = sample_setup<4>();
+    if (r == cudaSuccess) r = sample_setup<8>();
+    if (r == cudaSuccess) r = sample_setup<16>();
+    if (r != cudaSuccess) return r;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = kNumSMs;
+    const int cl = sample_clusters<16>() > 0 ? 16 : sample_clusters<8>() > 0 ? 8 : sample_clusters<4>() > 0 ? 4
+                   : sample_clusters<2>() > 0 ? 2 : 1;
+    v = (sms << 8) | cl;
+    return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
-  return launch_k(smp::sample_kernel, dim3(batch), dim3(smp::kThreads), sizeof(smp::Smem), s, logits, V,
-                  temperature, top_p, u, out);
+  const int sms = caps >> 8, cl_max = caps & 255;
+  // rows x CTAs per row about the SM count: a row of one sequence gets up to 16 SMs
+  int cl = 1;
+  while (cl < cl_max && batch * cl * 2 <= sms) cl *= 2;
+  switch (cl) {
+    case 16: return sample_launch<16>(logits, batch, V, temperature, top_p, u, out, s);
+    case 8: return sample_launch<8>(logits, batch, V, temperature, top_p, u, out, s);
+    case 4: return sample_launch<4>(logits, batch, V, temperature, top_p, u, out, s);
+    case 2: return sample_launch<2>(logits, batch, V, temperature, top_p, u, out, s);
+  }
+  return sample_launch<1>(logits, batch, V, temperature, top_p, u, out, s);
 }
 
 }  // namespace tq

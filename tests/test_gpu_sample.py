@@ -26,8 +26,10 @@ def _run(logits, temps, top_ps, us):
     return tq.tq_sample(lg, t, p, u).cpu().numpy()
 
 
-def _check(logits, temps, top_ps, us, min_exact):
-    got = _run(logits, temps, top_ps, us)
+def _check(logits, temps, top_ps, us, min_exact, rows_per_call=None):
+    k = rows_per_call or len(temps)
+    got = np.concatenate([_run(logits[i:i + k], temps[i:i + k], top_ps[i:i + k], us[i:i + k])
+                          for i in range(0, len(temps), k)])
     exact = 0
     for r in range(len(temps)):
         row = logits[r].astype(np.float64)
@@ -59,6 +61,22 @@ def test_sample_vocab_151936_matches_oracle():
     temps = [[0.0, 0.7, 1.0, 1.6][i % 4] for i in range(n)]
     top_ps = [[0.95, 0.5, 1.0, 0.9, 0.05, 0.99][i % 6] for i in range(n)]
     _check(logits, temps, top_ps, list(us), min_exact=16)
+
+
+@pytest.mark.parametrize("rows_per_call", [1, 8, 32])
+def test_sample_vocab_151936_per_call_batch(rows_per_call):
+    """The same rows sampled 1, 8 and 32 to a call: one row is split across a
+    cluster of up to 16 CTAs, 32 rows across 4 each."""
+    V = 151936
+    n = 32 if rows_per_call > 1 else 8
+    base = synth.host_normal(11, 1, 4 * V, sigma=1.0).reshape(4, V)
+    base[1] *= 3.0
+    base[3] = np.round(base[3] * 4.0) / 4.0
+    logits = np.repeat(base, n // 4, axis=0)
+    us = synth.uniform_below(11, 5, n, 1 << 24).astype(np.float64) / float(1 << 24)
+    temps = [[0.0, 0.7, 1.0, 1.6][i % 4] for i in range(n)]
+    top_ps = [[0.95, 0.5, 1.0, 0.9, 0.05, 0.99][i % 6] for i in range(n)]
+    _check(logits, temps, top_ps, list(us), min_exact=n // 3, rows_per_call=rows_per_call)
 
 
 def test_sample_small_vocab_and_ties():
