@@ -867,7 +867,7 @@ def run_sampling(dev, stream, pk, V, reps=20):
             **out,
             "roofline": {"bound": "hbm", "achieved": r32["achieved_gbs"], "peak": pk["hbm"], "unit": "GB/s",
                          "frac": r32["frac_of_hbm_peak"], "traffic": None,
-                         "kernel": "sample_kernel, 32 rows (one CTA per row; the row is read once per pass)",
+                         "kernel": "sample_kernel<4>, 32 rows (a 4-CTA cluster per row; the row is read once per pass)",
                          "bytes_per_launch": r32["bytes_per_call"], "launch_ms": round(r32["us_per_call"] / 1e3, 5),
                          "peak_kind": pk["kind"] + " copy bandwidth"}}
 
