@@ -125,14 +125,21 @@ __device__ __forceinline__ void walk_row(const float* row, int lo, int hi, Fn&& 
         const int j = j0 + u * kThreads + tid;
         v[u] = j < j_hi ? __ldg(r4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-#pragma unroll
+      // four copies of fn per pass, not 4 kU (the kernel's hot code then stays
+      // in the instruction cache); v[u] is picked by predicated moves, so
+      // the loads stay in registers
+#pragma unroll 1
       for (int u = 0; u < kU; ++u) {
+        float4 c = v[0];
+#pragma unroll
+        for (int w = 1; w < kU; ++w)
+          if (u == w) c = v[w];
         const int j = j0 + u * kThreads + tid;
         const bool ok = j < j_hi;
-        fn(4 * j, v[u].x, ok);
-        fn(4 * j + 1, v[u].y, ok);
-        fn(4 * j + 2, v[u].z, ok);
-        fn(4 * j + 3, v[u].w, ok);
+        fn(4 * j, c.x, ok);
+        fn(4 * j + 1, c.y, ok);
+        fn(4 * j + 2, c.z, ok);
+        fn(4 * j + 3, c.w, ok);
       }
     }
     const int i = 4 * j_hi + tid;  // hi % 4 tokens past the last whole float4
@@ -294,8 +301,8 @@ __device__ void sort_scan(Smem& sm, const float* row, float lmax, float sc, int 
 // down; larger digits come first in the order), then the r-th lowest index
 // among the tokens of that key.  Counts and masses per digit are summed over
 // each warp's lanes of equal digit before one shared-memory atomic.
-__device__ Pick radix_pick(Smem& sm, const float* row, int V, float lmax, float sc, int F, int bin, u64 base,
-                           u64 T) {
+__device__ __noinline__ Pick radix_pick(Smem& sm, const float* row, int V, float lmax, float sc, int F, int bin,
+                                        u64 base, u64 T) {
   const int tid = threadIdx.x;
   auto warp = cg::tiled_partition<32>(cg::this_thread_block());
   if (tid == 0) {
