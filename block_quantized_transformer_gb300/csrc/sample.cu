@@ -72,7 +72,7 @@ struct Smem {
   u64 wsum[kWarps];
   unsigned long long best[kWarps];
   float fred[kWarps];
-  int n_list, list_bin, found;
+  int n_list, found;
   u64 found_cum;
   unsigned prefix;
   u64 above;
@@ -510,10 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(const float* logits
     sm.cum[k] = 0ull;
     sm.cnt[k] = 0u;
   }
-  if (tid == 0) {
-    sm.list_bin = -1;
-    sm.n_list = 0;
-  }
+  if (tid == 0) sm.n_list = 0;
   __syncthreads();
   walk_row(row, i_lo, i_hi, [&](int, float l, bool ok) {
     const float d = (lmax - l) * sc;
