@@ -102,3 +102,41 @@ def test_bad_sequence_index_sets_status_and_poisons(kv):
     model.step(tok, seq, pos, last, block_table=bt)
     with pytest.raises(tq.TqPoisoned, match="out of range"):
         model.status()
+
+
+@pytest.mark.parametrize("base,kv", [(synth.TINY, "f16"), (synth.TINY, "f32"), (synth.TINY_GEMMA3, "f16")])
+def test_mixed_step_flash_blocks_tiny(base, kv):
+    """head_dim 64, two query heads per KV head (flash blocks of 64 rows): one
+    step carries a 70-row prompt of sequence 0 (rows 0..63 one flash block,
+    rows 64..69 with sequence 1's 5-row prompt left to the row-wise kernel),
+    then both sequences decode; pages in a shuffled order; the gemma3-style
+    recipe puts the sliding window on alternate layers."""
+    w = dataclasses.replace(base, kv=kv)
+    tol = 2e-3 if kv == "f32" else 1e-2
+    ref = om.OracleModel(w, om.synth_weights(w))
+    pa, pb = list(w.prompt(0, n=70)), list(w.prompt(1, n=5))
+    ca, cb = ref.new_cache(), ref.new_cache()
+    ref_l = [[ref.forward(pa, ca, 0)], [ref.forward(pb, cb, 0)]]
+    nxt = [om.argmax(ref_l[0][0]), om.argmax(ref_l[1][0])]
+    ref_l[0].append(ref.forward([nxt[0]], ca, 70))
+    ref_l[1].append(ref.forward([nxt[1]], cb, 5))
+
+    model = build_model(w, device=DEV, max_batch=2, max_ctx=128, max_prefill=80, page_size=32, n_pages=8)
+    bt = torch.tensor([[5, 2, 7, 0], [3, 6, 1, 4]], dtype=torch.int32, device=DEV)
+    i32 = lambda v: torch.tensor(v, dtype=torch.int32, device=DEV)
+    steps = [(pa + pb, [0] * 70 + [1] * 5, list(range(70)) + list(range(5)), [69, 74]),
+             (nxt, [0, 1], [70, 5], [0, 1])]
+    got_l, got_t = [[], []], [[], []]
+    for tok, seq, pos, last in steps:
+        lg = torch.empty(2, w.vocab, dtype=torch.float32, device=DEV)
+        am = model.step(i32(tok), i32(seq), i32(pos), i32(last), block_table=bt, logits=lg)
+        lg_h, am_h = lg.double().cpu().numpy(), am.cpu().numpy()
+        for b in range(2):
+            got_l[b].append(lg_h[b])
+            got_t[b].append(int(am_h[b]))
+    assert model.status() == 0
+    model.close()
+    for b in range(2):
+        errs = [rel_logit_err(g, r) for g, r in zip(got_l[b], ref_l[b])]
+        assert max(errs) <= tol, (b, errs)
+        check_tokens(got_t[b], ref_l[b], tol)
